@@ -1,0 +1,99 @@
+"""CPU restatement of the split-KV partition plan (test infrastructure only).
+
+FlashMLA PR #183 (*Add SM80 (Ampere/A100) dense MLA decode kernel*, section
+*How the occupancy work went*) describes the scheduler this follows: the KV
+work of the whole batch is cut into ``num_parts`` contiguous partitions, the
+part count follows from how many CTAs (here: CTA pairs) actually fit on the
+GPU, and every extra partition carries a fixed cost (Q reload, prologue and
+epilogue, one more combine row).  The page gives no formula, so the plan
+below is this library's own; it is written out plainly here so the GPU
+metadata can be compared with it integer for integer.  It is additionally
+pinned by invariants that do not depend on this code (every tile of every
+request is covered exactly once; the split counts add up; no part exceeds
+its budget except the last), see tests/test_sched.py.
+
+Plan
+----
+Work unit = one request b with n_b = ceil(L_b / 64) tiles of 64 keys.
+cost(b) = n_b + F for n_b > 0 (F = fixed cost of a split, in tiles).
+cap = ceil(sum_b cost(b) / P) + F.
+Parts p = 0..P-1 take consecutive ranges of (request, tile) in order.  A
+part completes whole requests while remaining + F fits in its budget, then
+takes ``budget - F`` tiles of the next request if that is positive, and
+stops.  The last part takes everything left.  Requests with n_b = 0 are
+skipped (they get 0 splits).
+
+Metadata (int32):
+  sched[p] = (begin_b, begin_t, end_b, end_t, begin_split, 0, 0, 0)
+    part p covers tiles [begin_t, ...) of begin_b, whole requests in
+    between, and tiles [0, end_t) of end_b (nothing of end_b if end_t = 0);
+    begin_split = how many earlier parts touched begin_b.
+  split_offset[B + 1]: prefix sum of per-request split counts.
+"""
+
+from __future__ import annotations
+
+TILE = 64
+
+
+def ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def plan(seqlens, num_parts: int, fixed_cost: int, tile: int = TILE):
+    B = len(seqlens)
+    nt = [ceil_div(max(int(L), 0), tile) for L in seqlens]
+    total = sum(n + fixed_cost for n in nt if n > 0)
+    cap = ceil_div(total, num_parts) + fixed_cost if total > 0 else 0
+    touched = [0] * B
+    sched = []
+    b, t = 0, 0
+    for p in range(num_parts):
+        while b < B and nt[b] == 0:
+            b, t = b + 1, 0
+        begin = (b, t)
+        begin_split = touched[b] if b < B else 0
+        if p == num_parts - 1:
+            b, t = B, 0
+        else:
+            budget = cap
+            while b < B:
+                if nt[b] == 0:
+                    b, t = b + 1, 0
+                    continue
+                rem = nt[b] - t
+                if rem + fixed_cost <= budget:
+                    budget -= rem + fixed_cost
+                    b, t = b + 1, 0
+                else:
+                    take = budget - fixed_cost
+                    if take > 0:
+                        t += take
+                    break
+        end = (b, t)
+        # requests this part touches
+        if begin != end:
+            last = end[0] if end[1] > 0 else end[0] - 1
+            for bb in range(begin[0], min(last, B - 1) + 1):
+                if nt[bb] > 0:
+                    touched[bb] += 1
+        sched.append((begin[0], begin[1], end[0], end[1], begin_split, 0, 0, 0))
+    split_offset = [0]
+    for bb in range(B):
+        split_offset.append(split_offset[-1] + touched[bb])
+    return sched, split_offset
+
+
+def part_ranges(entry, seqlens, tile: int = TILE):
+    """Expand one sched entry into [(b, t0, t1, split_local), ...]."""
+    b0, t0, b1, t1, s0 = entry[:5]
+    nt = [ceil_div(max(int(L), 0), tile) for L in seqlens]
+    out = []
+    b = b0
+    while b < len(seqlens) and (b < b1 or (b == b1 and t1 > 0)):
+        lo = t0 if b == b0 else 0
+        hi = t1 if b == b1 else nt[b]
+        if hi > lo:
+            out.append((b, lo, hi, s0 if b == b0 else 0))
+        b += 1
+    return out

@@ -1,0 +1,63 @@
+"""Invariants of the split-KV partition plan (CPU).
+
+These pin the plan's restatement in oracle/mla_sched.py without relying on
+it: whatever the plan is, every 64-key tile of every request must be covered
+exactly once, split counts must add up, split slots must be dense, and no
+part may exceed its budget except the last (which absorbs the remainder).
+"""
+
+import numpy as np
+import pytest
+
+from oracle import mla_sched as sp
+
+
+def cost_of(ranges, F):
+    return sum(t1 - t0 + F for (_, t0, t1, _) in ranges)
+
+
+@pytest.mark.parametrize("num_parts", [1, 2, 3, 7, 38, 76, 152])
+@pytest.mark.parametrize("F", [0, 1, 4])
+def test_plan_covers_every_tile_once(num_parts, F):
+    rng = np.random.default_rng(num_parts * 10 + F)
+    for trial in range(25):
+        B = int(rng.integers(1, 70))
+        L = rng.integers(0, 5000, size=B)
+        L[rng.random(B) < 0.1] = 0
+        sched, off = sp.plan(L.tolist(), num_parts, F)
+        assert len(sched) == num_parts and len(off) == B + 1
+        nt = [-(-int(x) // 64) for x in L]
+        seen = {b: np.zeros(nt[b], int) for b in range(B)}
+        splits = {b: [] for b in range(B)}
+        total = sum(n + F for n in nt if n > 0)
+        cap = -(-total // num_parts) + F if total else 0
+        for p, e in enumerate(sched):
+            rs = sp.part_ranges(e, L.tolist())
+            for (b, t0, t1, s) in rs:
+                assert 0 <= t0 < t1 <= nt[b]
+                seen[b][t0:t1] += 1
+                splits[b].append(s)
+            if p < num_parts - 1:
+                assert cost_of(rs, F) <= cap
+            else:
+                assert cost_of(rs, F) <= 2 * cap + F
+        for b in range(B):
+            assert (seen[b] == 1).all()
+            n = off[b + 1] - off[b]
+            assert n == len(splits[b])
+            assert splits[b] == list(range(n))        # split slots 0..n-1 in part order
+            assert (n == 0) == (nt[b] == 0)
+
+
+def test_plan_single_request_long_context():
+    sched, off = sp.plan([65536], 76, 4)
+    rs = [sp.part_ranges(e, [65536]) for e in sched]
+    sizes = [r[0][2] - r[0][1] for r in rs if r]
+    assert sum(sizes) == 1024 and off[1] == len(sizes)
+    assert max(sizes) - min(sizes[:-1]) <= 1 + 4
+
+
+def test_plan_all_empty():
+    sched, off = sp.plan([0, 0, 0], 5, 4)
+    assert off == [0, 0, 0, 0]
+    assert all(sp.part_ranges(e, [0, 0, 0]) == [] for e in sched)
