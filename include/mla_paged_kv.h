@@ -1,0 +1,180 @@
+/*
+ * mla_paged_kv.h -- C ABI of the GB300 (sm_103a) MLA paged-KV decode library.
+ *
+ * Multi-head latent attention decode: every query token has h_q heads that
+ * all attend to ONE latent KV head of 576 entries (512 "NoPE" + 64 "RoPE").
+ * The score is the dot product over all 576 entries; the value is the first
+ * 512 entries of the same row (FlashMLA PR #183 "Add SM80 (Ampere/A100)
+ * dense MLA decode kernel", section Design).  Keys live in a paged cache of
+ * 64-token pages addressed through a per-request block table (same page,
+ * section "How the occupancy work went").  Work is split along the keys
+ * (split-KV); every split writes a partial output and its log-sum-exp, and a
+ * combine kernel merges them (same page, Summary and "Modifications outside
+ * csrc/sm80/").  The sparse variant attends over top-k selected 656-byte FP8
+ * records addressed by physical slot index (FlashMLA PR #200 "[SM90] Add
+ * packed selected-KV sparse decode", sections Motivation and "SM90 packing
+ * kernel").
+ *
+ * Conventions for every entry point:
+ *  - All pointers named d_* are DEVICE pointers owned by the caller.  The
+ *    library never allocates or frees device memory and keeps no state
+ *    besides a per-device cache of kernel attributes.
+ *  - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  No call synchronises with the host.
+ *  - Host-detectable errors are returned BEFORE anything is launched.
+ *  - Errors found on the device (bad block-table entry, bad sparse index,
+ *    a pipeline wait that timed out) are written to *d_status (int32, must
+ *    be zeroed by the caller before the call; the first error wins).  The
+ *    output of the affected request is then unspecified.
+ *  - Layouts are row-major and contiguous.  A query "row" of request b is
+ *    r = i * h_q + h for query token i < s_q and head h < h_q.
+ *  - Every d_* pointer must be 16-byte aligned.
+ */
+#ifndef MLA_PAGED_KV_H_
+#define MLA_PAGED_KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mla_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, workspace too small */
+  MLA_ERR_UNSUPPORTED = 2, /* shape this build does not handle, or no sm_103a device */
+  MLA_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, attribute query) */
+  MLA_ERR_TIMEOUT = 4,     /* device: a pipeline wait exceeded its time budget */
+  MLA_ERR_BAD_INDEX = 5    /* device: block-table entry or sparse index outside the pool */
+} mla_status_t;
+
+/* Fixed geometry (FlashMLA PR #183 Design; PR #200 "SM90 packing kernel"). */
+#define MLA_PAGE_SIZE 64      /* tokens per page */
+#define MLA_D_QK 576          /* latent row: 512 NoPE + 64 RoPE */
+#define MLA_D_V 512           /* value = first 512 entries of the row */
+#define MLA_RECORD_BYTES 656  /* FP8 record: 512 E4M3 + 4 fp32 scales + 64 bf16 */
+#define MLA_ROWS_PER_BLOCK 128 /* query rows handled by one CTA pair */
+#define MLA_SCHED_INTS 8      /* int32 per partition in the scheduler metadata */
+#define MLA_SPLIT_FIXED_COST 4 /* per-split fixed cost, in 64-key tiles, used by the scheduler */
+
+/* Human-readable name of a status code.  Never returns NULL. */
+const char* mla_status_string(int status);
+
+/* Number of key partitions (CTA pairs per row block) the decode kernels run,
+ * derived from how many 2-CTA clusters of the kernel fit on the current
+ * device at once (FlashMLA PR #183, "How the occupancy work went": the
+ * split count follows the CTAs that actually fit).
+ *   rows_per_unit: query rows sharing one key set (dense: s_q*h_q;
+ *                  sparse: h_q), >= 1.
+ *   is_sparse_fp8: 0 for the dense bf16 kernel, 1 for the sparse FP8 one.
+ * Returns >= 1, or a negative mla_status_t on error. */
+int mla_num_parts(int rows_per_unit, int is_sparse_fp8);
+
+/* Bytes of split workspace needed: (n_units + num_parts) split slots, each
+ * rows_per_unit x 512 fp32 partial outputs plus rows_per_unit fp32 LSEs.
+ * n_units: dense = batch, sparse = batch*s_q. */
+size_t mla_workspace_bytes(int n_units, int rows_per_unit, int num_parts);
+
+/* Split-KV scheduler (FlashMLA PR #183: computed once per batch on device
+ * from the sequence lengths and reused by every layer).
+ *   d_lengths   int32 [n_units]: keys per unit (dense: cache_seqlens; sparse:
+ *               topk_length flattened over (b, i)).  May be NULL only when
+ *               default_length >= 0, in which case every unit has that many.
+ *   num_parts   from mla_num_parts().
+ *   d_sched     int32 [num_parts * MLA_SCHED_INTS] out: per partition
+ *               (begin_unit, begin_tile, end_unit, end_tile, begin_split, 0,0,0)
+ *               over 64-key tiles.
+ *   d_split_offset int32 [n_units + 1] out: prefix sum of splits per unit.
+ * The plan: cost(unit) = tiles + MLA_SPLIT_FIXED_COST; partitions take
+ * consecutive (unit, tile) ranges of at most ceil(total/num_parts) +
+ * MLA_SPLIT_FIXED_COST cost; the last one takes the rest.  One thread block. */
+int mla_get_metadata(const int32_t* d_lengths, int default_length, int n_units, int num_parts,
+                     int32_t* d_sched, int32_t* d_split_offset, mla_stream_t stream);
+
+/* Dense bf16 MLA decode: split-KV attention kernel, then the combine kernel
+ * (chained with programmatic dependent launch).
+ *   d_q            bf16 [batch, s_q, h_q, 576]
+ *   d_kv           bf16 [num_pages, 64, 576] paged latent cache (one KV head)
+ *   d_block_table  int32 [batch, max_pages]: logical page -> physical page
+ *   d_cache_seqlens int32 [batch]: keys of request b, including its s_q new
+ *                  tokens.  Key j of request b is row j%64 of page
+ *                  block_table[b][j/64].
+ *   causal         1: query token i sees keys j <= L_b - s_q + i.
+ *   softmax_scale  multiplies q.k (e.g. 1/sqrt(576)).
+ *   d_sched, d_split_offset, num_parts: from mla_get_metadata with
+ *                  d_lengths = d_cache_seqlens, n_units = batch.
+ *   d_workspace    >= mla_workspace_bytes(batch, s_q*h_q, num_parts) bytes.
+ *   d_out          [batch, s_q, h_q, 512], bf16 (out_fp32 = 0) or fp32 (1)
+ *   d_lse          fp32 [batch, s_q, h_q]: natural-log LSE of the scaled
+ *                  scores; -inf (and out = 0) for a row that sees no key.
+ *   d_status       int32, caller-zeroed; see conventions above. */
+int mla_decode_fwd(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
+                   int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int causal,
+                   float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
+                   void* d_workspace, size_t workspace_bytes, void* d_out, int out_fp32, float* d_lse,
+                   int32_t* d_status, mla_stream_t stream);
+
+/* The first half of mla_decode_fwd alone: the split-KV attention kernel.
+ * Units with exactly one split are written straight to d_out/d_lse; the
+ * others leave their partials in d_workspace for mla_combine (or for an
+ * exchange step before it).  Same arguments as mla_decode_fwd. */
+int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
+                      int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int causal,
+                      float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
+                      int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, int out_fp32,
+                      float* d_lse, int32_t* d_status, mla_stream_t stream);
+
+/* LSE-weighted combine of split partials (FlashMLA PR #183 Summary: the
+ * combine kernel merges the splits).  For every unit with != 1 split and
+ * every row r < rows_per_unit:
+ *   L = ln sum_s exp(lse_s);  out = sum_s exp(lse_s - L) * O_s;  lse = L,
+ * where splits with lse_s = -inf weigh 0; a unit with 0 splits, or whose
+ * splits are all -inf, gets out = 0, lse = -inf.  Units with exactly one
+ * split are left alone (the decode kernel wrote them).
+ *   d_workspace as filled by mla_decode_splits / the sparse kernel.
+ *   d_out [n_units, rows_per_unit, 512] bf16 or fp32, d_lse [n_units, rows].
+ * Launched with programmatic dependent launch: it may start before the
+ * previous kernel on the stream ends and waits for it on the device. */
+int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* d_split_offset, int n_units,
+                int rows_per_unit, int num_parts, void* d_out, int out_fp32, float* d_lse, mla_stream_t stream);
+
+/* Sparse FP8 MLA decode (FlashMLA PR #200).  Query token (b, i) attends to
+ * the records selected by d_indices[b][i][0 .. topk_length[b][i]); entry t
+ * is a physical slot: page idx/64, row idx%64 of d_kv8.  -1 anywhere is
+ * masked; a duplicated index counts twice; an index outside
+ * [0, num_pages*64) is masked and reported as MLA_ERR_BAD_INDEX.
+ * Record layout (656 B): [0,512) E4M3 codes, [512,528) four fp32 scales,
+ * [528,656) 64 bf16 RoPE values; key[d] = e4m3[d] * scale[d/128] (d < 512),
+ * key[512+e] = rope[e]; value = key[0..512).  In the kernel each NoPE value
+ * is rounded to bf16 after the fp32 multiply before the tensor-core product.
+ *   d_q           bf16 [batch, s_q, h_q, 576]
+ *   d_kv8         uint8 [num_pages, 64, 656]
+ *   d_indices     int32 [batch, s_q, topk]
+ *   d_topk_length int32 [batch, s_q] or NULL (= topk)
+ *   d_sched, d_split_offset, num_parts: from mla_get_metadata with
+ *                 d_lengths = d_topk_length (or NULL with default topk),
+ *                 n_units = batch*s_q, and mla_num_parts(h_q, 1).
+ *   d_workspace   >= mla_workspace_bytes(batch*s_q, h_q, num_parts)
+ *   d_out bf16 [batch, s_q, h_q, 512], d_lse fp32 [batch, s_q, h_q]. */
+int mla_sparse_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, int num_pages, const int32_t* d_indices,
+                              int topk, const int32_t* d_topk_length, int batch, int s_q, int h_q,
+                              float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
+                              int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out,
+                              float* d_lse, int32_t* d_status, mla_stream_t stream);
+
+/* Gather + unpack of selected records to fp32 key rows, bit-exact:
+ * k[d] = fp32(e4m3[d]) * scale[d/128] as one fp32 round-to-nearest-even
+ * multiply (d < 512), k[512+e] = fp32(bf16 rope[e]).  Index -1 or an index
+ * outside the pool gives a zero row (the latter also MLA_ERR_BAD_INDEX).
+ *   d_indices int32 [n], d_k_out fp32 [n, 576]. */
+int mla_sparse_fp8_unpack(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int n, float* d_k_out,
+                          int32_t* d_status, mla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_PAGED_KV_H_ */

@@ -1,0 +1,352 @@
+// C ABI of the MLA paged-KV decode library: argument checks, tensor maps,
+// partition counts and launches.  No device memory is allocated here.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/mla_paged_kv.h"
+#include "common.cuh"
+
+namespace mla {
+cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, void*, int, float*, cudaStream_t);
+cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int, cudaStream_t);
+int dense_smem_bytes();
+int dense_threads();
+const void* dense_kernel_ptr();
+cudaError_t launch_sparse(const CUtensorMap&, const DecodeParams&, int, cudaStream_t);
+int sparse_smem_bytes();
+int sparse_threads();
+const void* sparse_kernel_ptr();
+cudaError_t launch_unpack(const uint8_t*, int, const int32_t*, int, float*, int32_t*, cudaStream_t);
+}  // namespace mla
+
+using namespace mla;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int status = MLA_OK;
+  int dense_clusters = 0;
+  int sparse_clusters = 0;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+int max_clusters(const void* kernel, int threads, int smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 1024, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return -1;
+  return n;
+}
+
+// Per-device one-time setup: shared-memory opt-in and co-resident cluster counts.
+const DeviceInfo& device_info() {
+  int dev = 0;
+  static DeviceInfo bad;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    bad.status = MLA_ERR_CUDA;
+    return bad;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.ready) return d;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) {
+    d.status = MLA_ERR_UNSUPPORTED;  // built for sm_103a only
+    d.ready = true;
+    return d;
+  }
+  if (cudaFuncSetAttribute(dense_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(sparse_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           sparse_smem_bytes()) != cudaSuccess) {
+    cudaGetLastError();
+    d.status = MLA_ERR_CUDA;
+    d.ready = true;
+    return d;
+  }
+  d.dense_clusters = max_clusters(dense_kernel_ptr(), dense_threads(), dense_smem_bytes());
+  d.sparse_clusters = max_clusters(sparse_kernel_ptr(), sparse_threads(), sparse_smem_bytes());
+  if (d.dense_clusters <= 0 || d.sparse_clusters <= 0) {
+    cudaGetLastError();
+    d.status = MLA_ERR_CUDA;
+  }
+  d.ready = true;
+  return d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WorkspaceLayout {
+  size_t o_bytes, lse_off, total;
+};
+
+WorkspaceLayout ws_layout(int n_units, int rows, int num_parts) {
+  const size_t slots = static_cast<size_t>(n_units) + static_cast<size_t>(num_parts);
+  WorkspaceLayout w;
+  w.o_bytes = slots * rows * MLA_D_V * sizeof(float);
+  w.lse_off = align_up(w.o_bytes, 256);
+  w.total = align_up(w.lse_off + slots * rows * sizeof(float), 256);
+  return w;
+}
+
+int encode_q_map(CUtensorMap* m, const void* q, long long rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return MLA_ERR_CUDA;
+  cuuint64_t dims[2] = {MLA_D_QK, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {MLA_D_QK * 2};
+  cuuint32_t box[2] = {64, MLA_ROWS_PER_BLOCK};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
+}
+
+int encode_kv_map(CUtensorMap* m, const void* kv, int num_pages) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return MLA_ERR_CUDA;
+  cuuint64_t dims[3] = {MLA_D_QK, MLA_PAGE_SIZE, static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[2] = {MLA_D_QK * 2, static_cast<cuuint64_t>(MLA_D_QK) * 2 * MLA_PAGE_SIZE};
+  cuuint32_t box[3] = {64, MLA_PAGE_SIZE, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
+}
+
+int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int max_pages, int num_pages,
+                  const int32_t* seqlens, int batch, int s_q, int h_q, int causal, float scale,
+                  const int32_t* sched, const int32_t* split_offset, int num_parts, void* workspace,
+                  size_t workspace_bytes, void* out, int out_fp32, float* lse, int32_t* status, DecodeParams* p,
+                  CUtensorMap* q_map, CUtensorMap* kv_map) {
+  if (!q || !kv || !block_table || !seqlens || !sched || !split_offset || !workspace || !out || !lse || !status)
+    return MLA_ERR_INVALID_ARG;
+  if (batch < 1 || s_q < 1 || h_q < 1 || max_pages < 1 || num_pages < 1 || num_parts < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(s_q) * h_q;
+  if (rows > (1 << 20) || static_cast<long long>(batch) * rows > (1LL << 31) - 1) return MLA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(workspace) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  if (out_fp32 != 0 && out_fp32 != 1) return MLA_ERR_INVALID_ARG;
+  const WorkspaceLayout w = ws_layout(batch, static_cast<int>(rows), num_parts);
+  if (workspace_bytes < w.total) return MLA_ERR_INVALID_ARG;
+  const int row_blocks = static_cast<int>((rows + MLA_ROWS_PER_BLOCK - 1) / MLA_ROWS_PER_BLOCK);
+  if (2LL * num_parts * row_blocks > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  const DeviceInfo& d = device_info();
+  if (d.status != MLA_OK) return d.status;
+  int rc = encode_q_map(q_map, q, static_cast<long long>(batch) * rows);
+  if (rc != MLA_OK) return rc;
+  rc = encode_kv_map(kv_map, kv, num_pages);
+  if (rc != MLA_OK) return rc;
+  *p = DecodeParams{};
+  p->lengths = seqlens;
+  p->default_length = 0;
+  p->n_units = batch;
+  p->rows = static_cast<int>(rows);
+  p->row_blocks = row_blocks;
+  p->h_q = h_q;
+  p->s_q = s_q;
+  p->causal = causal ? 1 : 0;
+  p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p->block_table = block_table;
+  p->max_pages = max_pages;
+  p->num_pages = num_pages;
+  p->sched = sched;
+  p->split_offset = split_offset;
+  p->num_parts = num_parts;
+  p->o_accum = static_cast<float*>(workspace);
+  p->lse_accum = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.lse_off);
+  p->out = out;
+  p->out_fp32 = out_fp32;
+  p->lse = lse;
+  p->status = status;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: null pointer, bad size, misalignment or small workspace";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: shape or device not supported by this sm_103a build";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA runtime call failed";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a device pipeline wait ran out of time";
+    case MLA_ERR_BAD_INDEX: return "MLA_ERR_BAD_INDEX: block-table entry or sparse index outside the pool";
+    default: return "unknown mla status";
+  }
+}
+
+int mla_num_parts(int rows_per_unit, int is_sparse_fp8) {
+  if (rows_per_unit < 1 || (is_sparse_fp8 != 0 && is_sparse_fp8 != 1)) return -MLA_ERR_INVALID_ARG;
+  const DeviceInfo& d = device_info();
+  if (d.status != MLA_OK) return -d.status;
+  const int clusters = is_sparse_fp8 ? d.sparse_clusters : d.dense_clusters;
+  const int row_blocks = (rows_per_unit + MLA_ROWS_PER_BLOCK - 1) / MLA_ROWS_PER_BLOCK;
+  const int parts = clusters / row_blocks;
+  return parts > 0 ? parts : 1;
+}
+
+size_t mla_workspace_bytes(int n_units, int rows_per_unit, int num_parts) {
+  if (n_units < 0 || rows_per_unit < 1 || num_parts < 1) return 0;
+  return ws_layout(n_units, rows_per_unit, num_parts).total;
+}
+
+int mla_get_metadata(const int32_t* d_lengths, int default_length, int n_units, int num_parts, int32_t* d_sched,
+                     int32_t* d_split_offset, mla_stream_t stream) {
+  if (n_units < 1 || num_parts < 1 || !d_sched || !d_split_offset) return MLA_ERR_INVALID_ARG;
+  if (d_lengths == nullptr && default_length < 0) return MLA_ERR_INVALID_ARG;
+  return launch_sched(d_lengths, default_length, n_units, num_parts, d_sched, d_split_offset,
+                      reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
+                      int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int causal,
+                      float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
+                      void* d_workspace, size_t workspace_bytes, void* d_out, int out_fp32, float* d_lse,
+                      int32_t* d_status, mla_stream_t stream) {
+  DecodeParams p;
+  CUtensorMap qm, km;
+  const int rc = dense_prepare(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q,
+                               causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
+                               workspace_bytes, d_out, out_fp32, d_lse, d_status, &p, &qm, &km);
+  if (rc != MLA_OK) return rc;
+  return launch_dense(qm, km, p, num_parts, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
+                                                                                                    : MLA_ERR_CUDA;
+}
+
+int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* d_split_offset, int n_units,
+                int rows_per_unit, int num_parts, void* d_out, int out_fp32, float* d_lse, mla_stream_t stream) {
+  if (!d_workspace || !d_split_offset || !d_out || !d_lse) return MLA_ERR_INVALID_ARG;
+  if (n_units < 1 || n_units > 65535 || rows_per_unit < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
+  if (out_fp32 != 0 && out_fp32 != 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(d_workspace) || !aligned16(d_out)) return MLA_ERR_INVALID_ARG;
+  const WorkspaceLayout w = ws_layout(n_units, rows_per_unit, num_parts);
+  if (workspace_bytes < w.total) return MLA_ERR_INVALID_ARG;
+  const float* o = static_cast<const float*>(d_workspace);
+  const float* l = reinterpret_cast<const float*>(static_cast<const char*>(d_workspace) + w.lse_off);
+  return launch_combine(o, l, d_split_offset, n_units, rows_per_unit, d_out, out_fp32, d_lse,
+                        reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+int mla_decode_fwd(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages, int num_pages,
+                   const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int causal, float softmax_scale,
+                   const int32_t* d_sched, const int32_t* d_split_offset, int num_parts, void* d_workspace,
+                   size_t workspace_bytes, void* d_out, int out_fp32, float* d_lse, int32_t* d_status,
+                   mla_stream_t stream) {
+  if (batch > 65535) return MLA_ERR_UNSUPPORTED;
+  int rc = mla_decode_splits(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q,
+                             causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
+                             workspace_bytes, d_out, out_fp32, d_lse, d_status, stream);
+  if (rc != MLA_OK) return rc;
+  return mla_combine(d_workspace, workspace_bytes, d_split_offset, batch, s_q * h_q, num_parts, d_out, out_fp32,
+                     d_lse, stream);
+}
+
+int mla_sparse_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, int num_pages, const int32_t* d_indices,
+                              int topk, const int32_t* d_topk_length, int batch, int s_q, int h_q,
+                              float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
+                              int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
+                              int32_t* d_status, mla_stream_t stream) {
+  if (!d_q || !d_kv8 || !d_indices || !d_sched || !d_split_offset || !d_workspace || !d_out || !d_lse || !d_status)
+    return MLA_ERR_INVALID_ARG;
+  if (batch < 1 || s_q < 1 || h_q < 1 || num_pages < 1 || topk < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if (h_q > MLA_ROWS_PER_BLOCK) return MLA_ERR_UNSUPPORTED;
+  const long long units = static_cast<long long>(batch) * s_q;
+  if (units > 65535) return MLA_ERR_UNSUPPORTED;
+  if (!aligned16(d_q) || !aligned16(d_kv8) || !aligned16(d_workspace) || !aligned16(d_out))
+    return MLA_ERR_INVALID_ARG;
+  const WorkspaceLayout w = ws_layout(static_cast<int>(units), h_q, num_parts);
+  if (workspace_bytes < w.total) return MLA_ERR_INVALID_ARG;
+  const DeviceInfo& d = device_info();
+  if (d.status != MLA_OK) return d.status;
+  DecodeParams p{};
+  p.lengths = d_topk_length;
+  p.default_length = topk;
+  p.n_units = static_cast<int>(units);
+  p.rows = h_q;
+  p.row_blocks = 1;
+  p.h_q = h_q;
+  p.s_q = 1;
+  p.causal = 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+  p.num_pages = num_pages;
+  p.indices = d_indices;
+  p.topk = topk;
+  p.kv8 = d_kv8;
+  p.sched = d_sched;
+  p.split_offset = d_split_offset;
+  p.num_parts = num_parts;
+  p.o_accum = static_cast<float*>(d_workspace);
+  p.lse_accum = reinterpret_cast<float*>(static_cast<char*>(d_workspace) + w.lse_off);
+  p.out = d_out;
+  p.out_fp32 = 0;
+  p.lse = d_lse;
+  p.status = d_status;
+  CUtensorMap qm;
+  const int rc = encode_q_map(&qm, d_q, units * h_q);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_sparse(qm, p, num_parts, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return mla_combine(d_workspace, workspace_bytes, d_split_offset, static_cast<int>(units), h_q, num_parts, d_out,
+                     0, d_lse, stream);
+}
+
+int mla_sparse_fp8_unpack(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int n, float* d_k_out,
+                          int32_t* d_status, mla_stream_t stream) {
+  if (!d_kv8 || !d_indices || !d_k_out || !d_status || num_pages < 1 || n < 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(d_kv8) || !aligned16(d_k_out)) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  return launch_unpack(d_kv8, num_pages, d_indices, n, d_k_out, d_status, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// Shared definitions of the MLA decode kernels (device side).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mla_paged_kv.h"
+
+namespace mla {
+
+constexpr int kTile = MLA_PAGE_SIZE;        // keys per pipeline tile = one page
+constexpr int kRowsPerBlock = MLA_ROWS_PER_BLOCK;
+constexpr int kDqk = MLA_D_QK;
+constexpr int kDv = MLA_D_V;
+
+// First error wins; later ones are dropped so the caller sees the root cause.
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
+}
+
+__host__ __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int num_tiles(int len) { return len > 0 ? ceil_div_i(len, kTile) : 0; }
+
+// Everything the split-KV attention kernels read besides the tensor maps.
+struct DecodeParams {
+  // keys per unit (dense: cache_seqlens, sparse: topk_length or NULL)
+  const int32_t* lengths;
+  int default_length;       // used when lengths == NULL
+  int n_units;              // dense: batch; sparse: batch * s_q
+  int rows;                 // query rows per unit (dense s_q*h_q, sparse h_q)
+  int row_blocks;           // ceil(rows / 128)
+  int h_q;
+  int s_q;                  // dense: tokens per unit (causal alignment); sparse: 1
+  int causal;
+  float scale_log2;         // softmax_scale * log2(e)
+  // dense
+  const int32_t* block_table;
+  int max_pages;
+  int num_pages;
+  // sparse
+  const int32_t* indices;   // [n_units, topk]
+  int topk;
+  const uint8_t* kv8;       // [num_pages, 64, 656]
+  // schedule
+  const int32_t* sched;
+  const int32_t* split_offset;
+  int num_parts;
+  // outputs
+  float* o_accum;           // [slots, rows, 512]
+  float* lse_accum;         // [slots, rows]
+  void* out;                // [n_units, rows, 512]
+  int out_fp32;
+  float* lse;               // [n_units, rows]
+  int32_t* status;
+};
+
+}  // namespace mla

@@ -1,0 +1,119 @@
+"""Dense MLA decode on the GPU through the C ABI, element by element against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import mla_paged_kv_gb300 as mla
+from mla_paged_kv_gb300 import workloads as wl
+from oracle import mla_sched
+from tests.parity import compare, dense_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_dense(case, num_parts=None, split_path=False):
+    c = to_dev(case)
+    B, s_q, h_q = case.batch, case.s_q, case.h_q
+    pl = mla.plan(c.cache_seqlens, B, s_q * h_q, num_parts=num_parts)
+    out = torch.full((B, s_q, h_q, 512), float("nan"), device="cuda",
+                     dtype=torch.float32 if case.out_fp32 else torch.bfloat16)
+    lse = torch.full((B, s_q, h_q), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if split_path:
+        mla.mla_decode_splits(c.q, c.kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset, pl.num_parts,
+                              pl.workspace, out, lse, status, case.causal, case.scale)
+        mla.mla_combine(pl.workspace, pl.split_offset, B, s_q * h_q, pl.num_parts, out, lse)
+    else:
+        mla.mla_decode_fwd(c.q, c.kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset, pl.num_parts,
+                           pl.workspace, out, lse, status, case.causal, case.scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, mla.mla_status_string(int(status.item()))
+    return out, lse, pl
+
+
+@pytest.mark.parametrize("lens", [[1], [63], [64], [65], [127, 200], [1000, 3, 64]])
+@pytest.mark.parametrize("h_q", [16, 128])
+def test_dense_small_lengths(lens, h_q):
+    case = wl.dense_case(len(lens), 1, h_q, 0, seqlens=lens, seed=sum(lens) + h_q)
+    out, lse, _ = run_dense(case)
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("num_parts", [1, 2, 5, 40])
+def test_dense_split_counts(num_parts):
+    case = wl.dense_case(3, 1, 64, 0, seqlens=[900, 130, 2000], seed=num_parts)
+    out, lse, pl = run_dense(case, num_parts=num_parts)
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+    # scheduler metadata equals the plan, integer for integer
+    sched, off = mla_sched.plan(case.cache_seqlens.tolist(), num_parts, 4)
+    assert pl.sched.cpu().reshape(-1, 8).tolist() == [list(e) for e in sched]
+    assert pl.split_offset.cpu().tolist() == off
+
+
+def test_dense_splits_then_combine_entry_points():
+    case = wl.dense_case(2, 1, 32, 0, seqlens=[700, 1500], seed=3)
+    out, lse, _ = run_dense(case, num_parts=7, split_path=True)
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("lens", [[1, 2], [64, 65], [300, 129]])
+def test_dense_causal_two_tokens(lens):
+    case = wl.dense_case(len(lens), 2, 128, 0, seqlens=lens, causal=True, seed=11 + sum(lens))
+    out, lse, _ = run_dense(case)
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+def test_dense_peaky_queries():
+    case = wl.dense_case(2, 1, 128, 0, seqlens=[1500, 333], q_scale=8.0, seed=21)
+    out, lse, _ = run_dense(case)
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+def test_dense_tiny_fp32_out():
+    case = wl.make("dense_b1_hq16_sk256_fp32out")
+    out, lse, _ = run_dense(case)
+    assert out.dtype == torch.float32
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+def test_dense_empty_request():
+    case = wl.dense_case(3, 1, 16, 0, seqlens=[0, 70, 0], seed=5)
+    out, lse, _ = run_dense(case)
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+def test_dense_rows_spanning_two_blocks():
+    case = wl.dense_case(2, 2, 96, 0, seqlens=[260, 90], causal=True, seed=31)   # 192 rows per request
+    out, lse, _ = run_dense(case)
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+def test_dense_is_deterministic():
+    case = wl.dense_case(2, 1, 128, 0, seqlens=[1200, 800], seed=41)
+    o1, l1, _ = run_dense(case, num_parts=9)
+    o2, l2, _ = run_dense(case, num_parts=9)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_dense_block_table_permutation():
+    case = wl.dense_case(2, 1, 64, 0, seqlens=[500, 260], seed=51)
+    o1, l1, _ = run_dense(case, num_parts=4)
+    P = case.kv.shape[0]
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(1))
+    kv2 = torch.empty_like(case.kv)
+    kv2[perm] = case.kv
+    bt = case.block_table
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].to(torch.int32), bt)
+    case2 = wl.DenseCase(q=case.q, kv=kv2, block_table=bt2, cache_seqlens=case.cache_seqlens, causal=False,
+                         scale=case.scale, out_fp32=False)
+    o2, l2, _ = run_dense(case2, num_parts=4)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
