@@ -103,7 +103,7 @@ int mla_get_metadata(const int32_t* d_lengths, int default_length, int n_units, 
  *                  tokens.  Key j of request b is row j%64 of page
  *                  block_table[b][j/64].
  *   causal         1: query token i sees keys j <= L_b - s_q + i.
- *   softmax_scale  multiplies q.k (e.g. 1/sqrt(576)).
+ *   softmax_scale  multiplies q.k (e.g. 1/sqrt(576)); must be finite and > 0.
  *   d_sched, d_split_offset, num_parts: from mla_get_metadata with
  *                  d_lengths = d_cache_seqlens, n_units = batch.
  *   d_workspace    >= mla_workspace_bytes(batch, s_q*h_q, num_parts) bytes.

@@ -8,13 +8,14 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/mla_paged_kv.h"
+#include "mla_paged_kv.h"
 #include "common.cuh"
 
 namespace mla {
 cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, void*, int, float*, cudaStream_t);
-cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int, cudaStream_t);
+cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, const void*, int,
+                         cudaStream_t);
 int dense_smem_bytes();
 int dense_threads();
 const void* dense_kernel_ptr();
@@ -140,6 +141,7 @@ int encode_q_map(CUtensorMap* m, const void* q, long long rows) {
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
+// Dense KV pool as [num_pages][64][576] bf16; one box = 64 dims x 64 tokens of one page.
 int encode_kv_map(CUtensorMap* m, const void* kv, int num_pages) {
   auto fn = encode_fn();
   if (fn == nullptr) return MLA_ERR_CUDA;
@@ -162,7 +164,7 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
     return MLA_ERR_INVALID_ARG;
   if (batch < 1 || s_q < 1 || h_q < 1 || max_pages < 1 || num_pages < 1 || num_parts < 1)
     return MLA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return MLA_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(s_q) * h_q;
   if (rows > (1 << 20) || static_cast<long long>(batch) * rows > (1LL << 31) - 1) return MLA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(kv) || !aligned16(workspace) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
@@ -254,7 +256,7 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
                                causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
                                workspace_bytes, d_out, out_fp32, d_lse, d_status, &p, &qm, &km);
   if (rc != MLA_OK) return rc;
-  return launch_dense(qm, km, p, num_parts, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
+  return launch_dense(qm, km, p, d_q, num_parts, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
                                                                                                     : MLA_ERR_CUDA;
 }
 
@@ -296,7 +298,7 @@ int mla_sparse_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, int num_pag
   if (!d_q || !d_kv8 || !d_indices || !d_sched || !d_split_offset || !d_workspace || !d_out || !d_lse || !d_status)
     return MLA_ERR_INVALID_ARG;
   if (batch < 1 || s_q < 1 || h_q < 1 || num_pages < 1 || topk < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
-  if (!std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   if (h_q > MLA_ROWS_PER_BLOCK) return MLA_ERR_UNSUPPORTED;
   const long long units = static_cast<long long>(batch) * s_q;
   if (units > 65535) return MLA_ERR_UNSUPPORTED;

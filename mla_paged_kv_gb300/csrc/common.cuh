@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/mla_paged_kv.h"
+#include "mla_paged_kv.h"
 
 namespace mla {
 

@@ -131,6 +131,44 @@ __device__ __forceinline__ bool unit_in_part(const Part& P, int b, int n_units) 
   return b < n_units && (b < P.b1 || (b == P.b1 && P.t1 > 0));
 }
 
+// Walk over the (unit, tile) sequence of one partition.
+struct Cursor {
+  int b, k, lo, hi;  // unit, tile, tile range of the unit in this partition
+  int u;             // ordinal of the unit within the partition
+  uint32_t t;        // ordinal of the tile within the partition
+  bool valid;
+};
+
+__device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& P, Cursor& c, int from_b) {
+  for (int b = from_b; unit_in_part(P, b, p.n_units); ++b) {
+    int lo, hi;
+    unit_tiles(P, b, num_tiles(unit_len(p, b)), lo, hi);
+    if (hi > lo) {
+      c.b = b;
+      c.lo = lo;
+      c.hi = hi;
+      c.k = lo;
+      c.valid = true;
+      return;
+    }
+  }
+  c.valid = false;
+}
+
+__device__ __forceinline__ void cursor_init(const DecodeParams& p, const Part& P, Cursor& c) {
+  c.u = 0;
+  c.t = 0;
+  cursor_seek(p, P, c, P.b0);
+}
+
+__device__ __forceinline__ void cursor_next(const DecodeParams& p, const Part& P, Cursor& c) {
+  ++c.t;
+  if (++c.k == c.hi) {
+    ++c.u;
+    cursor_seek(p, P, c, c.b + 1);
+  }
+}
+
 __device__ __forceinline__ void set_abort(volatile int* abort_flag, int32_t* status, int code) {
   *abort_flag = 1;
   report(status, code);
@@ -366,61 +404,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
       const uint64_t kv_desc0 = sdesc_sw128(smem_u32(sKV), 16, 1024);
       const uint64_t v_desc0 = sdesc_sw128(smem_u32(sKV), kKVBoxBytes, 1024);
       const uint64_t p_desc0 = sdesc_sw128(smem_u32(sP), 16, 1024);
-      struct Pend {
-        bool valid, first, last;
-        uint32_t t;
-        int u;
-      } pend = {false, false, false, 0u, 0};
+      // Two cursors over the partition's (unit, tile) sequence: QK runs ahead of
+      // PV by at most the two S/KV buffers.  Whichever is ready is issued, PV
+      // first, so a KV stage is released as soon as its PV is issued.
+      Cursor cq, cv;
+      cursor_init(p, P, cq);
+      cursor_init(p, P, cv);
       bool ok = true;
-      auto issue_pv = [&](const Pend& q) -> bool {
-        const int pb = q.t & 1;
-        if (!mbar_wait(&bars[P_FULL + pb], (q.t >> 1) & 1, abort_flag)) return false;
-        if (q.first && q.u >= 1 && !mbar_wait(&bars[O_FREE], (q.u - 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint64_t a0 = p_desc0 + static_cast<uint64_t>((pb * kPBytes) >> 4);
-        const uint64_t b0 = v_desc0 + static_cast<uint64_t>((pb * kStageBytes) >> 4);
+      uint64_t t_last = globaltimer_ns();
+      while (cv.valid) {
+        bool progressed = false;
+        if (cv.t < cq.t) {
+          const int pb = cv.t & 1;
+          bool ready = mbar_test_wait(&bars[P_FULL + pb], (cv.t >> 1) & 1);
+          const bool first = cv.k == cv.lo, last = cv.k == cv.hi - 1;
+          if (ready && first && cv.u >= 1) ready = mbar_test_wait(&bars[O_FREE], (cv.u - 1) & 1);
+          if (ready) {
+            tc_fence_after();
+            const uint64_t a0 = p_desc0 + static_cast<uint64_t>((pb * kPBytes) >> 4);
+            const uint64_t b0 = v_desc0 + static_cast<uint64_t>((pb * kStageBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_f16(tmem + kTmemO, a0 + static_cast<uint64_t>((kk * 32) >> 4),
-                   b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (q.first && kk == 0) ? 0u : 1u);
-        umma_commit(&bars[P_FREE + pb]);
-        umma_commit(&bars[KV_EMPTY + pb]);
-        if (q.last) umma_commit(&bars[O_FULL]);
-        return true;
-      };
-      uint32_t t = 0;
-      int u = 0;
-      for (int b = P.b0; ok && unit_in_part(P, b, p.n_units); ++b) {
-        const int nt = num_tiles(unit_len(p, b));
-        int lo, hi;
-        unit_tiles(P, b, nt, lo, hi);
-        if (hi <= lo) continue;
-        ok = mbar_wait(&bars[Q_FULL], u & 1, abort_flag);
-        for (int k = lo; ok && k < hi; ++k, ++t) {
-          const int st = t & 1;
-          ok = mbar_wait(&bars[KV_FULL + st], (t >> 1) & 1, abort_flag);
-          if (ok && t >= 2) ok = mbar_wait(&bars[S_FREE + st], ((t - 2) >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t kvs = kv_desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
-          for (int ks = ks0; ks < ks1; ++ks) {
-            const int lb = (ks >> 2) - 4 * static_cast<int>(rank);
-            const uint32_t off_q = lb * kQBoxBytes + (ks & 3) * 32;
-            const uint32_t off_k = lb * kKVBoxBytes + (ks & 3) * 32;
-            umma_f16(tmem + kTmemS + 64u * st, q_desc0 + (off_q >> 4), kvs + (off_k >> 4), idesc_qk,
-                     ks > ks0 ? 1u : 0u);
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_f16(tmem + kTmemO, a0 + static_cast<uint64_t>((kk * 32) >> 4),
+                       b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
+            umma_commit(&bars[P_FREE + pb]);
+            umma_commit(&bars[KV_EMPTY + pb]);
+            if (last) umma_commit(&bars[O_FULL]);
+            cursor_next(p, P, cv);
+            progressed = true;
           }
-          umma_commit(&bars[S_FULL + st]);
-          if (k == hi - 1) umma_commit(&bars[Q_EMPTY]);
-          if (pend.valid) {
-            ok = issue_pv(pend);
-            if (!ok) break;
-          }
-          pend = Pend{true, k == lo, k == hi - 1, t, u};
         }
-        ++u;
+        if (cq.valid) {
+          const int st = cq.t & 1;
+          bool ready = true;
+          if (cq.k == cq.lo) ready = mbar_test_wait(&bars[Q_FULL], cq.u & 1);
+          ready = ready && mbar_test_wait(&bars[KV_FULL + st], (cq.t >> 1) & 1);
+          if (ready && cq.t >= 2) ready = mbar_test_wait(&bars[S_FREE + st], ((cq.t - 2) >> 1) & 1);
+          if (ready) {
+            tc_fence_after();
+            const uint64_t kvs = kv_desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
+            for (int ks = ks0; ks < ks1; ++ks) {
+              const int lb = (ks >> 2) - 4 * static_cast<int>(rank);
+              const uint32_t off_q = lb * kQBoxBytes + (ks & 3) * 32;
+              const uint32_t off_k = lb * kKVBoxBytes + (ks & 3) * 32;
+              umma_f16(tmem + kTmemS + 64u * st, q_desc0 + (off_q >> 4), kvs + (off_k >> 4), idesc_qk,
+                       ks > ks0 ? 1u : 0u);
+            }
+            umma_commit(&bars[S_FULL + st]);
+            if (cq.k == cq.hi - 1) umma_commit(&bars[Q_EMPTY]);
+            cursor_next(p, P, cq);
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_last = globaltimer_ns();
+        } else {
+          if (*abort_flag || globaltimer_ns() - t_last > MLA_WAIT_LIMIT_NS) {
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+        }
       }
-      if (ok && pend.valid) ok = issue_pv(pend);
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // every MMA has completed before TMEM is released
       umma_commit(&bars[DRAIN]);
@@ -674,19 +719,9 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
 
 }  // namespace dec
 
-int dense_smem_bytes() { return dec::kSmemBytes; }
-int dense_threads() { return dec::Roles<false>::kThreads; }
-const void* dense_kernel_ptr() { return reinterpret_cast<const void*>(&dec::mla_decode_kernel<false>); }
 int sparse_smem_bytes() { return dec::kSmemBytes; }
 int sparse_threads() { return dec::Roles<true>::kThreads; }
 const void* sparse_kernel_ptr() { return reinterpret_cast<const void*>(&dec::mla_decode_kernel<true>); }
-
-cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, const DecodeParams& p, int num_parts,
-                         cudaStream_t stream) {
-  const dim3 grid(2 * num_parts * p.row_blocks);
-  dec::mla_decode_kernel<false><<<grid, dec::Roles<false>::kThreads, dec::kSmemBytes, stream>>>(q_map, kv_map, p);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_sparse(const CUtensorMap& q_map, const DecodeParams& p, int num_parts, cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
