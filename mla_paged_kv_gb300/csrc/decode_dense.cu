@@ -99,7 +99,7 @@ enum : int {
 };
 
 #ifndef MLA_DENSE_PREFETCH_PAGES
-#define MLA_DENSE_PREFETCH_PAGES 8
+#define MLA_DENSE_PREFETCH_PAGES 0
 #endif
 constexpr int kPrefetch = MLA_DENSE_PREFETCH_PAGES;  // pages prefetched into L2 ahead of the TMA loads
 constexpr float kTau = 8.0f;  // lazy-rescale threshold (log2 units)
@@ -524,16 +524,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars[Q_FULL]);
     }
-    // l_sum: fp32 sum of the unrounded weights (gives the LSE);
-    // l_used: sum of the bf16 weights the tensor core multiplies (normalises O)
-    float m_used = -INFINITY, l_sum = 0.f, l_used = 0.f;
+    float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and fp32 row sum
     while (ok && c.valid) {
       const uint32_t t = c.t;
       const bool first = cursor_first(c), last = cursor_last(c);
       if (first) {
         m_used = -INFINITY;
         l_sum = 0.f;
-        l_used = 0.f;
       }
       const int jmax = p.causal ? (c.L - p.s_q + tok) : (c.L - 1);  // last visible key
       const int vis = jmax - c.k * kT;                                // keys 0..vis of this tile are visible
@@ -574,24 +571,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         alpha = ex2(m_used - mt);  // 0 when m_used == -inf
         rescale = !first;
         l_sum *= alpha;
-        l_used *= alpha;
         m_used = mt;
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
       uint32_t pk[kT / 2];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f}, lu[4] = {0.f, 0.f, 0.f, 0.f};
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < kT / 2; ++i) {
         const float p0 = ex2(fmaf(s[2 * i], c_log2, -mref));
         const float p1 = ex2(fmaf(s[2 * i + 1], c_log2, -mref));
         const __nv_bfloat162 hv = __floats2bfloat162_rn(p0, p1);
-        const uint32_t bits = *reinterpret_cast<const uint32_t*>(&hv);
-        pk[i] = bits;
+        pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
         ls[i & 3] += p0 + p1;
-        lu[i & 3] += __uint_as_float(bits << 16) + __uint_as_float(bits & 0xFFFF0000u);
       }
       l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      l_used += (lu[0] + lu[1]) + (lu[2] + lu[3]);
       const int pb = t & 1;
       if (t >= 2) {
         ok = warp_wait(&bars[P_FREE + pb], ((t - 2) >> 1) & 1, abort_flag);
@@ -641,7 +634,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int s_begin = p.split_offset[b_here];
       const int nsplit = p.split_offset[b_here + 1] - s_begin;
       const int slot = s_begin + ((b_here == P.b0) ? P.s0 : 0);
-      const float inv_l = l_used > 0.f ? 1.f / l_used : 0.f;
+      const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
       const size_t orow = static_cast<size_t>(b_here) * p.rows + row;
       const size_t arow = static_cast<size_t>(slot) * p.rows + row;
       const bool direct = (nsplit == 1);
