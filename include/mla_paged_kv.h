@@ -18,7 +18,8 @@
  * Conventions for every entry point:
  *  - All pointers named d_* are DEVICE pointers owned by the caller.  The
  *    library never allocates or frees device memory and keeps no state
- *    besides a per-device cache of kernel attributes.
+ *    besides a per-device cache of kernel attributes (and, for
+ *    mla_decode_fwd_static_ws only, one fixed device array and its address).
  *  - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
  *    the legacy default stream).  No call synchronises with the host.
  *  - Host-detectable errors are returned BEFORE anything is launched.
@@ -126,6 +127,39 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
                       float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
                       int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, int out_fp32,
                       float* d_lse, int32_t* d_status, mla_stream_t stream);
+
+/* Size of the device array mla_decode_fwd_static_ws keeps its split
+ * workspace in: 64 MiB on every GPU that loads the library. */
+#define MLA_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+
+/* mla_decode_fwd for callers that cannot provide device scratch.  Neither
+ * FlashMLA page has a counterpart: it is this library's own addition.  Some
+ * callers have no workspace to give: a plain C host program linked only
+ * against this library has no device allocator at hand, and a serving
+ * runtime that reserves nearly all of HBM for its KV pool at start-up may
+ * forbid allocation on the decode path, where a cudaMalloc could fail and
+ * would synchronise the device.  This call takes the same inputs and outputs
+ * as mla_decode_fwd minus d_workspace/workspace_bytes, allocates nothing,
+ * and keeps the partials in a file-scope device array of
+ * MLA_STATIC_WORKSPACE_BYTES, which every GPU that loads the library holds
+ * until the process exits.
+ *  - Returns MLA_ERR_UNSUPPORTED, before any launch, when
+ *    mla_workspace_bytes(batch, s_q*h_q, num_parts) exceeds
+ *    MLA_STATIC_WORKSPACE_BYTES (64 requests x 128 heads with 76 parts need
+ *    36.8 MB and fit).
+ *  - The first call on a device looks up the array's device address there
+ *    (cudaGetSymbolAddress with that device current) and caches it; make
+ *    that first call on each device before beginning any stream capture.
+ *  - All calls on a device share the one array, and it keeps what the last
+ *    call left.  Nothing in it needs to start at zero (the decode kernel
+ *    writes every partial the combine reads in the same call), but calls
+ *    that can overlap on the GPU (unordered streams) race on it and corrupt
+ *    each other's results: order them on one stream or with events. */
+int mla_decode_fwd_static_ws(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
+                             int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int causal,
+                             float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
+                             int num_parts, void* d_out, int out_fp32, float* d_lse, int32_t* d_status,
+                             mla_stream_t stream);
 
 /* LSE-weighted combine of split partials (FlashMLA PR #183 Summary: the
  * combine kernel merges the splits).  For every unit with != 1 split and

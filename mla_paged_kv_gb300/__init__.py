@@ -24,13 +24,15 @@ from .build import LIB_PATH
 __all__ = [
     "MlaError", "load_library", "mla_status_string", "mla_num_parts", "mla_workspace_bytes",
     "mla_get_metadata", "mla_decode_fwd", "mla_decode_splits", "mla_combine",
-    "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack", "plan", "decode", "sparse_decode",
+    "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws", "plan", "decode",
+    "sparse_decode",
     "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_num_parts", "mla_workspace_bytes", "mla_get_metadata", "mla_decode_fwd",
     "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack",
+    "mla_decode_fwd_static_ws",
 )
 
 _P = ctypes.c_void_p
@@ -50,6 +52,8 @@ _SIGS = {
     "mla_sparse_fp8_decode_fwd": (_I, [_P, _P, _I, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _P, _P,
                                        _P]),
     "mla_sparse_fp8_unpack": (_I, [_P, _I, _P, _I, _P, _P, _P]),
+    "mla_decode_fwd_static_ws": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _F, _P, _P, _I, _P, _I, _P, _P,
+                                      _P]),
 }
 
 _lib = None
@@ -167,6 +171,28 @@ def mla_decode_splits(q, kv, block_table, cache_seqlens, sched, split_offset, nu
     args = _dense_args(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse,
                        status, causal, softmax_scale, stream)
     _check(load_library().mla_decode_splits(*args), "mla_decode_splits")
+
+
+def mla_decode_fwd_static_ws(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, out, lse, status,
+                             causal=False, softmax_scale=1.0 / 24.0, stream=None):
+    """mla_decode_fwd for callers with no device scratch to give: the library
+    keeps the split partials in its own fixed device array (64 MiB per GPU).
+    Nothing is allocated; a problem whose partials do not fit raises
+    MLA_ERR_UNSUPPORTED."""
+    _need(q, torch.bfloat16, "q", 4)
+    _need(kv, torch.bfloat16, "kv", 3)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(cache_seqlens, torch.int32, "cache_seqlens", 1)
+    _need(lse, torch.float32, "lse")
+    _need(status, torch.int32, "status")
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bf16 or fp32")
+    B, s_q, h_q, _ = q.shape
+    rc = load_library().mla_decode_fwd_static_ws(
+        _ptr(q), _ptr(kv), _ptr(block_table), block_table.shape[1], kv.shape[0], _ptr(cache_seqlens), B, s_q, h_q,
+        int(bool(causal)), float(softmax_scale), _ptr(sched), _ptr(split_offset), int(num_parts), _ptr(out),
+        int(out.dtype == torch.float32), _ptr(lse), _ptr(status), _stream(stream))
+    _check(rc, "mla_decode_fwd_static_ws")
 
 
 def mla_combine(workspace, split_offset, n_units, rows_per_unit, num_parts, out, lse, stream=None):

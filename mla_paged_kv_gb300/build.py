@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libmla_paged_kv.so")
-SOURCES = ["api.cu", "sched.cu", "combine.cu", "decode_dense.cu", "decode_sparse.cu"]
+SOURCES = ["api.cu", "sched.cu", "combine.cu", "decode_dense.cu", "decode_sparse.cu", "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == sorted(["mla_status_string", "mla_num_parts", "mla_workspace_bytes", "mla_get_metadata",
                             "mla_decode_fwd", "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd",
-                            "mla_sparse_fp8_unpack"])
+                            "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws"])
 
 
 def test_library_exports_every_declared_symbol(lib_path):
