@@ -1,36 +1,38 @@
-// MLA split-KV decode kernels for sm_103a (tcgen05 + TMEM + TMA), dense bf16
-// and sparse FP8.
+// Sparse FP8 MLA split-KV decode for sm_103a (tcgen05 + TMEM + TMA), and the
+// bit-exact record unpack.
 //
-// What they compute (FlashMLA PR #183, "Add SM80 (Ampere/A100) dense MLA
-// decode kernel", section Design; FlashMLA PR #200, "[SM90] Add packed
-// selected-KV sparse decode", sections Motivation and "SM90 packing
-// kernel"): for the 128 query rows of one row block of a unit (all heads
-// share one latent KV head), over the keys of one split: S = Q K^T on 576
-// dims, online softmax, O = P V with V = the first 512 dims of the same
-// latent rows; then O / l and the split's LSE.  Dense keys come from 64-token
-// bf16 pages through the block table; sparse keys are 656-byte FP8 records
-// picked by physical slot index and dequantised in the kernel.
+// What it computes (FlashMLA PR #200, "[SM90] Add packed selected-KV sparse
+// decode", sections Motivation and "SM90 packing kernel"; the attention
+// itself as in FlashMLA PR #183, section Design): query token (b, i) attends
+// to the records its top-k list selects.  Entry t of the list is a physical
+// slot (page t/64, row t%64); -1, entries past topk_length and entries
+// outside the pool are masked.  A 656-byte record holds 512 E4M3 codes, four
+// fp32 scales (one per 128-dim group) and 64 bf16 RoPE values; the key is
+// code * scale (NoPE) followed by the RoPE values, the value is the NoPE
+// part.  Per split: S = Q K^T over 576 dims, online softmax, O = P V, then
+// O / l and the split's LSE; the combine kernel merges the splits.
 //
-// How (GB300 design, not the pages' SM80/SM90 ones):
-//  * One 2-CTA cluster per (partition, row block).  TMEM holds 512 fp32
-//    columns per SM, exactly one 128 x 512 accumulator, so the two CTAs
-//    split the value dims: rank c accumulates O[:, 256c : 256c+256).  To
-//    avoid computing Q K^T twice they also split the score dims: rank 0 sums
-//    dims [0, 288), rank 1 dims [288, 576), and the two partial score tiles
-//    are exchanged through distributed shared memory.  Both ranks then run
-//    the same softmax on the same sums, so P is identical on both.
-//  * Each CTA stages the 64-column boxes it needs: rank c boxes 4c .. 4c+4
-//    (320 dims: its score dims plus its value dims) of Q (once per unit) and
-//    of every 64-key tile, in a 2-stage mbarrier ring.  Dense: one TMA per
-//    box, 128-byte swizzle, page from the block table.  Sparse: a producer
-//    warpgroup gathers the records, dequantises E4M3 x fp32 scale to bf16
-//    and writes the same swizzled layout.
-//  * tcgen05.mma M=128: S (N=64) and O (N=256) accumulate in TMEM.  P is
-//    written as bf16 by the softmax threads into swizzled shared memory.
-//  * Online softmax in the log2 domain with a lazy rescale: O is rescaled
-//    only when the running max grows by more than 2^8.
-// Roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane),
-//        then the producer warp(s), then one MMA warp that owns TMEM.
+// How (GB300 design):
+//  * One 2-CTA cluster per (partition, row block of 128 heads).  The pair
+//    splits the four 128-dim NoPE groups: rank c owns groups 2c and 2c+1 for
+//    both the scores and the values (O[:, 256c : 256c+256) in its TMEM);
+//    rank 0 also owns the 64 RoPE dims of the scores.
+//  * Exact scores without a per-element dequantisation: the E4M3 codes are
+//    staged as bf16 (every E4M3 value is a bf16 value) and each group gets
+//    its own TMEM accumulator A_g = Q_g . codes_g (fp32).  The softmax
+//    threads form the rank's partial score sum_g scale_g[j] * A_g[j] (+ the
+//    RoPE product on rank 0) in fp32 and swap it with the peer through
+//    distributed shared memory, so both ranks see the same full score.
+//  * The value scale is folded into P: rank c multiplies P by scale_g[j] for
+//    each of its two groups and runs one N=128 PV product per group against
+//    the unscaled codes.
+//  * A producer warpgroup gathers the selected records (plain 8- and 16-byte
+//    loads through the index list) into 128-byte-swizzled tiles in a 2-stage
+//    ring; Q comes by TMA.  One elected thread issues every tcgen05.mma.
+//  * Online softmax in the log2 domain with a lazy rescale of O (only when
+//    the running max grows by more than 2^8).
+// Roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane), warps 4-7
+// gather producer, warp 8 MMA issuer and TMEM owner.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -39,56 +41,57 @@
 #include "ptx.cuh"
 
 namespace mla {
-namespace dec {
+namespace sp {
 
-constexpr int kBoxes = 5;
-constexpr int kQBoxBytes = kRowsPerBlock * 128;  // 128 rows x 64 bf16
-constexpr int kKVBoxBytes = kTile * 128;         // 64 keys x 64 bf16
+constexpr int kT = kTile;                         // selection slots per tile
+constexpr int kQBoxBytes = kRowsPerBlock * 128;   // 128 rows x 64 bf16
+constexpr int kBoxBytes = kT * 128;               // 64 keys x 64 bf16
+constexpr int kMaxBoxes = 5;                      // rank 0: 4 NoPE boxes + RoPE; rank 1: 4 NoPE boxes
 constexpr int kStages = 2;
-constexpr int kStageBytes = kBoxes * kKVBoxBytes;
-constexpr int kXBytes = kRowsPerBlock * kTile * 4;  // peer's partial scores
-constexpr int kPBytes = kRowsPerBlock * kTile * 2;  // P tile, bf16
+constexpr int kStageBytes = kMaxBoxes * kBoxBytes;
+constexpr int kScaleStageBytes = 2 * kT * 4;      // the rank's two group scales of 64 keys
+constexpr int kXBytes = kRowsPerBlock * kT * 4;   // the peer's partial scores
+constexpr int kPGroupBytes = kRowsPerBlock * kT * 2;
 
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kBoxes * kQBoxBytes;
+constexpr int kOffKV = kOffQ + kMaxBoxes * kQBoxBytes;
 constexpr int kOffX = kOffKV + kStages * kStageBytes;
 constexpr int kOffP = kOffX + kXBytes;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 26;
+constexpr int kOffScale = kOffP + 2 * kPGroupBytes;
+constexpr int kOffBar = kOffScale + kStages * kScaleStageBytes;
+constexpr int kNumBars = 21;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffKV % 1024 == 0 && kOffX % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1 KB alignment");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
-constexpr uint32_t kTmemS = 256;  // S buffers: [256, 320) and [320, 384)
+constexpr uint32_t kTmemS = 256;  // score accumulators: A_{2c}, A_{2c+1}, RoPE (rank 0), 64 columns each
+
+constexpr int kProducerWarps = 4;
+constexpr int kMmaWarp = 4 + kProducerWarps;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 
 enum : int {
   Q_FULL = 0,
   Q_EMPTY = 1,
   KV_FULL = 2,   // +stage
   KV_EMPTY = 4,  // +stage
-  S_FULL = 6,    // +buffer
-  S_FREE = 8,    // +buffer
-  P_FULL = 10,   // +buffer
-  P_FREE = 12,   // +buffer
-  O_FULL = 14,
-  O_FREE = 15,
-  X_FULL = 16,   // +warp
-  X_FREE = 20,   // +warp
-  DRAIN = 24,
+  S_FULL = 6,
+  S_FREE = 7,
+  P_FULL = 8,
+  P_FREE = 9,
+  O_FULL = 10,
+  O_FREE = 11,
+  X_FULL = 12,   // +warp
+  X_FREE = 16,   // +warp
+  DRAIN = 20,
 };
 
 constexpr float kTau = 8.0f;  // lazy-rescale threshold (log2 units)
 constexpr float kLn2 = 0.69314718055994530942f;
-
-template <bool kSparse>
-struct Roles {
-  static constexpr int kProducerWarps = kSparse ? 4 : 1;
-  static constexpr int kMmaWarp = 4 + kProducerWarps;
-  static constexpr int kThreads = 32 * (kMmaWarp + 1);
-};
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -114,12 +117,13 @@ __device__ __forceinline__ Part load_part(const int32_t* sched, int idx) {
   return Part{e[0], e[1], e[2], e[3], e[4]};
 }
 
-// Keys of unit b (sparse lengths are clamped to topk).
-__device__ __forceinline__ int unit_len(const DecodeParams& p, int b) {
-  int L = p.lengths != nullptr ? p.lengths[b] : p.default_length;
-  if (p.indices != nullptr) L = min(L, p.topk);
-  return max(L, 0);
+// Length of unit b as the scheduler saw it (tiles are counted from this)...
+__device__ __forceinline__ int sched_len(const DecodeParams& p, int b) {
+  return max(p.lengths != nullptr ? p.lengths[b] : p.default_length, 0);
 }
+
+// ...and the candidate slots that may be valid: clamped to the list size.
+__device__ __forceinline__ int unit_len(const DecodeParams& p, int b) { return min(sched_len(p, b), p.topk); }
 
 // Tile range [lo, hi) of unit b inside partition P.
 __device__ __forceinline__ void unit_tiles(const Part& P, int b, int nt, int& lo, int& hi) {
@@ -142,7 +146,7 @@ struct Cursor {
 __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& P, Cursor& c, int from_b) {
   for (int b = from_b; unit_in_part(P, b, p.n_units); ++b) {
     int lo, hi;
-    unit_tiles(P, b, num_tiles(unit_len(p, b)), lo, hi);
+    unit_tiles(P, b, num_tiles(sched_len(p, b)), lo, hi);
     if (hi > lo) {
       c.b = b;
       c.lo = lo;
@@ -182,8 +186,9 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
   return __all_sync(0xffffffffu, mbar_wait<true>(bar, parity, abort_flag));
 }
 
-// 8 E4M3 codes times one fp32 scale -> 8 bf16 (fp32 product rounded once to bf16).
-__device__ __forceinline__ uint4 dequant8(uint2 codes, float scale) {
+// 8 E4M3 codes -> 8 bf16 of the same values (E4M3 -> f16 -> f32 -> bf16 is
+// exact at every step: 3 mantissa bits, exponents within bf16's range).
+__device__ __forceinline__ uint4 codes_to_bf16(uint2 codes) {
   uint32_t w[4];
   const uint32_t src[2] = {codes.x, codes.y};
 #pragma unroll
@@ -193,20 +198,20 @@ __device__ __forceinline__ uint4 dequant8(uint2 codes, float scale) {
       const __nv_fp8x2_storage_t two = static_cast<__nv_fp8x2_storage_t>((src[h] >> (16 * q)) & 0xFFFFu);
       const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-      const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(f.x, scale), __fmul_rn(f.y, scale));
+      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
       w[2 * h + q] = *reinterpret_cast<const uint32_t*>(&b);
     }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Validity of sparse selection entry t of unit b (as the oracle defines it).
+// Validity of selection entry t of unit b (L = candidate slots of the unit).
 __device__ __forceinline__ bool sparse_valid(const DecodeParams& p, int b, int t, int L, int& idx) {
   idx = -1;
   if (t >= L) return false;
   idx = p.indices[static_cast<size_t>(b) * p.topk + t];
   if (idx == -1) return false;
-  if (idx < 0 || idx >= p.num_pages * kTile) {
+  if (idx < 0 || idx >= p.num_pages * kT) {
     report(p.status, MLA_ERR_BAD_INDEX);
     idx = -1;
     return false;
@@ -214,11 +219,48 @@ __device__ __forceinline__ bool sparse_valid(const DecodeParams& p, int b, int t
   return true;
 }
 
-template <bool kSparse>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
-                      const DecodeParams p) {
-  using R = Roles<kSparse>;
+// Q/KV box lb of rank `rank` -> first latent dim it holds.
+__device__ __forceinline__ int box_dim(uint32_t rank, int lb) {
+  return rank == 0 ? (lb < 4 ? 64 * lb : 512) : 256 + 64 * lb;
+}
+
+// S accumulators of one tile: kAcc = 3 (rank 0: two groups + RoPE) or 2.
+// Group accumulator a reads boxes 2a, 2a+1 (8 K-steps of 16 dims); the RoPE
+// accumulator reads box 4 (4 K-steps).  Fully unrolled: the descriptor
+// offsets are compile-time constants.
+template <int kAcc>
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint64_t q_desc0, uint64_t kv_desc_stage, uint32_t idesc) {
+#pragma unroll
+  for (int a = 0; a < kAcc; ++a) {
+    const int nks = a < 2 ? 8 : 4;
+#pragma unroll
+    for (int ks = 0; ks < nks; ++ks) {
+      const int lb = a < 2 ? 2 * a + (ks >> 2) : 4;
+      const uint32_t off_q = lb * kQBoxBytes + (ks & 3) * 32;
+      const uint32_t off_k = lb * kBoxBytes + (ks & 3) * 32;
+      umma_f16(tmem + kTmemS + 64u * a, q_desc0 + (off_q >> 4), kv_desc_stage + (off_k >> 4), idesc,
+               ks > 0 ? 1u : 0u);
+    }
+  }
+}
+
+// O[:, 128g : 128g+128) += P_g (128 x 64 keys) x codes of boxes 2g, 2g+1.
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint64_t p_desc0, uint64_t v_desc_stage, uint32_t idesc,
+                                         bool first) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+#pragma unroll
+    for (int kk = 0; kk < kT / 16; ++kk) {
+      const uint32_t off_p = g * kPGroupBytes + kk * 32;
+      const uint32_t off_v = 2 * g * kBoxBytes + kk * 2048;
+      umma_f16(tmem + kTmemO + 128u * g, p_desc0 + (off_p >> 4), v_desc_stage + (off_v >> 4), idesc,
+               (first && kk == 0) ? 0u : 1u);
+    }
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    sparse_decode_kernel(const __grid_constant__ CUtensorMap q_map, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -226,6 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
   uint8_t* sKV = smem + kOffKV;
   uint8_t* sX = smem + kOffX;
   uint8_t* sP = smem + kOffP;
+  float* sScale = reinterpret_cast<float*>(smem + kOffScale);  // [stage][2 groups][64 keys]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -237,19 +280,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
   const int cluster_id = blockIdx.x >> 1;
   const int part_idx = cluster_id / p.row_blocks;
   const int rb = cluster_id - part_idx * p.row_blocks;
+  const int n_boxes = rank == 0 ? 5 : 4;
 
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(&bars[Q_FULL], 1);
     mbar_init(&bars[Q_EMPTY], 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[KV_FULL + i], kSparse ? 32 * R::kProducerWarps : 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bars[KV_FULL + i], 32 * kProducerWarps);
       mbar_init(&bars[KV_EMPTY + i], 1);
-      mbar_init(&bars[S_FULL + i], 1);
-      mbar_init(&bars[S_FREE + i], 128);
-      mbar_init(&bars[P_FULL + i], 128);
-      mbar_init(&bars[P_FREE + i], 1);
     }
+    mbar_init(&bars[S_FULL], 1);
+    mbar_init(&bars[S_FREE], 128);
+    mbar_init(&bars[P_FULL], 128);
+    mbar_init(&bars[P_FREE], 1);
     mbar_init(&bars[O_FULL], 1);
     mbar_init(&bars[O_FREE], 128);
     for (int w = 0; w < 4; ++w) {
@@ -259,14 +303,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
     mbar_init(&bars[DRAIN], 1);
     fence_mbar_init_cluster();
   }
-  if (warp == R::kMmaWarp) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
-    prefetch_tmap(&q_map);
-    if (!kSparse) prefetch_tmap(&kv_map);
-  }
+  if (warp == 4 && lane == 0) prefetch_tmap(&q_map);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -277,136 +318,93 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
 
   const Part P = load_part(p.sched, part_idx);
 
-  if (warp >= 4 && warp < R::kMmaWarp) {
+  if (warp >= 4 && warp < kMmaWarp) {
     // ------------------------------------------------------------ producer
-    const int ptid = tid - 128;  // 0 .. 32*kProducerWarps-1
-    const uint64_t pol_kv = policy_evict_first();
+    const int ptid = tid - 128;  // 0 .. 127
     const uint64_t pol_q = policy_evict_last();
+    // chunks of 8 dims per key: 32 NoPE chunks of the rank's two groups, plus
+    // 8 RoPE chunks on rank 0
+    const int nc = rank == 0 ? 40 : 32;
+    const int nope0 = 256 * static_cast<int>(rank);
+    constexpr int kPerMax = kT * 40 / (32 * kProducerWarps);  // 20
     uint32_t t = 0;
     int u = 0;
     bool ok = true;
-    uint32_t issued[2] = {0u, 0u};
     uint32_t q_issued = 0;
     for (int b = P.b0; ok && unit_in_part(P, b, p.n_units); ++b) {
       const int L = unit_len(p, b);
-      const int nt = num_tiles(L);
+      const int nt = num_tiles(sched_len(p, b));
       int lo, hi;
       unit_tiles(P, b, nt, lo, hi);
       if (hi <= lo) continue;
       if (ptid == 0) {
         if (u >= 1) ok = mbar_wait(&bars[Q_EMPTY], (u - 1) & 1, abort_flag);
         if (ok) {
-          mbar_arrive_expect_tx(&bars[Q_FULL], kBoxes * kQBoxBytes);
+          mbar_arrive_expect_tx(&bars[Q_FULL], n_boxes * kQBoxBytes);
           const int row0 = b * p.rows + rb * kRowsPerBlock;
-#pragma unroll
-          for (int lb = 0; lb < kBoxes; ++lb)
-            tma_load_2d(sQ + lb * kQBoxBytes, &q_map, &bars[Q_FULL], 64 * (4 * static_cast<int>(rank) + lb), row0,
-                        pol_q);
+          for (int lb = 0; lb < n_boxes; ++lb)
+            tma_load_2d(sQ + lb * kQBoxBytes, &q_map, &bars[Q_FULL], box_dim(rank, lb), row0, pol_q);
           ++q_issued;
         }
       }
-      if constexpr (!kSparse) {
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        int page_reg = 0;
-        for (int k = lo; ok && k < hi; ++k, ++t) {
-          if (((k - lo) & 31) == 0) {
-            const int kk = k + lane;
-            int pg = 0;
-            if (kk < hi) {
-              pg = kk < p.max_pages ? p.block_table[static_cast<size_t>(b) * p.max_pages + kk] : -1;
-              if (pg < 0 || pg >= p.num_pages) {
-                report(p.status, MLA_ERR_BAD_INDEX);
-                pg = 0;
-              }
-            }
-            page_reg = pg;
-          }
-          const int page = __shfl_sync(0xffffffffu, page_reg, (k - lo) & 31);
-          const int st = t & 1;
-          if (lane == 0) {
-            if (t >= 2) ok = mbar_wait(&bars[KV_EMPTY + st], ((t - 2) >> 1) & 1, abort_flag);
-            if (ok) {
-              mbar_arrive_expect_tx(&bars[KV_FULL + st], kStageBytes);
+      for (int k = lo; ok && k < hi; ++k, ++t) {
+        const int st = t & 1;
+        if (t >= 2) ok = mbar_wait(&bars[KV_EMPTY + st], ((t - 2) >> 1) & 1, abort_flag);
+        if (!ok) break;
+        uint4 raw[kPerMax];
+        float sc[kPerMax];
 #pragma unroll
-              for (int lb = 0; lb < kBoxes; ++lb)
-                tma_load_3d(sKV + st * kStageBytes + lb * kKVBoxBytes, &kv_map, &bars[KV_FULL + st],
-                            64 * (4 * static_cast<int>(rank) + lb), 0, page, pol_kv);
-              ++issued[st];
+        for (int i = 0; i < kPerMax; ++i) {
+          const int q = ptid + 32 * kProducerWarps * i;
+          const int key = q / nc, c = q - nc * (q / nc);
+          raw[i] = make_uint4(0u, 0u, 0u, 0u);
+          sc[i] = 0.f;
+          int idx;
+          if (key < kT && sparse_valid(p, b, k * kT + key, L, idx)) {
+            const uint8_t* rec = p.kv8 + static_cast<size_t>(idx) * MLA_RECORD_BYTES;
+            if (c < 32) {
+              const int d = nope0 + 8 * c;
+              const uint2 v = __ldg(reinterpret_cast<const uint2*>(rec + d));
+              raw[i] = make_uint4(v.x, v.y, 0u, 0u);
+              sc[i] = __ldg(reinterpret_cast<const float*>(rec + 512) + (d >> 7));
+            } else {
+              raw[i] = __ldg(reinterpret_cast<const uint4*>(rec + 528 + 16 * (c - 32)));
             }
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-      } else {
-        // gather + dequant: 64 keys x 40 chunks of 8 dims (dims 256*rank + 8c)
-        constexpr int kChunks = kTile * 40;
-        constexpr int kPer = kChunks / (32 * R::kProducerWarps);
-        static_assert(kChunks % (32 * R::kProducerWarps) == 0, "chunk split");
-        const int dim0 = 256 * static_cast<int>(rank);
-        for (int k = lo; ok && k < hi; ++k, ++t) {
-          const int st = t & 1;
-          if (t >= 2) ok = mbar_wait(&bars[KV_EMPTY + st], ((t - 2) >> 1) & 1, abort_flag);
-          if (!ok) break;
-          uint4 raw[kPer];
-          float sc[kPer];
+        uint8_t* stage = sKV + st * kStageBytes;
+        float* scale_st = sScale + st * (2 * kT);
 #pragma unroll
-          for (int i = 0; i < kPer; ++i) {
-            const int q = ptid + 32 * R::kProducerWarps * i;
-            const int key = q / 40, c = q - 40 * (q / 40);
-            const int d = dim0 + 8 * c;
-            int idx;
-            raw[i] = make_uint4(0u, 0u, 0u, 0u);
-            sc[i] = 0.f;
-            if (sparse_valid(p, b, k * kTile + key, L, idx)) {
-              const uint8_t* rec = p.kv8 + static_cast<size_t>(idx) * MLA_RECORD_BYTES;
-              if (d < 512) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(rec + d));
-                raw[i] = make_uint4(v.x, v.y, 0u, 0u);
-                sc[i] = __ldg(reinterpret_cast<const float*>(rec + 512) + (d >> 7));
-              } else {
-                raw[i] = __ldg(reinterpret_cast<const uint4*>(rec + 528 + 2 * (d - 512)));
-                sc[i] = 1.f;
-              }
-            }
-          }
-          uint8_t* stage = sKV + st * kStageBytes;
-#pragma unroll
-          for (int i = 0; i < kPer; ++i) {
-            const int q = ptid + 32 * R::kProducerWarps * i;
-            const int key = q / 40, c = q - 40 * (q / 40);
-            const int d = dim0 + 8 * c;
-            const uint4 outv = (d < 512) ? dequant8(make_uint2(raw[i].x, raw[i].y), sc[i]) : raw[i];
+        for (int i = 0; i < kPerMax; ++i) {
+          const int q = ptid + 32 * kProducerWarps * i;
+          const int key = q / nc, c = q - nc * (q / nc);
+          if (key < kT) {
+            const uint4 outv = c < 32 ? codes_to_bf16(make_uint2(raw[i].x, raw[i].y)) : raw[i];
             const int lb = c >> 3, cc = c & 7;
-            *reinterpret_cast<uint4*>(stage + lb * kKVBoxBytes + key * 128 + ((cc ^ (key & 7)) << 4)) = outv;
+            *reinterpret_cast<uint4*>(stage + lb * kBoxBytes + key * 128 + ((cc ^ (key & 7)) << 4)) = outv;
+            if (c < 32 && (c & 15) == 0) scale_st[(c >> 4) * kT + key] = sc[i];
           }
-          fence_proxy_async_smem();
-          mbar_arrive(&bars[KV_FULL + st]);
         }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[KV_FULL + st]);
       }
       ++u;
     }
-    if (ptid == 0) {
-      if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
-      // no TMA write may land after this CTA exits
-      if (!kSparse)
-        for (int st = 0; st < 2; ++st)
-          if (issued[st] > 0) mbar_wait(&bars[KV_FULL + st], (issued[st] - 1) & 1, nullptr);
-      if (q_issued > 0) mbar_wait(&bars[Q_FULL], (q_issued - 1) & 1, nullptr);
-    }
-    if (kSparse && !ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
-  } else if (warp == R::kMmaWarp) {
+    if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+    // no TMA write may land after this CTA exits
+    if (ptid == 0 && q_issued > 0) mbar_wait(&bars[Q_FULL], (q_issued - 1) & 1, nullptr);
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(128, 256, true);
-      const int ks0 = rank == 0 ? 0 : 18;
-      const int ks1 = ks0 + 18;
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kT, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, true);
       const uint64_t q_desc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t kv_desc0 = sdesc_sw128(smem_u32(sKV), 16, 1024);
-      const uint64_t v_desc0 = sdesc_sw128(smem_u32(sKV), kKVBoxBytes, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(smem_u32(sKV), kBoxBytes, 1024);
       const uint64_t p_desc0 = sdesc_sw128(smem_u32(sP), 16, 1024);
-      // Two cursors over the partition's (unit, tile) sequence: QK runs ahead of
-      // PV by at most the two S/KV buffers.  Whichever is ready is issued, PV
-      // first, so a KV stage is released as soon as its PV is issued.
+      // Two cursors over the partition's (unit, tile) sequence: QK of tile t
+      // needs the single S buffer back from the softmax of tile t-1; PV of
+      // tile t needs P of tile t.  Whichever is ready is issued, PV first.
       Cursor cq, cv;
       cursor_init(p, P, cq);
       cursor_init(p, P, cv);
@@ -415,20 +413,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
       while (cv.valid) {
         bool progressed = false;
         if (cv.t < cq.t) {
-          const int pb = cv.t & 1;
-          bool ready = mbar_test_wait(&bars[P_FULL + pb], (cv.t >> 1) & 1);
+          bool ready = mbar_test_wait(&bars[P_FULL], cv.t & 1);
           const bool first = cv.k == cv.lo, last = cv.k == cv.hi - 1;
           if (ready && first && cv.u >= 1) ready = mbar_test_wait(&bars[O_FREE], (cv.u - 1) & 1);
           if (ready) {
             tc_fence_after();
-            const uint64_t a0 = p_desc0 + static_cast<uint64_t>((pb * kPBytes) >> 4);
-            const uint64_t b0 = v_desc0 + static_cast<uint64_t>((pb * kStageBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              umma_f16(tmem + kTmemO, a0 + static_cast<uint64_t>((kk * 32) >> 4),
-                       b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
-            umma_commit(&bars[P_FREE + pb]);
-            umma_commit(&bars[KV_EMPTY + pb]);
+            const int st = cv.t & 1;
+            issue_pv(tmem, p_desc0, v_desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4), idesc_pv, first);
+            umma_commit(&bars[P_FREE]);
+            umma_commit(&bars[KV_EMPTY + st]);
             if (last) umma_commit(&bars[O_FULL]);
             cursor_next(p, P, cv);
             progressed = true;
@@ -439,18 +432,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
           bool ready = true;
           if (cq.k == cq.lo) ready = mbar_test_wait(&bars[Q_FULL], cq.u & 1);
           ready = ready && mbar_test_wait(&bars[KV_FULL + st], (cq.t >> 1) & 1);
-          if (ready && cq.t >= 2) ready = mbar_test_wait(&bars[S_FREE + st], ((cq.t - 2) >> 1) & 1);
+          if (ready && cq.t >= 1) ready = mbar_test_wait(&bars[S_FREE], (cq.t - 1) & 1);
           if (ready) {
             tc_fence_after();
             const uint64_t kvs = kv_desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
-            for (int ks = ks0; ks < ks1; ++ks) {
-              const int lb = (ks >> 2) - 4 * static_cast<int>(rank);
-              const uint32_t off_q = lb * kQBoxBytes + (ks & 3) * 32;
-              const uint32_t off_k = lb * kKVBoxBytes + (ks & 3) * 32;
-              umma_f16(tmem + kTmemS + 64u * st, q_desc0 + (off_q >> 4), kvs + (off_k >> 4), idesc_qk,
-                       ks > ks0 ? 1u : 0u);
-            }
-            umma_commit(&bars[S_FULL + st]);
+            if (rank == 0)
+              issue_qk<3>(tmem, q_desc0, kvs, idesc_qk);
+            else
+              issue_qk<2>(tmem, q_desc0, kvs, idesc_qk);
+            umma_commit(&bars[S_FULL]);
             if (cq.k == cq.hi - 1) umma_commit(&bars[Q_EMPTY]);
             cursor_next(p, P, cq);
             progressed = true;
@@ -481,49 +471,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
     const uint32_t xfull_remote = mapa_shared(smem_u32(&bars[X_FULL + warp]), peer);
     const uint32_t xfree_remote = mapa_shared(smem_u32(&bars[X_FREE + warp]), peer);
     const uint32_t swz = static_cast<uint32_t>(r & 7);
+    const int n_acc = rank == 0 ? 3 : 2;
     uint32_t t = 0;
     int u = 0;
     bool ok = true;
     for (int b = P.b0; ok && unit_in_part(P, b, p.n_units); ++b) {
       const int L = unit_len(p, b);
-      const int nt = num_tiles(L);
+      const int nt = num_tiles(sched_len(p, b));
       int lo, hi;
       unit_tiles(P, b, nt, lo, hi);
       if (hi <= lo) continue;
       const int row = rb * kRowsPerBlock + r;
       const bool row_ok = row < p.rows;
-      const int tok = row_ok ? row / p.h_q : 0;
-      const int jmax = p.causal ? (L - p.s_q + tok) : (L - 1);  // dense: last visible key
-      // l_sum: fp32 sum of the unrounded weights (gives the LSE);
-      // l_used: sum of the bf16 weights the tensor core multiplies (normalises O)
-      float m_used = -INFINITY, l_sum = 0.f, l_used = 0.f;
+      float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and fp32 row sum
       for (int k = lo; ok && k < hi; ++k, ++t) {
-        // which of the tile's 64 keys this row may see
+        // which of the tile's 64 slots are valid (the same for every row)
         uint64_t vis_mask;
-        if constexpr (kSparse) {
+        {
           int idx;
-          const bool v0 = sparse_valid(p, b, k * kTile + lane, L, idx);
-          const bool v1 = sparse_valid(p, b, k * kTile + 32 + lane, L, idx);
+          const bool v0 = sparse_valid(p, b, k * kT + lane, L, idx);
+          const bool v1 = sparse_valid(p, b, k * kT + 32 + lane, L, idx);
           vis_mask = static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
                      (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
-        } else {
-          const int vis = jmax - k * kTile;  // keys 0..vis of this tile are visible
-          vis_mask = vis >= 63 ? ~0ull : (vis < 0 ? 0ull : ((2ull << vis) - 1ull));
         }
-        const int sb = t & 1;
-        ok = warp_wait(&bars[S_FULL + sb], (t >> 1) & 1, abort_flag);
+        const int st = t & 1;
+        // the stage's scales: visible once its KV_FULL phase has completed
+        ok = warp_wait(&bars[KV_FULL + st], (t >> 1) & 1, abort_flag);
+        if (ok) ok = warp_wait(&bars[S_FULL], t & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[64];
-        {
-          uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-          uint32_t (&hi32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-          tmem_ld32(tmem + lane_base + kTmemS + 64u * sb, lo32);
-          tmem_ld32(tmem + lane_base + kTmemS + 64u * sb + 32u, hi32);
-          tmem_wait_ld();
+        const uint32_t sc_base = smem_u32(sScale + st * (2 * kT));
+        // partial score of this rank: sum over its groups of scale_g[j] * A_g[j] (+ RoPE)
+        float s[kT];
+#pragma unroll
+        for (int j = 0; j < kT; ++j) s[j] = 0.f;
+#pragma unroll 1
+        for (int a = 0; a < n_acc; ++a) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + kTmemS + 64u * a + 32u * h, v);
+            tmem_wait_ld();
+            if (a < 2) {
+#pragma unroll
+              for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 sc = ld_shared_v4(sc_base + (a * kT + 32 * h + 4 * j4) * 4);
+                s[32 * h + 4 * j4 + 0] = fmaf(sc.x, __uint_as_float(v[4 * j4 + 0]), s[32 * h + 4 * j4 + 0]);
+                s[32 * h + 4 * j4 + 1] = fmaf(sc.y, __uint_as_float(v[4 * j4 + 1]), s[32 * h + 4 * j4 + 1]);
+                s[32 * h + 4 * j4 + 2] = fmaf(sc.z, __uint_as_float(v[4 * j4 + 2]), s[32 * h + 4 * j4 + 2]);
+                s[32 * h + 4 * j4 + 3] = fmaf(sc.w, __uint_as_float(v[4 * j4 + 3]), s[32 * h + 4 * j4 + 3]);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) s[32 * h + j] += __uint_as_float(v[j]);
+            }
+          }
         }
         tc_fence_before();
-        mbar_arrive(&bars[S_FREE + sb]);
+        mbar_arrive(&bars[S_FREE]);
         // swap partial scores with the peer CTA
         if (t >= 1) {
           ok = warp_wait_cluster(&bars[X_FREE + warp], (t - 1) & 1, abort_flag);
@@ -531,26 +536,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
         }
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          st_cluster_v4(x_remote + ((static_cast<uint32_t>(c) ^ swz) << 4), __uint_as_float(sr[4 * c]),
-                        __uint_as_float(sr[4 * c + 1]), __uint_as_float(sr[4 * c + 2]),
-                        __uint_as_float(sr[4 * c + 3]));
+          st_cluster_v4(x_remote + ((static_cast<uint32_t>(c) ^ swz) << 4), s[4 * c], s[4 * c + 1], s[4 * c + 2],
+                        s[4 * c + 3]);
         mbar_arrive_remote(xfull_remote);
         ok = warp_wait_cluster(&bars[X_FULL + warp], t & 1, abort_flag);
         if (!ok) break;
-        float s[64];
+        // full score = own partial + peer's partial (one fp32 add: the same bits on both ranks)
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const float4 o = ld_shared_v4(x_local + ((static_cast<uint32_t>(c) ^ swz) << 4));
-          s[4 * c + 0] = __uint_as_float(sr[4 * c + 0]) + o.x;
-          s[4 * c + 1] = __uint_as_float(sr[4 * c + 1]) + o.y;
-          s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + o.z;
-          s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + o.w;
+          s[4 * c + 0] += o.x;
+          s[4 * c + 1] += o.y;
+          s[4 * c + 2] += o.z;
+          s[4 * c + 3] += o.w;
         }
         mbar_arrive_remote(xfree_remote);
         // mask, scale into the log2 domain, tile max
         float mt = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
+        for (int j = 0; j < kT; ++j) {
           s[j] = ((vis_mask >> j) & 1ull) ? s[j] * p.scale_log2 : -INFINITY;
           mt = fmaxf(mt, s[j]);
         }
@@ -560,32 +564,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
           alpha = ex2(m_used - mt);  // 0 when m_used == -inf
           rescale = k > lo;
           l_sum *= alpha;
-          l_used *= alpha;
           m_used = mt;
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-        uint32_t pk[32];
-        float psum = 0.f, pused = 0.f;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(s[2 * i] - mref), p1 = ex2(s[2 * i + 1] - mref);
-          const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-          const float2 back = __bfloat1622float2(h);
-          psum += p0 + p1;
-          pused += back.x + back.y;
-          pk[i] = *reinterpret_cast<const uint32_t*>(&h);
+        for (int j = 0; j < kT; ++j) {
+          s[j] = ex2(s[j] - mref);
+          ls[j & 3] += s[j];
         }
-        l_sum += psum;
-        l_used += pused;
-        const int pb = t & 1;
-        if (t >= 2) {
-          ok = warp_wait(&bars[P_FREE + pb], ((t - 2) >> 1) & 1, abort_flag);
+        l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // P of the previous tile has been consumed (and O holds its PV)
+        if (t >= 1) {
+          ok = warp_wait(&bars[P_FREE], (t - 1) & 1, abort_flag);
           if (!ok) break;
         }
         if (__any_sync(0xffffffffu, rescale)) {
-          // O accumulated so far (through PV of the previous tile) times alpha
-          ok = warp_wait(&bars[P_FREE + (pb ^ 1)], ((t - 1) >> 1) & 1, abort_flag);
-          if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
           for (uint32_t c0 = 0; c0 < 256; c0 += 16) {
@@ -598,14 +592,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
           }
           tmem_wait_st();
         }
-        uint8_t* prow = sP + pb * kPBytes + r * 128;
+        // P_g[j] = p[j] * scale_g[j] for the rank's two groups, bf16, swizzled rows
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + ((static_cast<uint32_t>(c) ^ swz) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        for (int g = 0; g < 2; ++g) {
+          uint8_t* prow = sP + g * kPGroupBytes + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float4 sa = ld_shared_v4(sc_base + (g * kT + 8 * c) * 4);
+            const float4 sb = ld_shared_v4(sc_base + (g * kT + 8 * c + 4) * 4);
+            const float w[8] = {s[8 * c] * sa.x,     s[8 * c + 1] * sa.y, s[8 * c + 2] * sa.z, s[8 * c + 3] * sa.w,
+                                s[8 * c + 4] * sb.x, s[8 * c + 5] * sb.y, s[8 * c + 6] * sb.z, s[8 * c + 7] * sb.w};
+            uint32_t pk[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const __nv_bfloat162 hv = __floats2bfloat162_rn(w[2 * i], w[2 * i + 1]);
+              pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            *reinterpret_cast<uint4*>(prow + ((static_cast<uint32_t>(c) ^ swz) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+        }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bars[P_FULL + pb]);
+        mbar_arrive(&bars[P_FULL]);
       }
       if (!ok) break;
       // ---- epilogue of this (unit, split)
@@ -615,7 +624,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
       const int s_begin = p.split_offset[b];
       const int nsplit = p.split_offset[b + 1] - s_begin;
       const int slot = s_begin + ((b == P.b0) ? P.s0 : 0);
-      const float inv_l = l_used > 0.f ? 1.f / l_used : 0.f;
+      const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
       const size_t orow = static_cast<size_t>(b) * p.rows + row;
       const size_t arow = static_cast<size_t>(slot) * p.rows + row;
       const bool direct = (nsplit == 1);
@@ -667,7 +676,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kSparse>::kThr
   __syncthreads();
   cluster_arrive();  // the peer no longer touches this CTA's shared memory
   cluster_wait();
-  if (warp == R::kMmaWarp) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -717,16 +726,15 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
   dst[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
 
-}  // namespace dec
+}  // namespace sp
 
-int sparse_smem_bytes() { return dec::kSmemBytes; }
-int sparse_threads() { return dec::Roles<true>::kThreads; }
-const void* sparse_kernel_ptr() { return reinterpret_cast<const void*>(&dec::mla_decode_kernel<true>); }
+int sparse_smem_bytes() { return sp::kSmemBytes; }
+int sparse_threads() { return sp::kThreads; }
+const void* sparse_kernel_ptr() { return reinterpret_cast<const void*>(&sp::sparse_decode_kernel); }
 
 cudaError_t launch_sparse(const CUtensorMap& q_map, const DecodeParams& p, int num_parts, cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
-  // the KV map is unused by the sparse kernel; pass the Q map in its place
-  dec::mla_decode_kernel<true><<<grid, dec::Roles<true>::kThreads, dec::kSmemBytes, stream>>>(q_map, q_map, p);
+  sp::sparse_decode_kernel<<<grid, sp::kThreads, sp::kSmemBytes, stream>>>(q_map, p);
   return cudaGetLastError();
 }
 
@@ -734,7 +742,7 @@ cudaError_t launch_unpack(const uint8_t* kv8, int num_pages, const int32_t* indi
                           int32_t* status, cudaStream_t stream) {
   const long long threads = static_cast<long long>(n) * 72;
   const int blocks = static_cast<int>((threads + 255) / 256);
-  dec::unpack_kernel<<<blocks, 256, 0, stream>>>(kv8, num_pages, indices, n, k_out, status);
+  sp::unpack_kernel<<<blocks, 256, 0, stream>>>(kv8, num_pages, indices, n, k_out, status);
   return cudaGetLastError();
 }
 
