@@ -16,6 +16,9 @@ write) before every timed step, outside the timed events.
                KV bytes / its event-timed duration vs measured HBM bandwidth.
   cpu_baseline = the CPU fp64 oracle on a bounded sample of the same batch;
                its outputs also gate parity before anything is timed.
+  workloads  = the other named workloads (tiny, long context, two-token
+               causal, sparse FP8) timed the same way on one GPU: µs per
+               decode + combine call and bytes read per second.
 --impl reference times that oracle instead (the CPU reference arm).
 """
 
@@ -51,6 +54,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle sample")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-other", action="store_true", help="skip timing the other named workloads")
     return ap.parse_args()
 
 
@@ -176,6 +180,51 @@ def cpu_oracle_sample(case, budget_s, gpu_out=None, gpu_lse=None):
             break
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"kv_bytes": kv_bytes, "seconds": t_total, "requests": done, "cores": cores, "errors": errs}
+
+
+OTHER_WORKLOADS = ["dense_b1_hq16_sk256_fp32out", "dense_b1_hq64_sk65536", "dense_b16_sq2causal_hq128_sk4096to8192",
+                   "sparse_fp8_b16_hq128_topk2048"]
+
+
+def time_other_workloads(mla, wl, timed, steps):
+    """µs per mla_decode_fwd / mla_sparse_fp8_decode_fwd call (L2 flushed before each) on the other workloads."""
+    import torch
+    res = {}
+    for name in OTHER_WORKLOADS:
+        case = wl.make(name)
+        sparse = name.startswith("sparse")
+        q = case.q.cuda()
+        B, s_q, h_q = case.batch, case.s_q, case.h_q
+        out = torch.empty(B, s_q, h_q, 512, device="cuda",
+                          dtype=torch.float32 if getattr(case, "out_fp32", False) else torch.bfloat16)
+        lse = torch.empty(B, s_q, h_q, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if sparse:
+            kv8, ind, tl = case.kv8.cuda(), case.indices.cuda(), case.topk_length.cuda()
+            pl = mla.plan(tl.reshape(-1).contiguous(), B * s_q, h_q, sparse=True, default_length=ind.shape[2])
+
+            def fn():
+                mla.mla_sparse_fp8_decode_fwd(q, kv8, ind, tl, pl.sched, pl.split_offset, pl.num_parts,
+                                              pl.workspace, out, lse, status, case.scale)
+        else:
+            kv, bt, sl = case.kv.cuda(), case.block_table.cuda(), case.cache_seqlens.cuda()
+            pl = mla.plan(sl, B, s_q * h_q)
+
+            def fn():
+                mla.mla_decode_fwd(q, kv, bt, sl, pl.sched, pl.split_offset, pl.num_parts, pl.workspace, out, lse,
+                                   status, case.causal, case.scale)
+        for _ in range(5):
+            fn()
+        ms = timed(fn, steps)
+        mla.check_status(status, name)
+        us = 1e3 * statistics.mean(ms)
+        nbytes = case.kv_bytes()
+        res[name] = {"us_per_call": us, "gb_per_s": nbytes / (us * 1e-6) / 1e9, "bytes_per_call": nbytes,
+                     "bytes": "valid records x 656" if sparse else "sum of cache_seqlens x 1152",
+                     "num_parts": pl.num_parts, "splits": int(pl.split_offset[-1].item())}
+        del q, out, lse, fn
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_reference(args):
@@ -338,6 +387,10 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         mla.check_status(status, "e2e loop")
 
+    other = None
+    if world == 1 and not args.no_other:
+        other = time_other_workloads(mla, wl, timed, max(20, min(200, args.steps // 10)))
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -372,6 +425,8 @@ def main():
         "clocks": clocks,
         "e2e": e2e,
     }
+    if other is not None:
+        line["workloads"] = other
     if cpu is not None:
         line["cpu_baseline"] = {"value": cpu["kv_bytes"] / cpu["seconds"] / 1e9, "unit": "GB/s",
                                 "cores": cpu["cores"], "kind": "oracle",

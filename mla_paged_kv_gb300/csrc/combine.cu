@@ -3,7 +3,7 @@
 // FlashMLA PR #183 (Summary; "Modifications outside csrc/sm80/") merges the
 // per-split partial outputs with a combine kernel and bounds the split count
 // by a compile-time ladder.  Here the split count is a runtime loop bound, so
-// any number of splits is merged.  One warp per output row:
+// any number of splits is merged.  Per output row:
 //   m = max_s lse_s,  w_s = exp(lse_s - m),  Z = sum_s w_s,
 //   out = sum_s (w_s / Z) O_s,  lse = m + ln Z
 // with -inf splits weighing 0 and an all-empty row giving out 0, lse -inf.
@@ -31,28 +31,48 @@ __device__ __forceinline__ void store_row4(void* out, int out_fp32, size_t elem,
   }
 }
 
+__device__ __forceinline__ void acc4(float4& a, float w, const float4& v) {
+  if (w != 0.f) {  // a -inf split weighs exactly 0 whatever its partial holds
+    a.x = fmaf(w, v.x, a.x);
+    a.y = fmaf(w, v.y, a.y);
+    a.z = fmaf(w, v.z, a.z);
+    a.w = fmaf(w, v.w, a.w);
+  }
+}
+
+// kVec = float4 per lane per split: 4 -> a warp covers a whole 512-column
+// row (a block = 4 rows), 1 -> a warp covers a 128-column quarter (a block =
+// 1 row).  The quarter form gives 4x the warps for problems with few rows and
+// many splits (long context: one unit, dozens of splits), where the loop over
+// splits, not the grid, has to carry the parallelism.  Split weights are
+// computed with the lanes spread over the splits and broadcast by shuffle;
+// the partial rows of kBatch splits are loaded before any is summed.
+template <int kVec>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const float* __restrict__ o_accum, const float* __restrict__ lse_accum,
                    const int32_t* __restrict__ split_offset, int rows, void* __restrict__ out, int out_fp32,
                    float* __restrict__ lse) {
+  constexpr int kBatch = kVec == 4 ? 4 : 8;
   pdl_wait_prior_grid();
   const int unit = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kCombineWarps + warp;
+  const int row = kVec == 4 ? blockIdx.x * kCombineWarps + warp : blockIdx.x;
   if (row >= rows) return;
   const int s0 = split_offset[unit];
   const int n = split_offset[unit + 1] - s0;
   if (n == 1) return;  // written directly by the attention kernel
   const size_t orow = static_cast<size_t>(unit) * rows + row;
+  const size_t col = (kVec == 4 ? 0 : static_cast<size_t>(warp) * 128) + lane * 4;
+  const bool writes_lse = kVec == 4 ? lane == 0 : (warp == 0 && lane == 0);
 
   float m = -INFINITY;
   for (int s = lane; s < n; s += 32) m = fmaxf(m, lse_accum[static_cast<size_t>(s0 + s) * rows + row]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (n == 0 || m == -INFINITY) {
+  if (n <= 0 || m == -INFINITY) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) store_row4(out, out_fp32, orow * kDv + lane * 4 + 128 * k, 0.f, 0.f, 0.f, 0.f);
-    if (lane == 0) lse[orow] = -INFINITY;
+    for (int k = 0; k < kVec; ++k) store_row4(out, out_fp32, orow * kDv + col + 128 * k, 0.f, 0.f, 0.f, 0.f);
+    if (writes_lse) lse[orow] = -INFINITY;
     return;
   }
   float z = 0.f;
@@ -64,35 +84,48 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
   const float inv_z = 1.f / z;
 
-  float4 acc[4];
+  const size_t split_stride = static_cast<size_t>(rows) * kDv / 4;  // float4 between consecutive splits
+  float4 acc[kVec];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-  for (int s = 0; s < n; ++s) {
-    const size_t slot_row = static_cast<size_t>(s0 + s) * rows + row;
-    const float l = lse_accum[slot_row];
-    if (l == -INFINITY) continue;
-    const float w = expf(l - m) * inv_z;
-    const float4* src = reinterpret_cast<const float4*>(o_accum + slot_row * kDv);
+  for (int k = 0; k < kVec; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    const int cnt = min(32, n - c0);
+    const float l = lane < cnt ? lse_accum[static_cast<size_t>(s0 + c0 + lane) * rows + row] : -INFINITY;
+    const float w = (l == -INFINITY) ? 0.f : expf(l - m) * inv_z;
+    const float4* src = reinterpret_cast<const float4*>(o_accum + (static_cast<size_t>(s0 + c0) * rows + row) * kDv +
+                                                        col);
+    int j = 0;
+    for (; j + kBatch <= cnt; j += kBatch) {
+      float4 v[kBatch][kVec];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 v = src[lane + 32 * k];
-      acc[k].x = fmaf(w, v.x, acc[k].x);
-      acc[k].y = fmaf(w, v.y, acc[k].y);
-      acc[k].z = fmaf(w, v.z, acc[k].z);
-      acc[k].w = fmaf(w, v.w, acc[k].w);
+      for (int i = 0; i < kBatch; ++i)
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) v[i][k] = __ldg(src + static_cast<size_t>(j + i) * split_stride + 32 * k);
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const float wj = __shfl_sync(0xffffffffu, w, j + i);
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) acc4(acc[k], wj, v[i][k]);
+      }
+    }
+    for (; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) acc4(acc[k], wj, __ldg(src + static_cast<size_t>(j) * split_stride + 32 * k));
     }
   }
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    store_row4(out, out_fp32, orow * kDv + lane * 4 + 128 * k, acc[k].x, acc[k].y, acc[k].z, acc[k].w);
-  if (lane == 0) lse[orow] = m + logf(z);
+  for (int k = 0; k < kVec; ++k)
+    store_row4(out, out_fp32, orow * kDv + col + 128 * k, acc[k].x, acc[k].y, acc[k].z, acc[k].w);
+  if (writes_lse) lse[orow] = m + logf(z);
 }
 
 cudaError_t launch_combine(const float* o_accum, const float* lse_accum, const int32_t* split_offset, int n_units,
                            int rows, void* out, int out_fp32, float* lse, cudaStream_t stream) {
+  // whole-row warps once there are enough rows to fill the GPU several times over
+  const bool whole_rows = static_cast<long long>(n_units) * rows >= 8192;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ceil_div_i(rows, kCombineWarps), n_units, 1);
+  cfg.gridDim = whole_rows ? dim3(ceil_div_i(rows, kCombineWarps), n_units, 1) : dim3(rows, n_units, 1);
   cfg.blockDim = dim3(kCombineWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -101,7 +134,9 @@ cudaError_t launch_combine(const float* o_accum, const float* lse_accum, const i
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, o_accum, lse_accum, split_offset, rows, out, out_fp32, lse);
+  if (whole_rows)
+    return cudaLaunchKernelEx(&cfg, combine_kernel<4>, o_accum, lse_accum, split_offset, rows, out, out_fp32, lse);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<1>, o_accum, lse_accum, split_offset, rows, out, out_fp32, lse);
 }
 
 }  // namespace mla

@@ -1,0 +1,34 @@
+"""The five named workloads at their full sizes, in the launch configuration
+bench.py times (partition count from mla_num_parts, default plan), against the
+oracle on every request (the vectorised fp64 oracle takes well under a second
+per workload)."""
+
+import pytest
+import torch
+
+import mla_paged_kv_gb300 as mla
+from mla_paged_kv_gb300 import workloads as wl
+from tests.parity import compare, dense_oracle, sparse_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["dense_b1_hq16_sk256_fp32out", "dense_b64_hq128_sk2048to4096",
+                                  "dense_b1_hq64_sk65536", "dense_b16_sq2causal_hq128_sk4096to8192"])
+def test_dense_workload_full_size(name):
+    case = wl.make(name)
+    c = to_dev(case)
+    out, lse = mla.decode(c.q, c.kv, c.block_table, c.cache_seqlens, causal=case.causal, softmax_scale=case.scale,
+                          out_fp32=case.out_fp32)
+    torch.cuda.synchronize()
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+def test_sparse_workload_full_size():
+    case = wl.make("sparse_fp8_b16_hq128_topk2048")
+    c = to_dev(case)
+    out, lse = mla.sparse_decode(c.q, c.kv8, c.indices, c.topk_length, softmax_scale=case.scale)
+    torch.cuda.synchronize()
+    ro, rl = sparse_oracle(case)
+    compare(out, lse, ro, rl)
