@@ -71,6 +71,21 @@ def dist_setup(n):
     return rank, world, dist
 
 
+def max_over_ranks(x, dist, device):
+    """The slowest rank's value (all ranks get it); x itself on a single process."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, bytes_per_rank, ms_slowest):
+    """Whole-job GB/s: every rank processed its own batch in the slowest rank's time."""
+    return world * bytes_per_rank / (ms_slowest * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -333,11 +348,7 @@ def main():
     bus = getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None)
     clocks = sampler.stop(bus if isinstance(bus, str) else None)
     mla.check_status(status, "timed loop")
-    ms_step = sum(ms) / len(ms)
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(sum(ms) / len(ms), dist, dev)
 
     # the split-KV attention kernel alone (roofline); its exported entry point
     def splits_only():
@@ -376,14 +387,10 @@ def main():
         barrier()
         ms_e = timed(e2e_step, max(20, args.steps // 10))
         barrier()
-        e_ms = statistics.mean(ms_e)
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(statistics.mean(ms_e), dist, dev)
         h2d = hq.numel() * 2 + hbt.numel() * 4 + hsl.numel() * 4
         d2h = hout.numel() * 2 + hlse.numel() * 4
-        e2e = {"value": world * kv_bytes / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "us_per_call": 1e3 * e_ms,
+        e2e = {"value": job_throughput(world, kv_bytes, e_ms), "unit": "GB/s", "us_per_call": 1e3 * e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         mla.check_status(status, "e2e loop")
 
@@ -400,7 +407,7 @@ def main():
     traffic = profiled_traffic()
     line = {
         "metric": METRIC,
-        "value": world * kv_bytes / (ms_step * 1e-3) / 1e9,
+        "value": job_throughput(world, kv_bytes, ms_step),
         "unit": "GB/s",
         "us_per_call": 1e3 * ms_step,
         "n_gpus": world,
