@@ -10,28 +10,37 @@
 // How (GB300 design, not the page's SM80 one):
 //  * TMEM holds 512 fp32 columns per SM, exactly one 128 x 512 accumulator,
 //    so the two CTAs of a cluster split the value dims: rank c accumulates
-//    O[:, 256c : 256c+256).  Each computes the full Q K^T itself: on this
-//    part distributed shared memory moves ~14 B/clk per SM, far too little
-//    to share a 32 KB score tile per page between the two CTAs.
+//    O[:, 256c : 256c+256).
+//  * The two CTAs take turns on the pipeline tiles (one 64-key page each):
+//    tile t is "owned" by rank t & 1, which alone computes S = Q K^T for it,
+//    its softmax and its P.  The owner sends P (16 KB of bf16) to the other
+//    CTA with asynchronous bulk copies into distributed shared memory, and
+//    both run P V for their own value half.  Every score
+//    is computed once; only P crosses between the SMs.
+//  * Both halves of O must use the same softmax reference.  The reference
+//    after tile t is R_t = the running max (log2 units), raised only when a
+//    tile's max exceeds it by more than 2^8 (lazy rescale).  The owner of t
+//    needs R_{t-1} from the other CTA: it arrives as 128 floats in a small
+//    mailbox in distributed shared memory (a 128-byte bulk copy per warp),
+//    sent as soon as that tile's row max is known, long before its P.  When
+//    R changes, both CTAs rescale their O half in TMEM before that tile's
+//    P V.  Each CTA keeps the row sum l of its own tiles only (rescaled on
+//    every reference change); the two are added once per unit, before the
+//    epilogue, through a second mailbox.
+//  * The P V of a received tile waits only for its P to land (the MMA thread
+//    watches the copy's barrier) and for the softmax threads' go, given as
+//    soon as the tile's reference is known.
 //  * Q of the row block is the MMA A operand: dims [0, 384) sit in TMEM
 //    (packed bf16 pairs, written by the softmax threads once per unit), dims
 //    [384, 576) in shared memory (TMA, 128-byte swizzle).
-//  * One pipeline tile = one 64-key page = nine 64-dim TMA boxes.  The four
-//    boxes that are also this CTA's V (dims 256c .. 256c+255) go to a "V"
-//    ring and stay until P V has run; the other five go to a "K" ring that
-//    is released as soon as Q K^T has run.  Each ring has two slots and its
-//    own producer warp, and Q K^T reads the K-ring boxes first, so the next
-//    pages keep streaming while the softmax of the current one runs.  Pages
-//    a few tiles ahead are also prefetched into L2.
-//  * tcgen05.mma M=128: S (N=64) and O (N=256) accumulate in TMEM.  An MMA
-//    instruction costs at least ~45 cycles to issue, so N=64 is the smallest
-//    score tile that keeps the tensor pipe mostly busy, and each group of
-//    MMAs is issued as one fully unrolled block.  P is written as bf16 by
-//    the softmax threads into swizzled shared memory.
-//  * Online softmax in the log2 domain with a lazy rescale: O is rescaled
-//    only when the running max grows by more than 2^8.
+//  * One tile = nine 64-dim TMA boxes of one page.  The four boxes that are
+//    this CTA's V half go to a 3-slot "V" ring for every tile (P V reads
+//    them; for its own tiles Q K^T reads them too); the other five go to a
+//    "K" slot, for own tiles only, released as soon as Q K^T has read them.
+//  * tcgen05.mma M=128: S (N=64) and O (N=256) accumulate in TMEM; each
+//    group of MMAs is one fully unrolled block of compile-time descriptors.
 // Roles: warps 0-3 softmax + epilogue + Q-to-TMEM (thread = row = TMEM lane),
-//        warp 4 K-ring + Q producer, warp 5 V-ring producer,
+//        warp 4 K-slot + Q producer, warp 5 V-ring producer,
 //        warp 6 MMA issuer and TMEM owner.
 #include <cuda_bf16.h>
 
@@ -50,30 +59,64 @@ namespace mla {
 namespace dn {
 
 constexpr int kT = 64;                             // keys per pipeline tile (one page)
-constexpr int kBoxes = 9;                          // 64-dim boxes of a 576-dim row
 constexpr int kKBoxes = 5;                         // boxes only Q K^T reads
 constexpr int kVBoxes = 4;                         // boxes Q K^T and P V read
 constexpr int kQTmemBoxes = 6;                     // Q dims [0, 384) in TMEM
-constexpr int kQSmemBoxes = kBoxes - kQTmemBoxes;  // Q dims [384, 576) in shared memory
+constexpr int kQSmemBoxes = 3;                     // Q dims [384, 576) in shared memory
 constexpr int kQBoxBytes = kRowsPerBlock * 128;    // 128 rows x 64 bf16
 constexpr int kBoxBytes = kT * 128;                // 64 keys x 64 bf16
 constexpr int kKSlotBytes = kKBoxes * kBoxBytes;
 constexpr int kVSlotBytes = kVBoxes * kBoxBytes;
-constexpr int kSlots = 2;
-constexpr int kPBytes = kRowsPerBlock * kT * 2;  // one 64-key P tile, bf16
+constexpr int kKSlots = 1;
+constexpr int kVSlots = 3;
+constexpr int kPBytes = kRowsPerBlock * kT * 2;    // one 64-key P tile, bf16
+constexpr int kWarpPBytes = 32 * 128;              // the 32 P rows of one softmax warp
+constexpr int kVecBytes = kRowsPerBlock * 4;       // one fp32 per row (references, row sums)
 
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQSmemBoxes * kQBoxBytes;
-constexpr int kOffV = kOffK + kSlots * kKSlotBytes;
-constexpr int kOffP = kOffV + kSlots * kVSlotBytes;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 24;
+constexpr int kOffV = kOffK + kKSlots * kKSlotBytes;
+constexpr int kOffPOwn = kOffV + kVSlots * kVSlotBytes;
+constexpr int kOffPRecv = kOffPOwn + kPBytes;
+constexpr int kOffRefOut = kOffPRecv + kPBytes;   // this CTA's references, staged for the copy
+constexpr int kOffRefIn = kOffRefOut + kVecBytes;  // mailbox: the peer's references
+constexpr int kOffLOut = kOffRefIn + kVecBytes;    // this CTA's row sums, staged
+constexpr int kOffLIn = kOffLOut + kVecBytes;      // mailbox: the peer's row sums
+constexpr int kOffBar = kOffLIn + kVecBytes;
+
+enum : int {
+  Q_FULL = 0,
+  Q_EMPTY = 1,
+  K_FULL = 2,                     // +slot
+  K_EMPTY = K_FULL + kKSlots,     // +slot
+  V_FULL = K_EMPTY + kKSlots,     // +slot
+  V_EMPTY = V_FULL + kVSlots,     // +slot
+  S_FULL = V_EMPTY + kVSlots,
+  S_FREE,
+  OWN_GO,     // softmax -> MMA: P of an own tile written, O rescaled
+  OWN_FREE,   // own P buffer reusable: own P V done + the peer's P V done (its multicast commit)
+  RECV_FULL,  // the peer's P has landed (bulk-copy bytes); watched and re-armed by the MMA thread
+  RECV_GO,    // softmax -> MMA: received tile's reference applied (O rescaled if it changed)
+  R_FULL,     // reference mailbox filled (bulk-copy bytes)
+  R_FREE,     // the peer has read our last references (one remote arrival per warp)
+  L_FULL,     // row-sum mailbox filled (bulk-copy bytes)
+  L_FREE,     // the peer has read our last row sums (one remote arrival per warp)
+  PV_DONE,    // one completion per P V, in tile order
+  O_FULL,
+  O_FREE,
+  DRAIN,
+  kNumBars
+};
+
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0 && kKSlotBytes % 1024 == 0,
+static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffPOwn % 1024 == 0 && kOffPRecv % 1024 == 0 &&
+                  kKSlotBytes % 1024 == 0 && kVSlotBytes % 1024 == 0,
               "swizzle atoms need 1024-byte alignment");
+static_assert(kOffRefOut % 16 == 0 && kOffRefIn % 16 == 0 && kOffLOut % 16 == 0 && kOffLIn % 16 == 0,
+              "bulk copies need 16-byte alignment");
 
 constexpr int kThreads = 224;
 constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6;
@@ -82,26 +125,6 @@ constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
 constexpr uint32_t kTmemS = 256;  // S: [256, 320)
 constexpr uint32_t kTmemQ = 320;  // Q dims [0, 384) as packed bf16 pairs: [320, 512)
 
-enum : int {
-  Q_FULL = 0,
-  Q_EMPTY = 1,
-  KA_FULL = 2,   // +slot
-  KA_EMPTY = 4,  // +slot
-  KB_FULL = 6,   // +slot
-  KB_EMPTY = 8,  // +slot
-  S_FULL = 10,
-  S_FREE = 11,
-  P_FULL = 12,  // +buffer
-  P_FREE = 14,  // +buffer
-  O_FULL = 16,
-  O_FREE = 17,
-  DRAIN = 18,
-};
-
-#ifndef MLA_DENSE_PREFETCH_PAGES
-#define MLA_DENSE_PREFETCH_PAGES 0
-#endif
-constexpr int kPrefetch = MLA_DENSE_PREFETCH_PAGES;  // pages prefetched into L2 ahead of the TMA loads
 constexpr float kTau = 8.0f;  // lazy-rescale threshold (log2 units)
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -167,7 +190,7 @@ __device__ __forceinline__ void cursor_next(const DecodeParams& p, const Part& P
   }
 }
 
-// Global box held in slot position j of this rank's K ring: the other half's
+// Global box held in slot position j of this rank's K slot: the other half's
 // value dims, then the RoPE box.
 template <int kRank>
 __host__ __device__ constexpr int k_box(int j) {
@@ -183,11 +206,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
 }
 
-// Prefetch one page (all 9 boxes) into L2; bad ids are skipped.
-__device__ __forceinline__ void prefetch_page(const DecodeParams& p, int pg, const CUtensorMap* kv_map) {
-  if (pg < 0 || pg >= p.num_pages) return;
-#pragma unroll
-  for (int bx = 0; bx < kBoxes; ++bx) tma_prefetch_3d(kv_map, 64 * bx, 0, pg);
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait<true>(bar, parity, abort_flag));
 }
 
 // Page ids of 32 consecutive pages of unit c.b starting at `base`, one per lane
@@ -206,7 +226,7 @@ __device__ __forceinline__ int load_page_window(const DecodeParams& p, const Cur
 }
 
 // Q K^T over one 64-dim box kG (4 K-steps).  The A operand (Q) comes from TMEM
-// for kG < 6, else from shared memory; B is the box in a K or V ring slot.
+// for kG < 6, else from shared memory; B is the box in the K slot or V ring.
 template <int kG>
 __device__ __forceinline__ void qk_box(uint32_t d, uint32_t tmem, uint64_t q_desc0, uint64_t b_desc, bool first) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, kT, false);
@@ -221,7 +241,7 @@ __device__ __forceinline__ void qk_box(uint32_t d, uint32_t tmem, uint64_t q_des
   }
 }
 
-// Q K^T over this rank's K-ring boxes (first part of the score tile).
+// Q K^T over this rank's K-slot boxes (first part of the score tile).
 template <int kRank>
 __device__ __forceinline__ void issue_qk_k(uint32_t d, uint32_t tmem, uint64_t q_desc0, uint64_t kslot) {
   qk_box<k_box<kRank>(0)>(d, tmem, q_desc0, kslot + ((0 * kBoxBytes) >> 4), true);
@@ -267,6 +287,26 @@ __device__ __forceinline__ void load_q_to_tmem(const DecodeParams& p, const uint
   tmem_wait_st();
 }
 
+// O half (this thread's row) *= alpha.
+__device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
+#pragma unroll 1
+  for (uint32_t c0 = 0; c0 < 256; c0 += 16) {
+    uint32_t v[16];
+    tmem_ld16(taddr + kTmemO + c0, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+    tmem_st16(taddr + kTmemO + c0, v);
+  }
+  tmem_wait_st();
+}
+
+// O-rescale factor between two references; 1 when unchanged (also when both
+// are -inf), 0 when the old one is -inf and the new one finite.
+__device__ __forceinline__ float ref_alpha(float r_old, float r_new) {
+  return r_new == r_old ? 1.f : ex2(r_old - r_new);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     dense_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
                         const DecodeParams p, const uint16_t* __restrict__ q) {
@@ -276,7 +316,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
-  uint8_t* sP = smem + kOffP;
+  uint8_t* sPOwn = smem + kOffPOwn;
+  uint8_t* sPRecv = smem + kOffPRecv;
+  float* sRefOut = reinterpret_cast<float*>(smem + kOffRefOut);
+  float* sRefIn = reinterpret_cast<float*>(smem + kOffRefIn);
+  float* sLOut = reinterpret_cast<float*>(smem + kOffLOut);
+  float* sLIn = reinterpret_cast<float*>(smem + kOffLIn);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -284,6 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
   const int cluster_id = blockIdx.x >> 1;
   const int part_idx = cluster_id / p.row_blocks;
   const int rb = cluster_id - part_idx * p.row_blocks;
@@ -292,22 +338,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     mbar_init(&bars[Q_FULL], 128 + 1);  // softmax threads (TMEM part) + K producer (TMA part)
     mbar_init(&bars[Q_EMPTY], 1);
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&bars[KA_FULL + i], 1);
-      mbar_init(&bars[KA_EMPTY + i], 1);
-      mbar_init(&bars[KB_FULL + i], 1);
-      mbar_init(&bars[KB_EMPTY + i], 1);
+    for (int i = 0; i < kKSlots; ++i) {
+      mbar_init(&bars[K_FULL + i], 1);
+      mbar_init(&bars[K_EMPTY + i], 1);
+    }
+    for (int i = 0; i < kVSlots; ++i) {
+      mbar_init(&bars[V_FULL + i], 1);
+      mbar_init(&bars[V_EMPTY + i], 1);
     }
     mbar_init(&bars[S_FULL], 1);
     mbar_init(&bars[S_FREE], 128);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[P_FULL + i], 128);
-      mbar_init(&bars[P_FREE + i], 1);
-    }
+    mbar_init(&bars[OWN_GO], 128);
+    mbar_init(&bars[OWN_FREE], 2);
+    mbar_init(&bars[RECV_FULL], 1);
+    mbar_init(&bars[RECV_GO], 128);
+    mbar_init(&bars[R_FULL], 1);
+    mbar_init(&bars[R_FREE], 4);
+    mbar_init(&bars[L_FULL], 1);
+    mbar_init(&bars[L_FREE], 4);
+    mbar_init(&bars[PV_DONE], 1);
     mbar_init(&bars[O_FULL], 1);
     mbar_init(&bars[O_FREE], 128);
     mbar_init(&bars[DRAIN], 1);
     fence_mbar_init_cluster();
+    // armed for the first P, references and row sums the peer will send
+    mbar_arrive_expect_tx(&bars[RECV_FULL], kPBytes);
+    mbar_arrive_expect_tx(&bars[R_FULL], kVecBytes);
+    mbar_arrive_expect_tx(&bars[L_FULL], kVecBytes);
   }
   if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -320,25 +377,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  cluster_arrive();  // the peer's barriers are initialised before any remote access
+  cluster_wait();
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
 
   const Part P = load_part(p.sched, part_idx);
+  bool aborted = false;
+  uint32_t r_seen = 0, l_seen = 0;  // reference / row-sum messages received (armed phases)
 
   if (warp == kWarpK || warp == kWarpV) {
     // ------------------------------------------------------------ TMA producers
     const bool is_k = (warp == kWarpK);
     const uint64_t pol_kv = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
-    const int full_bar = is_k ? KA_FULL : KB_FULL;
-    const int empty_bar = is_k ? KA_EMPTY : KB_EMPTY;
-    uint8_t* ring = is_k ? sK : sV;
-    const int slot_bytes = is_k ? kKSlotBytes : kVSlotBytes;
     Cursor c;
     cursor_init(p, P, c);
     bool ok = true;
-    uint32_t issued[kSlots] = {0u, 0u};
-    uint32_t q_issued = 0;
+    uint32_t k_issued[kKSlots] = {}, v_issued[kVSlots] = {};
+    uint32_t q_issued = 0, own_k = 0;
     int page_reg = 0, page_base = -1, cur_b = -1;
     while (ok && c.valid) {
       if (is_k && cursor_first(c)) {
@@ -356,59 +413,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
       }
-      // page ids of the next 32 pages of this unit, one per lane; refreshed early
-      // enough that the L2 prefetch kPrefetch pages ahead stays inside the window
-      const bool fresh = c.b != cur_b;
-      if (fresh || c.k - page_base >= 32 - kPrefetch) {
-        cur_b = c.b;
-        page_base = c.k;
-        page_reg = load_page_window(p, c, page_base, lane);
-      }
-      const int page = __shfl_sync(0xffffffffu, page_reg, c.k - page_base);
-      if (is_k && kPrefetch > 0) {
-        int pf[kPrefetch > 0 ? kPrefetch : 1];
-#pragma unroll
-        for (int i = 0; i < kPrefetch; ++i)
-          pf[i] = __shfl_sync(0xffffffffu, page_reg, min(c.k + 1 + i - page_base, 31));
-        if (lane == 0) {
-          if (fresh) {
-#pragma unroll
-            for (int i = 0; i + 1 < kPrefetch; ++i)
-              if (c.k + 1 + i < c.hi) prefetch_page(p, pf[i], &kv_map);
-          }
-          if (c.k + kPrefetch < c.hi) prefetch_page(p, pf[kPrefetch - 1], &kv_map);
+      const bool mine = (c.t & 1u) == rank;
+      if (!is_k || mine) {
+        // page ids of the next 32 pages of this unit, one per lane
+        if (c.b != cur_b || c.k - page_base >= 32) {
+          cur_b = c.b;
+          page_base = c.k;
+          page_reg = load_page_window(p, c, page_base, lane);
         }
-      }
-      const int s = c.t & 1;
-      if (lane == 0) {
-        if (c.t >= kSlots) ok = mbar_wait(&bars[empty_bar + s], ((c.t >> 1) - 1) & 1, abort_flag);
-        if (ok) {
-          MLA_TRACE(is_k ? 0 : 7, c.t);
-          mbar_arrive_expect_tx(&bars[full_bar + s], slot_bytes);
-          uint8_t* dst = ring + s * slot_bytes;
+        const int page = __shfl_sync(0xffffffffu, page_reg, c.k - page_base);
+        if (lane == 0) {
           if (is_k) {
+            const uint32_t n = own_k / kKSlots;
+            const int s = static_cast<int>(own_k % kKSlots);
+            if (n >= 1) ok = mbar_wait(&bars[K_EMPTY + s], (n - 1) & 1, abort_flag);
+            if (ok) {
+              MLA_TRACE(9, c.t);
+              mbar_arrive_expect_tx(&bars[K_FULL + s], kKSlotBytes);
+              uint8_t* dst = sK + s * kKSlotBytes;
 #pragma unroll
-            for (int j = 0; j < kKBoxes; ++j) {
-              const int g = rank == 0 ? k_box<0>(j) : k_box<1>(j);
-              tma_load_3d(dst + j * kBoxBytes, &kv_map, &bars[full_bar + s], 64 * g, 0, page, pol_kv);
+              for (int j = 0; j < kKBoxes; ++j) {
+                const int g = rank == 0 ? k_box<0>(j) : k_box<1>(j);
+                tma_load_3d(dst + j * kBoxBytes, &kv_map, &bars[K_FULL + s], 64 * g, 0, page, pol_kv);
+              }
+              ++k_issued[s];
             }
           } else {
+            const uint32_t n = c.t / kVSlots;
+            const int s = static_cast<int>(c.t % kVSlots);
+            if (n >= 1) ok = mbar_wait(&bars[V_EMPTY + s], (n - 1) & 1, abort_flag);
+            if (ok) {
+              MLA_TRACE(7, c.t);
+              mbar_arrive_expect_tx(&bars[V_FULL + s], kVSlotBytes);
+              uint8_t* dst = sV + s * kVSlotBytes;
 #pragma unroll
-            for (int j = 0; j < kVBoxes; ++j)
-              tma_load_3d(dst + j * kBoxBytes, &kv_map, &bars[full_bar + s], 64 * (4 * static_cast<int>(rank) + j),
-                          0, page, pol_kv);
+              for (int j = 0; j < kVBoxes; ++j)
+                tma_load_3d(dst + j * kBoxBytes, &kv_map, &bars[V_FULL + s], 64 * (4 * static_cast<int>(rank) + j),
+                            0, page, pol_kv);
+              ++v_issued[s];
+            }
           }
-          ++issued[s];
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (is_k && mine) ++own_k;
       cursor_next(p, P, c);
     }
     if (lane == 0) {
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // no TMA write may land after this CTA exits
-      for (int s = 0; s < kSlots; ++s)
-        if (issued[s] > 0) mbar_wait(&bars[full_bar + s], (issued[s] - 1) & 1, nullptr);
+      for (int s = 0; s < kKSlots; ++s)
+        if (k_issued[s] > 0) mbar_wait(&bars[K_FULL + s], (k_issued[s] - 1) & 1, nullptr);
+      for (int s = 0; s < kVSlots; ++s)
+        if (v_issued[s] > 0) mbar_wait(&bars[V_FULL + s], (v_issued[s] - 1) & 1, nullptr);
       if (q_issued > 0) mbar_wait(&bars[Q_FULL], (q_issued - 1) & 1, nullptr);
     }
     __syncwarp();
@@ -420,88 +477,145 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t k_desc0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t vk_desc0 = sdesc_sw128(smem_u32(sV), 16, 1024);        // V boxes as K-major B of Q K^T
       const uint64_t vv_desc0 = sdesc_sw128(smem_u32(sV), kBoxBytes, 1024);  // V boxes as MN-major B of P V
-      const uint64_t p_desc0 = sdesc_sw128(smem_u32(sP), 16, 1024);
-      // Three jobs per tile, issued as soon as their inputs are ready, in the
-      // priority P V > Q K^T (V-ring part) > Q K^T (K-ring part):
-      //   QKa(t): needs the K slot, S read by the softmax of t-1, Q of the unit
-      //   QKb(t): needs QKa(t) issued and the V slot; completes S(t)
-      //   PV(t):  needs QKb(t) issued and P(t)
-      Cursor ca, cb, cv;
-      cursor_init(p, P, ca);
-      cursor_init(p, P, cb);
+      const uint64_t pown_desc = sdesc_sw128(smem_u32(sPOwn), 16, 1024);
+      const uint64_t precv_desc = sdesc_sw128(smem_u32(sPRecv), 16, 1024);
+      const uint16_t peer_mask = static_cast<uint16_t>(1u << peer);
+      // Two cursors over the partition's tiles:
+      //   cq: Q K^T of own tiles, in two halves (K slot part, then V ring part
+      //       -> S); it steps over the peer's tiles at once and releases Q at
+      //       every unit end (after the unit's Q has arrived, so that the Q
+      //       barriers' phases stay aligned even for a unit without own tiles);
+      //   cv: P V of every tile, in order, from the own or the received P.
+      // Each pass issues at most one job, P V first.
+      Cursor cq, cv;
+      cursor_init(p, P, cq);
       cursor_init(p, P, cv);
+      uint32_t a_own = 0, pv_own = 0, pv_recv = 0;
+      int q_phase = 0;          // 0: next is QKa of cq, 1: next is QKb of cq
+      bool q_have = false;      // Q of cq's unit has been seen complete
       bool ok = true;
       uint64_t t_last = globaltimer_ns();
+      // cq onto the next own tile, releasing the Q of every unit it leaves;
+      // returns false if it has to stop at a unit end whose Q has not arrived
+      auto advance_q = [&]() -> bool {
+        while (cq.valid) {
+          const bool mine = (cq.t & 1u) == rank;
+          if (mine && q_phase == 0) return true;  // at an own tile: its QKa is next
+          if (!mine || q_phase == 2) {
+            // leaving this tile; at the unit's end, Q of the unit is released
+            if (cursor_last(cq)) {
+              if (!q_have) {
+                if (!mbar_test_wait(&bars[Q_FULL], cq.u & 1)) return false;
+              }
+              umma_commit(&bars[Q_EMPTY]);
+              q_have = false;
+            }
+            cursor_next(p, P, cq);
+            q_phase = 0;
+            continue;
+          }
+          return true;  // own tile with QKb next
+        }
+        return true;
+      };
+      advance_q();
       while (cv.valid) {
         bool progressed = false;
-        if (cv.t < cb.t) {
-          const int pb = cv.t & 1;
+        {
+          const bool mine = (cv.t & 1u) == rank;
           const bool first = cursor_first(cv);
-          bool ready = mbar_test_wait(&bars[P_FULL + pb], (cv.t >> 1) & 1);
+          const int vs = static_cast<int>(cv.t % kVSlots);
+          bool ready = mine ? mbar_test_wait(&bars[OWN_GO], pv_own & 1)
+                            : (mbar_test_wait(&bars[RECV_GO], pv_recv & 1) &&
+                               mbar_test_wait(&bars[RECV_FULL], pv_recv & 1));
+          ready = ready && mbar_test_wait(&bars[V_FULL + vs], (cv.t / kVSlots) & 1);
           if (ready && first && cv.u >= 1) ready = mbar_test_wait(&bars[O_FREE], (cv.u - 1) & 1);
           if (ready) {
             MLA_TRACE(3, cv.t);
+            // armed for the next received P (it cannot be sent before this P V is done)
+            if (!mine) mbar_arrive_expect_tx(&bars[RECV_FULL], kPBytes);
             tc_fence_after();
-            const uint64_t a0 = p_desc0 + static_cast<uint64_t>((pb * kPBytes) >> 4);
-            const uint64_t b0 = vv_desc0 + static_cast<uint64_t>((pb * kVSlotBytes) >> 4);
+            const uint64_t a0 = mine ? pown_desc : precv_desc;
+            const uint64_t b0 = vv_desc0 + static_cast<uint64_t>((vs * kVSlotBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
               umma_f16(tmem + kTmemO, a0 + static_cast<uint64_t>((kk * 32) >> 4),
                        b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
-            umma_commit(&bars[P_FREE + pb]);
-            umma_commit(&bars[KB_EMPTY + pb]);
+            umma_commit(&bars[V_EMPTY + vs]);
+            umma_commit(&bars[PV_DONE]);
+            if (mine) {
+              umma_commit(&bars[OWN_FREE]);
+              ++pv_own;
+            } else {
+              // the peer may refill our receive buffer (and reuse its own copy of that P)
+              umma_commit_multicast(&bars[OWN_FREE], peer_mask);
+              ++pv_recv;
+            }
             if (cursor_last(cv)) umma_commit(&bars[O_FULL]);
+            MLA_TRACE(16, cv.t);
             cursor_next(p, P, cv);
             progressed = true;
           }
         }
-        if (!progressed && cb.t < ca.t) {
-          const int s = cb.t & 1;
-          if (mbar_test_wait(&bars[KB_FULL + s], (cb.t >> 1) & 1)) {
-            MLA_TRACE(8, cb.t);
-            tc_fence_after();
-            const uint64_t vslot = vk_desc0 + static_cast<uint64_t>((s * kVSlotBytes) >> 4);
-            if (rank == 0)
-              issue_qk_v<0>(tmem + kTmemS, tmem, q_desc0, vslot);
-            else
-              issue_qk_v<1>(tmem + kTmemS, tmem, q_desc0, vslot);
-            umma_commit(&bars[S_FULL]);
-            umma_commit(&bars[KA_EMPTY + s]);
-            MLA_TRACE(2, cb.t);
-            if (cursor_last(cb)) umma_commit(&bars[Q_EMPTY]);
-            cursor_next(p, P, cb);
-            progressed = true;
-          }
-        }
-        if (!progressed && ca.valid && ca.t == cb.t) {
-          const int s = ca.t & 1;
-          bool ready = true;
-          if (cursor_first(ca)) ready = mbar_test_wait(&bars[Q_FULL], ca.u & 1);
-          ready = ready && mbar_test_wait(&bars[KA_FULL + s], (ca.t >> 1) & 1);
-          if (ready && ca.t >= 1) ready = mbar_test_wait(&bars[S_FREE], (ca.t - 1) & 1);
-          if (ready) {
-            MLA_TRACE(1, ca.t);
-            tc_fence_after();
-            const uint64_t kslot = k_desc0 + static_cast<uint64_t>((s * kKSlotBytes) >> 4);
-            if (rank == 0)
-              issue_qk_k<0>(tmem + kTmemS, tmem, q_desc0, kslot);
-            else
-              issue_qk_k<1>(tmem + kTmemS, tmem, q_desc0, kslot);
-            cursor_next(p, P, ca);
-            progressed = true;
+        if (!progressed && cq.valid && advance_q() && cq.valid) {
+          if (q_phase == 0) {
+            const int ks = static_cast<int>(a_own % kKSlots);
+            bool ready = q_have || mbar_test_wait(&bars[Q_FULL], cq.u & 1);
+            if (ready) q_have = true;
+            ready = ready && mbar_test_wait(&bars[K_FULL + ks], (a_own / kKSlots) & 1);
+            if (ready && a_own >= 1) ready = mbar_test_wait(&bars[S_FREE], (a_own - 1) & 1);
+            if (ready) {
+              MLA_TRACE(1, cq.t);
+              tc_fence_after();
+              const uint64_t kslot = k_desc0 + static_cast<uint64_t>((ks * kKSlotBytes) >> 4);
+              if (rank == 0)
+                issue_qk_k<0>(tmem + kTmemS, tmem, q_desc0, kslot);
+              else
+                issue_qk_k<1>(tmem + kTmemS, tmem, q_desc0, kslot);
+              umma_commit(&bars[K_EMPTY + ks]);
+              MLA_TRACE(17, cq.t);
+              ++a_own;
+              q_phase = 1;
+              progressed = true;
+            }
+          } else {
+            const int vs = static_cast<int>(cq.t % kVSlots);
+            if (mbar_test_wait(&bars[V_FULL + vs], (cq.t / kVSlots) & 1)) {
+              MLA_TRACE(8, cq.t);
+              tc_fence_after();
+              const uint64_t vslot = vk_desc0 + static_cast<uint64_t>((vs * kVSlotBytes) >> 4);
+              if (rank == 0)
+                issue_qk_v<0>(tmem + kTmemS, tmem, q_desc0, vslot);
+              else
+                issue_qk_v<1>(tmem + kTmemS, tmem, q_desc0, vslot);
+              umma_commit(&bars[S_FULL]);
+              MLA_TRACE(2, cq.t);
+              q_phase = 2;
+              advance_q();
+              progressed = true;
+            }
           }
         }
         if (progressed) {
           t_last = globaltimer_ns();
         } else {
+          // spin: a sleeping issuer reacts to a ready job far later than the job takes
           if (*abort_flag || globaltimer_ns() - t_last > MLA_WAIT_LIMIT_NS) {
             ok = false;
             break;
           }
-          __nanosleep(20);
         }
       }
-      if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+      // the last units' Q (units after the last own tile) are released too
+      while (ok && cq.valid) {
+        if (advance_q()) break;
+        if (*abort_flag || globaltimer_ns() - t_last > MLA_WAIT_LIMIT_NS) ok = false;
+      }
+      if (!ok) {
+        set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+        // a P the peer already sent may still be landing in our receive buffer
+        mbar_wait<true>(&bars[RECV_FULL], pv_recv & 1, nullptr);
+      }
       // every MMA has completed before TMEM is released
       umma_commit(&bars[DRAIN]);
       mbar_wait(&bars[DRAIN], 0, nullptr);
@@ -511,111 +625,151 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax + epilogue
     const int r = tid;  // row of the block == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t taddr = tmem + lane_base;
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     const int row = rb * kRowsPerBlock + r;
     const bool row_ok = row < p.rows;
     const int tok = row_ok ? row / p.h_q : 0;
     const float c_log2 = p.scale_log2;
+    // the peer's buffers and barriers this warp sends to
+    const uint32_t peer_p = mapa_shared(smem_u32(sPRecv + warp * kWarpPBytes), peer);
+    const uint32_t peer_ref = mapa_shared(smem_u32(sRefIn + 32 * warp), peer);
+    const uint32_t peer_l = mapa_shared(smem_u32(sLIn + 32 * warp), peer);
+    const uint32_t peer_recv_full = mapa_shared(smem_u32(&bars[RECV_FULL]), peer);
+    const uint32_t peer_r_full = mapa_shared(smem_u32(&bars[R_FULL]), peer);
+    const uint32_t peer_r_free = mapa_shared(smem_u32(&bars[R_FREE]), peer);
+    const uint32_t peer_l_full = mapa_shared(smem_u32(&bars[L_FULL]), peer);
+    const uint32_t peer_l_free = mapa_shared(smem_u32(&bars[L_FREE]), peer);
     Cursor c;
     cursor_init(p, P, c);
     bool ok = true;
     if (c.valid) {  // Q of the first unit
-      load_q_to_tmem(p, q, c.b, row, tmem + lane_base);
+      load_q_to_tmem(p, q, c.b, row, taddr);
       tc_fence_before();
       mbar_arrive(&bars[Q_FULL]);
     }
-    float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and fp32 row sum
+    uint32_t own_i = 0, recv_i = 0, units = 0;
+    float r_cur = -INFINITY;  // reference (log2 units) after the last tile seen
+    float l_own = 0.f;        // fp32 row sum of this CTA's own tiles, relative to r_cur
+
     while (ok && c.valid) {
       const uint32_t t = c.t;
       const bool first = cursor_first(c), last = cursor_last(c);
+      const bool mine = (t & 1u) == rank;
       if (first) {
-        m_used = -INFINITY;
-        l_sum = 0.f;
+        r_cur = -INFINITY;
+        l_own = 0.f;
       }
-      const int jmax = p.causal ? (c.L - p.s_q + tok) : (c.L - 1);  // last visible key
-      const int vis = jmax - c.k * kT;                                // keys 0..vis of this tile are visible
-      ok = warp_wait(&bars[S_FULL], t & 1, abort_flag);
-      if (!ok) break;
-      if (tid == 0) MLA_TRACE(4, t);
-      tc_fence_after();
-      float s[kT];
-      {
-        uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
-        uint32_t (&hi32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
-        tmem_ld32(tmem + lane_base + kTmemS, lo32);
-        tmem_ld32(tmem + lane_base + kTmemS + 32u, hi32);
-        tmem_wait_ld();
-      }
-      tc_fence_before();
-      mbar_arrive(&bars[S_FREE]);
-      const int b_here = c.b, u_here = c.u;
-      // masked keys -> -inf; raw tile max (the scale is positive, so max commutes with it)
-      if (vis < kT - 1) {
-#pragma unroll
-        for (int j = 0; j < kT; ++j)
-          if (j > vis) s[j] = -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[i + 8]);
-#pragma unroll
-      for (int j = 16; j < kT; j += 8)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[j + i]);
-      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float mt = mraw * c_log2;  // -inf stays -inf
-      bool rescale = false;
-      float alpha = 1.f;
-      if (mt > m_used + kTau) {
-        alpha = ex2(m_used - mt);  // 0 when m_used == -inf
-        rescale = !first;
-        l_sum *= alpha;
-        m_used = mt;
-      }
-      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      uint32_t pk[kT / 2];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < kT / 2; ++i) {
-        const float p0 = ex2(fmaf(s[2 * i], c_log2, -mref));
-        const float p1 = ex2(fmaf(s[2 * i + 1], c_log2, -mref));
-        const __nv_bfloat162 hv = __floats2bfloat162_rn(p0, p1);
-        pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
-        ls[i & 3] += p0 + p1;
-      }
-      l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      const int pb = t & 1;
-      if (t >= 2) {
-        ok = warp_wait(&bars[P_FREE + pb], ((t - 2) >> 1) & 1, abort_flag);
+      float alpha;
+      if (mine) {
+        // ---- own tile: scores, reference, P
+        const int jmax = p.causal ? (c.L - p.s_q + tok) : (c.L - 1);  // last visible key
+        const int vis = jmax - c.k * kT;                                // keys 0..vis of this tile are visible
+        ok = warp_wait(&bars[S_FULL], own_i & 1, abort_flag);
         if (!ok) break;
+        if (tid == 0) MLA_TRACE(4, t);
+        tc_fence_after();
+        float s[kT];
+        {
+          uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+          uint32_t (&hi32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+          tmem_ld32(taddr + kTmemS, lo32);
+          tmem_ld32(taddr + kTmemS + 32u, hi32);
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[S_FREE]);
+        // masked keys -> -inf; raw tile max (the scale is positive, so max commutes with it)
+        if (vis < kT - 1) {
+#pragma unroll
+          for (int j = 0; j < kT; ++j)
+            if (j > vis) s[j] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+        for (int j = 16; j < kT; j += 8)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[j + i]);
+        const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mt = mraw * c_log2;  // -inf stays -inf
+        const float r_t = (mt > r_cur + kTau) ? mt : r_cur;
+        // the peer needs this tile's reference for its next tile and its O
+        if (own_i >= 1) {
+          ok = warp_wait_cluster(&bars[R_FREE], (own_i - 1) & 1, abort_flag);
+          if (!ok) break;
+        }
+        sRefOut[r] = r_t;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) bulk_copy_to_cluster(peer_ref, smem_u32(sRefOut + 32 * warp), 32 * 4, peer_r_full);
+        if (tid == 0) MLA_TRACE(13, t);
+        const float mref = (r_t == -INFINITY) ? 0.f : r_t;
+        uint32_t pk[kT / 2];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < kT / 2; ++i) {
+          const float p0 = ex2(fmaf(s[2 * i], c_log2, -mref));
+          const float p1 = ex2(fmaf(s[2 * i + 1], c_log2, -mref));
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(p0, p1);
+          pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
+          ls[i & 3] += p0 + p1;
+        }
+        const float rowsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // the own P buffer is free once our P V and the peer's P V of the
+        // previous own tile are done (the latter also means our copy landed)
+        if (own_i >= 1) {
+          ok = warp_wait_cluster(&bars[OWN_FREE], (own_i - 1) & 1, abort_flag);
+          if (!ok) break;
+        }
+        if (tid == 0) MLA_TRACE(14, t);
+        uint8_t* prow = sPOwn + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(prow + ((static_cast<uint32_t>(cc) ^ swz) << 4)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        // this warp's 32 P rows to the peer's receive buffer
+        if (lane == 0) bulk_copy_to_cluster(peer_p, smem_u32(sPOwn + warp * kWarpPBytes), kWarpPBytes, peer_recv_full);
+        if (tid == 0) MLA_TRACE(5, t);
+        alpha = ref_alpha(r_cur, r_t);
+        l_own = l_own * alpha + rowsum;
+        r_cur = r_t;
+      } else {
+        // ---- received tile: apply its reference now; its P V runs when its P lands
+        ok = warp_wait_cluster(&bars[R_FULL], recv_i & 1, abort_flag);
+        if (!ok) break;
+        if (tid == 0) mbar_arrive_expect_tx(&bars[R_FULL], kVecBytes);  // armed for the next message
+        // read (and use, so the load has completed) before the mailbox is released
+        const float r_t = __shfl_sync(0xffffffffu, sRefIn[r], lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(peer_r_free);
+        if (tid == 0) MLA_TRACE(10, t);
+        alpha = ref_alpha(r_cur, r_t);
+        l_own *= alpha;
+        r_cur = r_t;
       }
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O accumulated so far (through P V of the previous tile) times alpha
-        ok = warp_wait(&bars[P_FREE + (pb ^ 1)], ((t - 1) >> 1) & 1, abort_flag);
+      // O (through P V of the previous tile) to the new reference, then go
+      if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
+        ok = warp_wait(&bars[PV_DONE], (t - 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll 1
-        for (uint32_t c0 = 0; c0 < 256; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_base + kTmemO + c0, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-          tmem_st16(tmem + lane_base + kTmemO + c0, v);
-        }
-        tmem_wait_st();
+        rescale_o(taddr, alpha);
       }
-      // P row: 64 keys = eight 16-byte chunks of the 128-byte swizzled row
-      uint8_t* prow = sP + pb * kPBytes + r * 128;
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(prow + ((static_cast<uint32_t>(cc) ^ swz) << 4)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars[P_FULL + pb]);
-      if (tid == 0) MLA_TRACE(5, t);
+      if (mine) {
+        mbar_arrive(&bars[OWN_GO]);
+        if (tid == 0) MLA_TRACE(12, t);
+        ++own_i;
+      } else {
+        mbar_arrive(&bars[RECV_GO]);
+        if (tid == 0) MLA_TRACE(11, t);
+        ++recv_i;
+      }
+      const int b_here = c.b, u_here = c.u;
       cursor_next(p, P, c);
       if (!last) continue;
       if (c.valid) {
@@ -623,37 +777,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = warp_wait(&bars[Q_EMPTY], u_here & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        load_q_to_tmem(p, q, c.b, row, tmem + lane_base);
+        load_q_to_tmem(p, q, c.b, row, taddr);
         tc_fence_before();
         mbar_arrive(&bars[Q_FULL]);
       }
+      // ---- row sum of the unit: ours + the peer's, both relative to r_cur
+      if (units >= 1) {
+        ok = warp_wait_cluster(&bars[L_FREE], (units - 1) & 1, abort_flag);
+        if (!ok) break;
+      }
+      sLOut[r] = l_own;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) bulk_copy_to_cluster(peer_l, smem_u32(sLOut + 32 * warp), 32 * 4, peer_l_full);
+      ok = warp_wait_cluster(&bars[L_FULL], units & 1, abort_flag);
+      if (!ok) break;
+      if (tid == 0) mbar_arrive_expect_tx(&bars[L_FULL], kVecBytes);
+      const float l_peer = __shfl_sync(0xffffffffu, sLIn[r], lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(peer_l_free);
+      const float l_sum = l_own + l_peer;  // the same fp32 sum on both ranks
+      ++units;
       // ---- epilogue of this (unit, split)
+      // staging buffer: the own P buffer, free once both P V of our last own tile are done
       ok = warp_wait(&bars[O_FULL], u_here & 1, abort_flag);
+      if (ok && own_i >= 1) ok = warp_wait_cluster(&bars[OWN_FREE], (own_i - 1) & 1, abort_flag);
       if (!ok) break;
       tc_fence_after();
       const int s_begin = p.split_offset[b_here];
       const int nsplit = p.split_offset[b_here + 1] - s_begin;
       const int slot = s_begin + ((b_here == P.b0) ? P.s0 : 0);
       const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
-      const size_t orow = static_cast<size_t>(b_here) * p.rows + row;
-      const size_t arow = static_cast<size_t>(slot) * p.rows + row;
       const bool direct = (nsplit == 1);
       const bool bf16_out = direct && !p.out_fp32;
-      // O half -> global through the two P buffers (free: the unit's last P V
-      // has completed): each thread stages its row's 128 bytes of a column
-      // chunk, then the 128 threads store 16-byte pieces so that each warp
-      // writes whole 128-byte row segments.
+      // O half -> global through that buffer: each thread stages its row's
+      // 128 bytes of a column chunk, then the 128 threads store 16-byte pieces
+      // so that each warp writes whole 128-byte row segments.
       const int chunk_cols = bf16_out ? 64 : 32;  // 128 bytes of output per row
       const size_t base_row = direct ? static_cast<size_t>(b_here) * p.rows : static_cast<size_t>(slot) * p.rows;
+      uint8_t* stage = sPOwn;
 #pragma unroll 1
       for (int ch = 0; ch < 256 / chunk_cols; ++ch) {
-        uint8_t* stage = sP + (ch & 1) * kPBytes;
         uint32_t w[32];
         if (bf16_out) {
           uint32_t v[32];
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            tmem_ld32(tmem + lane_base + kTmemO + 64 * ch + 32 * hh, v);
+            tmem_ld32(taddr + kTmemO + 64 * ch + 32 * hh, v);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -663,11 +833,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          tmem_ld32(tmem + lane_base + kTmemO + 32 * ch, w);
+          tmem_ld32(taddr + kTmemO + 32 * ch, w);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * inv_l);
         }
+        named_bar_sync(1, 128);  // the previous chunk's stores have read the stage
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
           *reinterpret_cast<uint4*>(stage + r * 128 + ((static_cast<uint32_t>(cc) ^ swz) << 4)) =
@@ -689,27 +860,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       named_bar_sync(1, 128);  // staging reads done before the next unit writes P
-      (void)orow;
-      (void)arow;
       tc_fence_before();
       mbar_arrive(&bars[O_FREE]);
       if (tid == 0) MLA_TRACE(6, t);
       if (rank == 0 && row_ok) {
-        const size_t orow = static_cast<size_t>(b_here) * p.rows + row;
-        const size_t arow = static_cast<size_t>(slot) * p.rows + row;
-        const float lse = l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
+        const float lse = l_sum > 0.f ? (r_cur + __log2f(l_sum)) * kLn2 : -INFINITY;
         if (direct)
-          p.lse[orow] = lse;
+          p.lse[static_cast<size_t>(b_here) * p.rows + row] = lse;
         else
-          p.lse_accum[arow] = lse;
+          p.lse_accum[static_cast<size_t>(slot) * p.rows + row] = lse;
       }
     }
-    if (!ok && lane == 0) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+    if (!ok) {
+      if (lane == 0) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+      aborted = true;
+    }
+    r_seen = recv_i;
+    l_seen = units;
   }
 
   // ------------------------------------------------------------ teardown
+  // After a timeout the peer may still have a mailbox copy in flight to us:
+  // give the armed ones (bounded) time to land before the cluster can exit.
+  if (tid == 0 && (aborted || *abort_flag)) {
+    mbar_wait<true>(&bars[R_FULL], r_seen & 1, nullptr);
+    mbar_wait<true>(&bars[L_FULL], l_seen & 1, nullptr);
+  }
   tc_fence_before();
   __syncthreads();
+  cluster_arrive();  // the peer no longer touches this CTA's shared memory
+  cluster_wait();
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
