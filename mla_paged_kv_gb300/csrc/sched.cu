@@ -8,122 +8,180 @@
 // this library's plan (documented in include/mla_paged_kv.h):
 //   cost(unit) = tiles(unit) + F,  cap = ceil(sum cost / P) + F,
 // partitions take consecutive (unit, tile) ranges within their cap, the last
-// partition takes what is left.  The walk is inherently sequential and tiny
-// (n_units + num_parts steps), so one thread runs it; a block of threads
-// first turns the lengths into tile counts in shared memory when they fit.
+// partition takes what is left.
+//
+// One block.  The tile counts and the total cost come from all threads; the
+// greedy walk over the partitions is sequential (one thread, O(units +
+// partitions) steps, shared memory only); the per-unit split counts come from
+// a difference array written by the walk, and both prefix sums (counts, then
+// split offsets) are block-wide scans.
 #include "common.cuh"
 
 namespace mla {
 
+constexpr int kSchedThreads = 256;
 constexpr int kSchedMaxSmemUnits = 4096;
 
-__global__ void __launch_bounds__(256) sched_kernel(const int32_t* __restrict__ lengths, int default_length,
-                                                     int n_units, int num_parts, int fixed_cost,
-                                                     int32_t* __restrict__ sched, int32_t* __restrict__ split_offset) {
-  // tile counts and per-unit split counters live in shared memory when they
-  // fit, so the sequential walk below touches no global memory
-  __shared__ int s_nt[kSchedMaxSmemUnits];
-  __shared__ int s_touch[kSchedMaxSmemUnits];
-  __shared__ long long s_total;
-  const bool in_smem = n_units <= kSchedMaxSmemUnits;
-  if (threadIdx.x == 0) s_total = 0;
-  __syncthreads();
-  long long part = 0;
-  for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
-    const int len = lengths != nullptr ? lengths[u] : default_length;
-    const int nt = num_tiles(len);
-    if (in_smem) {
-      s_nt[u] = nt;
-      s_touch[u] = 0;
-    } else {
-      split_offset[u] = 0;
-    }
-    if (nt > 0) part += nt + fixed_cost;
+// Exclusive scan of one int per thread over the block; *total gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), static_cast<unsigned long long>(part));
+  if (lane == 31) s_warp[warp] = x;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    auto nt_of = [&](int u) -> int {
-      if (in_smem) return s_nt[u];
-      const int len = lengths != nullptr ? lengths[u] : default_length;
-      return num_tiles(len);
-    };
-    // per-unit "touched" counter: shared memory, or split_offset itself when too many units
-    int* touch = in_smem ? s_touch : reinterpret_cast<int*>(split_offset);
-    const long long total = s_total;
-    const long long cap = total > 0 ? (total + num_parts - 1) / num_parts + fixed_cost : 0;
-    int b = 0, t = 0;
-    for (int p = 0; p < num_parts; ++p) {
-      while (b < n_units && nt_of(b) == 0) {
-        ++b;
-        t = 0;
-      }
-      const int begin_b = b, begin_t = t;
-      const int begin_split = b < n_units ? touch[b] : 0;
-      if (p == num_parts - 1) {
-        b = n_units;
-        t = 0;
-      } else {
-        long long budget = cap;
-        while (b < n_units) {
-          const int nt = nt_of(b);
-          if (nt == 0) {
-            ++b;
-            t = 0;
-            continue;
-          }
-          const long long rem = nt - t;
-          if (rem + fixed_cost <= budget) {
-            budget -= rem + fixed_cost;
-            ++b;
-            t = 0;
-          } else {
-            const long long take = budget - fixed_cost;
-            if (take > 0) t += static_cast<int>(take);
-            break;
-          }
+  if (warp == 0) {
+    int w = lane < kSchedThreads / 32 ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kSchedThreads / 32) s_warp[lane] = w;  // inclusive warp prefix
+  }
+  __syncthreads();
+  const int base = warp > 0 ? s_warp[warp - 1] : 0;
+  *total = s_warp[kSchedThreads / 32 - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+// The greedy walk over the partitions (one thread).  NtOf is the tile count
+// of a unit (shared-memory array or a functor), Int the budget arithmetic
+// (32-bit when every budget fits).  Writes the partition table and the
+// difference array of the per-unit split counts.
+template <typename Int, typename NtOf>
+__device__ __forceinline__ void sched_walk(NtOf nt_of, int* diff, int n_units, int num_parts, int fixed_cost,
+                                           Int cap, int32_t* sched) {
+  int b = 0, t = 0;
+  // the last unit touched by an earlier partition, and by how many of them
+  int touch_unit = -1, touch_count = 0;
+  for (int p = 0; p < num_parts; ++p) {
+    while (b < n_units && nt_of[b] == 0) {
+      ++b;
+      t = 0;
+    }
+    const int begin_b = b, begin_t = t;
+    const int begin_split = (b < n_units && b == touch_unit) ? touch_count : 0;
+    if (p == num_parts - 1) {
+      b = n_units;
+      t = 0;
+    } else {
+      Int budget = cap;
+      while (b < n_units) {
+        const int nt = nt_of[b];
+        if (nt == 0) {
+          ++b;
+          t = 0;
+          continue;
+        }
+        const Int rem = static_cast<Int>(nt - t);
+        if (rem + fixed_cost <= budget) {
+          budget -= rem + fixed_cost;
+          ++b;
+          t = 0;
+        } else {
+          const Int take = budget - fixed_cost;
+          if (take > 0) t += static_cast<int>(take);
+          break;
         }
       }
-      const int end_b = b, end_t = t;
-      if (begin_b != end_b || begin_t != end_t) {
-        const int last = end_t > 0 ? end_b : end_b - 1;
-        for (int bb = begin_b; bb <= last && bb < n_units; ++bb)
-          if (nt_of(bb) > 0) touch[bb] += 1;
-      }
-      int4* e = reinterpret_cast<int4*>(sched + p * MLA_SCHED_INTS);
-      e[0] = make_int4(begin_b, begin_t, end_b, end_t);
-      e[1] = make_int4(begin_split, 0, 0, 0);
     }
-    if (in_smem) {
-      for (int u = 0; u < n_units; ++u) split_offset[u] = s_touch[u];
+    const int end_b = b, end_t = t;
+    if (begin_b != end_b || begin_t != end_t) {
+      const int last = min(end_t > 0 ? end_b : end_b - 1, n_units - 1);
+      diff[begin_b] += 1;
+      diff[last + 1] -= 1;
+      touch_count = (last == begin_b) ? begin_split + 1 : 1;
+      touch_unit = last;
     }
+    int4* e = reinterpret_cast<int4*>(sched + p * MLA_SCHED_INTS);
+    e[0] = make_int4(begin_b, begin_t, end_b, end_t);
+    e[1] = make_int4(begin_split, 0, 0, 0);
+  }
+}
+
+// Tile count of unit u straight from the lengths (for the many-units path).
+struct NtFromLengths {
+  const int32_t* lengths;
+  int default_length;
+  __device__ __forceinline__ int operator[](int u) const {
+    return num_tiles(lengths != nullptr ? lengths[u] : default_length);
+  }
+};
+
+__global__ void __launch_bounds__(kSchedThreads) sched_kernel(const int32_t* __restrict__ lengths,
+                                                               int default_length, int n_units, int num_parts,
+                                                               int fixed_cost, int32_t* __restrict__ sched,
+                                                               int32_t* __restrict__ split_offset) {
+  __shared__ int s_nt[kSchedMaxSmemUnits];
+  __shared__ int s_diff[kSchedMaxSmemUnits + 1];
+  __shared__ long long s_warp_cost[kSchedThreads / 32];
+  __shared__ int s_warp[kSchedThreads / 32];
+  const bool in_smem = n_units <= kSchedMaxSmemUnits;
+  // difference array of the per-unit split counts: shared memory, or the
+  // output array itself when there are too many units
+  int* diff = in_smem ? s_diff : reinterpret_cast<int*>(split_offset);
+  const NtFromLengths nt_of{lengths, default_length};
+
+  long long part = 0;
+  for (int u = threadIdx.x; u < n_units; u += kSchedThreads) {
+    const int nt = num_tiles(lengths != nullptr ? lengths[u] : default_length);
+    if (in_smem) s_nt[u] = nt;
+    diff[u] = 0;
+    if (nt > 0) part += nt + fixed_cost;
+  }
+  if (threadIdx.x == 0) diff[n_units] = 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if ((threadIdx.x & 31) == 0) s_warp_cost[threadIdx.x >> 5] = part;
+  __syncthreads();
+
+  if (threadIdx.x == 0) {
+    long long total = 0;
+    for (int w = 0; w < kSchedThreads / 32; ++w) total += s_warp_cost[w];
+    const long long cap = total > 0 ? (total + num_parts - 1) / num_parts + fixed_cost : 0;
+    if (in_smem && cap < (1LL << 30))
+      sched_walk<int, int*>(s_nt, s_diff, n_units, num_parts, fixed_cost, static_cast<int>(cap), sched);
+    else
+      sched_walk<long long>(nt_of, diff, n_units, num_parts, fixed_cost, cap, sched);
   }
   __syncthreads();
-  // exclusive prefix sum of the counts (one warp; n_units is small)
-  if (threadIdx.x < 32) {
-    int carry = 0;
-    for (int base = 0; base < n_units; base += 32) {
-      const int u = base + threadIdx.x;
-      const int c = u < n_units ? (in_smem ? s_touch[u] : split_offset[u]) : 0;
-      int x = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (threadIdx.x >= o) x += y;
-      }
-      __syncwarp();
-      if (u < n_units) split_offset[u] = carry + x - c;
-      carry += __shfl_sync(0xffffffffu, x, 31);
-      __syncwarp();
-    }
-    if (threadIdx.x == 0) split_offset[n_units] = carry;
+
+  // each thread scans a contiguous chunk of units
+  const int chunk = (n_units + kSchedThreads - 1) / kSchedThreads;
+  const int u0 = min(static_cast<int>(threadIdx.x) * chunk, n_units);
+  const int u1 = min(u0 + chunk, n_units);
+  int total = 0;
+  // pass 1: split count of unit u = (prefix sum of diff)[u], for units with tiles
+  int local = 0;
+  for (int u = u0; u < u1; ++u) local += diff[u];
+  int run = block_exclusive_scan(local, s_warp, &total);
+  int csum = 0;
+  for (int u = u0; u < u1; ++u) {
+    run += diff[u];
+    const int count = (in_smem ? s_nt[u] : nt_of[u]) > 0 ? run : 0;
+    diff[u] = count;
+    csum += count;
   }
+  __syncthreads();
+  // pass 2: split_offset = exclusive prefix sum of the counts
+  int off = block_exclusive_scan(csum, s_warp, &total);
+  for (int u = u0; u < u1; ++u) {
+    const int count = diff[u];
+    split_offset[u] = off;
+    off += count;
+  }
+  if (threadIdx.x == 0) split_offset[n_units] = total;
 }
 
 cudaError_t launch_sched(const int32_t* lengths, int default_length, int n_units, int num_parts,
                          int32_t* sched, int32_t* split_offset, cudaStream_t stream) {
-  sched_kernel<<<1, 256, 0, stream>>>(lengths, default_length, n_units, num_parts, MLA_SPLIT_FIXED_COST, sched,
-                                      split_offset);
+  sched_kernel<<<1, kSchedThreads, 0, stream>>>(lengths, default_length, n_units, num_parts, MLA_SPLIT_FIXED_COST,
+                                                sched, split_offset);
   return cudaGetLastError();
 }
 
