@@ -26,19 +26,29 @@
 //  * The value scale is folded into P: rank c multiplies P by scale_g[j] for
 //    each of its two groups and runs one N=128 PV product per group against
 //    the unscaled codes.
-//  * A producer warpgroup gathers the selected records (plain 8- and 16-byte
-//    loads through the index list) into 128-byte-swizzled tiles in a 2-stage
-//    ring; Q comes by TMA.  One elected thread issues every tcgen05.mma.
+//  * Three producer warps gather the selected records into 128-byte-swizzled
+//    tiles in a 2-stage ring: the tile's 64 slot indices first go to a small
+//    shared table, then the records of the next tile are loaded while the
+//    current one is converted (two tiles of scattered loads in flight).
+//    Q comes by TMA.  One elected thread issues every tcgen05.mma.
 //  * Online softmax in the log2 domain with a lazy rescale of O (only when
 //    the running max grows by more than 2^8).
-// Roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane), warps 4-7
-// gather producer, warp 8 MMA issuer and TMEM owner.
+// Roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane), warps 4-6
+// gather producer, warp 7 MMA issuer and TMEM owner.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
+
+// Timeline hooks: empty in the library; an instrumented build defines
+// MLA_TRACE(event, tile) to record timestamps.
+#ifndef MLA_TRACE
+#define MLA_TRACE(ev, tile) \
+  do {                       \
+  } while (0)
+#endif
 
 namespace mla {
 namespace sp {
@@ -58,7 +68,10 @@ constexpr int kOffKV = kOffQ + kMaxBoxes * kQBoxBytes;
 constexpr int kOffX = kOffKV + kStages * kStageBytes;
 constexpr int kOffP = kOffX + kXBytes;
 constexpr int kOffScale = kOffP + 2 * kPGroupBytes;
-constexpr int kOffBar = kOffScale + kStages * kScaleStageBytes;
+constexpr int kOffIdx = kOffScale + kStages * kScaleStageBytes;  // [2][64] record index or -1 (producer only)
+constexpr int kVisSlots = 4;
+constexpr int kOffVis = kOffIdx + 2 * kT * 4;                     // [4] 64-bit valid-slot masks
+constexpr int kOffBar = kOffVis + kVisSlots * 8;
 constexpr int kNumBars = 21;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 16;
@@ -70,7 +83,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
 constexpr uint32_t kTmemS = 256;  // score accumulators: A_{2c}, A_{2c+1}, RoPE (rank 0), 64 columns each
 
-constexpr int kProducerWarps = 4;
+constexpr int kProducerWarps = 3;
 constexpr int kMmaWarp = 4 + kProducerWarps;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
 
@@ -186,23 +199,20 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
   return __all_sync(0xffffffffu, mbar_wait<true>(bar, parity, abort_flag));
 }
 
-// 8 E4M3 codes -> 8 bf16 of the same values (E4M3 -> f16 -> f32 -> bf16 is
-// exact at every step: 3 mantissa bits, exponents within bf16's range).
+// Two E4M3 codes (bytes 0 and 1 of `pair`) -> two bf16 of the same values
+// (low half = byte 0): E4M3 -> f16 -> f32 -> bf16 is exact at every step
+// (3 mantissa bits, exponents well inside both formats).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t pair) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair & 0xFFFFu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// 8 E4M3 codes -> 8 bf16 of the same values.
 __device__ __forceinline__ uint4 codes_to_bf16(uint2 codes) {
-  uint32_t w[4];
-  const uint32_t src[2] = {codes.x, codes.y};
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const __nv_fp8x2_storage_t two = static_cast<__nv_fp8x2_storage_t>((src[h] >> (16 * q)) & 0xFFFFu);
-      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-      w[2 * h + q] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
+  return make_uint4(e4m3x2_to_bf16x2(codes.x), e4m3x2_to_bf16x2(codes.x >> 16), e4m3x2_to_bf16x2(codes.y),
+                    e4m3x2_to_bf16x2(codes.y >> 16));
 }
 
 // Validity of selection entry t of unit b (L = candidate slots of the unit).
@@ -217,6 +227,22 @@ __device__ __forceinline__ bool sparse_valid(const DecodeParams& p, int b, int t
     return false;
   }
   return true;
+}
+
+// Selection entry t of unit b as stored (no check yet); -1 past the list.
+__device__ __forceinline__ int load_slot(const DecodeParams& p, int b, int t, int L) {
+  return t < L ? __ldg(p.indices + static_cast<size_t>(b) * p.topk + t) : -1;
+}
+
+// A stored entry -> record index, or -1 when masked; an entry outside the
+// pool (other than -1) is reported.
+__device__ __forceinline__ int resolve_slot(const DecodeParams& p, int idx) {
+  if (idx == -1) return -1;
+  if (idx < 0 || idx >= p.num_pages * kT) {
+    report(p.status, MLA_ERR_BAD_INDEX);
+    return -1;
+  }
+  return idx;
 }
 
 // Q/KV box lb of rank `rank` -> first latent dim it holds.
@@ -269,6 +295,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sX = smem + kOffX;
   uint8_t* sP = smem + kOffP;
   float* sScale = reinterpret_cast<float*>(smem + kOffScale);  // [stage][2 groups][64 keys]
+  int* sIdx = reinterpret_cast<int*>(smem + kOffIdx);           // [tile & 1][64 slots]
+  uint32_t* sVis = reinterpret_cast<uint32_t*>(smem + kOffVis);  // [tile & 3][2 halves]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -297,11 +325,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[O_FULL], 1);
     mbar_init(&bars[O_FREE], 128);
     for (int w = 0; w < 4; ++w) {
-      mbar_init(&bars[X_FULL + w], 32);
-      mbar_init(&bars[X_FREE + w], 32);
+      mbar_init(&bars[X_FULL + w], 1);
+      mbar_init(&bars[X_FREE + w], 1);
     }
     mbar_init(&bars[DRAIN], 1);
     fence_mbar_init_cluster();
+    // armed for the peer's first partial scores (32 rows x 64 fp32 per warp)
+    for (int w = 0; w < 4; ++w) mbar_arrive_expect_tx(&bars[X_FULL + w], 32 * kT * 4);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -320,13 +350,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp >= 4 && warp < kMmaWarp) {
     // ------------------------------------------------------------ producer
-    const int ptid = tid - 128;  // 0 .. 127
+    const int ptid = tid - 128;  // 0 .. 32 * kProducerWarps - 1
     const uint64_t pol_q = policy_evict_last();
-    // chunks of 8 dims per key: 32 NoPE chunks of the rank's two groups, plus
-    // 8 RoPE chunks on rank 0
-    const int nc = rank == 0 ? 40 : 32;
+    // 16-byte chunks per key: 16 NoPE chunks (16 E4M3 codes each) of the
+    // rank's two groups, plus 8 RoPE chunks (8 bf16 each) on rank 0
+    const int nck = rank == 0 ? 24 : 16;
     const int nope0 = 256 * static_cast<int>(rank);
-    constexpr int kPerMax = kT * 40 / (32 * kProducerWarps);  // 20
+    constexpr int kPerMax = (kT * 24 + 32 * kProducerWarps - 1) / (32 * kProducerWarps);  // 16
     uint32_t t = 0;
     int u = 0;
     bool ok = true;
@@ -347,46 +377,96 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ++q_issued;
         }
       }
-      for (int k = lo; ok && k < hi; ++k, ++t) {
-        const int st = t & 1;
-        if (t >= 2) ok = mbar_wait(&bars[KV_EMPTY + st], ((t - 2) >> 1) & 1, abort_flag);
-        if (!ok) break;
-        uint4 raw[kPerMax];
-        float sc[kPerMax];
+      if (named_bar_or(2, 32 * kProducerWarps, !ok)) {
+        ok = false;
+        break;
+      }
+      // Software pipeline over the unit's tiles: the record loads of tile k+1
+      // are issued before tile k is converted, so two tiles' scattered record
+      // loads are in flight while one is being written.
+      uint4 raw[kPerMax];
+      float sc[kPerMax];
+      // phase 1 for tile tt: its 64 slot entries (loaded earlier, see below)
+      // -> record index or -1, and the tile's valid-slot mask for the softmax
+      auto publish_indices = [&](int entry, uint32_t tt) {
+        named_bar_sync(1, 32 * kProducerWarps);  // the slot's previous tile is no longer read
+        if (ptid < kT) {
+          const int idx = resolve_slot(p, entry);
+          sIdx[(tt & 1) * kT + ptid] = idx;
+          const uint32_t half = __ballot_sync(0xffffffffu, idx >= 0);
+          if (lane == 0) sVis[(tt & (kVisSlots - 1)) * 2 + (ptid >> 5)] = half;
+        }
+        named_bar_sync(1, 32 * kProducerWarps);
+      };
+      // phase 2 for tile tt: every chunk's loads (a masked slot reads record 0)
+      auto issue_loads = [&](uint32_t tt, uint4 (&rr)[kPerMax], float (&ss)[kPerMax]) {
+        const int* idx_t = sIdx + (tt & 1) * kT;
 #pragma unroll
         for (int i = 0; i < kPerMax; ++i) {
           const int q = ptid + 32 * kProducerWarps * i;
-          const int key = q / nc, c = q - nc * (q / nc);
-          raw[i] = make_uint4(0u, 0u, 0u, 0u);
-          sc[i] = 0.f;
-          int idx;
-          if (key < kT && sparse_valid(p, b, k * kT + key, L, idx)) {
-            const uint8_t* rec = p.kv8 + static_cast<size_t>(idx) * MLA_RECORD_BYTES;
-            if (c < 32) {
-              const int d = nope0 + 8 * c;
-              const uint2 v = __ldg(reinterpret_cast<const uint2*>(rec + d));
-              raw[i] = make_uint4(v.x, v.y, 0u, 0u);
-              sc[i] = __ldg(reinterpret_cast<const float*>(rec + 512) + (d >> 7));
-            } else {
-              raw[i] = __ldg(reinterpret_cast<const uint4*>(rec + 528 + 16 * (c - 32)));
-            }
-          }
+          const int key = min(q / nck, kT - 1), c = q - nck * (q / nck);
+          const int idx = idx_t[key];
+          const uint8_t* rec = p.kv8 + static_cast<size_t>(max(idx, 0)) * MLA_RECORD_BYTES;
+          const int off = c < 16 ? nope0 + 16 * c : 528 + 16 * (c - 16);
+          rr[i] = __ldg(reinterpret_cast<const uint4*>(rec + off));
+          ss[i] = __ldg(reinterpret_cast<const float*>(rec + 512) + ((nope0 + 16 * min(c, 15)) >> 7));
         }
+      };
+      // slot entries are loaded two tiles ahead of their records, so that no
+      // tile waits for an index load
+      int entry = ptid < kT ? load_slot(p, b, lo * kT + ptid, L) : -1;
+      int entry_n = (ptid < kT && lo + 1 < hi) ? load_slot(p, b, (lo + 1) * kT + ptid, L) : -1;
+      publish_indices(entry, t);
+      issue_loads(t, raw, sc);
+      for (int k = lo; ok && k < hi; ++k, ++t) {
+        const int st = t & 1;
+        uint4 raw_n[kPerMax];
+        float sc_n[kPerMax];
+        if (k + 1 < hi) {
+          publish_indices(entry_n, t + 1);
+          entry_n = (ptid < kT && k + 2 < hi) ? load_slot(p, b, (k + 2) * kT + ptid, L) : -1;
+          issue_loads(t + 1, raw_n, sc_n);
+        }
+        bool failed = false;
+        if (t >= 2) failed = !mbar_wait(&bars[KV_EMPTY + st], ((t - 2) >> 1) & 1, abort_flag);
+        // one decision for the whole producer group: its named barriers need every thread
+        if (named_bar_or(2, 32 * kProducerWarps, failed)) {
+          ok = false;
+          break;
+        }
+        if (ptid == 0) MLA_TRACE(0, t);
+        const int* idx_t = sIdx + (t & 1) * kT;
         uint8_t* stage = sKV + st * kStageBytes;
         float* scale_st = sScale + st * (2 * kT);
 #pragma unroll
         for (int i = 0; i < kPerMax; ++i) {
           const int q = ptid + 32 * kProducerWarps * i;
-          const int key = q / nc, c = q - nc * (q / nc);
+          const int key = q / nck, c = q - nck * (q / nck);
           if (key < kT) {
-            const uint4 outv = c < 32 ? codes_to_bf16(make_uint2(raw[i].x, raw[i].y)) : raw[i];
-            const int lb = c >> 3, cc = c & 7;
-            *reinterpret_cast<uint4*>(stage + lb * kBoxBytes + key * 128 + ((cc ^ (key & 7)) << 4)) = outv;
-            if (c < 32 && (c & 15) == 0) scale_st[(c >> 4) * kT + key] = sc[i];
+            const bool live = idx_t[key] >= 0;
+            const uint4 w = live ? raw[i] : make_uint4(0u, 0u, 0u, 0u);
+            uint8_t* row = stage + key * 128;
+            const uint32_t swz = static_cast<uint32_t>(key & 7);
+            if (c < 16) {
+              // 16 codes -> 16 bf16: two 16-byte pieces of box c/4, columns 2(c%4), 2(c%4)+1
+              uint8_t* box = row + (c >> 2) * kBoxBytes;
+              const uint32_t cc = 2u * static_cast<uint32_t>(c & 3);
+              *reinterpret_cast<uint4*>(box + ((cc ^ swz) << 4)) = codes_to_bf16(make_uint2(w.x, w.y));
+              *reinterpret_cast<uint4*>(box + (((cc + 1u) ^ swz) << 4)) = codes_to_bf16(make_uint2(w.z, w.w));
+              if ((c & 7) == 0) scale_st[(c >> 3) * kT + key] = live ? sc[i] : 0.f;
+            } else {
+              *reinterpret_cast<uint4*>(row + 4 * kBoxBytes + ((static_cast<uint32_t>(c - 16) ^ swz) << 4)) = w;
+            }
           }
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars[KV_FULL + st]);
+        if (ptid == 0) MLA_TRACE(1, t);
+#pragma unroll
+        for (int i = 0; i < kPerMax; ++i) {
+          raw[i] = raw_n[i];
+          sc[i] = sc_n[i];
+        }
       }
       ++u;
     }
@@ -419,6 +499,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (ready) {
             tc_fence_after();
             const int st = cv.t & 1;
+            MLA_TRACE(2, cv.t);
             issue_pv(tmem, p_desc0, v_desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4), idesc_pv, first);
             umma_commit(&bars[P_FREE]);
             umma_commit(&bars[KV_EMPTY + st]);
@@ -435,6 +516,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (ready && cq.t >= 1) ready = mbar_test_wait(&bars[S_FREE], (cq.t - 1) & 1);
           if (ready) {
             tc_fence_after();
+            MLA_TRACE(3, cq.t);
             const uint64_t kvs = kv_desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
             if (rank == 0)
               issue_qk<3>(tmem, q_desc0, kvs, idesc_qk);
@@ -485,20 +567,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool row_ok = row < p.rows;
       float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and fp32 row sum
       for (int k = lo; ok && k < hi; ++k, ++t) {
-        // which of the tile's 64 slots are valid (the same for every row)
-        uint64_t vis_mask;
-        {
-          int idx;
-          const bool v0 = sparse_valid(p, b, k * kT + lane, L, idx);
-          const bool v1 = sparse_valid(p, b, k * kT + 32 + lane, L, idx);
-          vis_mask = static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
-                     (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
-        }
         const int st = t & 1;
-        // the stage's scales: visible once its KV_FULL phase has completed
+        // the tile's valid-slot mask and scales: visible once its KV_FULL phase has completed
         ok = warp_wait(&bars[KV_FULL + st], (t >> 1) & 1, abort_flag);
-        if (ok) ok = warp_wait(&bars[S_FULL], t & 1, abort_flag);
         if (!ok) break;
+        // which of the tile's 64 slots are valid (the same for every row)
+        const uint64_t vis_mask = static_cast<uint64_t>(sVis[(t & (kVisSlots - 1)) * 2]) |
+                                  (static_cast<uint64_t>(sVis[(t & (kVisSlots - 1)) * 2 + 1]) << 32);
+        ok = warp_wait(&bars[S_FULL], t & 1, abort_flag);
+        if (!ok) break;
+        if (tid == 0) MLA_TRACE(4, t);
         tc_fence_after();
         const uint32_t sc_base = smem_u32(sScale + st * (2 * kT));
         // partial score of this rank: sum over its groups of scale_g[j] * A_g[j] (+ RoPE)
@@ -534,13 +612,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = warp_wait_cluster(&bars[X_FREE + warp], (t - 1) & 1, abort_flag);
           if (!ok) break;
         }
+        // asynchronous remote stores; their bytes complete the peer's X_FULL
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          st_cluster_v4(x_remote + ((static_cast<uint32_t>(c) ^ swz) << 4), s[4 * c], s[4 * c + 1], s[4 * c + 2],
-                        s[4 * c + 3]);
-        mbar_arrive_remote(xfull_remote);
+          st_async_v4(x_remote + ((static_cast<uint32_t>(c) ^ swz) << 4), s[4 * c], s[4 * c + 1], s[4 * c + 2],
+                      s[4 * c + 3], xfull_remote);
+        if (tid == 0) MLA_TRACE(5, t);
         ok = warp_wait_cluster(&bars[X_FULL + warp], t & 1, abort_flag);
         if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars[X_FULL + warp], 32 * kT * 4);  // armed for the next tile
+        if (tid == 0) MLA_TRACE(6, t);
         // full score = own partial + peer's partial (one fp32 add: the same bits on both ranks)
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -550,7 +631,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s[4 * c + 2] += o.z;
           s[4 * c + 3] += o.w;
         }
-        mbar_arrive_remote(xfree_remote);
+        __syncwarp();  // every lane has consumed its row (the adds above used the loads)
+        if (lane == 0) mbar_arrive_remote(xfree_remote);
         // mask, scale into the log2 domain, tile max
         float mt = -INFINITY;
 #pragma unroll
@@ -615,6 +697,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bars[P_FULL]);
+        if (tid == 0) MLA_TRACE(7, t);
       }
       if (!ok) break;
       // ---- epilogue of this (unit, split)
@@ -668,7 +751,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       ++u;
     }
-    if (!ok && lane == 0) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+    if (!ok && lane == 0) {
+      set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+      // partial scores the peer already sent may still be landing here
+      mbar_wait<true>(&bars[X_FULL + warp], t & 1, nullptr);
+    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -702,17 +789,13 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
   if (c < 64) {
     const uint2 codes = *reinterpret_cast<const uint2*>(rec + 8 * c);
     const float scale = reinterpret_cast<const float*>(rec + 512)[c >> 4];
-    const uint32_t src[2] = {codes.x, codes.y};
+    const uint4 b = codes_to_bf16(codes);
+    const uint32_t ws[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const __nv_fp8x2_storage_t two = static_cast<__nv_fp8x2_storage_t>((src[h] >> (16 * q)) & 0xFFFFu);
-        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
-        const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-        f[4 * h + 2 * q] = __fmul_rn(v.x, scale);
-        f[4 * h + 2 * q + 1] = __fmul_rn(v.y, scale);
-      }
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __fmul_rn(__uint_as_float(ws[i] << 16), scale);
+      f[2 * i + 1] = __fmul_rn(__uint_as_float(ws[i] & 0xFFFF0000u), scale);
+    }
   } else {
     const uint4 w = *reinterpret_cast<const uint4*>(rec + 528 + 16 * (c - 64));
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};

@@ -137,6 +137,21 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also ORs a predicate over its `nthreads` threads: every
+// participant gets the same result (keeps a thread group's decisions uniform).
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %3, 0;\n\t"
+      "bar.red.or.pred p, %1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(nthreads), "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- cluster
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -166,6 +181,17 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
 
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory (address from
+// mapa); completion is signalled as 16 transaction bytes on that CTA's
+// mbarrier (also from mapa).  The issuing thread does not wait for it.
+__device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, float a, float b, float c, float d,
+                                            uint32_t mbar_cluster) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   dst_cluster),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar_cluster)
+               : "memory");
 }
 
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from

@@ -119,3 +119,28 @@ def test_unpack_is_bit_exact():
     assert bad == 1 and int(status.item()) == 5
     got = k.cpu().numpy()
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_unpack_every_e4m3_code():
+    # two pages of records whose 512 code bytes run through all 256 codes
+    # (except the two NaN codes), with scales that are powers of two and
+    # arbitrary fp32 values, so the product is checked bit for bit
+    n = 128
+    kv8 = torch.zeros(2, 64, 656, dtype=torch.uint8)
+    flat = kv8.view(n, 656)
+    codes = torch.arange(512, dtype=torch.int64) % 256
+    codes[codes == 0x7F] = 0x7E
+    codes[codes == 0xFF] = 0xFE
+    for r in range(n):
+        flat[r, :512] = torch.roll(codes, shifts=r).to(torch.uint8)
+        sc = torch.tensor([1.0, 0.5 ** (r % 9), 3.0517578125e-05 * (r + 1), 1.7 + r], dtype=torch.float32)
+        flat[r, 512:528] = sc.view(torch.uint8)
+        flat[r, 528:656] = torch.randn(64, generator=torch.Generator().manual_seed(r)).to(torch.bfloat16).view(torch.uint8)
+    idx = torch.arange(n, dtype=torch.int32)
+    k = torch.full((n, 576), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_sparse_fp8_unpack(kv8.cuda(), idx.cuda(), k, status)
+    torch.cuda.synchronize()
+    ref, bad = orc.unpack_records(kv8.numpy(), idx.numpy())
+    assert bad == 0 and int(status.item()) == 0
+    assert np.array_equal(k.cpu().numpy().view(np.uint32), ref.view(np.uint32))
