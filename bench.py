@@ -237,8 +237,37 @@ def time_other_workloads(mla, wl, timed, steps):
         res[name] = {"us_per_call": us, "gb_per_s": nbytes / (us * 1e-6) / 1e9, "bytes_per_call": nbytes,
                      "bytes": "valid records x 656" if sparse else "sum of cache_seqlens x 1152",
                      "num_parts": pl.num_parts, "splits": int(pl.split_offset[-1].item())}
+        if sparse:
+            res[name + "_packed"] = time_packed(mla, case, q, kv8, ind, tl, pl, out, lse, status, timed, steps)
         del q, out, lse, fn
         torch.cuda.empty_cache()
+    return res
+
+
+def time_packed(mla, case, q, kv8, ind, tl, pl, out, lse, status, timed, steps):
+    """Packed selected-KV path on the sparse workload: µs of the pack and of the
+    packed attention (decode + combine), each timed alone with L2 flushed."""
+    import torch
+    B, s_q, topk = ind.shape
+    packed = torch.empty(mla.mla_packed_kv_workspace_bytes(B * s_q, topk), dtype=torch.uint8, device="cuda")
+
+    def pack():
+        mla.mla_pack_selected_kv(kv8, ind, tl, packed, status)
+
+    def attend():
+        mla.mla_sparse_fp8_packed_decode_fwd(q, packed, topk, tl, pl.sched, pl.split_offset, pl.num_parts,
+                                             pl.workspace, out, lse, status, case.scale)
+    res = {}
+    for key, fn in (("pack", pack), ("packed_attention", attend)):
+        for _ in range(5):
+            fn()
+        res[key + "_us"] = 1e3 * statistics.mean(timed(fn, steps))
+    mla.check_status(status, "packed path")
+    nvalid = int((ind >= 0).sum().item())
+    res["pack_bytes"] = nvalid * 656 * 2 + packed.numel() - nvalid * 656
+    res["pack_gb_per_s"] = res["pack_bytes"] / (res["pack_us"] * 1e-6) / 1e9
+    res["bytes_pack"] = "valid records read + whole packed workspace written"
+    del packed
     return res
 
 

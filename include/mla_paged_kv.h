@@ -199,6 +199,53 @@ int mla_sparse_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, int num_pag
                               int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out,
                               float* d_lse, int32_t* d_status, mla_stream_t stream);
 
+/* Packed selected-KV path (FlashMLA PR #200, "[SM90] Add packed selected-KV
+ * sparse decode": Summary, Motivation, "SM90 packing kernel", "Packed
+ * attention specialization").  The selection is resolved once, ahead of the
+ * attention, by mla_pack_selected_kv, which copies every selected record
+ * byte for byte into a caller-owned workspace; the packed attention then
+ * reads records at fixed positions, with no index load, check or page
+ * translation.  The two calls are separate so a caller can run the pack on
+ * another stream, overlapped with earlier work, and order it before the
+ * attention with an event.
+ *
+ * Packed workspace (opaque to callers; fixed here so tests can check it):
+ *   tiles = ceil(topk / 64), n_units = batch * s_q.
+ *   records: uint8 [n_units, tiles, 64, 656]; slot t of unit u at record
+ *            u * tiles * 64 + t.  Valid slots hold the selected record's 656
+ *            bytes, every other slot (past topk_length, index -1, a bad
+ *            index, the padding up to tiles * 64) holds 656 zero bytes.
+ *   masks:   uint64 [n_units, tiles], right after the records; bit j of
+ *            mask [u][k] is set iff slot 64k + j of unit u is valid.
+ * The pages pack a valid prefix and zero-fill its suffix; the per-tile masks
+ * here also carry -1 entries inside the prefix, so the packed result equals
+ * the native sparse result for every selection the native call accepts. */
+size_t mla_packed_kv_workspace_bytes(int n_units, int topk);
+
+/* Pack the selection of every query token into the packed workspace.
+ *   d_kv8, num_pages, d_indices, topk, d_topk_length: as for
+ *                 mla_sparse_fp8_decode_fwd; n_units = batch * s_q.
+ *   d_packed      16-byte aligned, >= mla_packed_kv_workspace_bytes(n_units,
+ *                 topk) bytes; every byte of that size is written.
+ * An index outside [-1, num_pages*64) is packed as masked and reported in
+ * *d_status as MLA_ERR_BAD_INDEX (stream-ordered). */
+int mla_pack_selected_kv(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int topk,
+                         const int32_t* d_topk_length, int n_units, void* d_packed, size_t packed_bytes,
+                         int32_t* d_status, mla_stream_t stream);
+
+/* Sparse FP8 decode over a packed workspace: the same result as
+ * mla_sparse_fp8_decode_fwd with the selection that was packed (bit for bit
+ * under the same plan: the same kernel runs, its records found through the
+ * masks).  d_topk_length must be the one given to the pack (it counts the
+ * tiles each unit schedules); the plan comes from mla_get_metadata exactly as
+ * for the native call (the pages' H=128 packed path keeps the native
+ * scheduler).  Other arguments as for mla_sparse_fp8_decode_fwd. */
+int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size_t packed_bytes, int topk,
+                                     const int32_t* d_topk_length, int batch, int s_q, int h_q, float softmax_scale,
+                                     const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
+                                     void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
+                                     int32_t* d_status, mla_stream_t stream);
+
 /* Gather + unpack of selected records to fp32 key rows, bit-exact:
  * k[d] = fp32(e4m3[d]) * scale[d/128] as one fp32 round-to-nearest-even
  * multiply (d < 512), k[512+e] = fp32(bf16 rope[e]).  Index -1 or an index

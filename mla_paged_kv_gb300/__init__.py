@@ -24,15 +24,17 @@ from .build import LIB_PATH
 __all__ = [
     "MlaError", "load_library", "mla_status_string", "mla_num_parts", "mla_workspace_bytes",
     "mla_get_metadata", "mla_decode_fwd", "mla_decode_splits", "mla_combine",
-    "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws", "plan", "decode",
-    "sparse_decode",
+    "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws",
+    "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd", "plan", "decode",
+    "sparse_decode", "pack_selected_kv", "packed_sparse_decode",
     "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_num_parts", "mla_workspace_bytes", "mla_get_metadata", "mla_decode_fwd",
     "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack",
-    "mla_decode_fwd_static_ws",
+    "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv",
+    "mla_sparse_fp8_packed_decode_fwd",
 )
 
 _P = ctypes.c_void_p
@@ -54,6 +56,10 @@ _SIGS = {
     "mla_sparse_fp8_unpack": (_I, [_P, _I, _P, _I, _P, _P, _P]),
     "mla_decode_fwd_static_ws": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _F, _P, _P, _I, _P, _I, _P, _P,
                                       _P]),
+    "mla_packed_kv_workspace_bytes": (_SZ, [_I, _I]),
+    "mla_pack_selected_kv": (_I, [_P, _I, _P, _I, _P, _I, _P, _SZ, _P, _P]),
+    "mla_sparse_fp8_packed_decode_fwd": (_I, [_P, _P, _SZ, _I, _P, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _P, _P,
+                                              _P]),
 }
 
 _lib = None
@@ -232,6 +238,38 @@ def mla_sparse_fp8_unpack(kv8, indices, k_out, status, stream=None):
                                                 _ptr(status), _stream(stream)), "mla_sparse_fp8_unpack")
 
 
+def mla_packed_kv_workspace_bytes(n_units: int, topk: int) -> int:
+    return int(load_library().mla_packed_kv_workspace_bytes(int(n_units), int(topk)))
+
+
+def mla_pack_selected_kv(kv8, indices, topk_length, packed, status, stream=None):
+    _need(kv8, torch.uint8, "kv8", 3)
+    _need(indices, torch.int32, "indices", 3)
+    if topk_length is not None:
+        _need(topk_length, torch.int32, "topk_length", 2)
+    _need(packed, torch.uint8, "packed")
+    B, s_q, topk = indices.shape
+    _check(load_library().mla_pack_selected_kv(_ptr(kv8), kv8.shape[0], _ptr(indices), topk, _ptr(topk_length),
+                                               B * s_q, _ptr(packed), packed.numel(), _ptr(status),
+                                               _stream(stream)), "mla_pack_selected_kv")
+
+
+def mla_sparse_fp8_packed_decode_fwd(q, packed, topk, topk_length, sched, split_offset, num_parts, workspace, out,
+                                     lse, status, softmax_scale=1.0 / 24.0, stream=None):
+    _need(q, torch.bfloat16, "q", 4)
+    _need(packed, torch.uint8, "packed")
+    if topk_length is not None:
+        _need(topk_length, torch.int32, "topk_length", 2)
+    _need(out, torch.bfloat16, "out", 4)
+    B, s_q, h_q, d = q.shape
+    if d != 576:
+        raise ValueError("q must be [B, s_q, h_q, 576]")
+    _check(load_library().mla_sparse_fp8_packed_decode_fwd(
+        _ptr(q), _ptr(packed), packed.numel(), int(topk), _ptr(topk_length), B, s_q, h_q, float(softmax_scale),
+        _ptr(sched), _ptr(split_offset), int(num_parts), _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
+        _ptr(status), _stream(stream)), "mla_sparse_fp8_packed_decode_fwd")
+
+
 # ---------------------------------------------------------------- helpers
 
 
@@ -299,4 +337,33 @@ def sparse_decode(q, kv8, indices, topk_length=None, softmax_scale=None, pl=None
                               out, lse, status, softmax_scale)
     if check:
         check_status(status, "mla_sparse_fp8_decode_fwd")
+    return out, lse
+
+
+def pack_selected_kv(kv8, indices, topk_length=None, check=True):
+    """Pack the selected records into a freshly allocated packed workspace."""
+    B, s_q, topk = indices.shape
+    packed = torch.empty(mla_packed_kv_workspace_bytes(B * s_q, topk), dtype=torch.uint8, device=kv8.device)
+    status = torch.zeros(1, dtype=torch.int32, device=kv8.device)
+    mla_pack_selected_kv(kv8, indices, topk_length, packed, status)
+    if check:
+        check_status(status, "mla_pack_selected_kv")
+    return packed
+
+
+def packed_sparse_decode(q, packed, topk, topk_length=None, softmax_scale=None, pl=None, check=True):
+    """Sparse FP8 decode over a packed workspace; returns (out, lse)."""
+    B, s_q, h_q, _ = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(576)
+    if pl is None:
+        lens = None if topk_length is None else topk_length.reshape(-1)
+        pl = plan(lens, B * s_q, h_q, sparse=True, default_length=topk, device=q.device)
+    out = torch.empty(B, s_q, h_q, 512, dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty(B, s_q, h_q, dtype=torch.float32, device=q.device)
+    status = torch.zeros(1, dtype=torch.int32, device=q.device)
+    mla_sparse_fp8_packed_decode_fwd(q, packed, topk, topk_length, pl.sched, pl.split_offset, pl.num_parts,
+                                     pl.workspace, out, lse, status, softmax_scale)
+    if check:
+        check_status(status, "mla_sparse_fp8_packed_decode_fwd")
     return out, lse

@@ -24,6 +24,8 @@ int sparse_smem_bytes();
 int sparse_threads();
 const void* sparse_kernel_ptr();
 cudaError_t launch_unpack(const uint8_t*, int, const int32_t*, int, float*, int32_t*, cudaStream_t);
+cudaError_t launch_pack(const uint8_t*, int, const int32_t*, int, const int32_t*, int, uint8_t*, uint64_t*,
+                        int32_t*, cudaStream_t);
 }  // namespace mla
 
 using namespace mla;
@@ -290,12 +292,16 @@ int mla_decode_fwd(const void* d_q, const void* d_kv, const int32_t* d_block_tab
                      d_lse, stream);
 }
 
-int mla_sparse_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, int num_pages, const int32_t* d_indices,
-                              int topk, const int32_t* d_topk_length, int batch, int s_q, int h_q,
-                              float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
-                              int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
-                              int32_t* d_status, mla_stream_t stream) {
-  if (!d_q || !d_kv8 || !d_indices || !d_sched || !d_split_offset || !d_workspace || !d_out || !d_lse || !d_status)
+namespace {
+
+// Sparse attention over a record pool: the native selection (indices into
+// the paged pool) or a packed one (masks over the packed records).
+int sparse_decode(const void* d_q, const uint8_t* d_kv8, int num_pages, const int32_t* d_indices,
+                  const uint64_t* d_masks, int topk, const int32_t* d_topk_length, int batch, int s_q, int h_q,
+                  float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
+                  void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse, int32_t* d_status,
+                  mla_stream_t stream) {
+  if (!d_q || !d_kv8 || (!d_indices && !d_masks) || !d_sched || !d_split_offset || !d_workspace || !d_out || !d_lse || !d_status)
     return MLA_ERR_INVALID_ARG;
   if (batch < 1 || s_q < 1 || h_q < 1 || num_pages < 1 || topk < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
@@ -320,6 +326,7 @@ int mla_sparse_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, int num_pag
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
   p.num_pages = num_pages;
   p.indices = d_indices;
+  p.packed_mask = d_masks;
   p.topk = topk;
   p.kv8 = d_kv8;
   p.sched = d_sched;
@@ -338,6 +345,75 @@ int mla_sparse_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, int num_pag
   if (launch_sparse(qm, p, num_parts, s) != cudaSuccess) return MLA_ERR_CUDA;
   return mla_combine(d_workspace, workspace_bytes, d_split_offset, static_cast<int>(units), h_q, num_parts, d_out,
                      0, d_lse, stream);
+}
+
+// Packed workspace layout: records, then one 64-bit mask per (unit, tile).
+struct PackedLayout {
+  long long tiles, records_bytes, total;
+};
+
+PackedLayout packed_layout(long long n_units, int topk) {
+  PackedLayout l;
+  l.tiles = (topk + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE;
+  l.records_bytes = n_units * l.tiles * MLA_PAGE_SIZE * MLA_RECORD_BYTES;
+  l.total = l.records_bytes + n_units * l.tiles * static_cast<long long>(sizeof(uint64_t));
+  return l;
+}
+
+}  // namespace
+
+int mla_sparse_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, int num_pages, const int32_t* d_indices,
+                              int topk, const int32_t* d_topk_length, int batch, int s_q, int h_q,
+                              float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
+                              int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
+                              int32_t* d_status, mla_stream_t stream) {
+  if (!d_indices) return MLA_ERR_INVALID_ARG;
+  return sparse_decode(d_q, d_kv8, num_pages, d_indices, nullptr, topk, d_topk_length, batch, s_q, h_q,
+                       softmax_scale, d_sched, d_split_offset, num_parts, d_workspace, workspace_bytes, d_out, d_lse,
+                       d_status, stream);
+}
+
+size_t mla_packed_kv_workspace_bytes(int n_units, int topk) {
+  if (n_units < 0 || topk < 1) return 0;
+  return static_cast<size_t>(packed_layout(n_units, topk).total);
+}
+
+int mla_pack_selected_kv(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int topk,
+                         const int32_t* d_topk_length, int n_units, void* d_packed, size_t packed_bytes,
+                         int32_t* d_status, mla_stream_t stream) {
+  if (!d_kv8 || !d_indices || !d_packed || !d_status) return MLA_ERR_INVALID_ARG;
+  if (num_pages < 1 || topk < 1 || n_units < 0) return MLA_ERR_INVALID_ARG;
+  if (n_units > 65535) return MLA_ERR_UNSUPPORTED;
+  if (!aligned16(d_kv8) || !aligned16(d_packed)) return MLA_ERR_INVALID_ARG;
+  const PackedLayout l = packed_layout(n_units, topk);
+  if (packed_bytes < static_cast<size_t>(l.total)) return MLA_ERR_INVALID_ARG;
+  if (n_units == 0) return MLA_OK;
+  uint8_t* records = static_cast<uint8_t*>(d_packed);
+  uint64_t* masks = reinterpret_cast<uint64_t*>(records + l.records_bytes);
+  return launch_pack(d_kv8, num_pages, d_indices, topk, d_topk_length, n_units, records, masks, d_status,
+                     reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size_t packed_bytes, int topk,
+                                     const int32_t* d_topk_length, int batch, int s_q, int h_q, float softmax_scale,
+                                     const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
+                                     void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
+                                     int32_t* d_status, mla_stream_t stream) {
+  if (!d_packed || topk < 1 || batch < 1 || s_q < 1) return MLA_ERR_INVALID_ARG;
+  const long long units = static_cast<long long>(batch) * s_q;
+  if (units > 65535) return MLA_ERR_UNSUPPORTED;
+  const PackedLayout l = packed_layout(units, topk);
+  if (packed_bytes < static_cast<size_t>(l.total)) return MLA_ERR_INVALID_ARG;
+  const uint8_t* records = static_cast<const uint8_t*>(d_packed);
+  const uint64_t* masks = reinterpret_cast<const uint64_t*>(records + l.records_bytes);
+  // the packed records form a pool of units * tiles pages of 64 records
+  const long long pool_pages = units * l.tiles;
+  if (pool_pages > (1LL << 31) / MLA_PAGE_SIZE) return MLA_ERR_UNSUPPORTED;
+  return sparse_decode(d_q, records, static_cast<int>(pool_pages), nullptr, masks, topk, d_topk_length, batch, s_q,
+                       h_q, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace, workspace_bytes, d_out,
+                       d_lse, d_status, stream);
 }
 
 int mla_sparse_fp8_unpack(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int n, float* d_k_out,

@@ -39,9 +39,10 @@ struct DecodeParams {
   int max_pages;
   int num_pages;
   // sparse
-  const int32_t* indices;   // [n_units, topk]
+  const int32_t* indices;   // [n_units, topk] (native selection), or NULL when packed
   int topk;
-  const uint8_t* kv8;       // [num_pages, 64, 656]
+  const uint8_t* kv8;       // [num_pages, 64, 656]; packed: the packed records
+  const uint64_t* packed_mask;  // packed: [n_units, ceil(topk/64)] valid-slot bits, else NULL
   // schedule
   const int32_t* sched;
   const int32_t* split_offset;

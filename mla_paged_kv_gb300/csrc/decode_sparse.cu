@@ -215,23 +215,18 @@ __device__ __forceinline__ uint4 codes_to_bf16(uint2 codes) {
                     e4m3x2_to_bf16x2(codes.y >> 16));
 }
 
-// Validity of selection entry t of unit b (L = candidate slots of the unit).
-__device__ __forceinline__ bool sparse_valid(const DecodeParams& p, int b, int t, int L, int& idx) {
-  idx = -1;
-  if (t >= L) return false;
-  idx = p.indices[static_cast<size_t>(b) * p.topk + t];
-  if (idx == -1) return false;
-  if (idx < 0 || idx >= p.num_pages * kT) {
-    report(p.status, MLA_ERR_BAD_INDEX);
-    idx = -1;
-    return false;
-  }
-  return true;
-}
-
 // Selection entry t of unit b as stored (no check yet); -1 past the list.
+// Packed selection: the record of slot t sits at ordinal b * tiles * 64 + t
+// of the packed records when its bit in the tile's valid mask is set.
 __device__ __forceinline__ int load_slot(const DecodeParams& p, int b, int t, int L) {
-  return t < L ? __ldg(p.indices + static_cast<size_t>(b) * p.topk + t) : -1;
+  if (t >= L) return -1;
+  if (p.packed_mask != nullptr) {
+    const int tiles = (p.topk + kT - 1) / kT;
+    const unsigned long long m =
+        __ldg(reinterpret_cast<const unsigned long long*>(p.packed_mask) + static_cast<size_t>(b) * tiles + t / kT);
+    return ((m >> (t % kT)) & 1ull) ? (b * tiles * kT + t) : -1;
+  }
+  return __ldg(p.indices + static_cast<size_t>(b) * p.topk + t);
 }
 
 // A stored entry -> record index, or -1 when masked; an entry outside the
@@ -769,6 +764,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// Selected-record packing (FlashMLA PR #200, "[SM90] Add packed selected-KV
+// sparse decode", sections Motivation and "SM90 packing kernel": the selected
+// records are copied byte for byte into a tile-major workspace ahead of the
+// attention, so that no index translation sits on its critical path).  One
+// block per (tile of 64 slots, unit): slot t < topk_length with a valid index
+// gets its 656-byte record, every other slot 656 zero bytes; the tile's
+// 64-bit valid mask goes to `masks`.  An index outside [-1, pool) is reported
+// (MLA_ERR_BAD_INDEX) and packed as masked.
+__global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ kv8, int num_pages,
+                                                   const int32_t* __restrict__ indices, int topk,
+                                                   const int32_t* __restrict__ topk_length, uint8_t* __restrict__ packed,
+                                                   uint64_t* __restrict__ masks, int32_t* status) {
+  constexpr int kChunks = MLA_RECORD_BYTES / 16;  // 41
+  __shared__ int s_idx[kT];
+  __shared__ uint32_t s_half[2];
+  const int tiles = gridDim.x, tile = blockIdx.x, unit = blockIdx.y;
+  const int tid = threadIdx.x;
+  if (tid < kT) {
+    const int t = tile * kT + tid;
+    const int L = topk_length != nullptr ? max(min(topk_length[unit], topk), 0) : topk;
+    int idx = -1;
+    if (t < L) {
+      idx = indices[static_cast<size_t>(unit) * topk + t];
+      if (idx != -1 && (idx < 0 || idx >= num_pages * kT)) {
+        report(status, MLA_ERR_BAD_INDEX);
+        idx = -1;
+      }
+    }
+    s_idx[tid] = idx;
+    const uint32_t half = __ballot_sync(0xffffffffu, idx >= 0);
+    if ((tid & 31) == 0) s_half[tid >> 5] = half;
+  }
+  __syncthreads();
+  if (tid == 0) masks[static_cast<size_t>(unit) * tiles + tile] = s_half[0] | (static_cast<uint64_t>(s_half[1]) << 32);
+  uint4* dst = reinterpret_cast<uint4*>(packed + (static_cast<size_t>(unit) * tiles + tile) * kT * MLA_RECORD_BYTES);
+  for (int c = tid; c < kT * kChunks; c += 256) {
+    const int key = c / kChunks, part = c - kChunks * (c / kChunks);
+    const int idx = s_idx[key];
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (idx >= 0) v = __ldg(reinterpret_cast<const uint4*>(kv8 + static_cast<size_t>(idx) * MLA_RECORD_BYTES) + part);
+    dst[c] = v;
+  }
+}
+
 // Bit-exact record unpack: one thread per (record, 8-dim chunk).
 __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__ kv8, int num_pages,
                                                      const int32_t* __restrict__ indices, int n,
@@ -818,6 +857,14 @@ const void* sparse_kernel_ptr() { return reinterpret_cast<const void*>(&sp::spar
 cudaError_t launch_sparse(const CUtensorMap& q_map, const DecodeParams& p, int num_parts, cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
   sp::sparse_decode_kernel<<<grid, sp::kThreads, sp::kSmemBytes, stream>>>(q_map, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const uint8_t* kv8, int num_pages, const int32_t* indices, int topk,
+                        const int32_t* topk_length, int n_units, uint8_t* packed, uint64_t* masks, int32_t* status,
+                        cudaStream_t stream) {
+  const dim3 grid((topk + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE, n_units);
+  sp::pack_kernel<<<grid, 256, 0, stream>>>(kv8, num_pages, indices, topk, topk_length, packed, masks, status);
   return cudaGetLastError();
 }
 

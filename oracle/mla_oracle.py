@@ -263,6 +263,81 @@ def sparse_decode(q, kv8, indices, topk_length, scale, batches=None):
 
 
 # --------------------------------------------------------------------------
+# Packed selected-KV path
+# --------------------------------------------------------------------------
+
+def packed_layout(n_units: int, topk: int):
+    """(tiles, records_bytes, total_bytes) of the packed workspace.
+
+    PR #200 *SM90 packing kernel*: an opaque workspace of 64-token tiles.
+    This library fixes it as uint8 [n_units, tiles, 64, 656] records, then
+    uint64 [n_units, tiles] valid masks, tiles = ceil(topk / 64).
+    """
+    tiles = -(-topk // PAGE_SIZE)
+    records = n_units * tiles * PAGE_SIZE * RECORD_BYTES
+    return tiles, records, records + n_units * tiles * 8
+
+
+def pack_selected(kv8, indices, topk_length):
+    """Byte-for-byte copy of every selected record into the packed layout.
+
+    PR #200 *SM90 packing kernel*: each selected record is copied unchanged;
+    slots past the valid prefix (topk_length) are zero-filled.  Slots the
+    native selection masks (-1, or an index outside the pool) are zero-filled
+    and left out of the tile's valid mask too.
+    Returns (packed uint8 1-D, bad_index_count).
+    """
+    kv8 = np.asarray(kv8, dtype=np.uint8)
+    B, s_q, topk = indices.shape
+    n_units = B * s_q
+    num_slots = kv8.shape[0] * PAGE_SIZE
+    tiles, rec_bytes, total = packed_layout(n_units, topk)
+    packed = np.zeros(total, dtype=np.uint8)
+    records = packed[:rec_bytes].reshape(n_units, tiles * PAGE_SIZE, RECORD_BYTES)
+    masks = np.zeros((n_units, tiles), dtype=np.uint64)
+    bad = 0
+    for b in range(B):
+        for i in range(s_q):
+            u = b * s_q + i
+            tl = topk if topk_length is None else int(topk_length[b, i])
+            for t in range(topk):
+                idx = int(indices[b, i, t])
+                ok, is_bad = slot_valid(idx, t, tl, num_slots)
+                bad += int(is_bad)
+                if ok:
+                    records[u, t] = kv8[idx // PAGE_SIZE, idx % PAGE_SIZE]
+                    masks[u, t // PAGE_SIZE] |= np.uint64(1) << np.uint64(t % PAGE_SIZE)
+    packed[rec_bytes:] = masks.reshape(-1).view(np.uint8)
+    return packed, bad
+
+
+def packed_decode(q, packed, topk, topk_length, scale):
+    """Sparse decode over a packed workspace (PR #200 *Packed attention
+    specialization*): slot t of unit u is a key iff t < topk_length and its
+    bit in the tile mask is set; its record sits at a fixed position.
+    Returns (out [B, s_q, h_q, 512], lse [B, s_q, h_q])."""
+    q = np.asarray(q, dtype=np.float64)
+    B, s_q, h_q, _ = q.shape
+    n_units = B * s_q
+    tiles, rec_bytes, total = packed_layout(n_units, topk)
+    packed = np.asarray(packed, dtype=np.uint8)
+    assert packed.shape == (total,)
+    records = packed[:rec_bytes].reshape(n_units, tiles * PAGE_SIZE, RECORD_BYTES)
+    masks = packed[rec_bytes:].view(np.uint64).reshape(n_units, tiles)
+    out = np.zeros((B, s_q, h_q, D_V), dtype=np.float64)
+    lse = np.full((B, s_q, h_q), -np.inf, dtype=np.float64)
+    for b in range(B):
+        for i in range(s_q):
+            u = b * s_q + i
+            tl = min(topk, topk if topk_length is None else int(topk_length[b, i]))
+            rows = [decode_record(records[u, t]) for t in range(max(tl, 0))
+                    if (int(masks[u, t // PAGE_SIZE]) >> (t % PAGE_SIZE)) & 1]
+            keys = np.stack(rows) if rows else np.zeros((0, D_QK), dtype=np.float64)
+            out[b, i], lse[b, i] = attend(q[b, i], keys, scale)
+    return out, lse
+
+
+# --------------------------------------------------------------------------
 # Split-KV partials and the combine step
 # --------------------------------------------------------------------------
 

@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == sorted(["mla_status_string", "mla_num_parts", "mla_workspace_bytes", "mla_get_metadata",
                             "mla_decode_fwd", "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd",
-                            "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws"])
+                            "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes",
+                            "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd"])
 
 
 def test_library_exports_every_declared_symbol(lib_path):
@@ -76,3 +77,16 @@ def test_host_validation_without_gpu(lib_path):
     lib.mla_sparse_fp8_unpack.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     assert lib.mla_sparse_fp8_unpack(null, 1, null, 4, null, null, null) == 1
+    # packed workspace: [units, tiles, 64, 656] records, then [units, tiles] uint64 masks
+    lib.mla_packed_kv_workspace_bytes.restype = ctypes.c_size_t
+    lib.mla_packed_kv_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
+    assert lib.mla_packed_kv_workspace_bytes(16, 2048) == 16 * 32 * (64 * 656 + 8)
+    assert lib.mla_packed_kv_workspace_bytes(3, 65) == 3 * 2 * (64 * 656 + 8)
+    assert lib.mla_packed_kv_workspace_bytes(3, 0) == 0
+    lib.mla_pack_selected_kv.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                         ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.mla_pack_selected_kv(null, 1, null, 64, null, 1, null, 0, null, null) == 1
+    # a workspace smaller than the layout is refused before any launch
+    p16 = ctypes.c_void_p(256)
+    assert lib.mla_pack_selected_kv(p16, 1, p16, 64, null, 1, p16, 64 * 656, p16, null) == 1

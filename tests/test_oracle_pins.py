@@ -384,3 +384,70 @@ def test_sparse_topk_length_prefix():
     ind[0, 0, 30:] = 0                        # entries past topk_length are ignored whatever they hold
     o2, l2, _ = orc.sparse_decode(q, sc.kv8.numpy(), ind.numpy(), sc.topk_length.numpy(), sc.scale)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------- packed selected-KV path
+
+def test_pack_by_hand():
+    """Each record's bytes encode its slot, so every packed slot can be checked
+    against a value written out here, without the oracle's gather."""
+    pages = 3
+    slot = np.arange(pages * 64)[:, None]
+    kv8 = ((slot * 7 + np.arange(656)[None, :]) % 251).astype(np.uint8).reshape(pages, 64, 656)
+    rng = np.random.default_rng(21)
+    ind = rng.integers(0, pages * 64, size=(1, 2, 70)).astype(np.int32)
+    ind[0, 0, 3] = -1
+    ind[0, 0, 10] = pages * 64                # outside the pool: masked, counted
+    ind[0, 1, 66] = -7                        # past unit 1's prefix: ignored, not counted
+    tl = np.array([[70, 65]], dtype=np.int32)
+    packed, bad = orc.pack_selected(kv8, ind, tl)
+    assert bad == 1
+    assert packed.size == 2 * 2 * (64 * 656 + 8)
+    records = packed[:2 * 128 * 656].reshape(2, 128, 656)
+    masks = packed[2 * 128 * 656:].view(np.uint64).reshape(2, 2)
+    for u in range(2):
+        for t in range(128):
+            valid = t < tl[0, u] and not (u == 0 and t in (3, 10))
+            want = (int(ind[0, u, t]) * 7 + np.arange(656)) % 251 if valid else np.zeros(656)
+            assert np.array_equal(records[u, t], want.astype(np.uint8)), (u, t)
+    full = (1 << 64) - 1
+    assert int(masks[0, 0]) == full & ~(1 << 3) & ~(1 << 10)
+    assert int(masks[0, 1]) == 0x3F           # slots 64..69
+    assert int(masks[1, 0]) == full and int(masks[1, 1]) == 0x1
+
+
+def test_packed_workspace_size_matches_page():
+    facts = json.load(open(os.path.join(GOLDEN, "page_facts.json")))
+    f = facts["packed_workspace_per_row_topk2048"]
+    tiles, rec, total = orc.packed_layout(1, f["topk"])
+    assert tiles == 32 and round(rec / 2 ** 20, 3) == f["value_mib"]
+    assert round(total / 2 ** 20, 3) == f["value_mib"]          # the masks add 256 B per row
+
+
+def test_packed_decode_equals_native_sparse():
+    sc = wl.sparse_case(2, 2, 8, topk=130, pages_per_req=4, topk_lengths=[[130, 77], [1, 0]], seed=22)
+    ind = sc.indices.clone()
+    ind[0, 0, ::9] = -1
+    ind[0, 1, 5] = sc.kv8.shape[0] * 64 + 3
+    q = f64(sc.q)
+    o1, l1, bad1 = orc.sparse_decode(q, sc.kv8.numpy(), ind.numpy(), sc.topk_length.numpy(), sc.scale)
+    packed, bad2 = orc.pack_selected(sc.kv8.numpy(), ind.numpy(), sc.topk_length.numpy())
+    o2, l2 = orc.packed_decode(q, packed, 130, sc.topk_length.numpy(), sc.scale)
+    assert bad1 == bad2 == 1
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    assert np.isneginf(l2[1, 1]).all() and not o2[1, 1].any()
+
+
+def test_packed_mask_bit_controls_the_slot():
+    """Clearing one mask bit equals masking that entry in the native selection."""
+    sc = wl.sparse_case(1, 1, 4, topk=64, pages_per_req=2, topk_lengths=[[64]], seed=23)
+    q = f64(sc.q)
+    packed, _ = orc.pack_selected(sc.kv8.numpy(), sc.indices.numpy(), None)
+    _, rec, _ = orc.packed_layout(1, 64)
+    m = packed[rec:].view(np.uint64)
+    m[0] &= ~np.uint64(1 << 17)
+    o1, l1 = orc.packed_decode(q, packed, 64, None, sc.scale)
+    ind = sc.indices.clone()
+    ind[0, 0, 17] = -1
+    o2, l2, _ = orc.sparse_decode(q, sc.kv8.numpy(), ind.numpy(), None, sc.scale)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
