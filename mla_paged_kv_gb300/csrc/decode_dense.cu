@@ -101,8 +101,8 @@ enum : int {
   R_FREE,     // the peer has read our last references (one remote arrival per warp)
   L_FULL,     // row-sum mailbox filled (bulk-copy bytes)
   L_FREE,     // the peer has read our last row sums (one remote arrival per warp)
-  PV_DONE,    // one completion per P V, in tile order
-  O_FULL,
+  PV_DONE,    // +(t&1): one completion per P V of a tile of that parity, in tile order
+  O_FULL = PV_DONE + 2,
   O_FREE,
   DRAIN,
   kNumBars
@@ -357,6 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[L_FULL], 1);
     mbar_init(&bars[L_FREE], 4);
     mbar_init(&bars[PV_DONE], 1);
+    mbar_init(&bars[PV_DONE + 1], 1);
     mbar_init(&bars[O_FULL], 1);
     mbar_init(&bars[O_FREE], 128);
     mbar_init(&bars[DRAIN], 1);
@@ -542,7 +543,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               umma_f16(tmem + kTmemO, a0 + static_cast<uint64_t>((kk * 32) >> 4),
                        b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
             umma_commit(&bars[V_EMPTY + vs]);
-            umma_commit(&bars[PV_DONE]);
+            umma_commit(&bars[PV_DONE + (cv.t & 1)]);
             if (mine) {
               umma_commit(&bars[OWN_FREE]);
               ++pv_own;
@@ -752,9 +753,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_own *= alpha;
         r_cur = r_t;
       }
-      // O (through P V of the previous tile) to the new reference, then go
+      // O (through P V of the previous tile) to the new reference, then go.
+      // P V t-1 completes phase (t-1)/2 of the barrier of its parity; the phase
+      // before it is P V t-3, which is complete here (own tile: its V slot was
+      // refilled for this tile; received tile: the last own tile's P waited for
+      // it), so the parity wait cannot pass on an older completion.  (With one
+      // barrier for all tiles it could, while P V t-2 was still in flight.)
       if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
-        ok = warp_wait(&bars[PV_DONE], (t - 1) & 1, abort_flag);
+        ok = warp_wait(&bars[PV_DONE + ((t - 1) & 1)], ((t - 1) >> 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         rescale_o(taddr, alpha);
