@@ -97,3 +97,53 @@ def part_ranges(entry, seqlens, tile: int = TILE):
             out.append((b, lo, hi, s0 if b == b0 else 0))
         b += 1
     return out
+
+
+def plan_request_local(seqlens, num_parts: int, fixed_cost: int, tile: int = TILE):
+    """Request-local plan: no part spans two work units.
+
+    FlashMLA PR #200 (*[SM90] Add packed selected-KV sparse decode*, section
+    *Scheduler policy*) names a "compact request-local scheduler" for its
+    H=64 path and says the native scheduler is kept where it measured faster;
+    the page does not define it.  Reading taken here: every part works on the
+    tiles of a single unit (query token), and the parts are shared out over
+    the units in proportion to their tile counts:
+      * units with n_b > 0 tiles: A of them; if A > P, or there are no tiles,
+        the native plan above is used instead;
+      * each active unit gets one part, and the other R = P - A parts go by
+        largest remainder: q_b, r_b = divmod(n_b * R, sum n), one more part to
+        the (R - sum q) units with the largest r_b (ties: lower b first);
+      * a unit never gets more parts than tiles;
+      * unit b's k-th of s_b parts covers tiles [k*n_b//s_b, (k+1)*n_b//s_b).
+    Parts are numbered in unit order; unused parts are empty (B, 0, B, 0).
+    Same metadata format as ``plan``.
+    """
+    B = len(seqlens)
+    nt = [ceil_div(max(int(L), 0), tile) for L in seqlens]
+    active = [b for b in range(B) if nt[b] > 0]
+    if not active or len(active) > num_parts:
+        return plan(seqlens, num_parts, fixed_cost, tile)
+    total = sum(nt)
+    spare = num_parts - len(active)
+    seats = [0] * B
+    remainders = []
+    given = 0
+    for b in active:
+        q, r = divmod(nt[b] * spare, total)
+        seats[b] = 1 + q
+        given += q
+        remainders.append((-r, b))
+    for _, b in sorted(remainders)[:spare - given]:
+        seats[b] += 1
+    sched = []
+    split_offset = [0]
+    for b in range(B):
+        s = min(seats[b], nt[b])
+        for k in range(s):
+            lo, hi = k * nt[b] // s, (k + 1) * nt[b] // s
+            end_b, end_t = (b, hi) if hi < nt[b] else (b + 1, 0)
+            sched.append((b, lo, end_b, end_t, k, 0, 0, 0))
+        split_offset.append(split_offset[-1] + s)
+    while len(sched) < num_parts:
+        sched.append((B, 0, B, 0, 0, 0, 0, 0))
+    return sched, split_offset

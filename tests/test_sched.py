@@ -61,3 +61,53 @@ def test_plan_all_empty():
     sched, off = sp.plan([0, 0, 0], 5, 4)
     assert off == [0, 0, 0, 0]
     assert all(sp.part_ranges(e, [0, 0, 0]) == [] for e in sched)
+
+
+# ---------------------------------------------------------------- request-local plan
+
+@pytest.mark.parametrize("num_parts", [1, 5, 16, 38, 76, 152])
+def test_request_local_plan_invariants(num_parts):
+    rng = np.random.default_rng(num_parts + 7)
+    for trial in range(40):
+        B = int(rng.integers(1, 40))
+        L = rng.integers(0, 5000, size=B)
+        L[rng.random(B) < 0.15] = 0
+        sched, off = sp.plan_request_local(L.tolist(), num_parts, 4)
+        nt = [-(-int(x) // 64) for x in L]
+        active = sum(1 for n in nt if n > 0)
+        assert len(sched) == num_parts and len(off) == B + 1
+        if active == 0 or active > num_parts:
+            assert (sched, off) == sp.plan(L.tolist(), num_parts, 4)
+            continue
+        seen = {b: np.zeros(nt[b], int) for b in range(B)}
+        per_unit = {b: [] for b in range(B)}
+        for e in sched:
+            rs = sp.part_ranges(e, L.tolist())
+            assert len(rs) <= 1                      # no part spans two units
+            for (b, t0, t1, s) in rs:
+                seen[b][t0:t1] += 1
+                per_unit[b].append((s, t1 - t0))
+        for b in range(B):
+            assert (seen[b] == 1).all()
+            n = off[b + 1] - off[b]
+            assert [s for s, _ in per_unit[b]] == list(range(n))
+            if nt[b]:
+                sizes = [z for _, z in per_unit[b]]
+                assert 1 <= n <= nt[b] and max(sizes) - min(sizes) <= 1
+            else:
+                assert n == 0
+        # every part is used unless a unit ran out of tiles to give
+        used = off[-1]
+        assert used == num_parts or any(off[b + 1] - off[b] == nt[b] for b in range(B) if nt[b])
+
+
+def test_request_local_plan_by_hand():
+    # 3 units with 10, 30, 0 and 20 tiles (64 keys each), 10 parts: 3 active, 7 spare;
+    # quotas 10*7/60 = 1 r 10, 30*7/60 = 3 r 30, 20*7/60 = 2 r 20 -> 6 given, one more to the
+    # largest remainder (unit 1): seats 2, 5, 0, 3.
+    L = [640, 1920, 0, 1280]
+    sched, off = sp.plan_request_local(L, 10, 4)
+    assert off == [0, 2, 7, 7, 10]
+    assert sched[:2] == [(0, 0, 0, 5, 0, 0, 0, 0), (0, 5, 1, 0, 1, 0, 0, 0)]
+    assert [e[1] for e in sched[2:7]] == [0, 6, 12, 18, 24] and sched[6][2:4] == (2, 0)
+    assert sched[7:] == [(3, 0, 3, 6, 0, 0, 0, 0), (3, 6, 3, 13, 1, 0, 0, 0), (3, 13, 4, 0, 2, 0, 0, 0)]
