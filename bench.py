@@ -198,7 +198,8 @@ def cpu_oracle_sample(case, budget_s, gpu_out=None, gpu_lse=None):
 
 
 OTHER_WORKLOADS = ["dense_b1_hq16_sk256_fp32out", "dense_b1_hq64_sk65536", "dense_b16_sq2causal_hq128_sk4096to8192",
-                   "sparse_fp8_b16_hq128_topk2048"]
+                   "sparse_fp8_b16_hq128_topk2048", "sparse_fp8_b4_sq4_hq64_topk2048",
+                   "sparse_fp8_b2_sq8_hq128_topk2048"]
 
 
 def time_other_workloads(mla, wl, timed, steps):
@@ -239,6 +240,19 @@ def time_other_workloads(mla, wl, timed, steps):
                      "num_parts": pl.num_parts, "splits": int(pl.split_offset[-1].item())}
         if sparse:
             res[name + "_packed"] = time_packed(mla, case, q, kv8, ind, tl, pl, out, lse, status, timed, steps)
+            # the same call under the request-local partition plan
+            pl_local = mla.plan(tl.reshape(-1).contiguous(), B * s_q, h_q, sparse=True, default_length=ind.shape[2],
+                                request_local=True)
+
+            def fn_local():
+                mla.mla_sparse_fp8_decode_fwd(q, kv8, ind, tl, pl_local.sched, pl_local.split_offset,
+                                              pl_local.num_parts, pl_local.workspace, out, lse, status, case.scale)
+            for _ in range(5):
+                fn_local()
+            us_local = 1e3 * statistics.mean(timed(fn_local, steps))
+            mla.check_status(status, name + " request-local plan")
+            res[name + "_request_local"] = {"us_per_call": us_local, "gb_per_s": nbytes / (us_local * 1e-6) / 1e9,
+                                            "splits": int(pl_local.split_offset[-1].item())}
         del q, out, lse, fn
         torch.cuda.empty_cache()
     return res

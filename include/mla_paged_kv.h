@@ -95,6 +95,21 @@ size_t mla_workspace_bytes(int n_units, int rows_per_unit, int num_parts);
 int mla_get_metadata(const int32_t* d_lengths, int default_length, int n_units, int num_parts,
                      int32_t* d_sched, int32_t* d_split_offset, mla_stream_t stream);
 
+/* Request-local split plan, in the same metadata format (FlashMLA PR #200,
+ * section "Scheduler policy", names a request-local scheduler for its H=64
+ * sparse path without defining it; this is the library's reading of it).
+ * No partition spans two units.  Each unit with tiles gets one partition; the
+ * other num_parts - (units with tiles) partitions are shared out in proportion
+ * to the tile counts, by largest remainder of tiles * spare / total tiles (ties
+ * to the lower unit), and a unit gets at most one partition per tile.  Unit
+ * u's k-th of s partitions covers tiles [k*n/s, (k+1)*n/s); partitions are
+ * numbered in unit order and unused ones are empty.  Falls back to
+ * mla_get_metadata's plan when no unit has tiles, when more units have tiles
+ * than there are partitions, or above 1024 units.  Arguments as for
+ * mla_get_metadata; both decode entry points accept either plan. */
+int mla_get_metadata_request_local(const int32_t* d_lengths, int default_length, int n_units, int num_parts,
+                                   int32_t* d_sched, int32_t* d_split_offset, mla_stream_t stream);
+
 /* Dense bf16 MLA decode: split-KV attention kernel, then the combine kernel
  * (chained with programmatic dependent launch).
  *   d_q            bf16 [batch, s_q, h_q, 576]

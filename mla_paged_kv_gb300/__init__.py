@@ -25,7 +25,8 @@ __all__ = [
     "MlaError", "load_library", "mla_status_string", "mla_num_parts", "mla_workspace_bytes",
     "mla_get_metadata", "mla_decode_fwd", "mla_decode_splits", "mla_combine",
     "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws",
-    "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd", "plan", "decode",
+    "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd",
+    "mla_get_metadata_request_local", "plan", "decode",
     "sparse_decode", "pack_selected_kv", "packed_sparse_decode",
     "EXPORTED_SYMBOLS",
 ]
@@ -34,7 +35,7 @@ EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_num_parts", "mla_workspace_bytes", "mla_get_metadata", "mla_decode_fwd",
     "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack",
     "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv",
-    "mla_sparse_fp8_packed_decode_fwd",
+    "mla_sparse_fp8_packed_decode_fwd", "mla_get_metadata_request_local",
 )
 
 _P = ctypes.c_void_p
@@ -47,6 +48,7 @@ _SIGS = {
     "mla_num_parts": (_I, [_I, _I]),
     "mla_workspace_bytes": (_SZ, [_I, _I, _I]),
     "mla_get_metadata": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "mla_get_metadata_request_local": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "mla_decode_fwd": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _I, _P, _P, _P]),
     "mla_decode_splits": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _I, _P, _P,
                                _P]),
@@ -130,15 +132,25 @@ def mla_workspace_bytes(n_units: int, rows_per_unit: int, num_parts: int) -> int
     return int(load_library().mla_workspace_bytes(int(n_units), int(rows_per_unit), int(num_parts)))
 
 
-def mla_get_metadata(lengths, n_units, num_parts, sched, split_offset, default_length=-1, stream=None):
+def _metadata(fn, lengths, n_units, num_parts, sched, split_offset, default_length, stream):
     if lengths is not None:
         _need(lengths, torch.int32, "lengths")
     _need(sched, torch.int32, "sched")
     _need(split_offset, torch.int32, "split_offset")
     if sched.numel() < num_parts * 8 or split_offset.numel() < n_units + 1:
         raise ValueError("sched / split_offset too small")
-    _check(load_library().mla_get_metadata(_ptr(lengths), int(default_length), int(n_units), int(num_parts),
-                                           _ptr(sched), _ptr(split_offset), _stream(stream)), "mla_get_metadata")
+    _check(getattr(load_library(), fn)(_ptr(lengths), int(default_length), int(n_units), int(num_parts),
+                                       _ptr(sched), _ptr(split_offset), _stream(stream)), fn)
+
+
+def mla_get_metadata(lengths, n_units, num_parts, sched, split_offset, default_length=-1, stream=None):
+    _metadata("mla_get_metadata", lengths, n_units, num_parts, sched, split_offset, default_length, stream)
+
+
+def mla_get_metadata_request_local(lengths, n_units, num_parts, sched, split_offset, default_length=-1,
+                                   stream=None):
+    _metadata("mla_get_metadata_request_local", lengths, n_units, num_parts, sched, split_offset, default_length,
+              stream)
 
 
 def _dense_args(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse, status,
@@ -286,13 +298,14 @@ class Plan:
 
 
 def plan(lengths, n_units, rows_per_unit, sparse=False, default_length=-1, num_parts=None, stream=None,
-         device=None) -> Plan:
-    """Run the scheduler kernel and allocate the split workspace."""
+         device=None, request_local=False) -> Plan:
+    """Run the scheduler kernel (native or request-local plan) and allocate the split workspace."""
     dev = device if device is not None else (lengths.device if lengths is not None else torch.device("cuda"))
     parts = mla_num_parts(rows_per_unit, sparse) if num_parts is None else int(num_parts)
     sched = torch.empty(parts * 8, dtype=torch.int32, device=dev)
     split_offset = torch.empty(n_units + 1, dtype=torch.int32, device=dev)
-    mla_get_metadata(lengths, n_units, parts, sched, split_offset, default_length, stream)
+    fn = mla_get_metadata_request_local if request_local else mla_get_metadata
+    fn(lengths, n_units, parts, sched, split_offset, default_length, stream)
     ws = torch.empty(mla_workspace_bytes(n_units, rows_per_unit, parts), dtype=torch.uint8, device=dev)
     return Plan(sched, split_offset, parts, n_units, rows_per_unit, ws)
 

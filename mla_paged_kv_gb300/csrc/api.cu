@@ -12,7 +12,7 @@
 #include "common.cuh"
 
 namespace mla {
-cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, int, cudaStream_t);
 cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, void*, int, float*, cudaStream_t);
 cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, const void*, int,
                          cudaStream_t);
@@ -237,14 +237,28 @@ size_t mla_workspace_bytes(int n_units, int rows_per_unit, int num_parts) {
   return ws_layout(n_units, rows_per_unit, num_parts).total;
 }
 
-int mla_get_metadata(const int32_t* d_lengths, int default_length, int n_units, int num_parts, int32_t* d_sched,
-                     int32_t* d_split_offset, mla_stream_t stream) {
+namespace {
+
+int get_metadata(const int32_t* d_lengths, int default_length, int n_units, int num_parts, int32_t* d_sched,
+                 int32_t* d_split_offset, int request_local, mla_stream_t stream) {
   if (n_units < 1 || num_parts < 1 || !d_sched || !d_split_offset) return MLA_ERR_INVALID_ARG;
   if (d_lengths == nullptr && default_length < 0) return MLA_ERR_INVALID_ARG;
-  return launch_sched(d_lengths, default_length, n_units, num_parts, d_sched, d_split_offset,
+  return launch_sched(d_lengths, default_length, n_units, num_parts, d_sched, d_split_offset, request_local,
                       reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+int mla_get_metadata(const int32_t* d_lengths, int default_length, int n_units, int num_parts, int32_t* d_sched,
+                     int32_t* d_split_offset, mla_stream_t stream) {
+  return get_metadata(d_lengths, default_length, n_units, num_parts, d_sched, d_split_offset, 0, stream);
+}
+
+int mla_get_metadata_request_local(const int32_t* d_lengths, int default_length, int n_units, int num_parts,
+                                   int32_t* d_sched, int32_t* d_split_offset, mla_stream_t stream) {
+  return get_metadata(d_lengths, default_length, n_units, num_parts, d_sched, d_split_offset, 1, stream);
 }
 
 int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,

@@ -113,14 +113,11 @@ struct NtFromLengths {
   }
 };
 
-__global__ void __launch_bounds__(kSchedThreads) sched_kernel(const int32_t* __restrict__ lengths,
-                                                               int default_length, int n_units, int num_parts,
-                                                               int fixed_cost, int32_t* __restrict__ sched,
-                                                               int32_t* __restrict__ split_offset) {
-  __shared__ int s_nt[kSchedMaxSmemUnits];
-  __shared__ int s_diff[kSchedMaxSmemUnits + 1];
-  __shared__ long long s_warp_cost[kSchedThreads / 32];
-  __shared__ int s_warp[kSchedThreads / 32];
+// The native plan (see the file comment); n_units <= kSchedMaxSmemUnits keeps
+// the tile counts and the split-count difference array in shared memory.
+__device__ void plan_native(const int32_t* __restrict__ lengths, int default_length, int n_units, int num_parts,
+                            int fixed_cost, int32_t* __restrict__ sched, int32_t* __restrict__ split_offset,
+                            int* s_nt, int* s_diff, long long* s_warp_cost, int* s_warp) {
   const bool in_smem = n_units <= kSchedMaxSmemUnits;
   // difference array of the per-unit split counts: shared memory, or the
   // output array itself when there are too many units
@@ -178,10 +175,146 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const int32_t* __r
   if (threadIdx.x == 0) split_offset[n_units] = total;
 }
 
+__global__ void __launch_bounds__(kSchedThreads) sched_kernel(const int32_t* __restrict__ lengths,
+                                                               int default_length, int n_units, int num_parts,
+                                                               int fixed_cost, int32_t* __restrict__ sched,
+                                                               int32_t* __restrict__ split_offset) {
+  __shared__ int s_nt[kSchedMaxSmemUnits];
+  __shared__ int s_diff[kSchedMaxSmemUnits + 1];
+  __shared__ long long s_warp_cost[kSchedThreads / 32];
+  __shared__ int s_warp[kSchedThreads / 32];
+  plan_native(lengths, default_length, n_units, num_parts, fixed_cost, sched, split_offset, s_nt, s_diff,
+              s_warp_cost, s_warp);
+}
+
+// Request-local plan (FlashMLA PR #200, section "Scheduler policy", names a
+// request-local scheduler for its H=64 path without defining it; this is the
+// library's reading): no part spans two units.  Each unit with tiles gets one
+// part; the other parts go out in proportion to the tile counts, by largest
+// remainder (ties to the lower unit); a unit gets at most one part per tile;
+// unit b's k-th of s parts covers tiles [k*n/s, (k+1)*n/s).  Parts are in unit
+// order, unused ones empty.  With no tiles, more units with tiles than parts,
+// or more than kSchedLocalMaxUnits units, the native plan is used.
+constexpr int kSchedLocalMaxUnits = 1024;
+
+__global__ void __launch_bounds__(kSchedThreads) sched_local_kernel(const int32_t* __restrict__ lengths,
+                                                                     int default_length, int n_units, int num_parts,
+                                                                     int fixed_cost, int32_t* __restrict__ sched,
+                                                                     int32_t* __restrict__ split_offset) {
+  __shared__ int s_nt[kSchedMaxSmemUnits];
+  __shared__ int s_diff[kSchedMaxSmemUnits + 1];
+  __shared__ long long s_warp_cost[kSchedThreads / 32];
+  __shared__ int s_warp[kSchedThreads / 32];
+  __shared__ long long s_rem[kSchedLocalMaxUnits];
+  __shared__ long long s_sum[2];  // total tiles, parts given by the quotas
+  __shared__ int s_active;
+  if (n_units <= kSchedLocalMaxUnits) {
+    long long tiles = 0;
+    int act = 0;
+    for (int u = threadIdx.x; u < n_units; u += kSchedThreads) {
+      const int nt = num_tiles(lengths != nullptr ? lengths[u] : default_length);
+      s_nt[u] = nt;
+      tiles += nt;
+      act += nt > 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
+      act += __shfl_xor_sync(0xffffffffu, act, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+      s_warp_cost[threadIdx.x >> 5] = tiles;
+      s_warp[threadIdx.x >> 5] = act;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      long long t = 0;
+      int a = 0;
+      for (int w = 0; w < kSchedThreads / 32; ++w) {
+        t += s_warp_cost[w];
+        a += s_warp[w];
+      }
+      s_sum[0] = t;
+      s_active = a;
+    }
+    __syncthreads();
+  }
+  const int active = n_units <= kSchedLocalMaxUnits ? s_active : 0;
+  if (active == 0 || active > num_parts) {
+    __syncthreads();
+    plan_native(lengths, default_length, n_units, num_parts, fixed_cost, sched, split_offset, s_nt, s_diff,
+                s_warp_cost, s_warp);
+    return;
+  }
+  const long long total = s_sum[0];
+  const long long spare = num_parts - active;
+  // quotas: one part each, plus floor(n * spare / total); remainders kept for the ranking
+  long long given = 0;
+  for (int u = threadIdx.x; u < n_units; u += kSchedThreads) {
+    const long long x = static_cast<long long>(s_nt[u]) * spare;
+    const long long q = s_nt[u] > 0 ? x / total : 0;
+    s_diff[u] = s_nt[u] > 0 ? 1 + static_cast<int>(q) : 0;
+    s_rem[u] = s_nt[u] > 0 ? x - q * total : -1;
+    given += q;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) given += __shfl_xor_sync(0xffffffffu, given, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) s_warp_cost[threadIdx.x >> 5] = given;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long g = 0;
+    for (int w = 0; w < kSchedThreads / 32; ++w) g += s_warp_cost[w];
+    s_sum[1] = g;
+  }
+  __syncthreads();
+  const long long extra = spare - s_sum[1];
+  // the `extra` largest remainders (ties: lower unit) get one more part
+  for (int u = threadIdx.x; u < n_units; u += kSchedThreads) {
+    if (s_nt[u] == 0) continue;
+    const long long r = s_rem[u];
+    int rank = 0;
+    for (int v = 0; v < n_units; ++v) rank += (s_rem[v] > r) || (s_rem[v] == r && v < u);
+    int seats = s_diff[u] + (rank < extra ? 1 : 0);
+    s_diff[u] = min(seats, s_nt[u]);
+  }
+  __syncthreads();
+  // split offsets = exclusive prefix sum of the part counts (contiguous chunk per thread)
+  const int chunk = (n_units + kSchedThreads - 1) / kSchedThreads;
+  const int u0 = min(static_cast<int>(threadIdx.x) * chunk, n_units);
+  const int u1 = min(u0 + chunk, n_units);
+  int csum = 0;
+  for (int u = u0; u < u1; ++u) csum += s_diff[u];
+  int used = 0;
+  int off = block_exclusive_scan(csum, s_warp, &used);
+  for (int u = u0; u < u1; ++u) {
+    split_offset[u] = off;
+    const int n = s_nt[u], parts = s_diff[u];
+    for (int k = 0; k < parts; ++k) {
+      const int lo = static_cast<int>(static_cast<long long>(k) * n / parts);
+      const int hi = static_cast<int>(static_cast<long long>(k + 1) * n / parts);
+      int4* e = reinterpret_cast<int4*>(sched + (off + k) * MLA_SCHED_INTS);
+      e[0] = hi < n ? make_int4(u, lo, u, hi) : make_int4(u, lo, u + 1, 0);
+      e[1] = make_int4(k, 0, 0, 0);
+    }
+    off += parts;
+  }
+  if (threadIdx.x == 0) split_offset[n_units] = used;
+  for (int p = used + static_cast<int>(threadIdx.x); p < num_parts; p += kSchedThreads) {
+    int4* e = reinterpret_cast<int4*>(sched + p * MLA_SCHED_INTS);
+    e[0] = make_int4(n_units, 0, n_units, 0);
+    e[1] = make_int4(0, 0, 0, 0);
+  }
+}
+
 cudaError_t launch_sched(const int32_t* lengths, int default_length, int n_units, int num_parts,
-                         int32_t* sched, int32_t* split_offset, cudaStream_t stream) {
-  sched_kernel<<<1, kSchedThreads, 0, stream>>>(lengths, default_length, n_units, num_parts, MLA_SPLIT_FIXED_COST,
-                                                sched, split_offset);
+                         int32_t* sched, int32_t* split_offset, int request_local, cudaStream_t stream) {
+  if (request_local)
+    sched_local_kernel<<<1, kSchedThreads, 0, stream>>>(lengths, default_length, n_units, num_parts,
+                                                        MLA_SPLIT_FIXED_COST, sched, split_offset);
+  else
+    sched_kernel<<<1, kSchedThreads, 0, stream>>>(lengths, default_length, n_units, num_parts, MLA_SPLIT_FIXED_COST,
+                                                  sched, split_offset);
   return cudaGetLastError();
 }
 

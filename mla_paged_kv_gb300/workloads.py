@@ -196,7 +196,7 @@ def sparse_case(batch, s_q, h_q, *, topk=2048, pages_per_req=512, topk_lo=1024,
                       scale=(1.0 / math.sqrt(D_QK)) if scale is None else scale, name=name)
 
 
-# The five workloads the benchmark and the parity tests use, named by shape.
+# The workloads the benchmark and the parity tests use, named by shape.
 WORKLOADS = {
     "dense_b1_hq16_sk256_fp32out": dict(kind="dense", batch=1, s_q=1, h_q=16, seqlen_lo=256,
                                         seqlen_hi=256, out_fp32=True, seed=1001),
@@ -210,6 +210,13 @@ WORKLOADS = {
     "sparse_fp8_b16_hq128_topk2048": dict(kind="sparse", batch=16, s_q=1, h_q=128, topk=2048,
                                           pages_per_req=512, topk_lo=1024, topk_hi=2048,
                                           seed=1005),
+    # the H=64 and S_q>1 query shapes of the packed-path page's grid, full top-k prefix
+    "sparse_fp8_b4_sq4_hq64_topk2048": dict(kind="sparse", batch=4, s_q=4, h_q=64, topk=2048,
+                                            pages_per_req=512, topk_lo=2048, topk_hi=2048,
+                                            seed=1006),
+    "sparse_fp8_b2_sq8_hq128_topk2048": dict(kind="sparse", batch=2, s_q=8, h_q=128, topk=2048,
+                                             pages_per_req=512, topk_lo=2048, topk_hi=2048,
+                                             seed=1007),
 }
 
 

@@ -117,3 +117,13 @@ def test_dense_block_table_permutation():
                          scale=case.scale, out_fp32=False)
     o2, l2, _ = run_dense(case2, num_parts=4)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_dense_request_local_plan():
+    case = wl.dense_case(5, 2, 64, 0, seqlens=[900, 130, 2000, 64, 3000], causal=True, seed=61)
+    c = to_dev(case)
+    pl = mla.plan(c.cache_seqlens, 5, 2 * 64, request_local=True)
+    out, lse = mla.decode(c.q, c.kv, c.block_table, c.cache_seqlens, causal=True, softmax_scale=case.scale, pl=pl)
+    torch.cuda.synchronize()
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)

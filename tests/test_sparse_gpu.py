@@ -144,3 +144,18 @@ def test_unpack_every_e4m3_code():
     ref, bad = orc.unpack_records(kv8.numpy(), idx.numpy())
     assert bad == 0 and int(status.item()) == 0
     assert np.array_equal(k.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("b,s_q,h_q", [(4, 4, 64), (2, 8, 128), (1, 16, 64)])
+def test_sparse_request_local_plan(b, s_q, h_q):
+    """h_q=64 and s_q>1 query shapes of the sparse path under the request-local plan,
+    and the same inputs under the native plan."""
+    case = wl.sparse_case(b, s_q, h_q, topk=512, pages_per_req=16, topk_lo=64, topk_hi=512, seed=b * 100 + s_q)
+    ro, rl, _ = oracle(case)
+    c = to_dev(case)
+    for local in (True, False):
+        pl = mla.plan(c.topk_length.reshape(-1).contiguous(), b * s_q, h_q, sparse=True, default_length=512,
+                      device=torch.device("cuda"), request_local=local)
+        out, lse = mla.sparse_decode(c.q, c.kv8, c.indices, c.topk_length, softmax_scale=case.scale, pl=pl)
+        torch.cuda.synchronize()
+        compare(out, lse, ro, rl)

@@ -1,4 +1,4 @@
-"""The five named workloads at their full sizes, in the launch configuration
+"""The named workloads at their full sizes, in the launch configuration
 bench.py times (partition count from mla_num_parts, default plan), against the
 oracle on every request (the vectorised fp64 oracle takes well under a second
 per workload)."""
@@ -25,8 +25,10 @@ def test_dense_workload_full_size(name):
     compare(out, lse, ro, rl)
 
 
-def test_sparse_workload_full_size():
-    case = wl.make("sparse_fp8_b16_hq128_topk2048")
+@pytest.mark.parametrize("name", ["sparse_fp8_b16_hq128_topk2048", "sparse_fp8_b4_sq4_hq64_topk2048",
+                                  "sparse_fp8_b2_sq8_hq128_topk2048"])
+def test_sparse_workload_full_size(name):
+    case = wl.make(name)
     c = to_dev(case)
     out, lse = mla.sparse_decode(c.q, c.kv8, c.indices, c.topk_length, softmax_scale=case.scale)
     torch.cuda.synchronize()
