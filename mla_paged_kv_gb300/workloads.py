@@ -66,9 +66,13 @@ class DenseCase:
     def h_q(self):
         return self.q.shape[2]
 
+    @property
+    def h_kv(self):
+        return 1 if self.kv.dim() == 3 else self.kv.shape[2]
+
     def kv_bytes(self) -> int:
-        """Unique KV bytes read: every valid token's 576 bf16 entries once."""
-        return int(self.cache_seqlens.to(torch.int64).sum().item()) * D_QK * 2
+        """Unique KV bytes read: every valid token's 576 16-bit entries once per KV head."""
+        return int(self.cache_seqlens.to(torch.int64).sum().item()) * D_QK * 2 * self.h_kv
 
 
 @dataclass
@@ -106,7 +110,11 @@ def _gen(seed: int) -> torch.Generator:
 
 def dense_case(batch, s_q, h_q, seqlen_lo, seqlen_hi=None, *, causal=False, seed=0,
                pool_factor=1.2, q_scale=1.0, out_fp32=False, seqlens=None,
-               scale=None, poison=True, name="") -> DenseCase:
+               scale=None, poison=True, name="", h_kv=1, dtype=torch.bfloat16) -> DenseCase:
+    """Seeded dense case: N(0,1) latent rows in a shuffled 64-token page pool
+    (1.2x the pages in use; unused slots hold +-1e3 poison), the block table,
+    and q.  h_kv > 1 gives a [pages, 64, h_kv, 576] cache; dtype is that of q
+    and the cache (bf16 or fp16)."""
     g = _gen(seed)
     if seqlens is None:
         hi = seqlen_lo if seqlen_hi is None else seqlen_hi
@@ -122,7 +130,8 @@ def dense_case(batch, s_q, h_q, seqlen_lo, seqlen_hi=None, *, causal=False, seed
     for b in range(batch):
         bt[b, :npg[b]] = perm[pos:pos + npg[b]].to(torch.int32)
         pos += npg[b]
-    kv = torch.randn(pool, PAGE, D_QK, generator=g)
+    kv = torch.randn(pool, PAGE, D_QK, generator=g) if h_kv == 1 else torch.randn(pool, PAGE, h_kv, D_QK,
+                                                                                      generator=g)
     if poison:
         used = torch.zeros(pool, PAGE, dtype=torch.bool)
         for b in range(batch):
@@ -131,9 +140,11 @@ def dense_case(batch, s_q, h_q, seqlen_lo, seqlen_hi=None, *, causal=False, seed
                 n = min(PAGE, L - lp * PAGE)
                 used[int(bt[b, lp]), :n] = True
         sign = torch.where(torch.rand(pool, PAGE, 1, generator=g) < 0.5, -1.0, 1.0)
-        kv = torch.where(used[:, :, None], kv, sign * POISON)
-    kv = kv.to(torch.bfloat16)
-    q = (torch.randn(batch, s_q, h_q, D_QK, generator=g) * q_scale).to(torch.bfloat16)
+        if h_kv > 1:
+            used, sign = used[:, :, None], sign[:, :, None]
+        kv = torch.where(used[..., None], kv, sign * POISON)
+    kv = kv.to(dtype)
+    q = (torch.randn(batch, s_q, h_q, D_QK, generator=g) * q_scale).to(dtype)
     return DenseCase(q=q, kv=kv, block_table=bt, cache_seqlens=seqlens.to(torch.int32),
                      causal=bool(causal), scale=(1.0 / math.sqrt(D_QK)) if scale is None else scale,
                      out_fp32=bool(out_fp32), name=name)

@@ -217,23 +217,34 @@ def causal_mask(s_q: int, h_q: int, L: int, causal: bool) -> np.ndarray:
 def dense_decode(q, kv, block_table, cache_seqlens, causal, scale, batches=None):
     """Dense MLA paged decode.
 
-    q: [B, s_q, h_q, 576], kv: [num_pages, 64, 576] (any real dtype; used as
-    float64), block_table: [B, max_pages] int, cache_seqlens: [B] int.
-    Returns out [B, s_q, h_q, 512] and lse [B, s_q, h_q] in float64.
-    ``batches`` restricts the work to a subset of requests (others stay 0/-inf).
+    q: [B, s_q, h_q, 576]; kv: [num_pages, 64, 576], or [num_pages, 64, h_kv,
+    576] for h_kv latent KV heads (PR #183 *Test plan* sweeps hk = 1..4); any
+    real dtype, used as float64.  Query head h reads KV head h // (h_q // h_kv)
+    (the pages do not spell the grouping out: consecutive query heads share a
+    KV head, the usual grouped-query reading).  block_table: [B, max_pages]
+    int, cache_seqlens: [B] int.  Returns out [B, s_q, h_q, 512] and lse
+    [B, s_q, h_q] in float64.  ``batches`` restricts the work to a subset of
+    requests (others stay 0/-inf).
     """
     q = np.asarray(q, dtype=np.float64)
     kv = np.asarray(kv)          # gathered rows are widened to float64 one by one
+    if kv.ndim == 3:
+        kv = kv[:, :, None, :]
     B, s_q, h_q, _ = q.shape
+    h_kv = kv.shape[2]
+    assert h_q % h_kv == 0
+    G = h_q // h_kv
     out = np.zeros((B, s_q, h_q, D_V), dtype=np.float64)
     lse = np.full((B, s_q, h_q), -np.inf, dtype=np.float64)
     for b in (range(B) if batches is None else batches):
         L = int(cache_seqlens[b])
-        keys = dense_keys(kv, block_table, b, L)
-        qrows = q[b].reshape(s_q * h_q, D_QK)
-        o, l = attend(qrows, keys, scale, causal_mask(s_q, h_q, L, causal))
-        out[b] = o.reshape(s_q, h_q, D_V)
-        lse[b] = l.reshape(s_q, h_q)
+        for g in range(h_kv):
+            keys = dense_keys(kv[:, :, g, :], block_table, b, L)
+            heads = slice(g * G, (g + 1) * G)
+            qrows = q[b][:, heads, :].reshape(s_q * G, D_QK)
+            o, l = attend(qrows, keys, scale, causal_mask(s_q, G, L, causal))
+            out[b][:, heads] = o.reshape(s_q, G, D_V)
+            lse[b][:, heads] = l.reshape(s_q, G)
     return out, lse
 
 

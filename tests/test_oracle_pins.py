@@ -451,3 +451,66 @@ def test_packed_mask_bit_controls_the_slot():
     ind[0, 0, 17] = -1
     o2, l2, _ = orc.sparse_decode(q, sc.kv8.numpy(), ind.numpy(), None, sc.scale)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------- several latent KV heads, fp16 inputs
+
+def sdpa_grouped_reference(case, b):
+    """torch fp64 SDPA with the KV heads expanded to the query heads by repeat_interleave
+    (enable_gqa-style grouping done by hand), keys gathered with torch indexing."""
+    L = int(case.cache_seqlens[b])
+    h_kv = case.kv.shape[2]
+    flat = case.kv.double().reshape(-1, h_kv, 576)             # [slots, h_kv, 576]
+    j = torch.arange(L)
+    slot = case.block_table[b].long()[j // 64] * 64 + (j % 64)
+    K = flat[slot].permute(1, 0, 2)                             # [h_kv, L, 576]
+    s_q, h_q = case.s_q, case.h_q
+    K = K.repeat_interleave(h_q // h_kv, dim=0)                 # [h_q, L, 576]
+    q = case.q[b].double().permute(1, 0, 2)                     # [h_q, s_q, 576]
+    tok = torch.arange(s_q)
+    allowed = (j[None, :] <= (L - s_q + tok[:, None])) if case.causal else torch.ones(s_q, L, dtype=torch.bool)
+    bias = torch.zeros(s_q, L, dtype=torch.float64).masked_fill(~allowed, float("-inf"))
+    out = torch.nn.functional.scaled_dot_product_attention(q, K, K[..., :512], attn_mask=bias, scale=case.scale)
+    lse = torch.logsumexp(q @ K.transpose(1, 2) * case.scale + bias, dim=-1)
+    return out.permute(1, 0, 2).numpy(), lse.T.numpy()
+
+
+@pytest.mark.parametrize("h_kv,h_q,s_q,causal", [(2, 8, 1, False), (4, 16, 2, True), (3, 6, 3, True)])
+def test_grouped_kv_heads_match_torch_sdpa(h_kv, h_q, s_q, causal):
+    case = wl.dense_case(2, s_q, h_q, 0, seqlens=[70, 150], causal=causal, h_kv=h_kv, seed=h_kv * 10 + s_q)
+    assert case.kv.shape[2] == h_kv
+    out, lse = orc.dense_decode(f64(case.q), f64(case.kv), case.block_table.numpy(), case.cache_seqlens.numpy(),
+                                case.causal, case.scale)
+    for b in range(2):
+        ro, rl = sdpa_grouped_reference(case, b)
+        assert np.abs(out[b] - ro).max() < TOL and np.abs(lse[b] - rl).max() < TOL
+
+
+def test_identical_kv_heads_reduce_to_one_head():
+    one = wl.dense_case(1, 2, 8, 0, seqlens=[200], causal=True, seed=77)
+    kv2 = torch.stack([one.kv, one.kv], dim=2)                 # [pages, 64, 2, 576], both heads equal
+    o1, l1 = orc.dense_decode(f64(one.q), f64(one.kv), one.block_table.numpy(), one.cache_seqlens.numpy(), True,
+                              one.scale)
+    o2, l2 = orc.dense_decode(f64(one.q), f64(kv2), one.block_table.numpy(), one.cache_seqlens.numpy(), True,
+                              one.scale)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_swapping_kv_heads_swaps_head_groups():
+    case = wl.dense_case(1, 1, 8, 0, seqlens=[130], h_kv=2, seed=78)
+    q = f64(case.q)
+    o, l = orc.dense_decode(q, f64(case.kv), case.block_table.numpy(), case.cache_seqlens.numpy(), False, case.scale)
+    q_sw = np.concatenate([q[:, :, 4:], q[:, :, :4]], axis=2)
+    o_sw, l_sw = orc.dense_decode(q_sw, f64(case.kv.flip(2)), case.block_table.numpy(), case.cache_seqlens.numpy(),
+                                  False, case.scale)
+    assert np.array_equal(o_sw[:, :, 4:], o[:, :, :4]) and np.array_equal(o_sw[:, :, :4], o[:, :, 4:])
+    assert np.array_equal(l_sw[:, :, 4:], l[:, :, :4])
+
+
+def test_fp16_case_holds_exact_fp16_values():
+    case = wl.dense_case(1, 1, 4, 0, seqlens=[64], dtype=torch.float16, seed=79)
+    assert case.q.dtype == torch.float16 and case.kv.dtype == torch.float16
+    out, lse = orc.dense_decode(f64(case.q), f64(case.kv), case.block_table.numpy(), case.cache_seqlens.numpy(),
+                                False, case.scale)
+    ro, rl = sdpa_dense_reference(case, 0)
+    assert np.abs(out[0] - ro).max() < TOL and np.abs(lse[0] - rl).max() < TOL
