@@ -52,6 +52,14 @@ typedef enum {
   MLA_ERR_BAD_INDEX = 5    /* device: block-table entry or sparse index outside the pool */
 } mla_status_t;
 
+/* Element types of query, cache and output tensors.  The values keep the
+ * meaning of an older 0/1 "fp32 output" flag: 0 = bf16, 1 = fp32. */
+typedef enum {
+  MLA_DTYPE_BF16 = 0,
+  MLA_DTYPE_FP32 = 1, /* outputs only */
+  MLA_DTYPE_FP16 = 2
+} mla_dtype_t;
+
 /* Fixed geometry (FlashMLA PR #183 Design; PR #200 "SM90 packing kernel"). */
 #define MLA_PAGE_SIZE 64      /* tokens per page */
 #define MLA_D_QK 576          /* latent row: 512 NoPE + 64 RoPE */
@@ -73,6 +81,12 @@ const char* mla_status_string(int status);
  *   is_sparse_fp8: 0 for the dense bf16 kernel, 1 for the sparse FP8 one.
  * Returns >= 1, or a negative mla_status_t on error. */
 int mla_num_parts(int rows_per_unit, int is_sparse_fp8);
+
+/* The same for the dense kernel with h_kv latent KV heads: one partition
+ * runs h_kv * (row blocks per head group) CTA pairs, counted exactly as
+ * mla_decode_fwd counts them.  For h_kv = 1 it equals
+ * mla_num_parts(s_q * h_q, 0).  Returns >= 1, or a negative mla_status_t. */
+int mla_num_parts_dense(int s_q, int h_q, int h_kv);
 
 /* Bytes of split workspace needed: (n_units + num_parts) split slots, each
  * rows_per_unit x 512 fp32 partial outputs plus rows_per_unit fp32 LSEs.
@@ -110,38 +124,46 @@ int mla_get_metadata(const int32_t* d_lengths, int default_length, int n_units, 
 int mla_get_metadata_request_local(const int32_t* d_lengths, int default_length, int n_units, int num_parts,
                                    int32_t* d_sched, int32_t* d_split_offset, mla_stream_t stream);
 
-/* Dense bf16 MLA decode: split-KV attention kernel, then the combine kernel
- * (chained with programmatic dependent launch).
- *   d_q            bf16 [batch, s_q, h_q, 576]
- *   d_kv           bf16 [num_pages, 64, 576] paged latent cache (one KV head)
+/* Dense MLA decode: split-KV attention kernel, then the combine kernel
+ * (chained with programmatic dependent launch).  FlashMLA PR #183 (Summary,
+ * Test plan) checks bf16 and fp16 and 1 to 4 KV heads; both are here.
+ *   d_q            [batch, s_q, h_q, 576], element type `dtype`
+ *   d_kv           [num_pages, 64, h_kv, 576] paged latent cache, type `dtype`
+ *                  (h_kv = 1: [num_pages, 64, 576])
  *   d_block_table  int32 [batch, max_pages]: logical page -> physical page
  *   d_cache_seqlens int32 [batch]: keys of request b, including its s_q new
  *                  tokens.  Key j of request b is row j%64 of page
  *                  block_table[b][j/64].
+ *   h_kv           latent KV heads, dividing h_q; query head h reads KV head
+ *                  h / (h_q / h_kv).  h_q / h_kv <= 128 when h_kv > 1.
+ *   dtype          MLA_DTYPE_BF16 or MLA_DTYPE_FP16 (q and kv alike; P is
+ *                  rounded to the same type before the P V product).
  *   causal         1: query token i sees keys j <= L_b - s_q + i.
  *   softmax_scale  multiplies q.k (e.g. 1/sqrt(576)); must be finite and > 0.
- *   d_sched, d_split_offset, num_parts: from mla_get_metadata with
- *                  d_lengths = d_cache_seqlens, n_units = batch.
+ *   d_sched, d_split_offset, num_parts: from mla_get_metadata (or its
+ *                  request-local form) with d_lengths = d_cache_seqlens,
+ *                  n_units = batch.
  *   d_workspace    >= mla_workspace_bytes(batch, s_q*h_q, num_parts) bytes.
- *   d_out          [batch, s_q, h_q, 512], bf16 (out_fp32 = 0) or fp32 (1)
+ *   d_out          [batch, s_q, h_q, 512] of out_type: MLA_DTYPE_BF16,
+ *                  MLA_DTYPE_FP16 or MLA_DTYPE_FP32 (0, 2, 1)
  *   d_lse          fp32 [batch, s_q, h_q]: natural-log LSE of the scaled
  *                  scores; -inf (and out = 0) for a row that sees no key.
  *   d_status       int32, caller-zeroed; see conventions above. */
 int mla_decode_fwd(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
-                   int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int causal,
-                   float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
-                   void* d_workspace, size_t workspace_bytes, void* d_out, int out_fp32, float* d_lse,
-                   int32_t* d_status, mla_stream_t stream);
+                   int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int h_kv,
+                   int dtype, int causal, float softmax_scale, const int32_t* d_sched,
+                   const int32_t* d_split_offset, int num_parts, void* d_workspace, size_t workspace_bytes,
+                   void* d_out, int out_type, float* d_lse, int32_t* d_status, mla_stream_t stream);
 
 /* The first half of mla_decode_fwd alone: the split-KV attention kernel.
  * Units with exactly one split are written straight to d_out/d_lse; the
  * others leave their partials in d_workspace for mla_combine (or for an
  * exchange step before it).  Same arguments as mla_decode_fwd. */
 int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
-                      int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int causal,
-                      float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
-                      int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, int out_fp32,
-                      float* d_lse, int32_t* d_status, mla_stream_t stream);
+                      int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int h_kv,
+                      int dtype, int causal, float softmax_scale, const int32_t* d_sched,
+                      const int32_t* d_split_offset, int num_parts, void* d_workspace, size_t workspace_bytes,
+                      void* d_out, int out_type, float* d_lse, int32_t* d_status, mla_stream_t stream);
 
 /* Size of the device array mla_decode_fwd_static_ws keeps its split
  * workspace in: 64 MiB on every GPU that loads the library. */
@@ -171,10 +193,10 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
  *    that can overlap on the GPU (unordered streams) race on it and corrupt
  *    each other's results: order them on one stream or with events. */
 int mla_decode_fwd_static_ws(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
-                             int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int causal,
-                             float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
-                             int num_parts, void* d_out, int out_fp32, float* d_lse, int32_t* d_status,
-                             mla_stream_t stream);
+                             int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int h_kv,
+                             int dtype, int causal, float softmax_scale, const int32_t* d_sched,
+                             const int32_t* d_split_offset, int num_parts, void* d_out, int out_type, float* d_lse,
+                             int32_t* d_status, mla_stream_t stream);
 
 /* LSE-weighted combine of split partials (FlashMLA PR #183 Summary: the
  * combine kernel merges the splits).  For every unit with != 1 split and
@@ -184,11 +206,12 @@ int mla_decode_fwd_static_ws(const void* d_q, const void* d_kv, const int32_t* d
  * splits are all -inf, gets out = 0, lse = -inf.  Units with exactly one
  * split are left alone (the decode kernel wrote them).
  *   d_workspace as filled by mla_decode_splits / the sparse kernel.
- *   d_out [n_units, rows_per_unit, 512] bf16 or fp32, d_lse [n_units, rows].
+ *   d_out [n_units, rows_per_unit, 512] of out_type (MLA_DTYPE_BF16, _FP32 or
+ *   _FP16), d_lse [n_units, rows].
  * Launched with programmatic dependent launch: it may start before the
  * previous kernel on the stream ends and waits for it on the device. */
 int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* d_split_offset, int n_units,
-                int rows_per_unit, int num_parts, void* d_out, int out_fp32, float* d_lse, mla_stream_t stream);
+                int rows_per_unit, int num_parts, void* d_out, int out_type, float* d_lse, mla_stream_t stream);
 
 /* Sparse FP8 MLA decode (FlashMLA PR #200).  Query token (b, i) attends to
  * the records selected by d_indices[b][i][0 .. topk_length[b][i]); entry t

@@ -26,7 +26,7 @@ __all__ = [
     "mla_get_metadata", "mla_decode_fwd", "mla_decode_splits", "mla_combine",
     "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws",
     "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd",
-    "mla_get_metadata_request_local", "plan", "decode",
+    "mla_get_metadata_request_local", "mla_num_parts_dense", "plan", "decode",
     "sparse_decode", "pack_selected_kv", "packed_sparse_decode",
     "EXPORTED_SYMBOLS",
 ]
@@ -35,7 +35,7 @@ EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_num_parts", "mla_workspace_bytes", "mla_get_metadata", "mla_decode_fwd",
     "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack",
     "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv",
-    "mla_sparse_fp8_packed_decode_fwd", "mla_get_metadata_request_local",
+    "mla_sparse_fp8_packed_decode_fwd", "mla_get_metadata_request_local", "mla_num_parts_dense",
 )
 
 _P = ctypes.c_void_p
@@ -46,18 +46,20 @@ _SZ = ctypes.c_size_t
 _SIGS = {
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_num_parts": (_I, [_I, _I]),
+    "mla_num_parts_dense": (_I, [_I, _I, _I]),
     "mla_workspace_bytes": (_SZ, [_I, _I, _I]),
     "mla_get_metadata": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "mla_get_metadata_request_local": (_I, [_P, _I, _I, _I, _P, _P, _P]),
-    "mla_decode_fwd": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _I, _P, _P, _P]),
-    "mla_decode_splits": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _I, _P, _P,
-                               _P]),
+    "mla_decode_fwd": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _I, _P,
+                            _P, _P]),
+    "mla_decode_splits": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _I,
+                               _P, _P, _P]),
     "mla_combine": (_I, [_P, _SZ, _P, _I, _I, _I, _P, _I, _P, _P]),
     "mla_sparse_fp8_decode_fwd": (_I, [_P, _P, _I, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _P, _P,
                                        _P]),
     "mla_sparse_fp8_unpack": (_I, [_P, _I, _P, _I, _P, _P, _P]),
-    "mla_decode_fwd_static_ws": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _F, _P, _P, _I, _P, _I, _P, _P,
-                                      _P]),
+    "mla_decode_fwd_static_ws": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _I, _P, _I,
+                                      _P, _P, _P]),
     "mla_packed_kv_workspace_bytes": (_SZ, [_I, _I]),
     "mla_pack_selected_kv": (_I, [_P, _I, _P, _I, _P, _I, _P, _SZ, _P, _P]),
     "mla_sparse_fp8_packed_decode_fwd": (_I, [_P, _P, _SZ, _I, _P, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _P, _P,
@@ -128,6 +130,13 @@ def mla_num_parts(rows_per_unit: int, is_sparse_fp8: bool = False) -> int:
     return n
 
 
+def mla_num_parts_dense(s_q: int, h_q: int, h_kv: int = 1) -> int:
+    n = load_library().mla_num_parts_dense(int(s_q), int(h_q), int(h_kv))
+    if n < 1:
+        raise MlaError(-n, "mla_num_parts_dense")
+    return n
+
+
 def mla_workspace_bytes(n_units: int, rows_per_unit: int, num_parts: int) -> int:
     return int(load_library().mla_workspace_bytes(int(n_units), int(rows_per_unit), int(num_parts)))
 
@@ -153,32 +162,50 @@ def mla_get_metadata_request_local(lengths, n_units, num_parts, sched, split_off
               stream)
 
 
-def _dense_args(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse, status,
-                causal, softmax_scale, stream):
-    _need(q, torch.bfloat16, "q", 4)
-    _need(kv, torch.bfloat16, "kv", 3)
+DTYPE_BF16, DTYPE_FP32, DTYPE_FP16 = 0, 1, 2          # mla_dtype_t
+_DTYPE_CODE = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_FP32, torch.float16: DTYPE_FP16}
+
+
+def _dense_inputs(q, kv, block_table, cache_seqlens, out, lse, status):
+    """Checks shared by the dense entry points; returns (h_kv, dtype code, out type code)."""
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("q must be bf16 or fp16")
+    _need(q, q.dtype, "q", 4)
+    if kv.dtype != q.dtype or kv.dim() not in (3, 4):
+        raise TypeError("kv must have q's dtype and be [pages, 64, 576] or [pages, 64, h_kv, 576]")
+    _need(kv, q.dtype, "kv")
     _need(block_table, torch.int32, "block_table", 2)
     _need(cache_seqlens, torch.int32, "cache_seqlens", 1)
-    _need(workspace, torch.uint8, "workspace")
     _need(lse, torch.float32, "lse")
     _need(status, torch.int32, "status")
-    if out.dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("out must be bf16 or fp32")
+    if out.dtype not in _DTYPE_CODE:
+        raise TypeError("out must be bf16, fp16 or fp32")
     B, s_q, h_q, d = q.shape
-    if d != 576 or kv.shape[1:] != (64, 576):
-        raise ValueError("q must be [B, s_q, h_q, 576] and kv [pages, 64, 576]")
+    h_kv = 1 if kv.dim() == 3 else kv.shape[2]
+    if d != 576 or kv.shape[1] != 64 or kv.shape[-1] != 576 or h_q % h_kv:
+        raise ValueError("q must be [B, s_q, h_q, 576], kv [pages, 64, (h_kv,) 576] with h_kv dividing h_q")
     if tuple(out.shape) != (B, s_q, h_q, 512) or tuple(lse.shape) != (B, s_q, h_q):
         raise ValueError("out must be [B, s_q, h_q, 512] and lse [B, s_q, h_q]")
     if block_table.shape[0] != B or cache_seqlens.shape[0] != B:
         raise ValueError("block_table / cache_seqlens batch mismatch")
+    return h_kv, _DTYPE_CODE[q.dtype], _DTYPE_CODE[out.dtype]
+
+
+def _dense_args(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse, status,
+                causal, softmax_scale, stream):
+    h_kv, dt, ot = _dense_inputs(q, kv, block_table, cache_seqlens, out, lse, status)
+    _need(workspace, torch.uint8, "workspace")
+    B, s_q, h_q, _ = q.shape
     return (_ptr(q), _ptr(kv), _ptr(block_table), block_table.shape[1], kv.shape[0], _ptr(cache_seqlens), B, s_q,
-            h_q, int(bool(causal)), float(softmax_scale), _ptr(sched), _ptr(split_offset), int(num_parts),
-            _ptr(workspace), workspace.numel(), _ptr(out), int(out.dtype == torch.float32), _ptr(lse),
-            _ptr(status), _stream(stream))
+            h_q, h_kv, dt, int(bool(causal)), float(softmax_scale), _ptr(sched), _ptr(split_offset),
+            int(num_parts), _ptr(workspace), workspace.numel(), _ptr(out), ot, _ptr(lse), _ptr(status),
+            _stream(stream))
 
 
 def mla_decode_fwd(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse, status,
                    causal=False, softmax_scale=1.0 / 24.0, stream=None):
+    """Dense decode.  q/kv bf16 or fp16 (same type); kv [pages, 64, 576] or
+    [pages, 64, h_kv, 576]; out bf16, fp16 or fp32."""
     args = _dense_args(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse,
                        status, causal, softmax_scale, stream)
     _check(load_library().mla_decode_fwd(*args), "mla_decode_fwd")
@@ -197,19 +224,12 @@ def mla_decode_fwd_static_ws(q, kv, block_table, cache_seqlens, sched, split_off
     keeps the split partials in its own fixed device array (64 MiB per GPU).
     Nothing is allocated; a problem whose partials do not fit raises
     MLA_ERR_UNSUPPORTED."""
-    _need(q, torch.bfloat16, "q", 4)
-    _need(kv, torch.bfloat16, "kv", 3)
-    _need(block_table, torch.int32, "block_table", 2)
-    _need(cache_seqlens, torch.int32, "cache_seqlens", 1)
-    _need(lse, torch.float32, "lse")
-    _need(status, torch.int32, "status")
-    if out.dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("out must be bf16 or fp32")
+    h_kv, dt, ot = _dense_inputs(q, kv, block_table, cache_seqlens, out, lse, status)
     B, s_q, h_q, _ = q.shape
     rc = load_library().mla_decode_fwd_static_ws(
         _ptr(q), _ptr(kv), _ptr(block_table), block_table.shape[1], kv.shape[0], _ptr(cache_seqlens), B, s_q, h_q,
-        int(bool(causal)), float(softmax_scale), _ptr(sched), _ptr(split_offset), int(num_parts), _ptr(out),
-        int(out.dtype == torch.float32), _ptr(lse), _ptr(status), _stream(stream))
+        h_kv, dt, int(bool(causal)), float(softmax_scale), _ptr(sched), _ptr(split_offset), int(num_parts),
+        _ptr(out), ot, _ptr(lse), _ptr(status), _stream(stream))
     _check(rc, "mla_decode_fwd_static_ws")
 
 
@@ -217,7 +237,7 @@ def mla_combine(workspace, split_offset, n_units, rows_per_unit, num_parts, out,
     _need(workspace, torch.uint8, "workspace")
     _check(load_library().mla_combine(_ptr(workspace), workspace.numel(), _ptr(split_offset), int(n_units),
                                       int(rows_per_unit), int(num_parts), _ptr(out),
-                                      int(out.dtype == torch.float32), _ptr(lse), _stream(stream)), "mla_combine")
+                                      _DTYPE_CODE[out.dtype], _ptr(lse), _stream(stream)), "mla_combine")
 
 
 def mla_sparse_fp8_decode_fwd(q, kv8, indices, topk_length, sched, split_offset, num_parts, workspace, out, lse,
@@ -323,8 +343,9 @@ def decode(q, kv, block_table, cache_seqlens, causal=False, softmax_scale=None, 
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(576)
     if pl is None:
-        pl = plan(cache_seqlens, B, s_q * h_q)
-    out = torch.empty(B, s_q, h_q, 512, dtype=torch.float32 if out_fp32 else torch.bfloat16, device=q.device)
+        h_kv = 1 if kv.dim() == 3 else kv.shape[2]
+        pl = plan(cache_seqlens, B, s_q * h_q, num_parts=mla_num_parts_dense(s_q, h_q, h_kv))
+    out = torch.empty(B, s_q, h_q, 512, dtype=torch.float32 if out_fp32 else q.dtype, device=q.device)
     lse = torch.empty(B, s_q, h_q, dtype=torch.float32, device=q.device)
     status = torch.zeros(1, dtype=torch.int32, device=q.device)
     mla_decode_fwd(q, kv, block_table, cache_seqlens, pl.sched, pl.split_offset, pl.num_parts, pl.workspace, out,

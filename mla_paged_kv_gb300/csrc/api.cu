@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -14,11 +15,11 @@
 namespace mla {
 cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, int, cudaStream_t);
 cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, void*, int, float*, cudaStream_t);
-cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, const void*, int,
+cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, const void*, int, int,
                          cudaStream_t);
 int dense_smem_bytes();
 int dense_threads();
-const void* dense_kernel_ptr();
+const void* dense_kernel_ptr(int half);
 cudaError_t launch_sparse(const CUtensorMap&, const DecodeParams&, int, cudaStream_t);
 int sparse_smem_bytes();
 int sparse_threads();
@@ -94,7 +95,9 @@ const DeviceInfo& device_info() {
     d.ready = true;
     return d;
   }
-  if (cudaFuncSetAttribute(dense_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
+  if (cudaFuncSetAttribute(dense_kernel_ptr(0), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(dense_kernel_ptr(1), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
           cudaSuccess ||
       cudaFuncSetAttribute(sparse_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            sparse_smem_bytes()) != cudaSuccess) {
@@ -103,7 +106,7 @@ const DeviceInfo& device_info() {
     d.ready = true;
     return d;
   }
-  d.dense_clusters = max_clusters(dense_kernel_ptr(), dense_threads(), dense_smem_bytes());
+  d.dense_clusters = max_clusters(dense_kernel_ptr(0), dense_threads(), dense_smem_bytes());
   d.sparse_clusters = max_clusters(sparse_kernel_ptr(), sparse_threads(), sparse_smem_bytes());
   if (d.dense_clusters <= 0 || d.sparse_clusters <= 0) {
     cudaGetLastError();
@@ -143,52 +146,93 @@ int encode_q_map(CUtensorMap* m, const void* q, long long rows) {
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
-// Dense KV pool as [num_pages][64][576] bf16; one box = 64 dims x 64 tokens of one page.
-int encode_kv_map(CUtensorMap* m, const void* kv, int num_pages) {
+// Dense KV pool as [num_pages][64][h_kv][576] (16-bit elements), dims listed
+// innermost first: (576, h_kv, 64, num_pages).  One box = 64 dims x 64 tokens
+// of one page and one KV head.
+int encode_kv_map(CUtensorMap* m, const void* kv, int num_pages, int h_kv) {
   auto fn = encode_fn();
   if (fn == nullptr) return MLA_ERR_CUDA;
-  cuuint64_t dims[3] = {MLA_D_QK, MLA_PAGE_SIZE, static_cast<cuuint64_t>(num_pages)};
-  cuuint64_t strides[2] = {MLA_D_QK * 2, static_cast<cuuint64_t>(MLA_D_QK) * 2 * MLA_PAGE_SIZE};
-  cuuint32_t box[3] = {64, MLA_PAGE_SIZE, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv), dims, strides, box, es,
+  const cuuint64_t row = static_cast<cuuint64_t>(MLA_D_QK) * 2;
+  cuuint64_t dims[4] = {MLA_D_QK, static_cast<cuuint64_t>(h_kv), MLA_PAGE_SIZE, static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {row, row * h_kv, row * h_kv * MLA_PAGE_SIZE};
+  cuuint32_t box[4] = {64, 1, MLA_PAGE_SIZE, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(kv), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
+}
+
+// Dense Q with h_kv > 1 as [tokens = batch*s_q][h_kv][group_heads][576], dims
+// innermost first: (576, group_heads, h_kv, tokens).  One box = 64 dims x
+// group_heads heads x block_tokens tokens of one head group.
+int encode_q_map_groups(CUtensorMap* m, const void* q, long long tokens, int h_kv, int group_heads,
+                        int block_tokens) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return MLA_ERR_CUDA;
+  const cuuint64_t row = static_cast<cuuint64_t>(MLA_D_QK) * 2;
+  cuuint64_t dims[4] = {MLA_D_QK, static_cast<cuuint64_t>(group_heads), static_cast<cuuint64_t>(h_kv),
+                        static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[3] = {row, row * group_heads, row * group_heads * h_kv};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(group_heads), 1, static_cast<cuuint32_t>(block_tokens)};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(q), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
 int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int max_pages, int num_pages,
-                  const int32_t* seqlens, int batch, int s_q, int h_q, int causal, float scale,
+                  const int32_t* seqlens, int batch, int s_q, int h_q, int h_kv, int dtype, int causal, float scale,
                   const int32_t* sched, const int32_t* split_offset, int num_parts, void* workspace,
-                  size_t workspace_bytes, void* out, int out_fp32, float* lse, int32_t* status, DecodeParams* p,
+                  size_t workspace_bytes, void* out, int out_type, float* lse, int32_t* status, DecodeParams* p,
                   CUtensorMap* q_map, CUtensorMap* kv_map) {
   if (!q || !kv || !block_table || !seqlens || !sched || !split_offset || !workspace || !out || !lse || !status)
     return MLA_ERR_INVALID_ARG;
-  if (batch < 1 || s_q < 1 || h_q < 1 || max_pages < 1 || num_pages < 1 || num_parts < 1)
+  if (batch < 1 || s_q < 1 || h_q < 1 || h_kv < 1 || max_pages < 1 || num_pages < 1 || num_parts < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (h_q % h_kv != 0) return MLA_ERR_INVALID_ARG;
+  if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_FP16) return MLA_ERR_INVALID_ARG;
+  if (out_type != MLA_DTYPE_BF16 && out_type != MLA_DTYPE_FP32 && out_type != MLA_DTYPE_FP16)
     return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return MLA_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(s_q) * h_q;
   if (rows > (1 << 20) || static_cast<long long>(batch) * rows > (1LL << 31) - 1) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_pages) * MLA_PAGE_SIZE * h_kv > (1LL << 31)) return MLA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(kv) || !aligned16(workspace) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
-  if (out_fp32 != 0 && out_fp32 != 1) return MLA_ERR_INVALID_ARG;
   const WorkspaceLayout w = ws_layout(batch, static_cast<int>(rows), num_parts);
   if (workspace_bytes < w.total) return MLA_ERR_INVALID_ARG;
-  const int row_blocks = static_cast<int>((rows + MLA_ROWS_PER_BLOCK - 1) / MLA_ROWS_PER_BLOCK);
+  const int group_heads = h_q / h_kv;
+  int block_tokens = 0, blocks_per_group = 0;
+  if (h_kv == 1) {
+    blocks_per_group = static_cast<int>((rows + MLA_ROWS_PER_BLOCK - 1) / MLA_ROWS_PER_BLOCK);
+  } else {
+    if (group_heads > MLA_ROWS_PER_BLOCK) return MLA_ERR_UNSUPPORTED;
+    block_tokens = std::min(s_q, MLA_ROWS_PER_BLOCK / group_heads);
+    blocks_per_group = (s_q + block_tokens - 1) / block_tokens;
+  }
+  const long long row_blocks = static_cast<long long>(h_kv) * blocks_per_group;
   if (2LL * num_parts * row_blocks > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
   const DeviceInfo& d = device_info();
   if (d.status != MLA_OK) return d.status;
-  int rc = encode_q_map(q_map, q, static_cast<long long>(batch) * rows);
+  int rc = h_kv == 1 ? encode_q_map(q_map, q, static_cast<long long>(batch) * rows)
+                     : encode_q_map_groups(q_map, q, static_cast<long long>(batch) * s_q, h_kv, group_heads,
+                                           block_tokens);
   if (rc != MLA_OK) return rc;
-  rc = encode_kv_map(kv_map, kv, num_pages);
+  rc = encode_kv_map(kv_map, kv, num_pages, h_kv);
   if (rc != MLA_OK) return rc;
   *p = DecodeParams{};
   p->lengths = seqlens;
   p->default_length = 0;
   p->n_units = batch;
   p->rows = static_cast<int>(rows);
-  p->row_blocks = row_blocks;
+  p->row_blocks = static_cast<int>(row_blocks);
   p->h_q = h_q;
   p->s_q = s_q;
+  p->h_kv = h_kv;
+  p->group_heads = group_heads;
+  p->block_tokens = block_tokens;
+  p->blocks_per_group = blocks_per_group;
   p->causal = causal ? 1 : 0;
   p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p->block_table = block_table;
@@ -200,7 +244,7 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
   p->o_accum = static_cast<float*>(workspace);
   p->lse_accum = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.lse_off);
   p->out = out;
-  p->out_fp32 = out_fp32;
+  p->out_type = out_type;
   p->lse = lse;
   p->status = status;
   return MLA_OK;
@@ -230,6 +274,23 @@ int mla_num_parts(int rows_per_unit, int is_sparse_fp8) {
   const int row_blocks = (rows_per_unit + MLA_ROWS_PER_BLOCK - 1) / MLA_ROWS_PER_BLOCK;
   const int parts = clusters / row_blocks;
   return parts > 0 ? parts : 1;
+}
+
+int mla_num_parts_dense(int s_q, int h_q, int h_kv) {
+  if (s_q < 1 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0) return -MLA_ERR_INVALID_ARG;
+  const int group_heads = h_q / h_kv;
+  if (h_kv > 1 && group_heads > MLA_ROWS_PER_BLOCK) return -MLA_ERR_UNSUPPORTED;
+  const DeviceInfo& d = device_info();
+  if (d.status != MLA_OK) return -d.status;
+  long long row_blocks;
+  if (h_kv == 1) {
+    row_blocks = (static_cast<long long>(s_q) * h_q + MLA_ROWS_PER_BLOCK - 1) / MLA_ROWS_PER_BLOCK;
+  } else {
+    const int block_tokens = std::min(s_q, MLA_ROWS_PER_BLOCK / group_heads);
+    row_blocks = static_cast<long long>(h_kv) * ((s_q + block_tokens - 1) / block_tokens);
+  }
+  const long long parts = d.dense_clusters / row_blocks;
+  return parts > 0 ? static_cast<int>(parts) : 1;
 }
 
 size_t mla_workspace_bytes(int n_units, int rows_per_unit, int num_parts) {
@@ -262,47 +323,50 @@ int mla_get_metadata_request_local(const int32_t* d_lengths, int default_length,
 }
 
 int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
-                      int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int causal,
-                      float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
-                      void* d_workspace, size_t workspace_bytes, void* d_out, int out_fp32, float* d_lse,
-                      int32_t* d_status, mla_stream_t stream) {
+                      int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int h_kv,
+                      int dtype, int causal, float softmax_scale, const int32_t* d_sched,
+                      const int32_t* d_split_offset, int num_parts, void* d_workspace, size_t workspace_bytes,
+                      void* d_out, int out_type, float* d_lse, int32_t* d_status, mla_stream_t stream) {
   DecodeParams p;
   CUtensorMap qm, km;
   const int rc = dense_prepare(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q,
-                               causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
-                               workspace_bytes, d_out, out_fp32, d_lse, d_status, &p, &qm, &km);
+                               h_kv, dtype, causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
+                               workspace_bytes, d_out, out_type, d_lse, d_status, &p, &qm, &km);
   if (rc != MLA_OK) return rc;
-  return launch_dense(qm, km, p, d_q, num_parts, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
-                                                                                                    : MLA_ERR_CUDA;
+  return launch_dense(qm, km, p, d_q, num_parts, dtype == MLA_DTYPE_FP16 ? 1 : 0,
+                      reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* d_split_offset, int n_units,
-                int rows_per_unit, int num_parts, void* d_out, int out_fp32, float* d_lse, mla_stream_t stream) {
+                int rows_per_unit, int num_parts, void* d_out, int out_type, float* d_lse, mla_stream_t stream) {
   if (!d_workspace || !d_split_offset || !d_out || !d_lse) return MLA_ERR_INVALID_ARG;
   if (n_units < 1 || n_units > 65535 || rows_per_unit < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
-  if (out_fp32 != 0 && out_fp32 != 1) return MLA_ERR_INVALID_ARG;
+  if (out_type != MLA_DTYPE_BF16 && out_type != MLA_DTYPE_FP32 && out_type != MLA_DTYPE_FP16)
+    return MLA_ERR_INVALID_ARG;
   if (!aligned16(d_workspace) || !aligned16(d_out)) return MLA_ERR_INVALID_ARG;
   const WorkspaceLayout w = ws_layout(n_units, rows_per_unit, num_parts);
   if (workspace_bytes < w.total) return MLA_ERR_INVALID_ARG;
   const float* o = static_cast<const float*>(d_workspace);
   const float* l = reinterpret_cast<const float*>(static_cast<const char*>(d_workspace) + w.lse_off);
-  return launch_combine(o, l, d_split_offset, n_units, rows_per_unit, d_out, out_fp32, d_lse,
+  return launch_combine(o, l, d_split_offset, n_units, rows_per_unit, d_out, out_type, d_lse,
                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
 }
 
 int mla_decode_fwd(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages, int num_pages,
-                   const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int causal, float softmax_scale,
-                   const int32_t* d_sched, const int32_t* d_split_offset, int num_parts, void* d_workspace,
-                   size_t workspace_bytes, void* d_out, int out_fp32, float* d_lse, int32_t* d_status,
-                   mla_stream_t stream) {
+                   const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int h_kv, int dtype, int causal,
+                   float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
+                   void* d_workspace, size_t workspace_bytes, void* d_out, int out_type, float* d_lse,
+                   int32_t* d_status, mla_stream_t stream) {
   if (batch > 65535) return MLA_ERR_UNSUPPORTED;
-  int rc = mla_decode_splits(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q,
-                             causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
-                             workspace_bytes, d_out, out_fp32, d_lse, d_status, stream);
+  int rc = mla_decode_splits(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q, h_kv,
+                             dtype, causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
+                             workspace_bytes, d_out, out_type, d_lse, d_status, stream);
   if (rc != MLA_OK) return rc;
-  return mla_combine(d_workspace, workspace_bytes, d_split_offset, batch, s_q * h_q, num_parts, d_out, out_fp32,
+  return mla_combine(d_workspace, workspace_bytes, d_split_offset, batch, s_q * h_q, num_parts, d_out, out_type,
                      d_lse, stream);
 }
 
@@ -349,7 +413,8 @@ int sparse_decode(const void* d_q, const uint8_t* d_kv8, int num_pages, const in
   p.o_accum = static_cast<float*>(d_workspace);
   p.lse_accum = reinterpret_cast<float*>(static_cast<char*>(d_workspace) + w.lse_off);
   p.out = d_out;
-  p.out_fp32 = 0;
+  p.out_type = MLA_DTYPE_BF16;
+  p.h_kv = 1;
   p.lse = d_lse;
   p.status = d_status;
   CUtensorMap qm;

@@ -9,6 +9,7 @@
 // with -inf splits weighing 0 and an all-empty row giving out 0, lse -inf.
 // Memory bound: every partial is read once with 512-byte coalesced rows.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -17,10 +18,17 @@ namespace mla {
 
 constexpr int kCombineWarps = 4;
 
-__device__ __forceinline__ void store_row4(void* out, int out_fp32, size_t elem, float a, float b, float c,
+__device__ __forceinline__ void store_row4(void* out, int out_type, size_t elem, float a, float b, float c,
                                            float d) {
-  if (out_fp32) {
+  if (out_type == MLA_DTYPE_FP32) {
     *reinterpret_cast<float4*>(static_cast<float*>(out) + elem) = make_float4(a, b, c, d);
+  } else if (out_type == MLA_DTYPE_FP16) {
+    __half2 lo = __floats2half2_rn(a, b);
+    __half2 hi = __floats2half2_rn(c, d);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&lo);
+    v.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(static_cast<__half*>(out) + elem) = v;
   } else {
     __nv_bfloat162 lo = __floats2bfloat162_rn(a, b);
     __nv_bfloat162 hi = __floats2bfloat162_rn(c, d);
@@ -50,7 +58,7 @@ __device__ __forceinline__ void acc4(float4& a, float w, const float4& v) {
 template <int kVec>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const float* __restrict__ o_accum, const float* __restrict__ lse_accum,
-                   const int32_t* __restrict__ split_offset, int rows, void* __restrict__ out, int out_fp32,
+                   const int32_t* __restrict__ split_offset, int rows, void* __restrict__ out, int out_type,
                    float* __restrict__ lse) {
   constexpr int kBatch = kVec == 4 ? 4 : 8;
   pdl_wait_prior_grid();
@@ -71,7 +79,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if (n <= 0 || m == -INFINITY) {
 #pragma unroll
-    for (int k = 0; k < kVec; ++k) store_row4(out, out_fp32, orow * kDv + col + 128 * k, 0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kVec; ++k) store_row4(out, out_type, orow * kDv + col + 128 * k, 0.f, 0.f, 0.f, 0.f);
     if (writes_lse) lse[orow] = -INFINITY;
     return;
   }
@@ -116,12 +124,12 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   }
 #pragma unroll
   for (int k = 0; k < kVec; ++k)
-    store_row4(out, out_fp32, orow * kDv + col + 128 * k, acc[k].x, acc[k].y, acc[k].z, acc[k].w);
+    store_row4(out, out_type, orow * kDv + col + 128 * k, acc[k].x, acc[k].y, acc[k].z, acc[k].w);
   if (writes_lse) lse[orow] = m + logf(z);
 }
 
 cudaError_t launch_combine(const float* o_accum, const float* lse_accum, const int32_t* split_offset, int n_units,
-                           int rows, void* out, int out_fp32, float* lse, cudaStream_t stream) {
+                           int rows, void* out, int out_type, float* lse, cudaStream_t stream) {
   // whole-row warps once there are enough rows to fill the GPU several times over
   const bool whole_rows = static_cast<long long>(n_units) * rows >= 8192;
   cudaLaunchConfig_t cfg = {};
@@ -135,8 +143,8 @@ cudaError_t launch_combine(const float* o_accum, const float* lse_accum, const i
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (whole_rows)
-    return cudaLaunchKernelEx(&cfg, combine_kernel<4>, o_accum, lse_accum, split_offset, rows, out, out_fp32, lse);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<1>, o_accum, lse_accum, split_offset, rows, out, out_fp32, lse);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<4>, o_accum, lse_accum, split_offset, rows, out, out_type, lse);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<1>, o_accum, lse_accum, split_offset, rows, out, out_type, lse);
 }
 
 }  // namespace mla

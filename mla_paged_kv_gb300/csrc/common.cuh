@@ -29,8 +29,15 @@ struct DecodeParams {
   int default_length;       // used when lengths == NULL
   int n_units;              // dense: batch; sparse: batch * s_q
   int rows;                 // query rows per unit (dense s_q*h_q, sparse h_q)
-  int row_blocks;           // ceil(rows / 128)
+  int row_blocks;           // CTA pairs per partition: h_kv * blocks_per_group
   int h_q;
+  // dense: latent KV heads.  Query head h reads KV head h / group_heads.  With
+  // h_kv = 1 a row block is 128 consecutive rows (token-major) of the unit;
+  // with h_kv > 1 it is block_tokens whole tokens of one head group.
+  int h_kv;
+  int group_heads;          // h_q / h_kv
+  int block_tokens;         // h_kv > 1: tokens per row block (group_heads * block_tokens <= 128)
+  int blocks_per_group;     // row blocks per head group
   int s_q;                  // dense: tokens per unit (causal alignment); sparse: 1
   int causal;
   float scale_log2;         // softmax_scale * log2(e)
@@ -51,7 +58,7 @@ struct DecodeParams {
   float* o_accum;           // [slots, rows, 512]
   float* lse_accum;         // [slots, rows]
   void* out;                // [n_units, rows, 512]
-  int out_fp32;
+  int out_type;             // MLA_DTYPE_BF16, MLA_DTYPE_FP32 or MLA_DTYPE_FP16
   float* lse;               // [n_units, rows]
   int32_t* status;
 };

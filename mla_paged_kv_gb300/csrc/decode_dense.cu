@@ -43,6 +43,7 @@
 //        warp 4 K-slot + Q producer, warp 5 V-ring producer,
 //        warp 6 MMA issuer and TMEM owner.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -227,9 +228,9 @@ __device__ __forceinline__ int load_page_window(const DecodeParams& p, const Cur
 
 // Q K^T over one 64-dim box kG (4 K-steps).  The A operand (Q) comes from TMEM
 // for kG < 6, else from shared memory; B is the box in the K slot or V ring.
-template <int kG>
+template <bool kHalf, int kG>
 __device__ __forceinline__ void qk_box(uint32_t d, uint32_t tmem, uint64_t q_desc0, uint64_t b_desc, bool first) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, kT, false);
+  constexpr uint32_t idesc = idesc_16bit_f32(128, kT, false, kHalf);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint64_t b = b_desc + static_cast<uint64_t>((k * 32) >> 4);
@@ -242,30 +243,57 @@ __device__ __forceinline__ void qk_box(uint32_t d, uint32_t tmem, uint64_t q_des
 }
 
 // Q K^T over this rank's K-slot boxes (first part of the score tile).
-template <int kRank>
+template <bool kHalf, int kRank>
 __device__ __forceinline__ void issue_qk_k(uint32_t d, uint32_t tmem, uint64_t q_desc0, uint64_t kslot) {
-  qk_box<k_box<kRank>(0)>(d, tmem, q_desc0, kslot + ((0 * kBoxBytes) >> 4), true);
-  qk_box<k_box<kRank>(1)>(d, tmem, q_desc0, kslot + ((1 * kBoxBytes) >> 4), false);
-  qk_box<k_box<kRank>(2)>(d, tmem, q_desc0, kslot + ((2 * kBoxBytes) >> 4), false);
-  qk_box<k_box<kRank>(3)>(d, tmem, q_desc0, kslot + ((3 * kBoxBytes) >> 4), false);
-  qk_box<k_box<kRank>(4)>(d, tmem, q_desc0, kslot + ((4 * kBoxBytes) >> 4), false);
+  qk_box<kHalf, k_box<kRank>(0)>(d, tmem, q_desc0, kslot + ((0 * kBoxBytes) >> 4), true);
+  qk_box<kHalf, k_box<kRank>(1)>(d, tmem, q_desc0, kslot + ((1 * kBoxBytes) >> 4), false);
+  qk_box<kHalf, k_box<kRank>(2)>(d, tmem, q_desc0, kslot + ((2 * kBoxBytes) >> 4), false);
+  qk_box<kHalf, k_box<kRank>(3)>(d, tmem, q_desc0, kslot + ((3 * kBoxBytes) >> 4), false);
+  qk_box<kHalf, k_box<kRank>(4)>(d, tmem, q_desc0, kslot + ((4 * kBoxBytes) >> 4), false);
 }
 
 // Q K^T over this rank's V-ring boxes (second part of the score tile).
-template <int kRank>
+template <bool kHalf, int kRank>
 __device__ __forceinline__ void issue_qk_v(uint32_t d, uint32_t tmem, uint64_t q_desc0, uint64_t vslot) {
-  qk_box<4 * kRank + 0>(d, tmem, q_desc0, vslot + ((0 * kBoxBytes) >> 4), false);
-  qk_box<4 * kRank + 1>(d, tmem, q_desc0, vslot + ((1 * kBoxBytes) >> 4), false);
-  qk_box<4 * kRank + 2>(d, tmem, q_desc0, vslot + ((2 * kBoxBytes) >> 4), false);
-  qk_box<4 * kRank + 3>(d, tmem, q_desc0, vslot + ((3 * kBoxBytes) >> 4), false);
+  qk_box<kHalf, 4 * kRank + 0>(d, tmem, q_desc0, vslot + ((0 * kBoxBytes) >> 4), false);
+  qk_box<kHalf, 4 * kRank + 1>(d, tmem, q_desc0, vslot + ((1 * kBoxBytes) >> 4), false);
+  qk_box<kHalf, 4 * kRank + 2>(d, tmem, q_desc0, vslot + ((2 * kBoxBytes) >> 4), false);
+  qk_box<kHalf, 4 * kRank + 3>(d, tmem, q_desc0, vslot + ((3 * kBoxBytes) >> 4), false);
+}
+
+// Two fp32 -> one packed pair of 16-bit floats (round to nearest even).
+template <bool kHalf>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (kHalf) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+// Row r of a CTA's 128-row block -> its row within the request's s_q * h_q
+// query rows (token-major); false for a padding row.  h_kv = 1: 128
+// consecutive rows per block.  h_kv > 1: block rb of head group grp holds
+// block_tokens whole tokens of that group's group_heads heads.
+__device__ __forceinline__ bool block_row(const DecodeParams& p, int grp, int rb, int r, int& qrow, int& tok) {
+  if (p.h_kv == 1) {
+    qrow = rb * kRowsPerBlock + r;
+    tok = qrow / p.h_q;
+    return qrow < p.rows;
+  }
+  const int t = r / p.group_heads;
+  tok = rb * p.block_tokens + t;
+  qrow = tok * p.h_q + grp * p.group_heads + (r - t * p.group_heads);
+  return t < p.block_tokens && tok < p.s_q;
 }
 
 // Q row `row` of unit b, dims [0, 384) -> this thread's TMEM lane, columns
 // [kTmemQ, kTmemQ + 192): column c holds dims (2c, 2c+1) as packed bf16.
-__device__ __forceinline__ void load_q_to_tmem(const DecodeParams& p, const uint16_t* q, int b, int row,
+__device__ __forceinline__ void load_q_to_tmem(const DecodeParams& p, const uint16_t* q, int b, int qrow, bool ok,
                                                uint32_t taddr) {
-  const bool ok = row < p.rows;
-  const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * p.rows + row) * kDqk);
+  const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * p.rows + (ok ? qrow : 0)) * kDqk);
 #pragma unroll 1
   for (int round = 0; round < 2; ++round) {
     uint4 w[24];  // all loads of the round in flight at once
@@ -307,6 +335,7 @@ __device__ __forceinline__ float ref_alpha(float r_old, float r_new) {
   return r_new == r_old ? 1.f : ex2(r_old - r_new);
 }
 
+template <bool kHalf>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     dense_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
                         const DecodeParams p, const uint16_t* __restrict__ q) {
@@ -328,11 +357,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  // Q rows staged per box: 128 (h_kv = 1) or the group's block_tokens tokens
+  const uint32_t q_box_bytes =
+      (p.h_kv == 1 ? kRowsPerBlock : p.group_heads * p.block_tokens) * 128u;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int cluster_id = blockIdx.x >> 1;
   const int part_idx = cluster_id / p.row_blocks;
-  const int rb = cluster_id - part_idx * p.row_blocks;
+  const int blk = cluster_id - part_idx * p.row_blocks;
+  const int grp = blk / p.blocks_per_group;  // KV head group (0 when h_kv = 1)
+  const int rb = blk - grp * p.blocks_per_group;
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -366,6 +400,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_arrive_expect_tx(&bars[RECV_FULL], kPBytes);
     mbar_arrive_expect_tx(&bars[R_FULL], kVecBytes);
     mbar_arrive_expect_tx(&bars[L_FULL], kVecBytes);
+  }
+  if (q_box_bytes < static_cast<uint32_t>(kQBoxBytes)) {
+    // Q boxes of a head group cover fewer than 128 rows: the rows past them stay zero
+    for (int i = tid; i < kQSmemBoxes * kQBoxBytes / 16; i += kThreads)
+      reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
   }
   if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -403,11 +443,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           if (c.u >= 1) ok = mbar_wait(&bars[Q_EMPTY], (c.u - 1) & 1, abort_flag);
           if (ok) {
-            mbar_arrive_expect_tx(&bars[Q_FULL], kQSmemBoxes * kQBoxBytes);
-            const int row0 = c.b * p.rows + rb * kRowsPerBlock;
+            mbar_arrive_expect_tx(&bars[Q_FULL], kQSmemBoxes * q_box_bytes);
+            if (p.h_kv == 1) {
+              const int row0 = c.b * p.rows + rb * kRowsPerBlock;
 #pragma unroll
-            for (int i = 0; i < kQSmemBoxes; ++i)
-              tma_load_2d(sQ + i * kQBoxBytes, &q_map, &bars[Q_FULL], 64 * (kQTmemBoxes + i), row0, pol_q);
+              for (int i = 0; i < kQSmemBoxes; ++i)
+                tma_load_2d(sQ + i * kQBoxBytes, &q_map, &bars[Q_FULL], 64 * (kQTmemBoxes + i), row0, pol_q);
+            } else {
+              // [batch * s_q][h_kv][group_heads][576]: block_tokens tokens of head group grp
+              const int tok0 = c.b * p.s_q + rb * p.block_tokens;
+#pragma unroll
+              for (int i = 0; i < kQSmemBoxes; ++i)
+                tma_load_4d(sQ + i * kQBoxBytes, &q_map, &bars[Q_FULL], 64 * (kQTmemBoxes + i), 0, grp, tok0,
+                            pol_q);
+            }
             ++q_issued;
           }
         }
@@ -435,7 +484,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < kKBoxes; ++j) {
                 const int g = rank == 0 ? k_box<0>(j) : k_box<1>(j);
-                tma_load_3d(dst + j * kBoxBytes, &kv_map, &bars[K_FULL + s], 64 * g, 0, page, pol_kv);
+                tma_load_4d(dst + j * kBoxBytes, &kv_map, &bars[K_FULL + s], 64 * g, grp, 0, page, pol_kv);
               }
               ++k_issued[s];
             }
@@ -449,8 +498,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               uint8_t* dst = sV + s * kVSlotBytes;
 #pragma unroll
               for (int j = 0; j < kVBoxes; ++j)
-                tma_load_3d(dst + j * kBoxBytes, &kv_map, &bars[V_FULL + s], 64 * (4 * static_cast<int>(rank) + j),
-                            0, page, pol_kv);
+                tma_load_4d(dst + j * kBoxBytes, &kv_map, &bars[V_FULL + s], 64 * (4 * static_cast<int>(rank) + j),
+                            grp, 0, page, pol_kv);
               ++v_issued[s];
             }
           }
@@ -473,7 +522,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_pv = idesc_bf16_f32(128, 256, true);
+      const uint32_t idesc_pv = idesc_16bit_f32(128, 256, true, kHalf);
       const uint64_t q_desc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t k_desc0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t vk_desc0 = sdesc_sw128(smem_u32(sV), 16, 1024);        // V boxes as K-major B of Q K^T
@@ -570,9 +619,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tc_fence_after();
               const uint64_t kslot = k_desc0 + static_cast<uint64_t>((ks * kKSlotBytes) >> 4);
               if (rank == 0)
-                issue_qk_k<0>(tmem + kTmemS, tmem, q_desc0, kslot);
+                issue_qk_k<kHalf, 0>(tmem + kTmemS, tmem, q_desc0, kslot);
               else
-                issue_qk_k<1>(tmem + kTmemS, tmem, q_desc0, kslot);
+                issue_qk_k<kHalf, 1>(tmem + kTmemS, tmem, q_desc0, kslot);
               umma_commit(&bars[K_EMPTY + ks]);
               MLA_TRACE(17, cq.t);
               ++a_own;
@@ -586,9 +635,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tc_fence_after();
               const uint64_t vslot = vk_desc0 + static_cast<uint64_t>((vs * kVSlotBytes) >> 4);
               if (rank == 0)
-                issue_qk_v<0>(tmem + kTmemS, tmem, q_desc0, vslot);
+                issue_qk_v<kHalf, 0>(tmem + kTmemS, tmem, q_desc0, vslot);
               else
-                issue_qk_v<1>(tmem + kTmemS, tmem, q_desc0, vslot);
+                issue_qk_v<kHalf, 1>(tmem + kTmemS, tmem, q_desc0, vslot);
               umma_commit(&bars[S_FULL]);
               MLA_TRACE(2, cq.t);
               q_phase = 2;
@@ -628,9 +677,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
     const uint32_t taddr = tmem + lane_base;
     const uint32_t swz = static_cast<uint32_t>(r & 7);
-    const int row = rb * kRowsPerBlock + r;
-    const bool row_ok = row < p.rows;
-    const int tok = row_ok ? row / p.h_q : 0;
+    int qrow, tok;
+    const bool row_ok = block_row(p, grp, rb, r, qrow, tok);
+    if (!row_ok) tok = 0;
     const float c_log2 = p.scale_log2;
     // the peer's buffers and barriers this warp sends to
     const uint32_t peer_p = mapa_shared(smem_u32(sPRecv + warp * kWarpPBytes), peer);
@@ -645,7 +694,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cursor_init(p, P, c);
     bool ok = true;
     if (c.valid) {  // Q of the first unit
-      load_q_to_tmem(p, q, c.b, row, taddr);
+      load_q_to_tmem(p, q, c.b, qrow, row_ok, taddr);
       tc_fence_before();
       mbar_arrive(&bars[Q_FULL]);
     }
@@ -714,8 +763,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kT / 2; ++i) {
           const float p0 = ex2(fmaf(s[2 * i], c_log2, -mref));
           const float p1 = ex2(fmaf(s[2 * i + 1], c_log2, -mref));
-          const __nv_bfloat162 hv = __floats2bfloat162_rn(p0, p1);
-          pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
+          pk[i] = pack2<kHalf>(p0, p1);
           ls[i & 3] += p0 + p1;
         }
         const float rowsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
@@ -783,7 +831,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = warp_wait(&bars[Q_EMPTY], u_here & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        load_q_to_tmem(p, q, c.b, row, taddr);
+        load_q_to_tmem(p, q, c.b, qrow, row_ok, taddr);
         tc_fence_before();
         mbar_arrive(&bars[Q_FULL]);
       }
@@ -815,7 +863,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int slot = s_begin + ((b_here == P.b0) ? P.s0 : 0);
       const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
       const bool direct = (nsplit == 1);
-      const bool bf16_out = direct && !p.out_fp32;
+      const bool bf16_out = direct && p.out_type != MLA_DTYPE_FP32;  // a 16-bit output (bf16 or fp16)
+      const bool fp16_out = p.out_type == MLA_DTYPE_FP16;
       // O half -> global through that buffer: each thread stages its row's
       // 128 bytes of a column chunk, then the 128 threads store 16-byte pieces
       // so that each warp writes whole 128-byte row segments.
@@ -833,9 +882,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const __nv_bfloat162 hv =
-                  __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l);
-              w[16 * hh + i] = *reinterpret_cast<const uint32_t*>(&hv);
+              const float a = __uint_as_float(v[2 * i]) * inv_l, b2 = __uint_as_float(v[2 * i + 1]) * inv_l;
+              w[16 * hh + i] = fp16_out ? pack2<true>(a, b2) : pack2<false>(a, b2);
             }
           }
         } else {
@@ -854,13 +902,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 8; ++i) {
           const int flat = tid + 128 * i;
           const int rr = flat >> 3, cc = flat & 7;
-          const int rg = rb * kRowsPerBlock + rr;
-          if (rg >= p.rows) continue;
+          int rg, rtok;
+          if (!block_row(p, grp, rb, rr, rg, rtok)) continue;
           const uint4 val =
               *reinterpret_cast<const uint4*>(stage + rr * 128 + ((static_cast<uint32_t>(cc ^ (rr & 7))) << 4));
           const size_t e = (base_row + rg) * kDv + 256u * rank + static_cast<size_t>(ch) * chunk_cols;
           if (bf16_out)
-            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + e)[cc] = val;
+            reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + e)[cc] = val;
           else
             reinterpret_cast<uint4*>((direct ? static_cast<float*>(p.out) : p.o_accum) + e)[cc] = val;
         }
@@ -872,9 +920,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (rank == 0 && row_ok) {
         const float lse = l_sum > 0.f ? (r_cur + __log2f(l_sum)) * kLn2 : -INFINITY;
         if (direct)
-          p.lse[static_cast<size_t>(b_here) * p.rows + row] = lse;
+          p.lse[static_cast<size_t>(b_here) * p.rows + qrow] = lse;
         else
-          p.lse_accum[static_cast<size_t>(slot) * p.rows + row] = lse;
+          p.lse_accum[static_cast<size_t>(slot) * p.rows + qrow] = lse;
       }
     }
     if (!ok) {
@@ -906,13 +954,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 int dense_smem_bytes() { return dn::kSmemBytes; }
 int dense_threads() { return dn::kThreads; }
-const void* dense_kernel_ptr() { return reinterpret_cast<const void*>(&dn::dense_decode_kernel); }
+const void* dense_kernel_ptr(int half) {
+  return half ? reinterpret_cast<const void*>(&dn::dense_decode_kernel<true>)
+              : reinterpret_cast<const void*>(&dn::dense_decode_kernel<false>);
+}
 
 cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, const DecodeParams& p, const void* q,
-                         int num_parts, cudaStream_t stream) {
+                         int num_parts, int half, cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
-  dn::dense_decode_kernel<<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, p,
-                                                                         static_cast<const uint16_t*>(q));
+  if (half)
+    dn::dense_decode_kernel<true><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, p,
+                                                                                 static_cast<const uint16_t*>(q));
+  else
+    dn::dense_decode_kernel<false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, p,
+                                                                                  static_cast<const uint16_t*>(q));
   return cudaGetLastError();
 }
 

@@ -713,7 +713,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         if (!row_ok) continue;
         const size_t col = 256u * rank + c0;
-        if (direct && !p.out_fp32) {
+        if (direct && p.out_type == MLA_DTYPE_BF16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * kDv + col);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {

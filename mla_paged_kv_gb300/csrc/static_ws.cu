@@ -57,9 +57,10 @@ int static_workspace(void** ptr) {
 
 extern "C" int mla_decode_fwd_static_ws(const void* d_q, const void* d_kv, const int32_t* d_block_table,
                                         int max_pages, int num_pages, const int32_t* d_cache_seqlens, int batch,
-                                        int s_q, int h_q, int causal, float softmax_scale, const int32_t* d_sched,
-                                        const int32_t* d_split_offset, int num_parts, void* d_out, int out_fp32,
-                                        float* d_lse, int32_t* d_status, mla_stream_t stream) {
+                                        int s_q, int h_q, int h_kv, int dtype, int causal, float softmax_scale,
+                                        const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
+                                        void* d_out, int out_type, float* d_lse, int32_t* d_status,
+                                        mla_stream_t stream) {
   if (batch < 1 || s_q < 1 || h_q < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
   const long long rows = static_cast<long long>(s_q) * h_q;
   if (rows > (1 << 20)) return MLA_ERR_UNSUPPORTED;
@@ -72,7 +73,7 @@ extern "C" int mla_decode_fwd_static_ws(const void* d_q, const void* d_kv, const
   if (rc != MLA_OK) return rc;
   // No part of the array needs clearing: in one call the decode kernel writes
   // every partial output and LSE that the combine then reads.
-  return mla_decode_fwd(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q, causal,
-                        softmax_scale, d_sched, d_split_offset, num_parts, ws, kStaticWorkspaceBytes, d_out, out_fp32,
-                        d_lse, d_status, stream);
+  return mla_decode_fwd(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q, h_kv,
+                        dtype, causal, softmax_scale, d_sched, d_split_offset, num_parts, ws, kStaticWorkspaceBytes,
+                        d_out, out_type, d_lse, d_status, stream);
 }

@@ -221,6 +221,11 @@ WORKLOADS = {
     "sparse_fp8_b16_hq128_topk2048": dict(kind="sparse", batch=16, s_q=1, h_q=128, topk=2048,
                                           pages_per_req=512, topk_lo=1024, topk_hi=2048,
                                           seed=1005),
+    # the dense page's fp16 instantiation and several latent KV heads
+    "dense_b64_hq128_sk2048to4096_fp16": dict(kind="dense", batch=64, s_q=1, h_q=128, seqlen_lo=2048,
+                                              seqlen_hi=4096, dtype=torch.float16, seed=1008),
+    "dense_b32_hkv2_hq128_sk2048to4096": dict(kind="dense", batch=32, s_q=1, h_q=128, seqlen_lo=2048,
+                                              seqlen_hi=4096, h_kv=2, seed=1009),
     # the H=64 and S_q>1 query shapes of the packed-path page's grid, full top-k prefix
     "sparse_fp8_b4_sq4_hq64_topk2048": dict(kind="sparse", batch=4, s_q=4, h_q=64, topk=2048,
                                             pages_per_req=512, topk_lo=2048, topk_hi=2048,

@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
                             "mla_decode_fwd", "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd",
                             "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes",
                             "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd",
-                            "mla_get_metadata_request_local"])
+                            "mla_get_metadata_request_local", "mla_num_parts_dense"])
 
 
 def test_library_exports_every_declared_symbol(lib_path):
@@ -69,9 +69,11 @@ def test_host_validation_without_gpu(lib_path):
                                      ctypes.c_void_p, ctypes.c_void_p]
     assert lib.mla_get_metadata(null, -1, 4, 2, null, null, null) == 1          # MLA_ERR_INVALID_ARG
     assert lib.mla_get_metadata(null, 10, 0, 2, ctypes.c_void_p(16), ctypes.c_void_p(16), null) == 1
-    args = [null] * 3 + [1, 1, null, 1, 1, 1, 0, 0.04, null, null, 1, null, 0, null, 0, null, null, null]
+    # q, kv, block_table, max_pages, num_pages, seqlens, batch, s_q, h_q, h_kv, dtype, causal, scale, sched,
+    # split_offset, num_parts, workspace, workspace_bytes, out, out_type, lse, status, stream
+    args = [null] * 3 + [1, 1, null, 1, 1, 1, 1, 0, 0, 0.04, null, null, 1, null, 0, null, 0, null, null, null]
     lib.mla_decode_fwd.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p] + \
-        [ctypes.c_int] * 4 + [ctypes.c_float] + [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_void_p,
+        [ctypes.c_int] * 6 + [ctypes.c_float] + [ctypes.c_void_p] * 2 + [ctypes.c_int, ctypes.c_void_p,
                                                                            ctypes.c_size_t, ctypes.c_void_p,
                                                                            ctypes.c_int] + [ctypes.c_void_p] * 3
     assert lib.mla_decode_fwd(*args) == 1

@@ -12,12 +12,15 @@ from tests.parity import compare, dense_oracle, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_dense(case, num_parts=None, split_path=False):
+def run_dense(case, num_parts=None, split_path=False, out_dtype=None):
     c = to_dev(case)
     B, s_q, h_q = case.batch, case.s_q, case.h_q
+    if num_parts is None:
+        num_parts = mla.mla_num_parts_dense(s_q, h_q, case.h_kv)
     pl = mla.plan(c.cache_seqlens, B, s_q * h_q, num_parts=num_parts)
-    out = torch.full((B, s_q, h_q, 512), float("nan"), device="cuda",
-                     dtype=torch.float32 if case.out_fp32 else torch.bfloat16)
+    if out_dtype is None:
+        out_dtype = torch.float32 if case.out_fp32 else case.q.dtype
+    out = torch.full((B, s_q, h_q, 512), float("nan"), device="cuda", dtype=out_dtype)
     lse = torch.full((B, s_q, h_q), float("nan"), device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     if split_path:
@@ -127,3 +130,64 @@ def test_dense_request_local_plan():
     torch.cuda.synchronize()
     ro, rl = dense_oracle(case)
     compare(out, lse, ro, rl)
+
+
+# ---------------------------------------------------------------- several latent KV heads; fp16
+
+@pytest.mark.parametrize("h_kv,h_q,s_q,causal", [(2, 128, 1, False), (4, 128, 2, True), (2, 64, 3, True),
+                                                 (4, 16, 1, False), (3, 96, 2, False), (2, 256, 1, False)])
+def test_dense_kv_heads(h_kv, h_q, s_q, causal):
+    case = wl.dense_case(3, s_q, h_q, 0, seqlens=[65, 700, 2000], causal=causal, h_kv=h_kv, seed=h_kv * h_q + s_q)
+    out, lse, _ = run_dense(case)
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("num_parts", [1, 40])
+def test_dense_kv_heads_split_counts(num_parts):
+    case = wl.dense_case(3, 2, 64, 0, seqlens=[900, 130, 2000], causal=True, h_kv=2, seed=num_parts + 500)
+    out, lse, _ = run_dense(case, num_parts=num_parts, split_path=True)
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("h_q,s_q,causal,out_dtype", [(128, 1, False, torch.float16), (64, 2, True, torch.float16),
+                                                      (128, 1, False, torch.float32), (16, 1, False, torch.bfloat16)])
+def test_dense_fp16(h_q, s_q, causal, out_dtype):
+    case = wl.dense_case(2, s_q, h_q, 0, seqlens=[300, 1500], causal=causal, dtype=torch.float16, seed=h_q + s_q)
+    out, lse, _ = run_dense(case, out_dtype=out_dtype)
+    assert out.dtype == out_dtype
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+def test_dense_fp16_kv_heads_peaky():
+    case = wl.dense_case(2, 2, 64, 0, seqlens=[1000, 2100], causal=True, h_kv=2, dtype=torch.float16, q_scale=8.0,
+                         seed=601)
+    out, lse, _ = run_dense(case, num_parts=7)
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+def test_dense_kv_heads_static_workspace():
+    case = wl.dense_case(2, 1, 128, 0, seqlens=[500, 1300], h_kv=4, dtype=torch.float16, seed=602)
+    c = to_dev(case)
+    pl = mla.plan(c.cache_seqlens, 2, 128)
+    out = torch.empty(2, 1, 128, 512, dtype=torch.float16, device="cuda")
+    lse = torch.empty(2, 1, 128, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_decode_fwd_static_ws(c.q, c.kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset, pl.num_parts,
+                                 out, lse, status, case.causal, case.scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
+def test_num_parts_dense_counts_row_blocks():
+    base = mla.mla_num_parts(128, False)
+    assert mla.mla_num_parts_dense(1, 128, 1) == base
+    assert mla.mla_num_parts_dense(2, 128, 1) == mla.mla_num_parts(256, False)
+    assert mla.mla_num_parts_dense(1, 128, 2) == max(base // 2, 1)      # two head groups of 64 heads
+    assert mla.mla_num_parts_dense(3, 96, 3) == max(base // 3, 1)       # 3 groups, each one block of 3 tokens x 32 heads
+    assert mla.mla_num_parts_dense(5, 64, 2) == max(base // 4, 1)       # 2 groups of 32 heads x 2 blocks (4 + 1 tokens)

@@ -14,7 +14,8 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("name", ["dense_b1_hq16_sk256_fp32out", "dense_b64_hq128_sk2048to4096",
-                                  "dense_b1_hq64_sk65536", "dense_b16_sq2causal_hq128_sk4096to8192"])
+                                  "dense_b1_hq64_sk65536", "dense_b16_sq2causal_hq128_sk4096to8192",
+                                  "dense_b64_hq128_sk2048to4096_fp16", "dense_b32_hkv2_hq128_sk2048to4096"])
 def test_dense_workload_full_size(name):
     case = wl.make(name)
     c = to_dev(case)

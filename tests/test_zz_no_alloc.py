@@ -26,8 +26,10 @@ STATIC_WORKSPACE_BYTES = 64 << 20
 
 def _null_call(lib, batch, s_q, h_q, num_parts):
     n = None
-    return lib.mla_decode_fwd_static_ws(n, n, n, 1, 1, n, batch, s_q, h_q, 0, 1.0 / 24.0, n, n, num_parts, n, 0, n,
-                                        n, ctypes.c_void_p(0))
+    # ..., batch, s_q, h_q, h_kv = 1, dtype = bf16, causal = 0, scale, sched, split_offset, num_parts, out,
+    # out_type = bf16, lse, status, stream
+    return lib.mla_decode_fwd_static_ws(n, n, n, 1, 1, n, batch, s_q, h_q, 1, 0, 0, 1.0 / 24.0, n, n, num_parts, n, 0,
+                                        n, n, ctypes.c_void_p(0))
 
 
 def test_static_ws_refuses_oversize_before_any_device_call():
