@@ -165,6 +165,71 @@ def _quantise_records(x: torch.Tensor, rope: torch.Tensor) -> torch.Tensor:
     return rec
 
 
+@dataclass
+class DenseFp8Case:
+    q: torch.Tensor              # bf16 [B, s_q, h_q, 576]
+    kv8: torch.Tensor            # uint8 [num_pages, 64, 656]
+    block_table: torch.Tensor    # int32 [B, max_pages]
+    cache_seqlens: torch.Tensor  # int32 [B]
+    causal: bool
+    scale: float
+    name: str = ""
+
+    @property
+    def batch(self):
+        return self.q.shape[0]
+
+    @property
+    def s_q(self):
+        return self.q.shape[1]
+
+    @property
+    def h_q(self):
+        return self.q.shape[2]
+
+    def kv_bytes(self) -> int:
+        """Record bytes read: every valid token's 656-byte record once."""
+        return int(self.cache_seqlens.to(torch.int64).sum().item()) * RECORD
+
+
+def dense_fp8_case(batch, s_q, h_q, seqlen_lo, seqlen_hi=None, *, causal=False, seed=0, pool_factor=1.2,
+                   q_scale=1.0, seqlens=None, scale=None, poison=True, name="") -> DenseFp8Case:
+    """Seeded paged cache of FP8 records (N(0,1) rows quantised as for the sparse cases, bf16
+    RoPE), shuffled pages (1.2x the pages in use) and the block table; unused slots carry
+    1e3x scales as poison."""
+    g = _gen(seed)
+    if seqlens is None:
+        hi = seqlen_lo if seqlen_hi is None else seqlen_hi
+        seqlens = torch.randint(seqlen_lo, hi + 1, (batch,), generator=g, dtype=torch.int64)
+    seqlens = torch.as_tensor(seqlens, dtype=torch.int64).reshape(batch)
+    npg = [(int(L) + PAGE - 1) // PAGE for L in seqlens.tolist()]
+    total = sum(npg)
+    pool = max(int(math.ceil(pool_factor * total)), total, 1)
+    perm = torch.randperm(pool, generator=g)
+    max_pages = max(max(npg), 1)
+    bt = torch.full((batch, max_pages), -1, dtype=torch.int32)
+    pos = 0
+    for b in range(batch):
+        bt[b, :npg[b]] = perm[pos:pos + npg[b]].to(torch.int32)
+        pos += npg[b]
+    x = torch.randn(pool * PAGE, 512, generator=g)
+    rope = torch.randn(pool * PAGE, 64, generator=g).to(torch.bfloat16)
+    kv8 = _quantise_records(x, rope).reshape(pool, PAGE, RECORD)
+    if poison:
+        used = torch.zeros(pool, PAGE, dtype=torch.bool)
+        for b in range(batch):
+            L = int(seqlens[b])
+            for lp in range(npg[b]):
+                used[int(bt[b, lp]), :min(PAGE, L - lp * PAGE)] = True
+        flat = kv8.view(pool * PAGE, RECORD)
+        scales = flat[:, 512:528].contiguous().view(torch.float32).reshape(-1, 4)
+        scales[~used.reshape(-1)] *= POISON
+        flat[:, 512:528] = scales.contiguous().view(torch.uint8).reshape(-1, 16)
+    q = (torch.randn(batch, s_q, h_q, D_QK, generator=g) * q_scale).to(torch.bfloat16)
+    return DenseFp8Case(q=q, kv8=kv8, block_table=bt, cache_seqlens=seqlens.to(torch.int32), causal=bool(causal),
+                        scale=(1.0 / math.sqrt(D_QK)) if scale is None else scale, name=name)
+
+
 def sparse_case(batch, s_q, h_q, *, topk=2048, pages_per_req=512, topk_lo=1024,
                 topk_hi=2048, seed=0, q_scale=1.0, poison=True, topk_lengths=None,
                 scale=None, name="") -> SparseCase:
@@ -226,6 +291,9 @@ WORKLOADS = {
                                               seqlen_hi=4096, dtype=torch.float16, seed=1008),
     "dense_b32_hkv2_hq128_sk2048to4096": dict(kind="dense", batch=32, s_q=1, h_q=128, seqlen_lo=2048,
                                               seqlen_hi=4096, h_kv=2, seed=1009),
+    # the dense decode over a paged cache of FP8 records
+    "dense_fp8_b64_hq128_sk2048to4096": dict(kind="dense_fp8", batch=64, s_q=1, h_q=128, seqlen_lo=2048,
+                                             seqlen_hi=4096, seed=1010),
     # the H=64 and S_q>1 query shapes of the packed-path page's grid, full top-k prefix
     "sparse_fp8_b4_sq4_hq64_topk2048": dict(kind="sparse", batch=4, s_q=4, h_q=64, topk=2048,
                                             pages_per_req=512, topk_lo=2048, topk_hi=2048,
@@ -241,4 +309,6 @@ def make(name: str):
     kind = spec.pop("kind")
     if kind == "dense":
         return dense_case(name=name, **spec)
+    if kind == "dense_fp8":
+        return dense_fp8_case(name=name, **spec)
     return sparse_case(name=name, **spec)

@@ -248,6 +248,34 @@ def dense_decode(q, kv, block_table, cache_seqlens, causal, scale, batches=None)
     return out, lse
 
 
+def dense_fp8_decode(q, kv8, block_table, cache_seqlens, causal, scale, batches=None):
+    """Dense decode over a paged cache of 656-byte FP8 records.
+
+    PR #183 (*Limitations / future work*) lists an FP8 KV cache as what the
+    SM80 dense kernel lacks, without a format; the only FP8 layout the pages
+    define is PR #200's record (*SM90 packing kernel*), so that is the reading
+    taken: kv8 [num_pages, 64, 656], token j of request b is record j % 64 of
+    page block_table[b][j // 64], its key is ``decode_record`` of it, and the
+    attention (all keys, causal alignment, LSE) is that of ``dense_decode``.
+    Returns out [B, s_q, h_q, 512] and lse [B, s_q, h_q] in float64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    kv8 = np.asarray(kv8, dtype=np.uint8)
+    B, s_q, h_q, _ = q.shape
+    out = np.zeros((B, s_q, h_q, D_V), dtype=np.float64)
+    lse = np.full((B, s_q, h_q), -np.inf, dtype=np.float64)
+    for b in (range(B) if batches is None else batches):
+        L = int(cache_seqlens[b])
+        keys = np.empty((L, D_QK), dtype=np.float64)
+        for j in range(L):
+            keys[j] = decode_record(kv8[int(block_table[b, j // PAGE_SIZE]), j % PAGE_SIZE])
+        qrows = q[b].reshape(s_q * h_q, D_QK)
+        o, l = attend(qrows, keys, scale, causal_mask(s_q, h_q, L, causal))
+        out[b] = o.reshape(s_q, h_q, D_V)
+        lse[b] = l.reshape(s_q, h_q)
+    return out, lse
+
+
 def sparse_decode(q, kv8, indices, topk_length, scale, batches=None):
     """Sparse FP8 MLA decode over selected 656-byte records.
 

@@ -514,3 +514,31 @@ def test_fp16_case_holds_exact_fp16_values():
                                 False, case.scale)
     ro, rl = sdpa_dense_reference(case, 0)
     assert np.abs(out[0] - ro).max() < TOL and np.abs(lse[0] - rl).max() < TOL
+
+
+# ---------------------------------------------------------------- dense decode over FP8 records
+
+@pytest.mark.parametrize("s_q,causal", [(1, False), (2, True), (3, True)])
+def test_dense_fp8_equals_dense_on_decoded_records(s_q, causal):
+    """Same keys, same order: decoding every record first and running the bf16-path oracle gives
+    the same fp64 result; the records are decoded by torch's own fp8/bf16 conversions here."""
+    case = wl.dense_fp8_case(2, s_q, 8, 0, seqlens=[70, 200], causal=causal, seed=80 + s_q)
+    kv = torch_decode_records(case.kv8, torch.arange(case.kv8.shape[0] * 64)).reshape(-1, 64, 576)
+    o1, l1 = orc.dense_fp8_decode(f64(case.q), case.kv8.numpy(), case.block_table.numpy(),
+                                  case.cache_seqlens.numpy(), causal, case.scale)
+    o2, l2 = orc.dense_decode(f64(case.q), kv.numpy(), case.block_table.numpy(), case.cache_seqlens.numpy(), causal,
+                              case.scale)
+    assert np.abs(o1 - o2).max() < TOL and np.abs(l1 - l2).max() < TOL
+
+
+def test_dense_fp8_equals_sparse_over_every_slot():
+    case = wl.dense_fp8_case(2, 1, 4, 0, seqlens=[130, 64], seed=84)
+    bt = case.block_table.numpy()
+    L = case.cache_seqlens.numpy()
+    ind = np.full((2, 1, 192), -1, dtype=np.int64)
+    for b in range(2):
+        j = np.arange(L[b])
+        ind[b, 0, :L[b]] = bt[b, j // 64] * 64 + j % 64
+    o1, l1 = orc.dense_fp8_decode(f64(case.q), case.kv8.numpy(), bt, L, False, case.scale)
+    o2, l2, bad = orc.sparse_decode(f64(case.q), case.kv8.numpy(), ind, None, case.scale)
+    assert bad == 0 and np.array_equal(o1, o2) and np.array_equal(l1, l2)
