@@ -199,6 +199,7 @@ def cpu_oracle_sample(case, budget_s, gpu_out=None, gpu_lse=None):
 
 OTHER_WORKLOADS = ["dense_b1_hq16_sk256_fp32out", "dense_b1_hq64_sk65536", "dense_b16_sq2causal_hq128_sk4096to8192",
                    "dense_b64_hq128_sk2048to4096_fp16", "dense_b32_hkv2_hq128_sk2048to4096",
+                   "dense_fp8_b64_hq128_sk2048to4096",
                    "sparse_fp8_b16_hq128_topk2048", "sparse_fp8_b4_sq4_hq64_topk2048",
                    "sparse_fp8_b2_sq8_hq128_topk2048"]
 
@@ -210,6 +211,7 @@ def time_other_workloads(mla, wl, timed, steps):
     for name in OTHER_WORKLOADS:
         case = wl.make(name)
         sparse = name.startswith("sparse")
+        fp8_dense = name.startswith("dense_fp8")
         q = case.q.cuda()
         B, s_q, h_q = case.batch, case.s_q, case.h_q
         out = torch.empty(B, s_q, h_q, 512, device="cuda",
@@ -223,6 +225,15 @@ def time_other_workloads(mla, wl, timed, steps):
             def fn():
                 mla.mla_sparse_fp8_decode_fwd(q, kv8, ind, tl, pl.sched, pl.split_offset, pl.num_parts,
                                               pl.workspace, out, lse, status, case.scale)
+        elif fp8_dense:
+            kv8, bt, sl = case.kv8.cuda(), case.block_table.cuda(), case.cache_seqlens.cuda()
+            ul = torch.empty(B * s_q, dtype=torch.int32, device="cuda")
+            mla.mla_dense_fp8_unit_lengths(sl, s_q, case.causal, ul)
+            pl = mla.plan(ul, B * s_q, h_q, sparse=True)
+
+            def fn():
+                mla.mla_dense_fp8_decode_fwd(q, kv8, bt, ul, pl.sched, pl.split_offset, pl.num_parts, pl.workspace,
+                                             out, lse, status, case.scale)
         else:
             kv, bt, sl = case.kv.cuda(), case.block_table.cuda(), case.cache_seqlens.cuda()
             pl = mla.plan(sl, B, s_q * h_q, num_parts=mla.mla_num_parts_dense(s_q, h_q, case.h_kv))
@@ -237,7 +248,8 @@ def time_other_workloads(mla, wl, timed, steps):
         us = 1e3 * statistics.mean(ms)
         nbytes = case.kv_bytes()
         res[name] = {"us_per_call": us, "gb_per_s": nbytes / (us * 1e-6) / 1e9, "bytes_per_call": nbytes,
-                     "bytes": "valid records x 656" if sparse else "sum of cache_seqlens x 1152 x h_kv",
+                     "bytes": ("valid records x 656" if sparse else "sum of cache_seqlens x 656" if fp8_dense
+                               else "sum of cache_seqlens x 1152 x h_kv"),
                      "num_parts": pl.num_parts, "splits": int(pl.split_offset[-1].item())}
         if sparse:
             res[name + "_packed"] = time_packed(mla, case, q, kv8, ind, tl, pl, out, lse, status, timed, steps)

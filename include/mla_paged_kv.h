@@ -284,6 +284,36 @@ int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size
                                      void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
                                      int32_t* d_status, mla_stream_t stream);
 
+/* Dense decode over a paged cache of FP8 records.  FlashMLA PR #183
+ * (Limitations / future work) names an FP8 KV cache as missing from its SM80
+ * dense kernel without a format; the FP8 format the pages define is PR #200's
+ * 656-byte record, so that is the cache format here: d_kv8 [num_pages, 64,
+ * 656], token j of request b is record j%64 of page block_table[b][j/64], and
+ * its key/value decode exactly as for mla_sparse_fp8_decode_fwd.  Every token
+ * is a key (no selection); the sparse kernel runs with block-table addressing.
+ *   d_q            bf16 [batch, s_q, h_q, 576], h_q <= 128
+ *   d_block_table  int32 [batch, max_pages]; a page outside [0, num_pages) at
+ *                  a position the unit reads is masked and reported
+ *                  (MLA_ERR_BAD_INDEX).
+ *   d_unit_lengths int32 [batch * s_q]: keys each query token sees, from
+ *                  mla_dense_fp8_unit_lengths (causal alignment as for
+ *                  mla_decode_fwd); also the d_lengths of the plan:
+ *                  mla_get_metadata(d_unit_lengths, -1, batch*s_q, num_parts,
+ *                  ...) with num_parts = mla_num_parts(h_q, 1).
+ *   d_workspace    >= mla_workspace_bytes(batch*s_q, h_q, num_parts)
+ *   d_out bf16 [batch, s_q, h_q, 512], d_lse fp32 [batch, s_q, h_q]. */
+int mla_dense_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, const int32_t* d_block_table, int max_pages,
+                             int num_pages, const int32_t* d_unit_lengths, int batch, int s_q, int h_q,
+                             float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
+                             int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
+                             int32_t* d_status, mla_stream_t stream);
+
+/* Keys seen by each query token of a dense cache: unit b*s_q + i gets
+ * max(L_b - s_q + i + 1, 0) when causal, else L_b (d_cache_seqlens int32
+ * [batch] -> d_unit_lengths int32 [batch * s_q]). */
+int mla_dense_fp8_unit_lengths(const int32_t* d_cache_seqlens, int batch, int s_q, int causal,
+                               int32_t* d_unit_lengths, mla_stream_t stream);
+
 /* Gather + unpack of selected records to fp32 key rows, bit-exact:
  * k[d] = fp32(e4m3[d]) * scale[d/128] as one fp32 round-to-nearest-even
  * multiply (d < 512), k[512+e] = fp32(bf16 rope[e]).  Index -1 or an index

@@ -25,6 +25,7 @@ int sparse_smem_bytes();
 int sparse_threads();
 const void* sparse_kernel_ptr();
 cudaError_t launch_unpack(const uint8_t*, int, const int32_t*, int, float*, int32_t*, cudaStream_t);
+cudaError_t launch_unit_lengths(const int32_t*, int, int, int, int32_t*, cudaStream_t);
 cudaError_t launch_pack(const uint8_t*, int, const int32_t*, int, const int32_t*, int, uint8_t*, uint64_t*,
                         int32_t*, cudaStream_t);
 }  // namespace mla
@@ -374,12 +375,20 @@ namespace {
 
 // Sparse attention over a record pool: the native selection (indices into
 // the paged pool) or a packed one (masks over the packed records).
-int sparse_decode(const void* d_q, const uint8_t* d_kv8, int num_pages, const int32_t* d_indices,
-                  const uint64_t* d_masks, int topk, const int32_t* d_topk_length, int batch, int s_q, int h_q,
-                  float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
-                  void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse, int32_t* d_status,
-                  mla_stream_t stream) {
-  if (!d_q || !d_kv8 || (!d_indices && !d_masks) || !d_sched || !d_split_offset || !d_workspace || !d_out || !d_lse || !d_status)
+// How a unit's slots address the record pool: an index list (native
+// sparse), per-tile masks over packed records, or a block table (dense FP8).
+struct SlotSource {
+  const int32_t* indices = nullptr;
+  const uint64_t* masks = nullptr;
+  const int32_t* block_table = nullptr;
+  int max_pages = 0;
+};
+
+int sparse_decode(const void* d_q, const uint8_t* d_kv8, int num_pages, SlotSource src, int topk,
+                  const int32_t* d_topk_length, int batch, int s_q, int h_q, float softmax_scale,
+                  const int32_t* d_sched, const int32_t* d_split_offset, int num_parts, void* d_workspace,
+                  size_t workspace_bytes, void* d_out, float* d_lse, int32_t* d_status, mla_stream_t stream) {
+  if (!d_q || !d_kv8 || (!src.indices && !src.masks && !src.block_table) || !d_sched || !d_split_offset || !d_workspace || !d_out || !d_lse || !d_status)
     return MLA_ERR_INVALID_ARG;
   if (batch < 1 || s_q < 1 || h_q < 1 || num_pages < 1 || topk < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
@@ -399,12 +408,14 @@ int sparse_decode(const void* d_q, const uint8_t* d_kv8, int num_pages, const in
   p.rows = h_q;
   p.row_blocks = 1;
   p.h_q = h_q;
-  p.s_q = 1;
+  p.s_q = src.block_table != nullptr ? s_q : 1;  // dense FP8: unit u is token u % s_q of request u / s_q
   p.causal = 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
   p.num_pages = num_pages;
-  p.indices = d_indices;
-  p.packed_mask = d_masks;
+  p.indices = src.indices;
+  p.packed_mask = src.masks;
+  p.block_table = src.block_table;
+  p.max_pages = src.max_pages;
   p.topk = topk;
   p.kv8 = d_kv8;
   p.sched = d_sched;
@@ -447,9 +458,10 @@ int mla_sparse_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, int num_pag
                               int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
                               int32_t* d_status, mla_stream_t stream) {
   if (!d_indices) return MLA_ERR_INVALID_ARG;
-  return sparse_decode(d_q, d_kv8, num_pages, d_indices, nullptr, topk, d_topk_length, batch, s_q, h_q,
-                       softmax_scale, d_sched, d_split_offset, num_parts, d_workspace, workspace_bytes, d_out, d_lse,
-                       d_status, stream);
+  SlotSource src;
+  src.indices = d_indices;
+  return sparse_decode(d_q, d_kv8, num_pages, src, topk, d_topk_length, batch, s_q, h_q, softmax_scale, d_sched,
+                       d_split_offset, num_parts, d_workspace, workspace_bytes, d_out, d_lse, d_status, stream);
 }
 
 size_t mla_packed_kv_workspace_bytes(int n_units, int topk) {
@@ -490,9 +502,38 @@ int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size
   // the packed records form a pool of units * tiles pages of 64 records
   const long long pool_pages = units * l.tiles;
   if (pool_pages > (1LL << 31) / MLA_PAGE_SIZE) return MLA_ERR_UNSUPPORTED;
-  return sparse_decode(d_q, records, static_cast<int>(pool_pages), nullptr, masks, topk, d_topk_length, batch, s_q,
-                       h_q, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace, workspace_bytes, d_out,
-                       d_lse, d_status, stream);
+  SlotSource src;
+  src.masks = masks;
+  return sparse_decode(d_q, records, static_cast<int>(pool_pages), src, topk, d_topk_length, batch, s_q, h_q,
+                       softmax_scale, d_sched, d_split_offset, num_parts, d_workspace, workspace_bytes, d_out, d_lse,
+                       d_status, stream);
+}
+
+int mla_dense_fp8_unit_lengths(const int32_t* d_cache_seqlens, int batch, int s_q, int causal,
+                               int32_t* d_unit_lengths, mla_stream_t stream) {
+  if (!d_cache_seqlens || !d_unit_lengths || batch < 1 || s_q < 1) return MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(batch) * s_q > 65535) return MLA_ERR_UNSUPPORTED;
+  return launch_unit_lengths(d_cache_seqlens, batch, s_q, causal ? 1 : 0, d_unit_lengths,
+                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+int mla_dense_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, const int32_t* d_block_table, int max_pages,
+                             int num_pages, const int32_t* d_unit_lengths, int batch, int s_q, int h_q,
+                             float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
+                             int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
+                             int32_t* d_status, mla_stream_t stream) {
+  if (!d_block_table || !d_unit_lengths || max_pages < 1) return MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(max_pages) * MLA_PAGE_SIZE > (1LL << 30) ||
+      static_cast<long long>(num_pages) * MLA_PAGE_SIZE > (1LL << 30))
+    return MLA_ERR_UNSUPPORTED;
+  SlotSource src;
+  src.block_table = d_block_table;
+  src.max_pages = max_pages;
+  return sparse_decode(d_q, d_kv8, num_pages, src, max_pages * MLA_PAGE_SIZE, d_unit_lengths, batch, s_q, h_q,
+                       softmax_scale, d_sched, d_split_offset, num_parts, d_workspace, workspace_bytes, d_out, d_lse,
+                       d_status, stream);
 }
 
 int mla_sparse_fp8_unpack(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int n, float* d_k_out,

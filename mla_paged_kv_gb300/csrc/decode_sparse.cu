@@ -218,8 +218,17 @@ __device__ __forceinline__ uint4 codes_to_bf16(uint2 codes) {
 // Selection entry t of unit b as stored (no check yet); -1 past the list.
 // Packed selection: the record of slot t sits at ordinal b * tiles * 64 + t
 // of the packed records when its bit in the tile's valid mask is set.
+// Dense FP8 cache: every token is a key; slot t of unit b (query token
+// b % s_q of request b / s_q) is record t % 64 of page block_table[b/s_q][t/64];
+// a page outside the pool comes back as -2 (reported, masked).
 __device__ __forceinline__ int load_slot(const DecodeParams& p, int b, int t, int L) {
   if (t >= L) return -1;
+  if (p.block_table != nullptr) {
+    const int pg = t / kT;
+    const int page =
+        pg < p.max_pages ? __ldg(p.block_table + static_cast<size_t>(b / p.s_q) * p.max_pages + pg) : -1;
+    return (page < 0 || page >= p.num_pages) ? -2 : page * kT + (t - pg * kT);
+  }
   if (p.packed_mask != nullptr) {
     const int tiles = (p.topk + kT - 1) / kT;
     const unsigned long long m =
@@ -808,6 +817,17 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ k
   }
 }
 
+// Keys each query token sees in a dense cache: token i of request b sees the
+// first L_b - s_q + i + 1 keys when causal (bottom-right alignment), all L_b otherwise.
+__global__ void unit_lengths_kernel(const int32_t* __restrict__ seqlens, int batch, int s_q, int causal,
+                                    int32_t* __restrict__ unit_len) {
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= batch * s_q) return;
+  const int b = u / s_q, i = u - b * s_q;
+  const int L = max(seqlens[b], 0);
+  unit_len[u] = causal ? max(L - s_q + i + 1, 0) : L;
+}
+
 // Bit-exact record unpack: one thread per (record, 8-dim chunk).
 __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__ kv8, int num_pages,
                                                      const int32_t* __restrict__ indices, int n,
@@ -865,6 +885,13 @@ cudaError_t launch_pack(const uint8_t* kv8, int num_pages, const int32_t* indice
                         cudaStream_t stream) {
   const dim3 grid((topk + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE, n_units);
   sp::pack_kernel<<<grid, 256, 0, stream>>>(kv8, num_pages, indices, topk, topk_length, packed, masks, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unit_lengths(const int32_t* seqlens, int batch, int s_q, int causal, int32_t* unit_len,
+                                cudaStream_t stream) {
+  const int n = batch * s_q;
+  sp::unit_lengths_kernel<<<(n + 255) / 256, 256, 0, stream>>>(seqlens, batch, s_q, causal, unit_len);
   return cudaGetLastError();
 }
 
