@@ -15,8 +15,7 @@
 namespace mla {
 cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, int, cudaStream_t);
 cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, void*, int, float*, cudaStream_t);
-cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, const void*, int, int,
-                         cudaStream_t);
+cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int, int, cudaStream_t);
 int dense_smem_bytes();
 int dense_threads();
 const void* dense_kernel_ptr(int half);
@@ -334,7 +333,7 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
                                h_kv, dtype, causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
                                workspace_bytes, d_out, out_type, d_lse, d_status, &p, &qm, &km);
   if (rc != MLA_OK) return rc;
-  return launch_dense(qm, km, p, d_q, num_parts, dtype == MLA_DTYPE_FP16 ? 1 : 0,
+  return launch_dense(qm, km, p, num_parts, dtype == MLA_DTYPE_FP16 ? 1 : 0,
                       reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;

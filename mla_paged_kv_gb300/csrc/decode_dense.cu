@@ -31,17 +31,21 @@
 //    watches the copy's barrier) and for the softmax threads' go, given as
 //    soon as the tile's reference is known.
 //  * Q of the row block is the MMA A operand: dims [0, 384) sit in TMEM
-//    (packed bf16 pairs, written by the softmax threads once per unit), dims
-//    [384, 576) in shared memory (TMA, 128-byte swizzle).
+//    (packed bf16 pairs), dims [384, 576) in shared memory (TMA, 128-byte
+//    swizzle).  A Q warp streams a unit's nine 64-dim Q boxes through the
+//    three box slots of that shared-memory buffer; the MMA thread moves
+//    boxes 0-5 (dims [0, 384)) into TMEM with tcgen05.cp as they land, and
+//    boxes 6-8 stay.  The next unit's Q is prefetched into L2 meanwhile, and
+//    the softmax warps write the epilogue while Q streams in.
 //  * One tile = nine 64-dim TMA boxes of one page.  The four boxes that are
 //    this CTA's V half go to a 3-slot "V" ring for every tile (P V reads
 //    them; for its own tiles Q K^T reads them too); the other five go to a
 //    "K" slot, for own tiles only, released as soon as Q K^T has read them.
 //  * tcgen05.mma M=128: S (N=64) and O (N=256) accumulate in TMEM; each
 //    group of MMAs is one fully unrolled block of compile-time descriptors.
-// Roles: warps 0-3 softmax + epilogue + Q-to-TMEM (thread = row = TMEM lane),
-//        warp 4 K-slot + Q producer, warp 5 V-ring producer,
-//        warp 6 MMA issuer and TMEM owner.
+// Roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane),
+//        warp 4 K-slot producer, warp 5 V-ring producer,
+//        warp 6 MMA issuer and TMEM owner, warp 7 Q producer.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -86,9 +90,10 @@ constexpr int kOffLIn = kOffLOut + kVecBytes;      // mailbox: the peer's row su
 constexpr int kOffBar = kOffLIn + kVecBytes;
 
 enum : int {
-  Q_FULL = 0,
-  Q_EMPTY = 1,
-  K_FULL = 2,                     // +slot
+  Q_EMPTY = 0,                    // the unit's last Q K^T is done: Q may be replaced
+  QB_FULL = 1,                    // +slot: a Q box has landed in that slot of the Q buffer (TMA bytes)
+  QB_EMPTY = QB_FULL + kQSmemBoxes,  // +slot: the box in that slot has been copied into TMEM
+  K_FULL = QB_EMPTY + kQSmemBoxes,   // +slot
   K_EMPTY = K_FULL + kKSlots,     // +slot
   V_FULL = K_EMPTY + kKSlots,     // +slot
   V_EMPTY = V_FULL + kVSlots,     // +slot
@@ -119,8 +124,8 @@ static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffPOwn % 1024 == 0 && 
 static_assert(kOffRefOut % 16 == 0 && kOffRefIn % 16 == 0 && kOffLOut % 16 == 0 && kOffLIn % 16 == 0,
               "bulk copies need 16-byte alignment");
 
-constexpr int kThreads = 224;
-constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6;
+constexpr int kThreads = 256;
+constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6, kWarpQ = 7;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
 constexpr uint32_t kTmemS = 256;  // S: [256, 320)
@@ -289,32 +294,6 @@ __device__ __forceinline__ bool block_row(const DecodeParams& p, int grp, int rb
   return t < p.block_tokens && tok < p.s_q;
 }
 
-// Q row `row` of unit b, dims [0, 384) -> this thread's TMEM lane, columns
-// [kTmemQ, kTmemQ + 192): column c holds dims (2c, 2c+1) as packed bf16.
-__device__ __forceinline__ void load_q_to_tmem(const DecodeParams& p, const uint16_t* q, int b, int qrow, bool ok,
-                                               uint32_t taddr) {
-  const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * p.rows + (ok ? qrow : 0)) * kDqk);
-#pragma unroll 1
-  for (int round = 0; round < 2; ++round) {
-    uint4 w[24];  // all loads of the round in flight at once
-#pragma unroll
-    for (int i = 0; i < 24; ++i) w[i] = ok ? __ldg(src + round * 24 + i) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int g = 0; g < 6; ++g) {
-      uint32_t v[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[4 * j + 0] = w[4 * g + j].x;
-        v[4 * j + 1] = w[4 * g + j].y;
-        v[4 * j + 2] = w[4 * g + j].z;
-        v[4 * j + 3] = w[4 * g + j].w;
-      }
-      tmem_st16(taddr + kTmemQ + round * 96 + g * 16, v);
-    }
-  }
-  tmem_wait_st();
-}
-
 // O half (this thread's row) *= alpha.
 __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
 #pragma unroll 1
@@ -338,7 +317,7 @@ __device__ __forceinline__ float ref_alpha(float r_old, float r_new) {
 template <bool kHalf>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     dense_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
-                        const DecodeParams p, const uint16_t* __restrict__ q) {
+                        const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -370,8 +349,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     *abort_flag = 0;
-    mbar_init(&bars[Q_FULL], 128 + 1);  // softmax threads (TMEM part) + K producer (TMA part)
     mbar_init(&bars[Q_EMPTY], 1);
+    for (int i = 0; i < kQSmemBoxes; ++i) {
+      mbar_init(&bars[QB_FULL + i], 1);
+      mbar_init(&bars[QB_EMPTY + i], 1);
+    }
     for (int i = 0; i < kKSlots; ++i) {
       mbar_init(&bars[K_FULL + i], 1);
       mbar_init(&bars[K_EMPTY + i], 1);
@@ -411,10 +393,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpK && lane == 0) {
-    prefetch_tmap(&q_map);
-    prefetch_tmap(&kv_map);
-  }
+  if (warp == kWarpQ && lane == 0) prefetch_tmap(&q_map);
+  if (warp == kWarpK && lane == 0) prefetch_tmap(&kv_map);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -431,38 +411,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producers
     const bool is_k = (warp == kWarpK);
     const uint64_t pol_kv = policy_evict_first();
-    const uint64_t pol_q = policy_evict_last();
     Cursor c;
     cursor_init(p, P, c);
     bool ok = true;
     uint32_t k_issued[kKSlots] = {}, v_issued[kVSlots] = {};
-    uint32_t q_issued = 0, own_k = 0;
+    uint32_t own_k = 0;
     int page_reg = 0, page_base = -1, cur_b = -1;
     while (ok && c.valid) {
-      if (is_k && cursor_first(c)) {
-        if (lane == 0) {
-          if (c.u >= 1) ok = mbar_wait(&bars[Q_EMPTY], (c.u - 1) & 1, abort_flag);
-          if (ok) {
-            mbar_arrive_expect_tx(&bars[Q_FULL], kQSmemBoxes * q_box_bytes);
-            if (p.h_kv == 1) {
-              const int row0 = c.b * p.rows + rb * kRowsPerBlock;
-#pragma unroll
-              for (int i = 0; i < kQSmemBoxes; ++i)
-                tma_load_2d(sQ + i * kQBoxBytes, &q_map, &bars[Q_FULL], 64 * (kQTmemBoxes + i), row0, pol_q);
-            } else {
-              // [batch * s_q][h_kv][group_heads][576]: block_tokens tokens of head group grp
-              const int tok0 = c.b * p.s_q + rb * p.block_tokens;
-#pragma unroll
-              for (int i = 0; i < kQSmemBoxes; ++i)
-                tma_load_4d(sQ + i * kQBoxBytes, &q_map, &bars[Q_FULL], 64 * (kQTmemBoxes + i), 0, grp, tok0,
-                            pol_q);
-            }
-            ++q_issued;
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-      }
       const bool mine = (c.t & 1u) == rank;
       if (!is_k || mine) {
         // page ids of the next 32 pages of this unit, one per lane
@@ -516,7 +471,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (k_issued[s] > 0) mbar_wait(&bars[K_FULL + s], (k_issued[s] - 1) & 1, nullptr);
       for (int s = 0; s < kVSlots; ++s)
         if (v_issued[s] > 0) mbar_wait(&bars[V_FULL + s], (v_issued[s] - 1) & 1, nullptr);
-      if (q_issued > 0) mbar_wait(&bars[Q_FULL], (q_issued - 1) & 1, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == kWarpQ) {
+    // ------------------------------------------------------------ Q producer
+    // Per unit, the nine 64-dim boxes of Q in order through the three slots
+    // of the shared-memory Q buffer: box j goes to slot j % 3.  Boxes 0-5
+    // (dims [0, 384)) are copied into TMEM by the MMA thread, which frees
+    // the slot for box j + 3; boxes 6-8 stay until the unit's last Q K^T.
+    if (lane == 0) {
+      const uint64_t pol_q = policy_evict_last();
+      Cursor c;
+      cursor_init(p, P, c);
+      bool ok = true;
+      uint32_t qb_issued[kQSmemBoxes] = {};
+      // box j of unit b into slot j % 3; into L2 only when bar is null
+      auto q_box = [&](int b, int j, uint64_t* bar) {
+        uint8_t* dst = sQ + (j % kQSmemBoxes) * kQBoxBytes;
+        if (p.h_kv == 1) {
+          const int row0 = b * p.rows + rb * kRowsPerBlock;
+          if (bar)
+            tma_load_2d(dst, &q_map, bar, 64 * j, row0, pol_q);
+          else
+            tma_prefetch_2d(&q_map, 64 * j, row0);
+        } else {
+          // [batch * s_q][h_kv][group_heads][576]: block_tokens tokens of head group grp
+          const int tok0 = b * p.s_q + rb * p.block_tokens;
+          if (bar)
+            tma_load_4d(dst, &q_map, bar, 64 * j, 0, grp, tok0, pol_q);
+          else
+            tma_prefetch_4d(&q_map, 64 * j, 0, grp, tok0);
+        }
+      };
+      if (c.valid)
+        for (int j = 3; j < 9; ++j) q_box(c.b, j, nullptr);
+      while (ok && c.valid) {
+        if (c.u >= 1) ok = mbar_wait(&bars[Q_EMPTY], (c.u - 1) & 1, abort_flag);
+        for (int j = 0; ok && j < 9; ++j) {
+          const int sl = j % kQSmemBoxes;
+          // the slot's previous box (j - 3) has been copied into TMEM
+          if (j >= kQSmemBoxes) ok = mbar_wait(&bars[QB_EMPTY + sl], (2 * c.u + j / 3 - 1) & 1, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars[QB_FULL + sl], q_box_bytes);
+          q_box(c.b, j, &bars[QB_FULL + sl]);
+          ++qb_issued[sl];
+        }
+        // on to the next unit; its Q into L2 while this one is worked on
+        c.t += static_cast<uint32_t>(c.hi - c.k);
+        ++c.u;
+        cursor_seek(p, P, c, c.b + 1);
+        if (ok && c.valid)
+          for (int j = 0; j < 9; ++j) q_box(c.b, j, nullptr);
+      }
+      if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+      // no TMA write may land after this CTA exits
+      for (int sl = 0; sl < kQSmemBoxes; ++sl)
+        if (qb_issued[sl] > 0) mbar_wait(&bars[QB_FULL + sl], (qb_issued[sl] - 1) & 1, nullptr);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
@@ -542,7 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       cursor_init(p, P, cv);
       uint32_t a_own = 0, pv_own = 0, pv_recv = 0;
       int q_phase = 0;          // 0: next is QKa of cq, 1: next is QKb of cq
-      bool q_have = false;      // Q of cq's unit has been seen complete
+      uint32_t qb_seen = 0;     // Q boxes seen landed (nine per unit, in order)
       bool ok = true;
       uint64_t t_last = globaltimer_ns();
       // cq onto the next own tile, releasing the Q of every unit it leaves;
@@ -554,11 +564,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!mine || q_phase == 2) {
             // leaving this tile; at the unit's end, Q of the unit is released
             if (cursor_last(cq)) {
-              if (!q_have) {
-                if (!mbar_test_wait(&bars[Q_FULL], cq.u & 1)) return false;
-              }
+              if (qb_seen < 9u * static_cast<uint32_t>(cq.u + 1)) return false;
               umma_commit(&bars[Q_EMPTY]);
-              q_have = false;
             }
             cursor_next(p, P, cq);
             q_phase = 0;
@@ -566,6 +573,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           return true;  // own tile with QKb next
         }
+        return true;
+      };
+      // the next Q box: boxes 0-5 are copied into TMEM (four copies of 128
+      // rows x 16 dims, the K steps the MMAs read) and their slot released;
+      // boxes 6-8 are only counted (they stay for the MMAs)
+      auto q_copy = [&]() -> bool {
+        const uint32_t uq = qb_seen / 9u, j = qb_seen % 9u, sl = j % kQSmemBoxes;
+        if (!mbar_test_wait(&bars[QB_FULL + sl], (3u * uq + j / 3u) & 1u)) return false;
+        if (j < 6u) {
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t k = 0; k < 4; ++k)
+            tmem_cp_128x256b(tmem + kTmemQ + 32u * j + 8u * k,
+                             q_desc0 + static_cast<uint64_t>((sl * kQBoxBytes + k * 32u) >> 4));
+          umma_commit(&bars[QB_EMPTY + sl]);
+        }
+        ++qb_seen;
         return true;
       };
       advance_q();
@@ -607,11 +631,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             progressed = true;
           }
         }
+        if (!progressed) progressed = q_copy();
         if (!progressed && cq.valid && advance_q() && cq.valid) {
           if (q_phase == 0) {
             const int ks = static_cast<int>(a_own % kKSlots);
-            bool ready = q_have || mbar_test_wait(&bars[Q_FULL], cq.u & 1);
-            if (ready) q_have = true;
+            bool ready = qb_seen >= 9u * static_cast<uint32_t>(cq.u + 1);
             ready = ready && mbar_test_wait(&bars[K_FULL + ks], (a_own / kKSlots) & 1);
             if (ready && a_own >= 1) ready = mbar_test_wait(&bars[S_FREE], (a_own - 1) & 1);
             if (ready) {
@@ -658,6 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // the last units' Q (units after the last own tile) are released too
       while (ok && cq.valid) {
+        if (q_copy()) t_last = globaltimer_ns();
         if (advance_q()) break;
         if (*abort_flag || globaltimer_ns() - t_last > MLA_WAIT_LIMIT_NS) ok = false;
       }
@@ -693,11 +718,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Cursor c;
     cursor_init(p, P, c);
     bool ok = true;
-    if (c.valid) {  // Q of the first unit
-      load_q_to_tmem(p, q, c.b, qrow, row_ok, taddr);
-      tc_fence_before();
-      mbar_arrive(&bars[Q_FULL]);
-    }
     uint32_t own_i = 0, recv_i = 0, units = 0;
     float r_cur = -INFINITY;  // reference (log2 units) after the last tile seen
     float l_own = 0.f;        // fp32 row sum of this CTA's own tiles, relative to r_cur
@@ -826,15 +846,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int b_here = c.b, u_here = c.u;
       cursor_next(p, P, c);
       if (!last) continue;
-      if (c.valid) {
-        // Q of this unit is no longer read (its last Q K^T finished): stage the next unit's Q
-        ok = warp_wait(&bars[Q_EMPTY], u_here & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        load_q_to_tmem(p, q, c.b, qrow, row_ok, taddr);
-        tc_fence_before();
-        mbar_arrive(&bars[Q_FULL]);
-      }
       // ---- row sum of the unit: ours + the peer's, both relative to r_cur
       if (units >= 1) {
         ok = warp_wait_cluster(&bars[L_FREE], (units - 1) & 1, abort_flag);
@@ -959,15 +970,13 @@ const void* dense_kernel_ptr(int half) {
               : reinterpret_cast<const void*>(&dn::dense_decode_kernel<false>);
 }
 
-cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, const DecodeParams& p, const void* q,
-                         int num_parts, int half, cudaStream_t stream) {
+cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, const DecodeParams& p, int num_parts,
+                         int half, cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
   if (half)
-    dn::dense_decode_kernel<true><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, p,
-                                                                                 static_cast<const uint16_t*>(q));
+    dn::dense_decode_kernel<true><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, p);
   else
-    dn::dense_decode_kernel<false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, p,
-                                                                                  static_cast<const uint16_t*>(q));
+    dn::dense_decode_kernel<false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, p);
   return cudaGetLastError();
 }
 

@@ -258,6 +258,20 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, 
                : "memory");
 }
 
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 // Shared-memory matrix descriptor, 128-byte swizzle (atoms of 8 rows x 128 B,
@@ -308,6 +322,15 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Shared memory -> TMEM: 128 rows x 32 bytes (lane = row, 8 consecutive
+// 32-bit columns from t_addr), the rows found through a shared-memory matrix
+// descriptor exactly as an MMA operand's K step of 16 16-bit elements is.
+// Asynchronous; ordered before later MMAs of the same thread and tracked by
+// its next tcgen05.commit.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t t_addr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(t_addr), "l"(s_desc) : "memory");
 }
 
 // Arrive (once) on a CTA-local mbarrier when all previously issued MMAs of
