@@ -45,7 +45,10 @@
 //    group of MMAs is one fully unrolled block of compile-time descriptors.
 // Roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane),
 //        warp 4 K-slot producer, warp 5 V-ring producer,
-//        warp 6 MMA issuer and TMEM owner, warp 7 Q producer.
+//        warp 6 Q K^T issuer (and Q copies into TMEM) and TMEM owner,
+//        warp 7 Q producer, warp 8 P V issuer.  Q K^T and P V come from two
+//        threads so that a ready P V does not wait for a Q K^T block to
+//        finish issuing; they touch different TMEM accumulators.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -124,8 +127,8 @@ static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffPOwn % 1024 == 0 && 
 static_assert(kOffRefOut % 16 == 0 && kOffRefIn % 16 == 0 && kOffLOut % 16 == 0 && kOffLIn % 16 == 0,
               "bulk copies need 16-byte alignment");
 
-constexpr int kThreads = 256;
-constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6, kWarpQ = 7;
+constexpr int kThreads = 288;
+constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6, kWarpQ = 7, kWarpPV = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
 constexpr uint32_t kTmemS = 256;  // S: [256, 320)
@@ -376,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[PV_DONE + 1], 1);
     mbar_init(&bars[O_FULL], 1);
     mbar_init(&bars[O_FREE], 128);
-    mbar_init(&bars[DRAIN], 1);
+    mbar_init(&bars[DRAIN], 2);  // the Q K^T issuer and the P V issuer
     fence_mbar_init_cluster();
     // armed for the first P, references and row sums the peer will send
     mbar_arrive_expect_tx(&bars[RECV_FULL], kPBytes);
@@ -529,28 +532,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (qb_issued[sl] > 0) mbar_wait(&bars[QB_FULL + sl], (qb_issued[sl] - 1) & 1, nullptr);
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kWarpPV) {
+    // ------------------------------------------------------------ P V issuer
+    // P V of every tile in order, from the own or the received P; issued by a
+    // thread of its own so that a ready P V enters the tensor pipe without
+    // waiting for a Q K^T block to finish issuing.
     if (lane == 0) {
       const uint32_t idesc_pv = idesc_16bit_f32(128, 256, true, kHalf);
-      const uint64_t q_desc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t k_desc0 = sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t vk_desc0 = sdesc_sw128(smem_u32(sV), 16, 1024);        // V boxes as K-major B of Q K^T
       const uint64_t vv_desc0 = sdesc_sw128(smem_u32(sV), kBoxBytes, 1024);  // V boxes as MN-major B of P V
       const uint64_t pown_desc = sdesc_sw128(smem_u32(sPOwn), 16, 1024);
       const uint64_t precv_desc = sdesc_sw128(smem_u32(sPRecv), 16, 1024);
       const uint16_t peer_mask = static_cast<uint16_t>(1u << peer);
-      // Two cursors over the partition's tiles:
-      //   cq: Q K^T of own tiles, in two halves (K slot part, then V ring part
-      //       -> S); it steps over the peer's tiles at once and releases Q at
-      //       every unit end (after the unit's Q has arrived, so that the Q
-      //       barriers' phases stay aligned even for a unit without own tiles);
-      //   cv: P V of every tile, in order, from the own or the received P.
-      // Each pass issues at most one job, P V first.
-      Cursor cq, cv;
-      cursor_init(p, P, cq);
+      Cursor cv;
       cursor_init(p, P, cv);
-      uint32_t a_own = 0, pv_own = 0, pv_recv = 0;
+      uint32_t pv_own = 0, pv_recv = 0;
+      bool ok = true;
+      uint64_t t_last = globaltimer_ns();
+      while (cv.valid) {
+        bool progressed = false;
+        {
+          const bool mine = (cv.t & 1u) == rank;
+          const bool first = cursor_first(cv);
+          const int vs = static_cast<int>(cv.t % kVSlots);
+          bool ready = mine ? mbar_test_wait(&bars[OWN_GO], pv_own & 1)
+                            : (mbar_test_wait(&bars[RECV_GO], pv_recv & 1) &&
+                               mbar_test_wait(&bars[RECV_FULL], pv_recv & 1));
+          ready = ready && mbar_test_wait(&bars[V_FULL + vs], (cv.t / kVSlots) & 1);
+          if (ready && first && cv.u >= 1) ready = mbar_test_wait(&bars[O_FREE], (cv.u - 1) & 1);
+          if (ready) {
+            MLA_TRACE(3, cv.t);
+            // armed for the next received P (it cannot be sent before this P V is done)
+            if (!mine) mbar_arrive_expect_tx(&bars[RECV_FULL], kPBytes);
+            tc_fence_after();
+            const uint64_t a0 = mine ? pown_desc : precv_desc;
+            const uint64_t b0 = vv_desc0 + static_cast<uint64_t>((vs * kVSlotBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              umma_f16(tmem + kTmemO, a0 + static_cast<uint64_t>((kk * 32) >> 4),
+                       b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
+            umma_commit(&bars[V_EMPTY + vs]);
+            umma_commit(&bars[PV_DONE + (cv.t & 1)]);
+            if (mine) {
+              umma_commit(&bars[OWN_FREE]);
+              ++pv_own;
+            } else {
+              // the peer may refill our receive buffer (and reuse its own copy of that P)
+              umma_commit_multicast(&bars[OWN_FREE], peer_mask);
+              ++pv_recv;
+            }
+            if (cursor_last(cv)) umma_commit(&bars[O_FULL]);
+            MLA_TRACE(16, cv.t);
+            cursor_next(p, P, cv);
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_last = globaltimer_ns();
+        } else if (*abort_flag || globaltimer_ns() - t_last > MLA_WAIT_LIMIT_NS) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) {
+        set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+        // a P the peer already sent may still be landing in our receive buffer
+        mbar_wait<true>(&bars[RECV_FULL], pv_recv & 1, nullptr);
+      }
+      umma_commit(&bars[DRAIN]);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint64_t q_desc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t k_desc0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t vk_desc0 = sdesc_sw128(smem_u32(sV), 16, 1024);        // V boxes as K-major B of Q K^T
+      // cq: Q K^T of own tiles, in two halves (K slot part, then V ring part
+      // -> S); it steps over the peer's tiles at once and releases Q at every
+      // unit end (after the unit's Q has arrived, so that the Q barriers'
+      // phases stay aligned even for a unit without own tiles).  Each pass
+      // issues at most one job: a landed Q box's copies into TMEM, else the
+      // next Q K^T half.
+      Cursor cq;
+      cursor_init(p, P, cq);
+      uint32_t a_own = 0;
       int q_phase = 0;          // 0: next is QKa of cq, 1: next is QKb of cq
       uint32_t qb_seen = 0;     // Q boxes seen landed (nine per unit, in order)
       bool ok = true;
@@ -593,45 +658,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return true;
       };
       advance_q();
-      while (cv.valid) {
-        bool progressed = false;
-        {
-          const bool mine = (cv.t & 1u) == rank;
-          const bool first = cursor_first(cv);
-          const int vs = static_cast<int>(cv.t % kVSlots);
-          bool ready = mine ? mbar_test_wait(&bars[OWN_GO], pv_own & 1)
-                            : (mbar_test_wait(&bars[RECV_GO], pv_recv & 1) &&
-                               mbar_test_wait(&bars[RECV_FULL], pv_recv & 1));
-          ready = ready && mbar_test_wait(&bars[V_FULL + vs], (cv.t / kVSlots) & 1);
-          if (ready && first && cv.u >= 1) ready = mbar_test_wait(&bars[O_FREE], (cv.u - 1) & 1);
-          if (ready) {
-            MLA_TRACE(3, cv.t);
-            // armed for the next received P (it cannot be sent before this P V is done)
-            if (!mine) mbar_arrive_expect_tx(&bars[RECV_FULL], kPBytes);
-            tc_fence_after();
-            const uint64_t a0 = mine ? pown_desc : precv_desc;
-            const uint64_t b0 = vv_desc0 + static_cast<uint64_t>((vs * kVSlotBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < kT / 16; ++kk)
-              umma_f16(tmem + kTmemO, a0 + static_cast<uint64_t>((kk * 32) >> 4),
-                       b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
-            umma_commit(&bars[V_EMPTY + vs]);
-            umma_commit(&bars[PV_DONE + (cv.t & 1)]);
-            if (mine) {
-              umma_commit(&bars[OWN_FREE]);
-              ++pv_own;
-            } else {
-              // the peer may refill our receive buffer (and reuse its own copy of that P)
-              umma_commit_multicast(&bars[OWN_FREE], peer_mask);
-              ++pv_recv;
-            }
-            if (cursor_last(cv)) umma_commit(&bars[O_FULL]);
-            MLA_TRACE(16, cv.t);
-            cursor_next(p, P, cv);
-            progressed = true;
-          }
-        }
-        if (!progressed) progressed = q_copy();
+      while (ok && cq.valid) {
+        bool progressed = q_copy();
         if (!progressed && cq.valid && advance_q() && cq.valid) {
           if (q_phase == 0) {
             const int ks = static_cast<int>(a_own % kKSlots);
@@ -680,18 +708,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // the last units' Q (units after the last own tile) are released too
-      while (ok && cq.valid) {
-        if (q_copy()) t_last = globaltimer_ns();
-        if (advance_q()) break;
-        if (*abort_flag || globaltimer_ns() - t_last > MLA_WAIT_LIMIT_NS) ok = false;
-      }
-      if (!ok) {
-        set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
-        // a P the peer already sent may still be landing in our receive buffer
-        mbar_wait<true>(&bars[RECV_FULL], pv_recv & 1, nullptr);
-      }
-      // every MMA has completed before TMEM is released
+      if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+      // every MMA (of both issuers) has completed before TMEM is released
       umma_commit(&bars[DRAIN]);
       mbar_wait(&bars[DRAIN], 0, nullptr);
     }
