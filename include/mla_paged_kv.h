@@ -57,7 +57,8 @@ typedef enum {
 typedef enum {
   MLA_DTYPE_BF16 = 0,
   MLA_DTYPE_FP32 = 1, /* outputs only */
-  MLA_DTYPE_FP16 = 2
+  MLA_DTYPE_FP16 = 2,
+  MLA_DTYPE_FP8_RECORD = 3 /* KV only: the pool of 656-byte FP8 records, bf16 Q */
 } mla_dtype_t;
 
 /* Fixed geometry (FlashMLA PR #183 Design; PR #200 "SM90 packing kernel"). */
@@ -137,7 +138,20 @@ int mla_get_metadata_request_local(const int32_t* d_lengths, int default_length,
  *   h_kv           latent KV heads, dividing h_q; query head h reads KV head
  *                  h / (h_q / h_kv).  h_q / h_kv <= 128 when h_kv > 1.
  *   dtype          MLA_DTYPE_BF16 or MLA_DTYPE_FP16 (q and kv alike; P is
- *                  rounded to the same type before the P V product).
+ *                  rounded to the same type before the P V product), or
+ *                  MLA_DTYPE_FP8_RECORD: d_kv is a paged cache of FP8 records
+ *                  [num_pages, 64, 656] (FlashMLA PR #200, "FP8 KV cache
+ *                  format": 512 E4M3 NoPE codes, four fp32 scales, one per
+ *                  128 dims, 64 bf16 RoPE dims), q is bf16, h_kv must be 1.
+ *                  Token j of request b is record j%64 of page
+ *                  block_table[b][j/64].  The kernel turns each NoPE value
+ *                  into fp16(code * scale) (relative error <= 2^-11 + 2^-20
+ *                  inside fp16's normal range) and q and the RoPE dims into
+ *                  fp16 (exact inside that range), then runs the fp16 path:
+ *                  a score moves by at most scale * (2^-11 + 2^-20) *
+ *                  sum_d |q_d k_d|.  Values must lie inside fp16's range.
+ *                  mla_dense_fp8_decode_fwd keeps the scores exact in the
+ *                  codes and scales instead (slower).
  *   causal         1: query token i sees keys j <= L_b - s_q + i.
  *   softmax_scale  multiplies q.k (e.g. 1/sqrt(576)); must be finite and > 0.
  *   d_sched, d_split_offset, num_parts: from mla_get_metadata (or its

@@ -166,18 +166,25 @@ def mla_get_metadata_request_local(lengths, n_units, num_parts, sched, split_off
               stream)
 
 
-DTYPE_BF16, DTYPE_FP32, DTYPE_FP16 = 0, 1, 2          # mla_dtype_t
+DTYPE_BF16, DTYPE_FP32, DTYPE_FP16, DTYPE_FP8_RECORD = 0, 1, 2, 3   # mla_dtype_t
 _DTYPE_CODE = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_FP32, torch.float16: DTYPE_FP16}
 
 
 def _dense_inputs(q, kv, block_table, cache_seqlens, out, lse, status):
-    """Checks shared by the dense entry points; returns (h_kv, dtype code, out type code)."""
+    """Checks shared by the dense entry points; returns (h_kv, dtype code, out type code).
+    kv is the 16-bit latent cache of q's dtype, or (uint8 [pages, 64, 656])
+    a cache of FP8 records with a bf16 q."""
     if q.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError("q must be bf16 or fp16")
     _need(q, q.dtype, "q", 4)
-    if kv.dtype != q.dtype or kv.dim() not in (3, 4):
+    if kv.dtype == torch.uint8:
+        if q.dtype != torch.bfloat16 or kv.dim() != 3 or kv.shape[1] != 64 or kv.shape[2] != 656:
+            raise TypeError("an FP8 record cache is uint8 [pages, 64, 656] and goes with a bf16 q")
+        _need(kv, torch.uint8, "kv")
+    elif kv.dtype != q.dtype or kv.dim() not in (3, 4):
         raise TypeError("kv must have q's dtype and be [pages, 64, 576] or [pages, 64, h_kv, 576]")
-    _need(kv, q.dtype, "kv")
+    else:
+        _need(kv, q.dtype, "kv")
     _need(block_table, torch.int32, "block_table", 2)
     _need(cache_seqlens, torch.int32, "cache_seqlens", 1)
     _need(lse, torch.float32, "lse")
@@ -185,14 +192,15 @@ def _dense_inputs(q, kv, block_table, cache_seqlens, out, lse, status):
     if out.dtype not in _DTYPE_CODE:
         raise TypeError("out must be bf16, fp16 or fp32")
     B, s_q, h_q, d = q.shape
+    fp8 = kv.dtype == torch.uint8
     h_kv = 1 if kv.dim() == 3 else kv.shape[2]
-    if d != 576 or kv.shape[1] != 64 or kv.shape[-1] != 576 or h_q % h_kv:
+    if d != 576 or kv.shape[1] != 64 or (kv.shape[-1] != 576 and not fp8) or h_q % h_kv:
         raise ValueError("q must be [B, s_q, h_q, 576], kv [pages, 64, (h_kv,) 576] with h_kv dividing h_q")
     if tuple(out.shape) != (B, s_q, h_q, 512) or tuple(lse.shape) != (B, s_q, h_q):
         raise ValueError("out must be [B, s_q, h_q, 512] and lse [B, s_q, h_q]")
     if block_table.shape[0] != B or cache_seqlens.shape[0] != B:
         raise ValueError("block_table / cache_seqlens batch mismatch")
-    return h_kv, _DTYPE_CODE[q.dtype], _DTYPE_CODE[out.dtype]
+    return h_kv, (DTYPE_FP8_RECORD if fp8 else _DTYPE_CODE[q.dtype]), _DTYPE_CODE[out.dtype]
 
 
 def _dense_args(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse, status,

@@ -15,10 +15,11 @@
 namespace mla {
 cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, int, cudaStream_t);
 cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, void*, int, float*, cudaStream_t);
-cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int, int, cudaStream_t);
+cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                         const DecodeParams&, int, int, cudaStream_t);
 int dense_smem_bytes();
-int dense_threads();
-const void* dense_kernel_ptr(int half);
+int dense_threads(int kind);
+const void* dense_kernel_ptr(int kind);
 cudaError_t launch_sparse(const CUtensorMap&, const DecodeParams&, int, cudaStream_t);
 int sparse_smem_bytes();
 int sparse_threads();
@@ -99,6 +100,8 @@ const DeviceInfo& device_info() {
           cudaSuccess ||
       cudaFuncSetAttribute(dense_kernel_ptr(1), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
           cudaSuccess ||
+      cudaFuncSetAttribute(dense_kernel_ptr(2), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
+          cudaSuccess ||
       cudaFuncSetAttribute(sparse_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            sparse_smem_bytes()) != cudaSuccess) {
     cudaGetLastError();
@@ -106,7 +109,8 @@ const DeviceInfo& device_info() {
     d.ready = true;
     return d;
   }
-  d.dense_clusters = max_clusters(dense_kernel_ptr(0), dense_threads(), dense_smem_bytes());
+  d.dense_clusters = std::min(max_clusters(dense_kernel_ptr(0), dense_threads(0), dense_smem_bytes()),
+                              max_clusters(dense_kernel_ptr(2), dense_threads(2), dense_smem_bytes()));
   d.sparse_clusters = max_clusters(sparse_kernel_ptr(), sparse_threads(), sparse_smem_bytes());
   if (d.dense_clusters <= 0 || d.sparse_clusters <= 0) {
     cudaGetLastError();
@@ -163,6 +167,25 @@ int encode_kv_map(CUtensorMap* m, const void* kv, int num_pages, int h_kv) {
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
+// Pool of FP8 records [num_pages][64][656] as a 2-D byte tensor (656, rows =
+// num_pages * 64); one box covers the 64 records of a page.  kind 0: the
+// E4M3 codes of one 64-dim box (64 B per record, unswizzled, 4 KB); 1: the
+// four fp32 scales (16 B per record, 1 KB); 2: the 64 bf16 RoPE dims (128 B
+// per record, 128-byte swizzle: lands as the bf16 box an MMA reads).
+int encode_fp8_record_map(CUtensorMap* m, const void* kv8, int num_pages, int kind) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return MLA_ERR_CUDA;
+  cuuint64_t dims[2] = {656, static_cast<cuuint64_t>(num_pages) * MLA_PAGE_SIZE};
+  cuuint64_t strides[1] = {656};
+  const cuuint32_t inner = kind == 0 ? 64 : (kind == 1 ? 16 : 128);
+  cuuint32_t box[2] = {inner, MLA_PAGE_SIZE};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv8), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, kind == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
+}
+
 // Dense Q with h_kv > 1 as [tokens = batch*s_q][h_kv][group_heads][576], dims
 // innermost first: (576, group_heads, h_kv, tokens).  One box = 64 dims x
 // group_heads heads x block_tokens tokens of one head group.
@@ -186,13 +209,14 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
                   const int32_t* seqlens, int batch, int s_q, int h_q, int h_kv, int dtype, int causal, float scale,
                   const int32_t* sched, const int32_t* split_offset, int num_parts, void* workspace,
                   size_t workspace_bytes, void* out, int out_type, float* lse, int32_t* status, DecodeParams* p,
-                  CUtensorMap* q_map, CUtensorMap* kv_map) {
+                  CUtensorMap* q_map, CUtensorMap* kv_map, CUtensorMap* sc_map, CUtensorMap* rope_map) {
   if (!q || !kv || !block_table || !seqlens || !sched || !split_offset || !workspace || !out || !lse || !status)
     return MLA_ERR_INVALID_ARG;
   if (batch < 1 || s_q < 1 || h_q < 1 || h_kv < 1 || max_pages < 1 || num_pages < 1 || num_parts < 1)
     return MLA_ERR_INVALID_ARG;
   if (h_q % h_kv != 0) return MLA_ERR_INVALID_ARG;
-  if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_FP16) return MLA_ERR_INVALID_ARG;
+  if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_FP16 && dtype != MLA_DTYPE_FP8_RECORD) return MLA_ERR_INVALID_ARG;
+  if (dtype == MLA_DTYPE_FP8_RECORD && h_kv != 1) return MLA_ERR_UNSUPPORTED;
   if (out_type != MLA_DTYPE_BF16 && out_type != MLA_DTYPE_FP32 && out_type != MLA_DTYPE_FP16)
     return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return MLA_ERR_INVALID_ARG;
@@ -219,7 +243,16 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
                      : encode_q_map_groups(q_map, q, static_cast<long long>(batch) * s_q, h_kv, group_heads,
                                            block_tokens);
   if (rc != MLA_OK) return rc;
-  rc = encode_kv_map(kv_map, kv, num_pages, h_kv);
+  if (dtype == MLA_DTYPE_FP8_RECORD) {
+    if (static_cast<long long>(num_pages) * MLA_PAGE_SIZE > (1LL << 31) - 1) return MLA_ERR_UNSUPPORTED;
+    rc = encode_fp8_record_map(kv_map, kv, num_pages, 0);
+    if (rc == MLA_OK) rc = encode_fp8_record_map(sc_map, kv, num_pages, 1);
+    if (rc == MLA_OK) rc = encode_fp8_record_map(rope_map, kv, num_pages, 2);
+  } else {
+    rc = encode_kv_map(kv_map, kv, num_pages, h_kv);
+    *sc_map = *kv_map;  // unused
+    *rope_map = *kv_map;
+  }
   if (rc != MLA_OK) return rc;
   *p = DecodeParams{};
   p->lengths = seqlens;
@@ -328,12 +361,13 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
                       const int32_t* d_split_offset, int num_parts, void* d_workspace, size_t workspace_bytes,
                       void* d_out, int out_type, float* d_lse, int32_t* d_status, mla_stream_t stream) {
   DecodeParams p;
-  CUtensorMap qm, km;
+  CUtensorMap qm, km, sm, rm;
   const int rc = dense_prepare(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q,
                                h_kv, dtype, causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
-                               workspace_bytes, d_out, out_type, d_lse, d_status, &p, &qm, &km);
+                               workspace_bytes, d_out, out_type, d_lse, d_status, &p, &qm, &km, &sm, &rm);
   if (rc != MLA_OK) return rc;
-  return launch_dense(qm, km, p, num_parts, dtype == MLA_DTYPE_FP16 ? 1 : 0,
+  return launch_dense(qm, km, sm, rm, p, num_parts,
+                      dtype == MLA_DTYPE_FP16 ? 1 : (dtype == MLA_DTYPE_FP8_RECORD ? 2 : 0),
                       reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;

@@ -51,6 +51,7 @@
 //        finish issuing; they touch different TMEM accumulators.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -114,7 +115,10 @@ enum : int {
   O_FULL = PV_DONE + 2,
   O_FREE,
   DRAIN,
-  kNumBars
+  RAW_K,                      // +slot, FP8 records: the K slot's raw bytes have landed
+  RAW_V = RAW_K + kKSlots,    // +slot, FP8 records: a V slot's raw bytes have landed
+  QB_READY = RAW_V + kVSlots, // +slot, FP8 records: a landed Q box has been turned into fp16
+  kNumBars = QB_READY + kQSmemBoxes
 };
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -127,8 +131,18 @@ static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffPOwn % 1024 == 0 && 
 static_assert(kOffRefOut % 16 == 0 && kOffRefIn % 16 == 0 && kOffLOut % 16 == 0 && kOffLIn % 16 == 0,
               "bulk copies need 16-byte alignment");
 
-constexpr int kThreads = 288;
+constexpr int kThreads = 288;      // bf16 / fp16 KV
+constexpr int kThreadsFp8 = 384;   // FP8 record KV: three more warps convert the records
 constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6, kWarpQ = 7, kWarpPV = 8;
+constexpr int kWarpConv = 9, kConvWarps = 3;  // FP8 record converters: warps 9-11
+// FP8 records (FlashMLA PR #200, section "FP8 KV cache format"): 656 bytes =
+// 512 E4M3 NoPE codes, four fp32 scales (one per 128 dims), 64 bf16 RoPE.
+constexpr int kRecBytes = 656;
+static_assert(512 + 16 + 128 == kRecBytes, "record layout");
+constexpr int kFp8CodeBytes = kT * 64;      // one 64-dim box of codes: 4 KB, lands at the box's start
+constexpr int kFp8ScaleBytes = kT * 16;     // the tile's scales: 1 KB, lands at box + 4096
+constexpr int kFp8KSlotTx = 4 * (kFp8CodeBytes + kFp8ScaleBytes) + kBoxBytes;  // 4 NoPE boxes + RoPE
+constexpr int kFp8VSlotTx = 4 * (kFp8CodeBytes + kFp8ScaleBytes);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
 constexpr uint32_t kTmemS = 256;  // S: [256, 320)
@@ -269,6 +283,75 @@ __device__ __forceinline__ void issue_qk_v(uint32_t d, uint32_t tmem, uint64_t q
   qk_box<kHalf, 4 * kRank + 3>(d, tmem, q_desc0, vslot + ((3 * kBoxBytes) >> 4), false);
 }
 
+// One 64-dim NoPE box of a page of FP8 records, in place: the box's 64 x 64
+// E4M3 codes (4 KB, record-major) and the tile's 64 x 4 fp32 scales (1 KB at
+// +4096) become the 64 x 64 fp16 box (8 KB, 128-byte swizzle) that an MMA
+// reads, value = code * scale rounded to fp16.  Per value pair: one
+// conversion (two E4M3 codes -> two exact fp16) and three fp16x2 ops.  The
+// record's scale s is split as s = 2^e * (s_hi + s_lo), s_hi = fp16(s / 2^e)
+// with s / 2^e in [1, 2) and s_lo = fp16(s / 2^e - s_hi); then
+// v = fma(c, s_hi, c * s_lo) is c * s / 2^e rounded once up to a relative
+// 2^-21, and v * 2^e is exact (a power of two) unless it falls below fp16's
+// normal range.  So each value carries a relative error <= 2^-11 + 2^-20
+// inside fp16's normal range.  One warp: every read is in registers before
+// the first write.  `sg` = the box's scale group.
+__device__ __forceinline__ void convert_fp8_box(uint8_t* box, int sg, int lane) {
+  uint4 code[8];
+  __half2 s_hi[8], s_lo[8], s_pow[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    // 16-byte piece `lane` of the k-th 512 bytes: record 8k + lane/4, codes 16 * (lane % 4) ...
+    code[k] = reinterpret_cast<const uint4*>(box)[k * 32 + lane];
+    const uint32_t sb =
+        __float_as_uint(reinterpret_cast<const float*>(box + kFp8CodeBytes + (8 * k + (lane >> 2)) * 16)[sg]);
+    const float sm = __uint_as_float((sb & 0x807FFFFFu) | (127u << 23));  // s / 2^e in [1, 2) (sign kept)
+    const __half hi = __float2half_rn(sm);
+    s_hi[k] = __half2half2(hi);
+    s_lo[k] = __half2half2(__float2half_rn(sm - __half2float(hi)));
+    s_pow[k] = __half2half2(__float2half_rn(__uint_as_float(sb & 0x7F800000u)));  // 2^e
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int row = 8 * k + (lane >> 2);
+    const uint32_t c = static_cast<uint32_t>(lane & 3);
+    const uint32_t in[4] = {code[k].x, code[k].y, code[k].z, code[k].w};
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __half2_raw hr =
+          __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((in[i >> 1] >> (16 * (i & 1))) & 0xFFFFu),
+                                     __NV_E4M3);
+      const __half2 cv = *reinterpret_cast<const __half2*>(&hr);
+      const __half2 v = __hmul2(__hfma2(cv, s_hi[k], __hmul2(cv, s_lo[k])), s_pow[k]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    uint8_t* rowp = box + row * 128;
+    const uint32_t sw = static_cast<uint32_t>(row & 7);
+    *reinterpret_cast<uint4*>(rowp + (((2u * c) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(rowp + (((2u * c + 1u) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// A box of `words` 32-bit words of bf16 pairs -> fp16 pairs, in place, by
+// one warp (elementwise, so any swizzle is kept).  bf16 -> f32 is exact and
+// f32 -> fp16 rounds to nearest even: exact for values inside fp16's normal
+// range (bf16 carries 8 significant bits, fp16 11).
+__device__ __forceinline__ void bf16_box_to_fp16(uint8_t* box, int words, int lane) {
+  uint4* v = reinterpret_cast<uint4*>(box);
+#pragma unroll 4
+  for (int i = lane; i < words / 4; i += 32) {
+    uint4 x = v[i];
+    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+      w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    v[i] = x;
+  }
+}
+
 // Two fp32 -> one packed pair of 16-bit floats (round to nearest even).
 template <bool kHalf>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -317,10 +400,19 @@ __device__ __forceinline__ float ref_alpha(float r_old, float r_new) {
   return r_new == r_old ? 1.f : ex2(r_old - r_new);
 }
 
-template <bool kHalf>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// kHalf: the MMAs take fp16 operands (else bf16).  kFp8 (with kHalf): KV is
+// a pool of FP8 records (kv_map = their codes in 64-byte boxes, sc_map =
+// scales, rope_map = RoPE as a swizzled bf16 box) and Q is bf16; both are
+// turned into fp16 in shared memory (records: fp16(code * scale); Q and
+// RoPE: bf16 -> fp16).  Otherwise kv_map is the 16-bit pool and sc_map /
+// rope_map are unused.
+template <bool kHalf, bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     dense_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
+                        const __grid_constant__ CUtensorMap sc_map, const __grid_constant__ CUtensorMap rope_map,
                         const DecodeParams p) {
+  static_assert(!kFp8 || kHalf, "FP8 records are converted to fp16");
+  constexpr int kNThreads = kFp8 ? kThreadsFp8 : kThreads;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -356,15 +448,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kQSmemBoxes; ++i) {
       mbar_init(&bars[QB_FULL + i], 1);
       mbar_init(&bars[QB_EMPTY + i], 1);
+      mbar_init(&bars[QB_READY + i], 1);
     }
     for (int i = 0; i < kKSlots; ++i) {
-      mbar_init(&bars[K_FULL + i], 1);
+      mbar_init(&bars[K_FULL + i], kFp8 ? kConvWarps : 1);
       mbar_init(&bars[K_EMPTY + i], 1);
     }
+    // FP8 records: a slot is full when the converter warps are done with it
+    // rather than when its TMA bytes land
     for (int i = 0; i < kVSlots; ++i) {
-      mbar_init(&bars[V_FULL + i], 1);
+      mbar_init(&bars[V_FULL + i], kFp8 ? kConvWarps : 1);
       mbar_init(&bars[V_EMPTY + i], 1);
     }
+    for (int i = 0; i < kKSlots; ++i) mbar_init(&bars[RAW_K + i], 1);
+    for (int i = 0; i < kVSlots; ++i) mbar_init(&bars[RAW_V + i], 1);
     mbar_init(&bars[S_FULL], 1);
     mbar_init(&bars[S_FREE], 128);
     mbar_init(&bars[OWN_GO], 128);
@@ -388,7 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (q_box_bytes < static_cast<uint32_t>(kQBoxBytes)) {
     // Q boxes of a head group cover fewer than 128 rows: the rows past them stay zero
-    for (int i = tid; i < kQSmemBoxes * kQBoxBytes / 16; i += kThreads)
+    for (int i = tid; i < kQSmemBoxes * kQBoxBytes / 16; i += kNThreads)
       reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
@@ -397,7 +494,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kWarpQ && lane == 0) prefetch_tmap(&q_map);
-  if (warp == kWarpK && lane == 0) prefetch_tmap(&kv_map);
+  if (warp == kWarpK && lane == 0) {
+    prefetch_tmap(&kv_map);
+    if constexpr (kFp8) {
+      prefetch_tmap(&sc_map);
+      prefetch_tmap(&rope_map);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -437,12 +540,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (n >= 1) ok = mbar_wait(&bars[K_EMPTY + s], (n - 1) & 1, abort_flag);
             if (ok) {
               MLA_TRACE(9, c.t);
-              mbar_arrive_expect_tx(&bars[K_FULL + s], kKSlotBytes);
               uint8_t* dst = sK + s * kKSlotBytes;
+              if constexpr (kFp8) {
+                // raw bytes; the K converter makes the bf16 boxes and fills K_FULL
+                uint64_t* bar = &bars[RAW_K + s];
+                mbar_arrive_expect_tx(bar, kFp8KSlotTx);
 #pragma unroll
-              for (int j = 0; j < kKBoxes; ++j) {
-                const int g = rank == 0 ? k_box<0>(j) : k_box<1>(j);
-                tma_load_4d(dst + j * kBoxBytes, &kv_map, &bars[K_FULL + s], 64 * g, grp, 0, page, pol_kv);
+                for (int j = 0; j < kKBoxes; ++j) {
+                  const int g = rank == 0 ? k_box<0>(j) : k_box<1>(j);
+                  if (g < 8) {
+                    tma_load_2d(dst + j * kBoxBytes, &kv_map, bar, 64 * g, page * kT, pol_kv);
+                    tma_load_2d(dst + j * kBoxBytes + kFp8CodeBytes, &sc_map, bar, 512, page * kT, pol_kv);
+                  } else {
+                    tma_load_2d(dst + j * kBoxBytes, &rope_map, bar, 528, page * kT, pol_kv);
+                  }
+                }
+              } else {
+                mbar_arrive_expect_tx(&bars[K_FULL + s], kKSlotBytes);
+#pragma unroll
+                for (int j = 0; j < kKBoxes; ++j) {
+                  const int g = rank == 0 ? k_box<0>(j) : k_box<1>(j);
+                  tma_load_4d(dst + j * kBoxBytes, &kv_map, &bars[K_FULL + s], 64 * g, grp, 0, page, pol_kv);
+                }
               }
               ++k_issued[s];
             }
@@ -452,12 +571,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (n >= 1) ok = mbar_wait(&bars[V_EMPTY + s], (n - 1) & 1, abort_flag);
             if (ok) {
               MLA_TRACE(7, c.t);
-              mbar_arrive_expect_tx(&bars[V_FULL + s], kVSlotBytes);
               uint8_t* dst = sV + s * kVSlotBytes;
+              if constexpr (kFp8) {
+                uint64_t* bar = &bars[RAW_V + s];
+                mbar_arrive_expect_tx(bar, kFp8VSlotTx);
 #pragma unroll
-              for (int j = 0; j < kVBoxes; ++j)
-                tma_load_4d(dst + j * kBoxBytes, &kv_map, &bars[V_FULL + s], 64 * (4 * static_cast<int>(rank) + j),
-                            grp, 0, page, pol_kv);
+                for (int j = 0; j < kVBoxes; ++j) {
+                  tma_load_2d(dst + j * kBoxBytes, &kv_map, bar, 64 * (4 * static_cast<int>(rank) + j), page * kT,
+                              pol_kv);
+                  tma_load_2d(dst + j * kBoxBytes + kFp8CodeBytes, &sc_map, bar, 512, page * kT, pol_kv);
+                }
+              } else {
+                mbar_arrive_expect_tx(&bars[V_FULL + s], kVSlotBytes);
+#pragma unroll
+                for (int j = 0; j < kVBoxes; ++j)
+                  tma_load_4d(dst + j * kBoxBytes, &kv_map, &bars[V_FULL + s],
+                              64 * (4 * static_cast<int>(rank) + j), grp, 0, page, pol_kv);
+              }
               ++v_issued[s];
             }
           }
@@ -471,18 +601,122 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // no TMA write may land after this CTA exits
       for (int s = 0; s < kKSlots; ++s)
-        if (k_issued[s] > 0) mbar_wait(&bars[K_FULL + s], (k_issued[s] - 1) & 1, nullptr);
+        if (k_issued[s] > 0) mbar_wait(&bars[(kFp8 ? RAW_K : K_FULL) + s], (k_issued[s] - 1) & 1, nullptr);
       for (int s = 0; s < kVSlots; ++s)
-        if (v_issued[s] > 0) mbar_wait(&bars[V_FULL + s], (v_issued[s] - 1) & 1, nullptr);
+        if (v_issued[s] > 0) mbar_wait(&bars[(kFp8 ? RAW_V : V_FULL) + s], (v_issued[s] - 1) & 1, nullptr);
     }
     __syncwarp();
+  } else if (warp >= kWarpConv) {
+    // ------------------------------------------------------------ FP8 record converters
+    // (FP8 instance only.)  The boxes of a tile are shared round-robin by the
+    // three converter warps, rotating with the tile: an own tile's K slot
+    // (jobs 0-4: four NoPE boxes and the RoPE box) first, then its V slot
+    // (jobs 5-8).  Each warp waits for the slot's raw bytes, converts its
+    // boxes in place, makes its writes visible to the tensor cores and
+    // arrives on the slot's FULL (every warp once per slot use).
+    if constexpr (kFp8) {
+      const uint32_t cw = static_cast<uint32_t>(warp - kWarpConv);
+      Cursor c;
+      cursor_init(p, P, c);
+      bool ok = true;
+      uint32_t own_k = 0;
+      while (ok && c.valid) {
+        const bool mine = (c.t & 1u) == rank;
+        const uint32_t rot = c.t % kConvWarps;
+        if (mine) {
+          const int s = static_cast<int>(own_k % kKSlots);
+          ok = warp_wait(&bars[RAW_K + s], (own_k / kKSlots) & 1, abort_flag);
+          if (!ok) break;
+          uint8_t* slot = sK + s * kKSlotBytes;
+#pragma unroll 1
+          for (int j = 0; j < kKBoxes; ++j) {
+            if ((static_cast<uint32_t>(j) + rot) % kConvWarps != cw) continue;
+            const int g = rank == 0 ? k_box<0>(j) : k_box<1>(j);
+            if (g < 8)
+              convert_fp8_box(slot + j * kBoxBytes, g >> 1, lane);
+            else
+              bf16_box_to_fp16(slot + j * kBoxBytes, kBoxBytes / 4, lane);  // RoPE
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[K_FULL + s]);
+          ++own_k;
+        }
+        {
+          const int s = static_cast<int>(c.t % kVSlots);
+          ok = warp_wait(&bars[RAW_V + s], (c.t / kVSlots) & 1, abort_flag);
+          if (!ok) break;
+          uint8_t* slot = sV + s * kVSlotBytes;
+#pragma unroll 1
+          for (int j = 0; j < kVBoxes; ++j) {
+            if ((static_cast<uint32_t>(j + kKBoxes) + rot) % kConvWarps != cw) continue;
+            convert_fp8_box(slot + j * kBoxBytes, (4 * static_cast<int>(rank) + j) >> 1, lane);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[V_FULL + s]);
+        }
+        cursor_next(p, P, c);
+      }
+      if (!ok && lane == 0) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+    }
   } else if (warp == kWarpQ) {
     // ------------------------------------------------------------ Q producer
     // Per unit, the nine 64-dim boxes of Q in order through the three slots
     // of the shared-memory Q buffer: box j goes to slot j % 3.  Boxes 0-5
     // (dims [0, 384)) are copied into TMEM by the MMA thread, which frees
     // the slot for box j + 3; boxes 6-8 stay until the unit's last Q K^T.
-    if (lane == 0) {
+    if constexpr (kFp8) {
+      // FP8 records (h_kv = 1): the same nine boxes, but the whole warp turns
+      // each landed box into fp16 in place and then signals QB_READY; a slot
+      // is refilled with box j + 3 once the MMA thread has copied box j.
+      const uint64_t pol_q = policy_evict_last();
+      Cursor c;
+      cursor_init(p, P, c);
+      bool ok = true;
+      uint32_t qb_issued[kQSmemBoxes] = {};
+      const auto q_load = [&](int b, int j) {  // lane 0
+        const int sl = j % kQSmemBoxes;
+        mbar_arrive_expect_tx(&bars[QB_FULL + sl], q_box_bytes);
+        tma_load_2d(sQ + sl * kQBoxBytes, &q_map, &bars[QB_FULL + sl], 64 * j, b * p.rows + rb * kRowsPerBlock,
+                    pol_q);
+        ++qb_issued[sl];
+      };
+      while (ok && c.valid) {
+        if (lane == 0) {
+          if (c.u >= 1) ok = mbar_wait(&bars[Q_EMPTY], (c.u - 1) & 1, abort_flag);
+          if (ok)
+            for (int j = 0; j < kQSmemBoxes; ++j) q_load(c.b, j);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        for (int j = 0; ok && j < 9; ++j) {
+          const int sl = j % kQSmemBoxes;
+          ok = warp_wait(&bars[QB_FULL + sl], (3 * c.u + j / 3) & 1, abort_flag);
+          if (!ok) break;
+          bf16_box_to_fp16(sQ + sl * kQBoxBytes, static_cast<int>(q_box_bytes / 4), lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars[QB_READY + sl]);
+            if (j + kQSmemBoxes < 9) {
+              ok = mbar_wait(&bars[QB_EMPTY + sl], (2 * c.u + j / 3) & 1, abort_flag);
+              if (ok) q_load(c.b, j + kQSmemBoxes);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+        c.t += static_cast<uint32_t>(c.hi - c.k);
+        ++c.u;
+        cursor_seek(p, P, c, c.b + 1);
+        if (ok && c.valid && lane == 0)
+          for (int j = 0; j < 9; ++j) tma_prefetch_2d(&q_map, 64 * j, c.b * p.rows + rb * kRowsPerBlock);
+      }
+      if (lane == 0) {
+        if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+        for (int sl = 0; sl < kQSmemBoxes; ++sl)
+          if (qb_issued[sl] > 0) mbar_wait(&bars[QB_FULL + sl], (qb_issued[sl] - 1) & 1, nullptr);
+      }
+    } else if (lane == 0) {
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
       cursor_init(p, P, c);
@@ -645,7 +879,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // boxes 6-8 are only counted (they stay for the MMAs)
       auto q_copy = [&]() -> bool {
         const uint32_t uq = qb_seen / 9u, j = qb_seen % 9u, sl = j % kQSmemBoxes;
-        if (!mbar_test_wait(&bars[QB_FULL + sl], (3u * uq + j / 3u) & 1u)) return false;
+        if (!mbar_test_wait(&bars[(kFp8 ? QB_READY : QB_FULL) + sl], (3u * uq + j / 3u) & 1u)) return false;
         if (j < 6u) {
           tc_fence_after();
 #pragma unroll
@@ -982,19 +1216,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace dn
 
 int dense_smem_bytes() { return dn::kSmemBytes; }
-int dense_threads() { return dn::kThreads; }
-const void* dense_kernel_ptr(int half) {
-  return half ? reinterpret_cast<const void*>(&dn::dense_decode_kernel<true>)
-              : reinterpret_cast<const void*>(&dn::dense_decode_kernel<false>);
+// kind 0: bf16, 1: fp16, 2: FP8 records (bf16 Q)
+int dense_threads(int kind) { return kind == 2 ? dn::kThreadsFp8 : dn::kThreads; }
+const void* dense_kernel_ptr(int kind) {
+  if (kind == 1) return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false>);
+  if (kind == 2) return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true>);
+  return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false>);
 }
 
-cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, const DecodeParams& p, int num_parts,
-                         int half, cudaStream_t stream) {
+cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
+                         const CUtensorMap& rope_map, const DecodeParams& p, int num_parts, int kind,
+                         cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
-  if (half)
-    dn::dense_decode_kernel<true><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, p);
+  if (kind == 1)
+    dn::dense_decode_kernel<true, false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                        rope_map, p);
+  else if (kind == 2)
+    dn::dense_decode_kernel<true, true><<<grid, dn::kThreadsFp8, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                          rope_map, p);
   else
-    dn::dense_decode_kernel<false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, p);
+    dn::dense_decode_kernel<false, false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                         rope_map, p);
   return cudaGetLastError();
 }
 

@@ -49,3 +49,17 @@ def test_dense_fp8_workload_full_size():
     ro, rl = orc.dense_fp8_decode(case.q.double().numpy(), case.kv8.numpy(), case.block_table.numpy(),
                                   case.cache_seqlens.numpy(), False, case.scale, batches=bs)
     compare(out[bs], lse[bs], ro[bs], rl[bs])
+
+
+def test_dense_fp8_records_workload_full_size():
+    """The same FP8 record cache through the dense kernel (dtype FP8_RECORD), in
+    the launch configuration the bench times; the oracle checks 6 requests."""
+    from oracle import mla_oracle as orc
+    case = wl.make("dense_fp8_b64_hq128_sk2048to4096")
+    out, lse = mla.decode(case.q.cuda(), case.kv8.cuda(), case.block_table.cuda(), case.cache_seqlens.cuda(),
+                          softmax_scale=case.scale)
+    torch.cuda.synchronize()
+    bs = [0, 2, 19, 33, 48, 62]
+    ro, rl = orc.dense_fp8_decode(case.q.double().numpy(), case.kv8.numpy(), case.block_table.numpy(),
+                                  case.cache_seqlens.numpy(), False, case.scale, batches=bs)
+    compare(out[bs], lse[bs], ro[bs], rl[bs])
