@@ -14,7 +14,7 @@
 
 namespace mla {
 cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, int, cudaStream_t);
-cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, void*, int, float*, cudaStream_t);
+cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, int, void*, int, float*, cudaStream_t);
 cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                          const DecodeParams&, int, int, cudaStream_t);
 int dense_smem_bytes();
@@ -384,7 +384,7 @@ int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* 
   if (workspace_bytes < w.total) return MLA_ERR_INVALID_ARG;
   const float* o = static_cast<const float*>(d_workspace);
   const float* l = reinterpret_cast<const float*>(static_cast<const char*>(d_workspace) + w.lse_off);
-  return launch_combine(o, l, d_split_offset, n_units, rows_per_unit, d_out, out_type, d_lse,
+  return launch_combine(o, l, d_split_offset, n_units, rows_per_unit, num_parts, d_out, out_type, d_lse,
                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;

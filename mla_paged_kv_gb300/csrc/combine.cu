@@ -49,12 +49,13 @@ __device__ __forceinline__ void acc4(float4& a, float w, const float4& v) {
 }
 
 // kVec = float4 per lane per split: 4 -> a warp covers a whole 512-column
-// row (a block = 4 rows), 1 -> a warp covers a 128-column quarter (a block =
-// 1 row).  The quarter form gives 4x the warps for problems with few rows and
-// many splits (long context: one unit, dozens of splits), where the loop over
-// splits, not the grid, has to carry the parallelism.  Split weights are
-// computed with the lanes spread over the splits and broadcast by shuffle;
-// the partial rows of kBatch splits are loaded before any is summed.
+// row (a block = 4 rows), used when there are rows enough to fill the GPU
+// several times over; 1 -> a warp covers a 128-column quarter (a block = 1
+// row), 4x the warps for fewer rows.  Few rows with many splits per unit
+// (long context) go to combine_split_kernel instead.
+// Split weights are computed with the lanes spread over the splits and
+// broadcast by shuffle; the partial rows of kBatch splits are loaded before
+// any is summed.
 template <int kVec>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const float* __restrict__ o_accum, const float* __restrict__ lse_accum,
@@ -128,13 +129,92 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   if (writes_lse) lse[orow] = m + logf(z);
 }
 
+// Few rows, many splits (long context: one unit, dozens of splits): one
+// block per (row, 128-column quarter); its kSubsets warps take every
+// kSubsets-th split each, so a warp's loop is n / kSubsets long, and the
+// warps' sums are added through shared memory.  The split weights are the
+// same as above (every warp computes m and Z over all splits).
+constexpr int kSubsets = 8;
+
+__global__ void __launch_bounds__(kSubsets * 32)
+    combine_split_kernel(const float* __restrict__ o_accum, const float* __restrict__ lse_accum,
+                         const int32_t* __restrict__ split_offset, int rows, void* __restrict__ out, int out_type,
+                         float* __restrict__ lse) {
+  constexpr int kBatch = 4;
+  __shared__ float4 part[kSubsets][32];
+  pdl_wait_prior_grid();
+  const int unit = blockIdx.y;
+  const int row = blockIdx.x >> 2, quarter = blockIdx.x & 3;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (row >= rows) return;  // uniform over the block
+  const int s0 = split_offset[unit];
+  const int n = split_offset[unit + 1] - s0;
+  if (n == 1) return;  // written directly by the attention kernel
+  const size_t orow = static_cast<size_t>(unit) * rows + row;
+  const size_t col = static_cast<size_t>(quarter) * 128 + lane * 4;
+
+  float m = -INFINITY;
+  for (int s = lane; s < n; s += 32) m = fmaxf(m, lse_accum[static_cast<size_t>(s0 + s) * rows + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (n <= 0 || m == -INFINITY) {
+    if (warp == 0) {
+      store_row4(out, out_type, orow * kDv + col, 0.f, 0.f, 0.f, 0.f);
+      if (quarter == 0 && lane == 0) lse[orow] = -INFINITY;
+    }
+    return;
+  }
+  float z = 0.f;
+  for (int s = lane; s < n; s += 32) {
+    const float l = lse_accum[static_cast<size_t>(s0 + s) * rows + row];
+    z += (l == -INFINITY) ? 0.f : expf(l - m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  const float inv_z = 1.f / z;
+
+  const size_t split_stride = static_cast<size_t>(rows) * kDv / 4;  // float4 between consecutive splits
+  const float4* src = reinterpret_cast<const float4*>(o_accum + (static_cast<size_t>(s0) * rows + row) * kDv + col);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = warp; s < n; s += kSubsets * kBatch) {
+    float4 v[kBatch];
+    float w[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int si = s + i * kSubsets;
+      const float l = si < n ? lse_accum[static_cast<size_t>(s0 + si) * rows + row] : -INFINITY;
+      w[i] = (l == -INFINITY) ? 0.f : expf(l - m) * inv_z;
+      v[i] = si < n ? __ldg(src + static_cast<size_t>(si) * split_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) acc4(acc, w[i], v[i]);
+  }
+  part[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float4 t = part[0][lane];
+#pragma unroll
+    for (int k = 1; k < kSubsets; ++k) {
+      t.x += part[k][lane].x;
+      t.y += part[k][lane].y;
+      t.z += part[k][lane].z;
+      t.w += part[k][lane].w;
+    }
+    store_row4(out, out_type, orow * kDv + col, t.x, t.y, t.z, t.w);
+    if (quarter == 0 && lane == 0) lse[orow] = m + logf(z);
+  }
+}
+
 cudaError_t launch_combine(const float* o_accum, const float* lse_accum, const int32_t* split_offset, int n_units,
-                           int rows, void* out, int out_type, float* lse, cudaStream_t stream) {
-  // whole-row warps once there are enough rows to fill the GPU several times over
+                           int rows, int num_parts, void* out, int out_type, float* lse, cudaStream_t stream) {
+  // whole-row warps once there are enough rows to fill the GPU several times
+  // over; else split-parallel blocks when the units average 8 or more splits
   const bool whole_rows = static_cast<long long>(n_units) * rows >= 8192;
+  const bool split_par = !whole_rows && num_parts >= 8 * n_units;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = whole_rows ? dim3(ceil_div_i(rows, kCombineWarps), n_units, 1) : dim3(rows, n_units, 1);
-  cfg.blockDim = dim3(kCombineWarps * 32, 1, 1);
+  cfg.gridDim = whole_rows ? dim3(ceil_div_i(rows, kCombineWarps), n_units, 1)
+                           : dim3(split_par ? 4 * rows : rows, n_units, 1);
+  cfg.blockDim = dim3((split_par ? kSubsets : kCombineWarps) * 32, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -144,6 +224,8 @@ cudaError_t launch_combine(const float* o_accum, const float* lse_accum, const i
   cfg.numAttrs = 1;
   if (whole_rows)
     return cudaLaunchKernelEx(&cfg, combine_kernel<4>, o_accum, lse_accum, split_offset, rows, out, out_type, lse);
+  if (split_par)
+    return cudaLaunchKernelEx(&cfg, combine_split_kernel, o_accum, lse_accum, split_offset, rows, out, out_type, lse);
   return cudaLaunchKernelEx(&cfg, combine_kernel<1>, o_accum, lse_accum, split_offset, rows, out, out_type, lse);
 }
 
