@@ -102,6 +102,10 @@ const DeviceInfo& device_info() {
           cudaSuccess ||
       cudaFuncSetAttribute(dense_kernel_ptr(2), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
           cudaSuccess ||
+      cudaFuncSetAttribute(dense_kernel_ptr(3), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(dense_kernel_ptr(4), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
+          cudaSuccess ||
       cudaFuncSetAttribute(sparse_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            sparse_smem_bytes()) != cudaSuccess) {
     cudaGetLastError();
@@ -268,6 +272,11 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
   p->blocks_per_group = blocks_per_group;
   p->causal = causal ? 1 : 0;
   p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  // with many partitions per request their CTAs read the same Q, which is
+  // then an L2 hit: all nine boxes at once (staged in the empty V ring) beat
+  // streaming them through three slots; with one or two partitions per
+  // request the burst crowds the TMA queue and the streamed path wins
+  p->q_vring = num_parts >= 4 * batch ? 1 : 0;
   p->block_table = block_table;
   p->max_pages = max_pages;
   p->num_pages = num_pages;
@@ -366,8 +375,8 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
                                h_kv, dtype, causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
                                workspace_bytes, d_out, out_type, d_lse, d_status, &p, &qm, &km, &sm, &rm);
   if (rc != MLA_OK) return rc;
-  return launch_dense(qm, km, sm, rm, p, num_parts,
-                      dtype == MLA_DTYPE_FP16 ? 1 : (dtype == MLA_DTYPE_FP8_RECORD ? 2 : 0),
+  const int kind = dtype == MLA_DTYPE_FP8_RECORD ? 2 : (dtype == MLA_DTYPE_FP16 ? 1 : 0) + (p.q_vring ? 3 : 0);
+  return launch_dense(qm, km, sm, rm, p, num_parts, kind,
                       reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;

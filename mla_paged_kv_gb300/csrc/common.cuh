@@ -42,6 +42,7 @@ struct DecodeParams {
   int causal;
   float scale_log2;         // softmax_scale * log2(e)
   // dense
+  int q_vring;              // host: 1 selects the kernel instance that stages the first unit's Q in the V ring
   const int32_t* block_table;
   int max_pages;
   int num_pages;

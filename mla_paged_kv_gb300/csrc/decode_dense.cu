@@ -118,7 +118,9 @@ enum : int {
   RAW_K,                      // +slot, FP8 records: the K slot's raw bytes have landed
   RAW_V = RAW_K + kKSlots,    // +slot, FP8 records: a V slot's raw bytes have landed
   QB_READY = RAW_V + kVSlots, // +slot, FP8 records: a landed Q box has been turned into fp16
-  kNumBars = QB_READY + kQSmemBoxes
+  VQ_FULL = QB_READY + kQSmemBoxes,  // 16-bit KV: the first unit's Q boxes 0-5 have landed in the V ring
+  VQ_EMPTY,                          // ... and have been copied into TMEM: the V ring is free
+  kNumBars
 };
 
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -400,18 +402,23 @@ __device__ __forceinline__ float ref_alpha(float r_old, float r_new) {
   return r_new == r_old ? 1.f : ex2(r_old - r_new);
 }
 
+// kQV: the first unit's Q boxes 0-5 are staged in the (still empty) V ring
+// and all nine boxes load at once (a separate instance, chosen when many
+// partitions share each request, so that the other instances keep their
+// code unchanged).
 // kHalf: the MMAs take fp16 operands (else bf16).  kFp8 (with kHalf): KV is
 // a pool of FP8 records (kv_map = their codes in 64-byte boxes, sc_map =
 // scales, rope_map = RoPE as a swizzled bf16 box) and Q is bf16; both are
 // turned into fp16 in shared memory (records: fp16(code * scale); Q and
 // RoPE: bf16 -> fp16).  Otherwise kv_map is the 16-bit pool and sc_map /
 // rope_map are unused.
-template <bool kHalf, bool kFp8>
+template <bool kHalf, bool kFp8, bool kQV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     dense_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
                         const __grid_constant__ CUtensorMap sc_map, const __grid_constant__ CUtensorMap rope_map,
                         const DecodeParams p) {
   static_assert(!kFp8 || kHalf, "FP8 records are converted to fp16");
+  static_assert(!(kFp8 && kQV), "the V-ring Q stage is for 16-bit KV");
   constexpr int kNThreads = kFp8 ? kThreadsFp8 : kThreads;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -450,6 +457,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       mbar_init(&bars[QB_EMPTY + i], 1);
       mbar_init(&bars[QB_READY + i], 1);
     }
+    mbar_init(&bars[VQ_FULL], 1);
+    mbar_init(&bars[VQ_EMPTY], 1);
     for (int i = 0; i < kKSlots; ++i) {
       mbar_init(&bars[K_FULL + i], kFp8 ? kConvWarps : 1);
       mbar_init(&bars[K_EMPTY + i], 1);
@@ -483,10 +492,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     mbar_arrive_expect_tx(&bars[R_FULL], kVecBytes);
     mbar_arrive_expect_tx(&bars[L_FULL], kVecBytes);
   }
+  static_assert(kVSlots * kVSlotBytes == 6 * kQBoxBytes, "the V ring holds Q boxes 0-5 at the start");
   if (q_box_bytes < static_cast<uint32_t>(kQBoxBytes)) {
-    // Q boxes of a head group cover fewer than 128 rows: the rows past them stay zero
+    // Q boxes of a head group cover fewer than 128 rows: the rows past them stay
+    // zero (in the Q buffer, and in the V ring where the first unit's Q lands)
     for (int i = tid; i < kQSmemBoxes * kQBoxBytes / 16; i += kNThreads)
       reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (kQV)
+      for (int i = tid; i < 6 * kQBoxBytes / 16; i += kNThreads)
+        reinterpret_cast<uint4*>(sV)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
   if (warp == kWarpMma) {
@@ -569,6 +583,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
             const uint32_t n = c.t / kVSlots;
             const int s = static_cast<int>(c.t % kVSlots);
             if (n >= 1) ok = mbar_wait(&bars[V_EMPTY + s], (n - 1) & 1, abort_flag);
+            // 16-bit KV: the ring holds the first unit's Q until it is in TMEM
+            if constexpr (kQV) {
+              if (c.t == 0 && ok) ok = mbar_wait(&bars[VQ_EMPTY], 0, abort_flag);
+            }
             if (ok) {
               MLA_TRACE(7, c.t);
               uint8_t* dst = sV + s * kVSlotBytes;
@@ -716,6 +734,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         for (int sl = 0; sl < kQSmemBoxes; ++sl)
           if (qb_issued[sl] > 0) mbar_wait(&bars[QB_FULL + sl], (qb_issued[sl] - 1) & 1, nullptr);
       }
+    } else if (kQV && lane == 0) {
+      // 16-bit KV, V-ring instance.  The first unit: boxes 0-5 go into the V
+      // ring, still empty at the start (the MMA thread copies them into TMEM
+      // and frees the ring for the V producer), boxes 6-8 into the Q slots,
+      // all nine at once.  Later units: box j through slot j % 3 as below.
+      const uint64_t pol_q = policy_evict_last();
+      Cursor c;
+      cursor_init(p, P, c);
+      bool ok = true;
+      uint32_t qb_issued[kQSmemBoxes] = {}, vq_issued = 0;
+      // box j of unit b into dst; into L2 only when bar is null
+      auto q_box = [&](int b, int j, uint8_t* dst, uint64_t* bar) {
+        if (p.h_kv == 1) {
+          const int row0 = b * p.rows + rb * kRowsPerBlock;
+          if (bar)
+            tma_load_2d(dst, &q_map, bar, 64 * j, row0, pol_q);
+          else
+            tma_prefetch_2d(&q_map, 64 * j, row0);
+        } else {
+          // [batch * s_q][h_kv][group_heads][576]: block_tokens tokens of head group grp
+          const int tok0 = b * p.s_q + rb * p.block_tokens;
+          if (bar)
+            tma_load_4d(dst, &q_map, bar, 64 * j, 0, grp, tok0, pol_q);
+          else
+            tma_prefetch_4d(&q_map, 64 * j, 0, grp, tok0);
+        }
+      };
+      while (ok && c.valid) {
+        if (c.u == 0) {
+          mbar_arrive_expect_tx(&bars[VQ_FULL], 6 * q_box_bytes);
+          for (int j = 0; j < 6; ++j) q_box(c.b, j, sV + j * kQBoxBytes, &bars[VQ_FULL]);
+          ++vq_issued;
+          for (int sl = 0; sl < kQSmemBoxes; ++sl) {
+            mbar_arrive_expect_tx(&bars[QB_FULL + sl], q_box_bytes);
+            q_box(c.b, 6 + sl, sQ + sl * kQBoxBytes, &bars[QB_FULL + sl]);
+            ++qb_issued[sl];
+          }
+        } else {
+          const int us = c.u - 1;  // units streamed through the slots before this one
+          ok = mbar_wait(&bars[Q_EMPTY], (c.u - 1) & 1, abort_flag);
+          for (int j = 0; ok && j < 9; ++j) {
+            const int sl = j % kQSmemBoxes;
+            // the slot's previous box (j - 3) has been copied into TMEM (two copies a slot per streamed unit)
+            if (j >= kQSmemBoxes) ok = mbar_wait(&bars[QB_EMPTY + sl], (2 * us + j / 3 - 1) & 1, abort_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars[QB_FULL + sl], q_box_bytes);
+            q_box(c.b, j, sQ + sl * kQBoxBytes, &bars[QB_FULL + sl]);
+            ++qb_issued[sl];
+          }
+        }
+        // on to the next unit; its Q into L2 while this one is worked on
+        c.t += static_cast<uint32_t>(c.hi - c.k);
+        ++c.u;
+        cursor_seek(p, P, c, c.b + 1);
+        if (ok && c.valid)
+          for (int j = 0; j < 9; ++j) q_box(c.b, j, nullptr, nullptr);
+      }
+      if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+      // no TMA write may land after this CTA exits
+      if (vq_issued > 0) mbar_wait(&bars[VQ_FULL], 0, nullptr);
+      for (int sl = 0; sl < kQSmemBoxes; ++sl)
+        if (qb_issued[sl] > 0) mbar_wait(&bars[QB_FULL + sl], (qb_issued[sl] - 1) & 1, nullptr);
     } else if (lane == 0) {
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
@@ -879,7 +959,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       // boxes 6-8 are only counted (they stay for the MMAs)
       auto q_copy = [&]() -> bool {
         const uint32_t uq = qb_seen / 9u, j = qb_seen % 9u, sl = j % kQSmemBoxes;
-        if (!mbar_test_wait(&bars[(kFp8 ? QB_READY : QB_FULL) + sl], (3u * uq + j / 3u) & 1u)) return false;
+        // completion of this box's slot barrier: three per unit, except one
+        // (boxes 6-8) for a first unit staged in the V ring
+        const uint32_t idx = !kQV ? 3u * uq + j / 3u : (uq == 0 ? 0u : 1u + 3u * (uq - 1u) + j / 3u);
+        if (!mbar_test_wait(&bars[(kFp8 ? QB_READY : QB_FULL) + sl], idx & 1u)) return false;
         if (j < 6u) {
           tc_fence_after();
 #pragma unroll
@@ -891,6 +974,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         ++qb_seen;
         return true;
       };
+      if (kQV && cq.valid) {
+        // the first unit's boxes 0-5, staged in the V ring: into TMEM (once,
+        // before the issue loop), then the ring goes to the V producer
+        ok = mbar_wait(&bars[VQ_FULL], 0, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          const uint64_t vq_desc0 = sdesc_sw128(smem_u32(sV), 16, 1024);
+#pragma unroll 1
+          for (uint32_t jj = 0; jj < 6; ++jj)
+#pragma unroll
+            for (uint32_t k = 0; k < 4; ++k)
+              tmem_cp_128x256b(tmem + kTmemQ + 32u * jj + 8u * k,
+                               vq_desc0 + static_cast<uint64_t>((jj * kQBoxBytes + k * 32u) >> 4));
+          umma_commit(&bars[VQ_EMPTY]);
+          qb_seen = 6;
+        }
+      }
       advance_q();
       while (ok && cq.valid) {
         bool progressed = q_copy();
@@ -1216,27 +1316,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
 }  // namespace dn
 
 int dense_smem_bytes() { return dn::kSmemBytes; }
-// kind 0: bf16, 1: fp16, 2: FP8 records (bf16 Q)
+// kind 0: bf16, 1: fp16, 2: FP8 records (bf16 Q), 3: bf16 with the V-ring Q
+// stage, 4: fp16 with it
 int dense_threads(int kind) { return kind == 2 ? dn::kThreadsFp8 : dn::kThreads; }
 const void* dense_kernel_ptr(int kind) {
-  if (kind == 1) return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false>);
-  if (kind == 2) return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true>);
-  return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false>);
+  switch (kind) {
+    case 1: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, false>);
+    case 2: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true, false>);
+    case 3: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, true>);
+    case 4: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, true>);
+    default: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, false>);
+  }
 }
 
 cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
                          const CUtensorMap& rope_map, const DecodeParams& p, int num_parts, int kind,
                          cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
-  if (kind == 1)
-    dn::dense_decode_kernel<true, false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                        rope_map, p);
-  else if (kind == 2)
-    dn::dense_decode_kernel<true, true><<<grid, dn::kThreadsFp8, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+  const int threads = dense_threads(kind);
+  switch (kind) {
+    case 1:
+      dn::dense_decode_kernel<true, false, false><<<grid, threads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                           rope_map, p);
+      break;
+    case 2:
+      dn::dense_decode_kernel<true, true, false><<<grid, threads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
                                                                                           rope_map, p);
-  else
-    dn::dense_decode_kernel<false, false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                         rope_map, p);
+      break;
+    case 3:
+      dn::dense_decode_kernel<false, false, true><<<grid, threads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                           rope_map, p);
+      break;
+    case 4:
+      dn::dense_decode_kernel<true, false, true><<<grid, threads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                          rope_map, p);
+      break;
+    default:
+      dn::dense_decode_kernel<false, false, false><<<grid, threads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                            rope_map, p);
+  }
   return cudaGetLastError();
 }
 
