@@ -5,7 +5,8 @@
 // of a request (all heads share one latent KV head), over the keys of one
 // split: S = Q K^T on 576 dims, online softmax, O = P V with V = the first
 // 512 dims of the same latent rows; then O / l and the split's LSE.  Keys
-// come from 64-token bf16 pages through the block table.
+// come from 64-token pages (bf16 or fp16, one or more latent KV heads, or
+// FlashMLA PR #200's 656-byte FP8 records) through the block table.
 //
 // How (GB300 design, not the page's SM80 one):
 //  * TMEM holds 512 fp32 columns per SM, exactly one 128 x 512 accumulator,
@@ -27,16 +28,21 @@
 //    P V.  Each CTA keeps the row sum l of its own tiles only (rescaled on
 //    every reference change); the two are added once per unit, before the
 //    epilogue, through a second mailbox.
-//  * The P V of a received tile waits only for its P to land (the MMA thread
+//  * The P V of a received tile waits only for its P to land (the P V thread
 //    watches the copy's barrier) and for the softmax threads' go, given as
 //    soon as the tile's reference is known.
 //  * Q of the row block is the MMA A operand: dims [0, 384) sit in TMEM
 //    (packed bf16 pairs), dims [384, 576) in shared memory (TMA, 128-byte
 //    swizzle).  A Q warp streams a unit's nine 64-dim Q boxes through the
-//    three box slots of that shared-memory buffer; the MMA thread moves
+//    three box slots of that shared-memory buffer; the Q K^T thread moves
 //    boxes 0-5 (dims [0, 384)) into TMEM with tcgen05.cp as they land, and
 //    boxes 6-8 stay.  The next unit's Q is prefetched into L2 meanwhile, and
-//    the softmax warps write the epilogue while Q streams in.
+//    the softmax warps write the epilogue while Q streams in.  (Instance
+//    kQV: the first unit's nine boxes load at once, boxes 0-5 staged in the
+//    still-empty V ring.)
+//  * FP8 records (instance kFp8): the producers bring each box in as raw
+//    codes and scales, three converter warps turn them into fp16 boxes in
+//    place (Q and RoPE go bf16 -> fp16), and the rest is the fp16 path.
 //  * One tile = nine 64-dim TMA boxes of one page.  The four boxes that are
 //    this CTA's V half go to a 3-slot "V" ring for every tile (P V reads
 //    them; for its own tiles Q K^T reads them too); the other five go to a
@@ -46,9 +52,10 @@
 // Roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane),
 //        warp 4 K-slot producer, warp 5 V-ring producer,
 //        warp 6 Q K^T issuer (and Q copies into TMEM) and TMEM owner,
-//        warp 7 Q producer, warp 8 P V issuer.  Q K^T and P V come from two
-//        threads so that a ready P V does not wait for a Q K^T block to
-//        finish issuing; they touch different TMEM accumulators.
+//        warp 7 Q producer, warp 8 P V issuer (warps 9-11: FP8 converters).
+//        Q K^T and P V come from two threads so that a ready P V does not
+//        wait for a Q K^T block to finish issuing; they touch different TMEM
+//        accumulators.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -103,10 +110,10 @@ enum : int {
   V_EMPTY = V_FULL + kVSlots,     // +slot
   S_FULL = V_EMPTY + kVSlots,
   S_FREE,
-  OWN_GO,     // softmax -> MMA: P of an own tile written, O rescaled
+  OWN_GO,     // softmax -> P V thread: P of an own tile written, O rescaled
   OWN_FREE,   // own P buffer reusable: own P V done + the peer's P V done (its multicast commit)
-  RECV_FULL,  // the peer's P has landed (bulk-copy bytes); watched and re-armed by the MMA thread
-  RECV_GO,    // softmax -> MMA: received tile's reference applied (O rescaled if it changed)
+  RECV_FULL,  // the peer's P has landed (bulk-copy bytes); watched and re-armed by the P V thread
+  RECV_GO,    // softmax -> P V thread: received tile's reference applied (O rescaled if it changed)
   R_FULL,     // reference mailbox filled (bulk-copy bytes)
   R_FREE,     // the peer has read our last references (one remote arrival per warp)
   L_FULL,     // row-sum mailbox filled (bulk-copy bytes)
@@ -682,12 +689,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     // ------------------------------------------------------------ Q producer
     // Per unit, the nine 64-dim boxes of Q in order through the three slots
     // of the shared-memory Q buffer: box j goes to slot j % 3.  Boxes 0-5
-    // (dims [0, 384)) are copied into TMEM by the MMA thread, which frees
+    // (dims [0, 384)) are copied into TMEM by the Q K^T thread, which frees
     // the slot for box j + 3; boxes 6-8 stay until the unit's last Q K^T.
     if constexpr (kFp8) {
       // FP8 records (h_kv = 1): the same nine boxes, but the whole warp turns
       // each landed box into fp16 in place and then signals QB_READY; a slot
-      // is refilled with box j + 3 once the MMA thread has copied box j.
+      // is refilled with box j + 3 once the Q K^T thread has copied box j.
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
       cursor_init(p, P, c);
@@ -736,7 +743,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       }
     } else if (kQV && lane == 0) {
       // 16-bit KV, V-ring instance.  The first unit: boxes 0-5 go into the V
-      // ring, still empty at the start (the MMA thread copies them into TMEM
+      // ring, still empty at the start (the Q K^T thread copies them into TMEM
       // and frees the ring for the V producer), boxes 6-8 into the Q slots,
       // all nine at once.  Later units: box j through slot j % 3 as below.
       const uint64_t pol_q = policy_evict_last();
@@ -916,7 +923,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ Q K^T issuer
     if (lane == 0) {
       const uint64_t q_desc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t k_desc0 = sdesc_sw128(smem_u32(sK), 16, 1024);
