@@ -302,29 +302,30 @@ __device__ __forceinline__ void issue_qk_v(uint32_t d, uint32_t tmem, uint64_t q
 // v = fma(c, s_hi, c * s_lo) is c * s / 2^e rounded once up to a relative
 // 2^-21, and v * 2^e is exact (a power of two) unless it falls below fp16's
 // normal range.  So each value carries a relative error <= 2^-11 + 2^-20
-// inside fp16's normal range.  One warp: every read is in registers before
-// the first write.  `sg` = the box's scale group.
+// inside fp16's normal range.  `sg` = the box's scale group.
+// One warp, compact code (the kernel is large; instruction fetch matters):
+// each lane keeps the scales of records lane and lane + 32 in registers, and
+// the eight 512-byte code groups are converted last to first - group k
+// (records 8k..8k+7) writes bytes [1024k, 1024k + 1024), which never holds
+// codes of a group not yet read; the scale bytes are overwritten only after
+// every scale is in registers.
 __device__ __forceinline__ void convert_fp8_box(uint8_t* box, int sg, int lane) {
-  uint4 code[8];
-  __half2 s_hi[8], s_lo[8], s_pow[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  const float* scales = reinterpret_cast<const float*>(box + kFp8CodeBytes);
+  const float sc_lo = scales[lane * 4 + sg], sc_hi = scales[(lane + 32) * 4 + sg];
+  __syncwarp();
+#pragma unroll 1
+  for (int k = 7; k >= 0; --k) {
+    const int row = 8 * k + (lane >> 2);
     // 16-byte piece `lane` of the k-th 512 bytes: record 8k + lane/4, codes 16 * (lane % 4) ...
-    code[k] = reinterpret_cast<const uint4*>(box)[k * 32 + lane];
-    const uint32_t sb =
-        __float_as_uint(reinterpret_cast<const float*>(box + kFp8CodeBytes + (8 * k + (lane >> 2)) * 16)[sg]);
+    const uint4 code = reinterpret_cast<const uint4*>(box)[k * 32 + lane];
+    const uint32_t sb = __float_as_uint(__shfl_sync(0xffffffffu, k < 4 ? sc_lo : sc_hi, row & 31));
+    __syncwarp();  // every lane has read group k before any lane writes
     const float sm = __uint_as_float((sb & 0x807FFFFFu) | (127u << 23));  // s / 2^e in [1, 2) (sign kept)
     const __half hi = __float2half_rn(sm);
-    s_hi[k] = __half2half2(hi);
-    s_lo[k] = __half2half2(__float2half_rn(sm - __half2float(hi)));
-    s_pow[k] = __half2half2(__float2half_rn(__uint_as_float(sb & 0x7F800000u)));  // 2^e
-  }
-  __syncwarp();
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int row = 8 * k + (lane >> 2);
-    const uint32_t c = static_cast<uint32_t>(lane & 3);
-    const uint32_t in[4] = {code[k].x, code[k].y, code[k].z, code[k].w};
+    const __half2 s_hi = __half2half2(hi);
+    const __half2 s_lo = __half2half2(__float2half_rn(sm - __half2float(hi)));
+    const __half2 s_pow = __half2half2(__float2half_rn(__uint_as_float(sb & 0x7F800000u)));  // 2^e
+    const uint32_t in[4] = {code.x, code.y, code.z, code.w};
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -332,10 +333,11 @@ __device__ __forceinline__ void convert_fp8_box(uint8_t* box, int sg, int lane) 
           __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((in[i >> 1] >> (16 * (i & 1))) & 0xFFFFu),
                                      __NV_E4M3);
       const __half2 cv = *reinterpret_cast<const __half2*>(&hr);
-      const __half2 v = __hmul2(__hfma2(cv, s_hi[k], __hmul2(cv, s_lo[k])), s_pow[k]);
+      const __half2 v = __hmul2(__hfma2(cv, s_hi, __hmul2(cv, s_lo)), s_pow);
       w[i] = *reinterpret_cast<const uint32_t*>(&v);
     }
     uint8_t* rowp = box + row * 128;
+    const uint32_t c = static_cast<uint32_t>(lane & 3);
     const uint32_t sw = static_cast<uint32_t>(row & 7);
     *reinterpret_cast<uint4*>(rowp + (((2u * c) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
     *reinterpret_cast<uint4*>(rowp + (((2u * c + 1u) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
@@ -348,7 +350,7 @@ __device__ __forceinline__ void convert_fp8_box(uint8_t* box, int sg, int lane) 
 // range (bf16 carries 8 significant bits, fp16 11).
 __device__ __forceinline__ void bf16_box_to_fp16(uint8_t* box, int words, int lane) {
   uint4* v = reinterpret_cast<uint4*>(box);
-#pragma unroll 4
+#pragma unroll 2
   for (int i = lane; i < words / 4; i += 32) {
     uint4 x = v[i];
     uint32_t* w = reinterpret_cast<uint32_t*>(&x);
