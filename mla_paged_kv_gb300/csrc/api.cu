@@ -173,15 +173,15 @@ int encode_kv_map(CUtensorMap* m, const void* kv, int num_pages, int h_kv) {
 
 // Pool of FP8 records [num_pages][64][656] as a 2-D byte tensor (656, rows =
 // num_pages * 64); one box covers the 64 records of a page.  kind 0: the
-// E4M3 codes of one 64-dim box (64 B per record, unswizzled, 4 KB); 1: the
-// four fp32 scales (16 B per record, 1 KB); 2: the 64 bf16 RoPE dims (128 B
-// per record, 128-byte swizzle: lands as the bf16 box an MMA reads).
+// E4M3 codes of one 128-dim scale group (128 B per record, unswizzled, 8 KB);
+// 1: the four fp32 scales (16 B per record, 1 KB); 2: the 64 bf16 RoPE dims
+// (128 B per record, 128-byte swizzle: lands as the 16-bit box an MMA reads).
 int encode_fp8_record_map(CUtensorMap* m, const void* kv8, int num_pages, int kind) {
   auto fn = encode_fn();
   if (fn == nullptr) return MLA_ERR_CUDA;
   cuuint64_t dims[2] = {656, static_cast<cuuint64_t>(num_pages) * MLA_PAGE_SIZE};
   cuuint64_t strides[1] = {656};
-  const cuuint32_t inner = kind == 0 ? 64 : (kind == 1 ? 16 : 128);
+  const cuuint32_t inner = kind == 1 ? 16 : 128;
   cuuint32_t box[2] = {inner, MLA_PAGE_SIZE};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv8), dims, strides, box, es,

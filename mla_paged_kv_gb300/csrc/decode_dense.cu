@@ -148,10 +148,14 @@ constexpr int kWarpConv = 9, kConvWarps = 3;  // FP8 record converters: warps 9-
 // 512 E4M3 NoPE codes, four fp32 scales (one per 128 dims), 64 bf16 RoPE.
 constexpr int kRecBytes = 656;
 static_assert(512 + 16 + 128 == kRecBytes, "record layout");
-constexpr int kFp8CodeBytes = kT * 64;      // one 64-dim box of codes: 4 KB, lands at the box's start
-constexpr int kFp8ScaleBytes = kT * 16;     // the tile's scales: 1 KB, lands at box + 4096
-constexpr int kFp8KSlotTx = 4 * (kFp8CodeBytes + kFp8ScaleBytes) + kBoxBytes;  // 4 NoPE boxes + RoPE
-constexpr int kFp8VSlotTx = 4 * (kFp8CodeBytes + kFp8ScaleBytes);
+// Raw bytes of a pair of 64-dim NoPE boxes (one 128-dim scale group): the
+// codes as one box of 64 records x 128 B (8 KB, unswizzled), landing in the
+// pair's second box, and the page's scales (64 x 16 B), landing at the start
+// of the pair's first box.
+constexpr int kFp8PairCodeBytes = kT * 128;
+constexpr int kFp8ScaleBytes = kT * 16;
+constexpr int kFp8KSlotTx = 2 * (kFp8PairCodeBytes + kFp8ScaleBytes) + kBoxBytes;  // two pairs + RoPE
+constexpr int kFp8VSlotTx = 2 * (kFp8PairCodeBytes + kFp8ScaleBytes);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
 constexpr uint32_t kTmemS = 256;  // S: [256, 320)
@@ -292,55 +296,66 @@ __device__ __forceinline__ void issue_qk_v(uint32_t d, uint32_t tmem, uint64_t q
   qk_box<kHalf, 4 * kRank + 3>(d, tmem, q_desc0, vslot + ((3 * kBoxBytes) >> 4), false);
 }
 
-// One 64-dim NoPE box of a page of FP8 records, in place: the box's 64 x 64
-// E4M3 codes (4 KB, record-major) and the tile's 64 x 4 fp32 scales (1 KB at
-// +4096) become the 64 x 64 fp16 box (8 KB, 128-byte swizzle) that an MMA
-// reads, value = code * scale rounded to fp16.  Per value pair: one
-// conversion (two E4M3 codes -> two exact fp16) and three fp16x2 ops.  The
-// record's scale s is split as s = 2^e * (s_hi + s_lo), s_hi = fp16(s / 2^e)
-// with s / 2^e in [1, 2) and s_lo = fp16(s / 2^e - s_hi); then
-// v = fma(c, s_hi, c * s_lo) is c * s / 2^e rounded once up to a relative
-// 2^-21, and v * 2^e is exact (a power of two) unless it falls below fp16's
-// normal range.  So each value carries a relative error <= 2^-11 + 2^-20
-// inside fp16's normal range.  `sg` = the box's scale group.
-// One warp, compact code (the kernel is large; instruction fetch matters):
-// each lane keeps the scales of records lane and lane + 32 in registers, and
-// the eight 512-byte code groups are converted last to first - group k
-// (records 8k..8k+7) writes bytes [1024k, 1024k + 1024), which never holds
-// codes of a group not yet read; the scale bytes are overwritten only after
-// every scale is in registers.
-__device__ __forceinline__ void convert_fp8_box(uint8_t* box, int sg, int lane) {
-  const float* scales = reinterpret_cast<const float*>(box + kFp8CodeBytes);
-  const float sc_lo = scales[lane * 4 + sg], sc_hi = scales[(lane + 32) * 4 + sg];
+// A pair of 64-dim NoPE boxes of a page of FP8 records, in place: the raw
+// codes of both (64 records x 128 B, record-major, in `hi`) and the page's
+// 64 x 4 fp32 scales (at the start of `lo`) become the two 64 x 64 fp16 boxes
+// (8 KB each, 128-byte swizzle) that the MMAs read, value = code * scale
+// rounded to fp16.  Per value pair: one conversion (two E4M3 codes -> two
+// exact fp16) and three fp16x2 ops.  The record's scale s is split as
+// s = 2^e * (s_hi + s_lo), s_hi = fp16(s / 2^e) with s / 2^e in [1, 2) and
+// s_lo = fp16(s / 2^e - s_hi); then v = fma(c, s_hi, c * s_lo) is c * s / 2^e
+// rounded once up to a relative 2^-21, and v * 2^e is exact (a power of two)
+// unless it falls below fp16's normal range.  So each value carries a
+// relative error <= 2^-11 + 2^-20 inside fp16's normal range.  `sg` = the
+// pair's scale group.
+// One warp, compact code (the kernel is large; instruction fetch matters).
+// Each lane first takes the scales of records lane and lane + 32 into
+// registers (the scale bytes are overwritten later).  Then, group by group,
+// the 8 records 8k..8k+7: their 1 KB of raw codes is read, and the same
+// bytes of `hi` (its rows 8k..8k+7) and rows 8k..8k+7 of `lo` are written.
+__device__ __forceinline__ void convert_fp8_pair(uint8_t* lo, uint8_t* hi, int sg, int lane) {
+  const float* scales = reinterpret_cast<const float*>(lo);
+  const float sc0 = scales[lane * 4 + sg], sc1 = scales[(lane + 32) * 4 + sg];
   __syncwarp();
 #pragma unroll 1
-  for (int k = 7; k >= 0; --k) {
-    const int row = 8 * k + (lane >> 2);
-    // 16-byte piece `lane` of the k-th 512 bytes: record 8k + lane/4, codes 16 * (lane % 4) ...
-    const uint4 code = reinterpret_cast<const uint4*>(box)[k * 32 + lane];
-    const uint32_t sb = __float_as_uint(__shfl_sync(0xffffffffu, k < 4 ? sc_lo : sc_hi, row & 31));
-    __syncwarp();  // every lane has read group k before any lane writes
-    const float sm = __uint_as_float((sb & 0x807FFFFFu) | (127u << 23));  // s / 2^e in [1, 2) (sign kept)
-    const __half hi = __float2half_rn(sm);
-    const __half2 s_hi = __half2half2(hi);
-    const __half2 s_lo = __half2half2(__float2half_rn(sm - __half2float(hi)));
-    const __half2 s_pow = __half2half2(__float2half_rn(__uint_as_float(sb & 0x7F800000u)));  // 2^e
-    const uint32_t in[4] = {code.x, code.y, code.z, code.w};
-    uint32_t w[8];
+  for (int k = 0; k < 8; ++k) {
+    // lane L: 16 codes at raw bytes 16L and 512 + 16L of the group: records
+    // 8k + L/8 and 8k + 4 + L/8, dims 16 * (L % 8) .. of the pair's 128
+    const uint4 c0 = reinterpret_cast<const uint4*>(hi + 1024 * k)[lane];
+    const uint4 c1 = reinterpret_cast<const uint4*>(hi + 1024 * k)[32 + lane];
+    const int r0 = 8 * k + (lane >> 3), r1 = r0 + 4;
+    const uint32_t sb0 = __float_as_uint(__shfl_sync(0xffffffffu, k < 4 ? sc0 : sc1, r0 & 31));
+    const uint32_t sb1 = __float_as_uint(__shfl_sync(0xffffffffu, k < 4 ? sc0 : sc1, r1 & 31));
+    __syncwarp();  // the group's raw bytes are all read before any lane writes them
+    const int d = lane & 7;                 // 16-code chunk of the pair's 128 dims
+    uint8_t* box = d < 4 ? lo : hi;          // dims 0-63 -> lo, 64-127 -> hi
+    const uint32_t cc = 2u * static_cast<uint32_t>(d & 3);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const __half2_raw hr =
-          __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((in[i >> 1] >> (16 * (i & 1))) & 0xFFFFu),
-                                     __NV_E4M3);
-      const __half2 cv = *reinterpret_cast<const __half2*>(&hr);
-      const __half2 v = __hmul2(__hfma2(cv, s_hi, __hmul2(cv, s_lo)), s_pow);
-      w[i] = *reinterpret_cast<const uint32_t*>(&v);
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t sb = h ? sb1 : sb0;
+      const uint4 code = h ? c1 : c0;
+      const int row = h ? r1 : r0;
+      const float sm = __uint_as_float((sb & 0x807FFFFFu) | (127u << 23));  // s / 2^e in [1, 2) (sign kept)
+      const __half shi = __float2half_rn(sm);
+      const __half2 s_hi = __half2half2(shi);
+      const __half2 s_lo = __half2half2(__float2half_rn(sm - __half2float(shi)));
+      const __half2 s_pow = __half2half2(__float2half_rn(__uint_as_float(sb & 0x7F800000u)));  // 2^e
+      const uint32_t in[4] = {code.x, code.y, code.z, code.w};
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const __half2_raw hr =
+            __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((in[i >> 1] >> (16 * (i & 1))) & 0xFFFFu),
+                                       __NV_E4M3);
+        const __half2 cv = *reinterpret_cast<const __half2*>(&hr);
+        const __half2 v = __hmul2(__hfma2(cv, s_hi, __hmul2(cv, s_lo)), s_pow);
+        w[i] = *reinterpret_cast<const uint32_t*>(&v);
+      }
+      uint8_t* rowp = box + row * 128;
+      const uint32_t sw = static_cast<uint32_t>(row & 7);
+      *reinterpret_cast<uint4*>(rowp + ((cc ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(rowp + (((cc + 1u) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
     }
-    uint8_t* rowp = box + row * 128;
-    const uint32_t c = static_cast<uint32_t>(lane & 3);
-    const uint32_t sw = static_cast<uint32_t>(row & 7);
-    *reinterpret_cast<uint4*>(rowp + (((2u * c) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(rowp + (((2u * c + 1u) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
   }
 }
 
@@ -565,19 +580,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
               MLA_TRACE(9, c.t);
               uint8_t* dst = sK + s * kKSlotBytes;
               if constexpr (kFp8) {
-                // raw bytes; the K converter makes the bf16 boxes and fills K_FULL
+                // raw bytes (the other value half as two code pairs + scales, and
+                // the RoPE box); the converters make the fp16 boxes and fill K_FULL
                 uint64_t* bar = &bars[RAW_K + s];
                 mbar_arrive_expect_tx(bar, kFp8KSlotTx);
+                const int x0 = 256 * (1 - static_cast<int>(rank));
 #pragma unroll
-                for (int j = 0; j < kKBoxes; ++j) {
-                  const int g = rank == 0 ? k_box<0>(j) : k_box<1>(j);
-                  if (g < 8) {
-                    tma_load_2d(dst + j * kBoxBytes, &kv_map, bar, 64 * g, page * kT, pol_kv);
-                    tma_load_2d(dst + j * kBoxBytes + kFp8CodeBytes, &sc_map, bar, 512, page * kT, pol_kv);
-                  } else {
-                    tma_load_2d(dst + j * kBoxBytes, &rope_map, bar, 528, page * kT, pol_kv);
-                  }
+                for (int pr = 0; pr < 2; ++pr) {
+                  tma_load_2d(dst + (2 * pr + 1) * kBoxBytes, &kv_map, bar, x0 + 128 * pr, page * kT, pol_kv);
+                  tma_load_2d(dst + (2 * pr) * kBoxBytes, &sc_map, bar, 512, page * kT, pol_kv);
                 }
+                tma_load_2d(dst + 4 * kBoxBytes, &rope_map, bar, 528, page * kT, pol_kv);
               } else {
                 mbar_arrive_expect_tx(&bars[K_FULL + s], kKSlotBytes);
 #pragma unroll
@@ -602,11 +615,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
               if constexpr (kFp8) {
                 uint64_t* bar = &bars[RAW_V + s];
                 mbar_arrive_expect_tx(bar, kFp8VSlotTx);
+                const int x0 = 256 * static_cast<int>(rank);
 #pragma unroll
-                for (int j = 0; j < kVBoxes; ++j) {
-                  tma_load_2d(dst + j * kBoxBytes, &kv_map, bar, 64 * (4 * static_cast<int>(rank) + j), page * kT,
-                              pol_kv);
-                  tma_load_2d(dst + j * kBoxBytes + kFp8CodeBytes, &sc_map, bar, 512, page * kT, pol_kv);
+                for (int pr = 0; pr < 2; ++pr) {
+                  tma_load_2d(dst + (2 * pr + 1) * kBoxBytes, &kv_map, bar, x0 + 128 * pr, page * kT, pol_kv);
+                  tma_load_2d(dst + (2 * pr) * kBoxBytes, &sc_map, bar, 512, page * kT, pol_kv);
                 }
               } else {
                 mbar_arrive_expect_tx(&bars[V_FULL + s], kVSlotBytes);
@@ -635,12 +648,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     __syncwarp();
   } else if (warp >= kWarpConv) {
     // ------------------------------------------------------------ FP8 record converters
-    // (FP8 instance only.)  The boxes of a tile are shared round-robin by the
-    // three converter warps, rotating with the tile: an own tile's K slot
-    // (jobs 0-4: four NoPE boxes and the RoPE box) first, then its V slot
-    // (jobs 5-8).  Each warp waits for the slot's raw bytes, converts its
-    // boxes in place, makes its writes visible to the tensor cores and
-    // arrives on the slot's FULL (every warp once per slot use).
+    // (FP8 instance only.)  A tile's conversion jobs are shared round-robin by
+    // the three converter warps, rotating with the tile: an own tile's K slot
+    // first (jobs 0, 1: the other value half's two box pairs; job 2: the RoPE
+    // box, bf16 -> fp16), then its V slot (jobs 3, 4: this CTA's value half's
+    // two box pairs).  Each warp waits for the slot's raw bytes, converts its
+    // jobs in place, makes its writes visible to the tensor cores and arrives
+    // on the slot's FULL (every warp once per slot use).
     if constexpr (kFp8) {
       const uint32_t cw = static_cast<uint32_t>(warp - kWarpConv);
       Cursor c;
@@ -656,13 +670,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
           if (!ok) break;
           uint8_t* slot = sK + s * kKSlotBytes;
 #pragma unroll 1
-          for (int j = 0; j < kKBoxes; ++j) {
+          for (int j = 0; j < 3; ++j) {
             if ((static_cast<uint32_t>(j) + rot) % kConvWarps != cw) continue;
-            const int g = rank == 0 ? k_box<0>(j) : k_box<1>(j);
-            if (g < 8)
-              convert_fp8_box(slot + j * kBoxBytes, g >> 1, lane);
+            if (j < 2)
+              convert_fp8_pair(slot + 2 * j * kBoxBytes, slot + (2 * j + 1) * kBoxBytes,
+                               2 * (1 - static_cast<int>(rank)) + j, lane);
             else
-              bf16_box_to_fp16(slot + j * kBoxBytes, kBoxBytes / 4, lane);  // RoPE
+              bf16_box_to_fp16(slot + 4 * kBoxBytes, kBoxBytes / 4, lane);  // RoPE
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -675,9 +689,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
           if (!ok) break;
           uint8_t* slot = sV + s * kVSlotBytes;
 #pragma unroll 1
-          for (int j = 0; j < kVBoxes; ++j) {
-            if ((static_cast<uint32_t>(j + kKBoxes) + rot) % kConvWarps != cw) continue;
-            convert_fp8_box(slot + j * kBoxBytes, (4 * static_cast<int>(rank) + j) >> 1, lane);
+          for (int j = 0; j < 2; ++j) {
+            if ((static_cast<uint32_t>(j + 3) + rot) % kConvWarps != cw) continue;
+            convert_fp8_pair(slot + 2 * j * kBoxBytes, slot + (2 * j + 1) * kBoxBytes,
+                             2 * static_cast<int>(rank) + j, lane);
           }
           fence_proxy_async_smem();
           __syncwarp();
