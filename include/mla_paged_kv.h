@@ -285,13 +285,20 @@ int mla_pack_selected_kv(const uint8_t* d_kv8, int num_pages, const int32_t* d_i
                          const int32_t* d_topk_length, int n_units, void* d_packed, size_t packed_bytes,
                          int32_t* d_status, mla_stream_t stream);
 
-/* Sparse FP8 decode over a packed workspace: the same result as
- * mla_sparse_fp8_decode_fwd with the selection that was packed (bit for bit
- * under the same plan: the same kernel runs, its records found through the
- * masks).  d_topk_length must be the one given to the pack (it counts the
- * tiles each unit schedules); the plan comes from mla_get_metadata exactly as
- * for the native call (the pages' H=128 packed path keeps the native
- * scheduler).  Other arguments as for mla_sparse_fp8_decode_fwd. */
+/* Sparse FP8 decode over a packed workspace (FlashMLA PR #200, "Packed
+ * attention specialization"): attention of each query token over the
+ * records that were packed for it.  The packed records are contiguous pages,
+ * so the dense decode kernel runs over them (its FP8-record instance: page
+ * u * tiles + t is tile t of unit u, the per-tile masks hide the slots whose
+ * index was -1).  Each NoPE value enters the MMAs as fp16(code * scale) and
+ * q and the RoPE dims as fp16, as for mla_decode_fwd with
+ * MLA_DTYPE_FP8_RECORD: a score moves by at most
+ * scale * (2^-11 + 2^-20) * sum_d |q_d k_d| from the exact one, where
+ * mla_sparse_fp8_decode_fwd keeps the scores exact.  d_topk_length must be
+ * the one given to the pack (it counts the tiles each unit schedules); the
+ * plan comes from mla_get_metadata exactly as for the native call (the
+ * pages' H=128 packed path keeps the native scheduler).  h_q <= 128.  Other
+ * arguments as for mla_sparse_fp8_decode_fwd. */
 int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size_t packed_bytes, int topk,
                                      const int32_t* d_topk_length, int batch, int s_q, int h_q, float softmax_scale,
                                      const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,

@@ -191,9 +191,22 @@ struct Cursor {
   bool valid;
 };
 
+// Keys of unit b.  kRec (FP8-record instance) also serves packed selections
+// (FlashMLA PR #200, "Packed attention specialization"): with packed_mask set,
+// a unit is one query token, its keys the first min(topk_length, topk) slots
+// (all topk when no lengths are given).
+template <bool kRec>
+__device__ __forceinline__ int unit_keys(const DecodeParams& p, int b) {
+  if constexpr (kRec) {
+    if (p.packed_mask != nullptr) return min(p.lengths != nullptr ? max(p.lengths[b], 0) : p.default_length, p.topk);
+  }
+  return max(p.lengths[b], 0);
+}
+
+template <bool kRec>
 __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& P, Cursor& c, int from_b) {
   for (int b = from_b; unit_in_part(P, b, p.n_units); ++b) {
-    const int L = max(p.lengths[b], 0);
+    const int L = unit_keys<kRec>(p, b);
     const int lo = (b == P.b0) ? P.t0 : 0;
     const int hi = (b == P.b1) ? P.t1 : num_tiles(L);
     if (hi > lo) {
@@ -209,20 +222,22 @@ __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& P
   c.valid = false;
 }
 
+template <bool kRec>
 __device__ __forceinline__ void cursor_init(const DecodeParams& p, const Part& P, Cursor& c) {
   c.u = 0;
   c.t = 0;
-  cursor_seek(p, P, c, P.b0);
+  cursor_seek<kRec>(p, P, c, P.b0);
 }
 
 __device__ __forceinline__ bool cursor_first(const Cursor& c) { return c.k == c.lo; }
 __device__ __forceinline__ bool cursor_last(const Cursor& c) { return c.k == c.hi - 1; }
 
+template <bool kRec>
 __device__ __forceinline__ void cursor_next(const DecodeParams& p, const Part& P, Cursor& c) {
   ++c.t;
   if (++c.k == c.hi) {
     ++c.u;
-    cursor_seek(p, P, c, c.b + 1);
+    cursor_seek<kRec>(p, P, c, c.b + 1);
   }
 }
 
@@ -248,9 +263,14 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
 
 // Page ids of 32 consecutive pages of unit c.b starting at `base`, one per lane
 // (0 past the partition's range; ids outside the pool are reported and read as 0).
+template <bool kRec>
 __device__ __forceinline__ int load_page_window(const DecodeParams& p, const Cursor& c, int base, int lane) {
   const int kk = base + lane;
   int pg = 0;
+  if constexpr (kRec) {
+    // packed selection: the unit's tiles are consecutive pages of the packed records
+    if (p.packed_mask != nullptr) return kk < c.hi ? c.b * ((p.topk + kT - 1) / kT) + kk : 0;
+  }
   if (kk < c.hi) {
     pg = kk < p.max_pages ? p.block_table[static_cast<size_t>(c.b) * p.max_pages + kk] : -1;
     if (pg < 0 || pg >= p.num_pages) {
@@ -556,7 +576,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     const bool is_k = (warp == kWarpK);
     const uint64_t pol_kv = policy_evict_first();
     Cursor c;
-    cursor_init(p, P, c);
+    cursor_init<kFp8>(p, P, c);
     bool ok = true;
     uint32_t k_issued[kKSlots] = {}, v_issued[kVSlots] = {};
     uint32_t own_k = 0;
@@ -568,7 +588,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         if (c.b != cur_b || c.k - page_base >= 32) {
           cur_b = c.b;
           page_base = c.k;
-          page_reg = load_page_window(p, c, page_base, lane);
+          page_reg = load_page_window<kFp8>(p, c, page_base, lane);
         }
         const int page = __shfl_sync(0xffffffffu, page_reg, c.k - page_base);
         if (lane == 0) {
@@ -635,7 +655,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       if (is_k && mine) ++own_k;
-      cursor_next(p, P, c);
+      cursor_next<kFp8>(p, P, c);
     }
     if (lane == 0) {
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
@@ -658,7 +678,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     if constexpr (kFp8) {
       const uint32_t cw = static_cast<uint32_t>(warp - kWarpConv);
       Cursor c;
-      cursor_init(p, P, c);
+      cursor_init<kFp8>(p, P, c);
       bool ok = true;
       uint32_t own_k = 0;
       while (ok && c.valid) {
@@ -698,7 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[V_FULL + s]);
         }
-        cursor_next(p, P, c);
+        cursor_next<kFp8>(p, P, c);
       }
       if (!ok && lane == 0) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
     }
@@ -714,7 +734,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       // is refilled with box j + 3 once the Q K^T thread has copied box j.
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
-      cursor_init(p, P, c);
+      cursor_init<kFp8>(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {};
       const auto q_load = [&](int b, int j) {  // lane 0
@@ -749,7 +769,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         }
         c.t += static_cast<uint32_t>(c.hi - c.k);
         ++c.u;
-        cursor_seek(p, P, c, c.b + 1);
+        cursor_seek<kFp8>(p, P, c, c.b + 1);
         if (ok && c.valid && lane == 0)
           for (int j = 0; j < 9; ++j) tma_prefetch_2d(&q_map, 64 * j, c.b * p.rows + rb * kRowsPerBlock);
       }
@@ -765,7 +785,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       // all nine at once.  Later units: box j through slot j % 3 as below.
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
-      cursor_init(p, P, c);
+      cursor_init<kFp8>(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {}, vq_issued = 0;
       // box j of unit b into dst; into L2 only when bar is null
@@ -811,7 +831,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // on to the next unit; its Q into L2 while this one is worked on
         c.t += static_cast<uint32_t>(c.hi - c.k);
         ++c.u;
-        cursor_seek(p, P, c, c.b + 1);
+        cursor_seek<kFp8>(p, P, c, c.b + 1);
         if (ok && c.valid)
           for (int j = 0; j < 9; ++j) q_box(c.b, j, nullptr, nullptr);
       }
@@ -823,7 +843,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     } else if (lane == 0) {
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
-      cursor_init(p, P, c);
+      cursor_init<kFp8>(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {};
       // box j of unit b into slot j % 3; into L2 only when bar is null
@@ -860,7 +880,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // on to the next unit; its Q into L2 while this one is worked on
         c.t += static_cast<uint32_t>(c.hi - c.k);
         ++c.u;
-        cursor_seek(p, P, c, c.b + 1);
+        cursor_seek<kFp8>(p, P, c, c.b + 1);
         if (ok && c.valid)
           for (int j = 0; j < 9; ++j) q_box(c.b, j, nullptr);
       }
@@ -882,7 +902,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       const uint64_t precv_desc = sdesc_sw128(smem_u32(sPRecv), 16, 1024);
       const uint16_t peer_mask = static_cast<uint16_t>(1u << peer);
       Cursor cv;
-      cursor_init(p, P, cv);
+      cursor_init<kFp8>(p, P, cv);
       uint32_t pv_own = 0, pv_recv = 0;
       bool ok = true;
       uint64_t t_last = globaltimer_ns();
@@ -920,7 +940,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
             }
             if (cursor_last(cv)) umma_commit(&bars[O_FULL]);
             MLA_TRACE(16, cv.t);
-            cursor_next(p, P, cv);
+            cursor_next<kFp8>(p, P, cv);
             progressed = true;
           }
         }
@@ -952,7 +972,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       // issues at most one job: a landed Q box's copies into TMEM, else the
       // next Q K^T half.
       Cursor cq;
-      cursor_init(p, P, cq);
+      cursor_init<kFp8>(p, P, cq);
       uint32_t a_own = 0;
       int q_phase = 0;          // 0: next is QKa of cq, 1: next is QKb of cq
       uint32_t qb_seen = 0;     // Q boxes seen landed (nine per unit, in order)
@@ -970,7 +990,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
               if (qb_seen < 9u * static_cast<uint32_t>(cq.u + 1)) return false;
               umma_commit(&bars[Q_EMPTY]);
             }
-            cursor_next(p, P, cq);
+            cursor_next<kFp8>(p, P, cq);
             q_phase = 0;
             continue;
           }
@@ -1092,7 +1112,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     const uint32_t peer_l_full = mapa_shared(smem_u32(&bars[L_FULL]), peer);
     const uint32_t peer_l_free = mapa_shared(smem_u32(&bars[L_FREE]), peer);
     Cursor c;
-    cursor_init(p, P, c);
+    cursor_init<kFp8>(p, P, c);
     bool ok = true;
     uint32_t own_i = 0, recv_i = 0, units = 0;
     float r_cur = -INFINITY;  // reference (log2 units) after the last tile seen
@@ -1111,6 +1131,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // ---- own tile: scores, reference, P
         const int jmax = p.causal ? (c.L - p.s_q + tok) : (c.L - 1);  // last visible key
         const int vis = jmax - c.k * kT;                                // keys 0..vis of this tile are visible
+        uint64_t pmask = ~0ull;  // packed selection: the tile's valid slots (read before the wait)
+        if constexpr (kFp8) {
+          if (p.packed_mask != nullptr) pmask = p.packed_mask[static_cast<size_t>(c.b) * ((p.topk + kT - 1) / kT) + c.k];
+        }
         ok = warp_wait(&bars[S_FULL], own_i & 1, abort_flag);
         if (!ok) break;
         if (tid == 0) MLA_TRACE(4, t);
@@ -1130,6 +1154,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
 #pragma unroll
           for (int j = 0; j < kT; ++j)
             if (j > vis) s[j] = -INFINITY;
+        }
+        if constexpr (kFp8) {
+          if (pmask != ~0ull) {
+#pragma unroll
+            for (int j = 0; j < kT; ++j)
+              if (!((pmask >> j) & 1ull)) s[j] = -INFINITY;
+          }
         }
         float mx[8];
 #pragma unroll
@@ -1220,7 +1251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         ++recv_i;
       }
       const int b_here = c.b, u_here = c.u;
-      cursor_next(p, P, c);
+      cursor_next<kFp8>(p, P, c);
       if (!last) continue;
       // ---- row sum of the unit: ours + the peer's, both relative to r_cur
       if (units >= 1) {

@@ -1,7 +1,8 @@
 """Packed selected-KV path on the GPU (FlashMLA PR #200, sections "SM90
 packing kernel" and "Packed attention specialization"): the pack against the
-oracle's byte-for-byte gather, the packed attention against the oracle, and
-the packed result against the native sparse call under the same plan."""
+oracle's byte-for-byte gather, the packed attention (the dense kernel over
+the packed records) against the oracle, and the packed result against the
+native sparse call under the same plan."""
 
 import numpy as np
 import pytest
@@ -80,7 +81,10 @@ def test_packed_decode_matches_oracle(h_q, topk, s_q):
 
 
 @pytest.mark.parametrize("num_parts", [1, 7, None])
-def test_packed_equals_native_under_the_same_plan(num_parts):
+def test_packed_agrees_with_native_under_the_same_plan(num_parts):
+    """The packed attention runs the dense kernel on fp16(code * scale) keys,
+    the native sparse kernel keeps the scores exact: the two agree within the
+    same bars as each does with the oracle."""
     case, ind = case_with_holes(3, 1, 128, 384, 16, [[384], [200], [1]], seed=41)
     got, st = gpu_pack(case, ind)
     assert st == 0
@@ -93,7 +97,7 @@ def test_packed_equals_native_under_the_same_plan(num_parts):
                                   pl.split_offset, pl.num_parts, pl.workspace, out_n, lse_n, status, case.scale)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    assert torch.equal(out_p, out_n) and torch.equal(lse_p, lse_n)
+    compare(out_p, lse_p, out_n.double().cpu().numpy(), lse_n.double().cpu().numpy())
 
 
 def test_packed_full_size_workload():
