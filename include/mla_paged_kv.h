@@ -90,7 +90,10 @@ int mla_num_parts(int rows_per_unit, int is_sparse_fp8);
 int mla_num_parts_dense(int s_q, int h_q, int h_kv);
 
 /* Bytes of split workspace needed: (n_units + num_parts) split slots, each
- * rows_per_unit x 512 fp32 partial outputs plus rows_per_unit fp32 LSEs.
+ * rows_per_unit x 512 fp32 partial outputs plus rows_per_unit fp32 LSEs,
+ * then n_units x rows_per_unit x 576 fp16 values (the fp16 copy of Q that
+ * the FP8-record calls make once per call; other calls leave it unused),
+ * each region starting on a 256-byte boundary.
  * n_units: dense = batch, sparse = batch*s_q. */
 size_t mla_workspace_bytes(int n_units, int rows_per_unit, int num_parts);
 
@@ -147,7 +150,9 @@ int mla_get_metadata_request_local(const int32_t* d_lengths, int default_length,
  *                  block_table[b][j/64].  The kernel turns each NoPE value
  *                  into fp16(code * scale) (relative error <= 2^-11 + 2^-20
  *                  inside fp16's normal range) and q and the RoPE dims into
- *                  fp16 (exact inside that range), then runs the fp16 path:
+ *                  fp16 (exact inside that range; q's fp16 copy is written
+ *                  to the workspace by a kernel launched just before the
+ *                  decode), then runs the fp16 path:
  *                  a score moves by at most scale * (2^-11 + 2^-20) *
  *                  sum_d |q_d k_d|.  Values must lie inside fp16's range.
  *                  mla_dense_fp8_decode_fwd keeps the scores exact in the
@@ -197,7 +202,7 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
  *  - Returns MLA_ERR_UNSUPPORTED, before any launch, when
  *    mla_workspace_bytes(batch, s_q*h_q, num_parts) exceeds
  *    MLA_STATIC_WORKSPACE_BYTES (64 requests x 128 heads with 76 parts need
- *    36.8 MB and fit).
+ *    46.2 MB and fit).
  *  - The first call on a device looks up the array's device address there
  *    (cudaGetSymbolAddress with that device current) and caches it; make
  *    that first call on each device before beginning any stream capture.

@@ -15,6 +15,7 @@
 namespace mla {
 cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, int, cudaStream_t);
 cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, int, void*, int, float*, cudaStream_t);
+cudaError_t launch_q_fp16(const void*, void*, size_t, int, cudaStream_t);
 cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                          const DecodeParams&, int, int, cudaStream_t);
 int dense_smem_bytes();
@@ -41,6 +42,7 @@ struct DeviceInfo {
   int status = MLA_OK;
   int dense_clusters = 0;
   int sparse_clusters = 0;
+  int sms = 0;
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -106,6 +108,8 @@ const DeviceInfo& device_info() {
           cudaSuccess ||
       cudaFuncSetAttribute(dense_kernel_ptr(4), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
           cudaSuccess ||
+      cudaFuncSetAttribute(dense_kernel_ptr(5), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
+          cudaSuccess ||
       cudaFuncSetAttribute(sparse_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            sparse_smem_bytes()) != cudaSuccess) {
     cudaGetLastError();
@@ -116,7 +120,8 @@ const DeviceInfo& device_info() {
   d.dense_clusters = std::min(max_clusters(dense_kernel_ptr(0), dense_threads(0), dense_smem_bytes()),
                               max_clusters(dense_kernel_ptr(2), dense_threads(2), dense_smem_bytes()));
   d.sparse_clusters = max_clusters(sparse_kernel_ptr(), sparse_threads(), sparse_smem_bytes());
-  if (d.dense_clusters <= 0 || d.sparse_clusters <= 0) {
+  cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (d.dense_clusters <= 0 || d.sparse_clusters <= 0 || d.sms <= 0) {
     cudaGetLastError();
     d.status = MLA_ERR_CUDA;
   }
@@ -129,7 +134,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WorkspaceLayout {
-  size_t o_bytes, lse_off, total;
+  size_t o_bytes, lse_off, q16_off, total;
 };
 
 WorkspaceLayout ws_layout(int n_units, int rows, int num_parts) {
@@ -137,7 +142,9 @@ WorkspaceLayout ws_layout(int n_units, int rows, int num_parts) {
   WorkspaceLayout w;
   w.o_bytes = slots * rows * MLA_D_V * sizeof(float);
   w.lse_off = align_up(w.o_bytes, 256);
-  w.total = align_up(w.lse_off + slots * rows * sizeof(float), 256);
+  // then the fp16 copy of Q that the FP8-record calls make once per call
+  w.q16_off = align_up(w.lse_off + slots * rows * sizeof(float), 256);
+  w.total = align_up(w.q16_off + static_cast<size_t>(n_units) * rows * MLA_D_QK * 2, 256);
   return w;
 }
 
@@ -213,7 +220,8 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
                   const int32_t* seqlens, int batch, int s_q, int h_q, int h_kv, int dtype, int causal, float scale,
                   const int32_t* sched, const int32_t* split_offset, int num_parts, void* workspace,
                   size_t workspace_bytes, void* out, int out_type, float* lse, int32_t* status, DecodeParams* p,
-                  CUtensorMap* q_map, CUtensorMap* kv_map, CUtensorMap* sc_map, CUtensorMap* rope_map) {
+                  CUtensorMap* q_map, CUtensorMap* kv_map, CUtensorMap* sc_map, CUtensorMap* rope_map,
+                  void** q16) {
   if (!q || !kv || !block_table || !seqlens || !sched || !split_offset || !workspace || !out || !lse || !status)
     return MLA_ERR_INVALID_ARG;
   if (batch < 1 || s_q < 1 || h_q < 1 || h_kv < 1 || max_pages < 1 || num_pages < 1 || num_parts < 1)
@@ -243,7 +251,9 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
   if (2LL * num_parts * row_blocks > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
   const DeviceInfo& d = device_info();
   if (d.status != MLA_OK) return d.status;
-  int rc = h_kv == 1 ? encode_q_map(q_map, q, static_cast<long long>(batch) * rows)
+  // FP8 records: the kernel reads the fp16 copy of Q in the workspace
+  *q16 = dtype == MLA_DTYPE_FP8_RECORD ? static_cast<char*>(workspace) + w.q16_off : nullptr;
+  int rc = h_kv == 1 ? encode_q_map(q_map, *q16 ? *q16 : q, static_cast<long long>(batch) * rows)
                      : encode_q_map_groups(q_map, q, static_cast<long long>(batch) * s_q, h_kv, group_heads,
                                            block_tokens);
   if (rc != MLA_OK) return rc;
@@ -371,15 +381,17 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
                       void* d_out, int out_type, float* d_lse, int32_t* d_status, mla_stream_t stream) {
   DecodeParams p;
   CUtensorMap qm, km, sm, rm;
+  void* q16 = nullptr;
   const int rc = dense_prepare(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q,
                                h_kv, dtype, causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
-                               workspace_bytes, d_out, out_type, d_lse, d_status, &p, &qm, &km, &sm, &rm);
+                               workspace_bytes, d_out, out_type, d_lse, d_status, &p, &qm, &km, &sm, &rm, &q16);
   if (rc != MLA_OK) return rc;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (q16 != nullptr &&
+      launch_q_fp16(d_q, q16, static_cast<size_t>(batch) * p.rows * MLA_D_QK, device_info().sms, cs) != cudaSuccess)
+    return MLA_ERR_CUDA;
   const int kind = dtype == MLA_DTYPE_FP8_RECORD ? 2 : (dtype == MLA_DTYPE_FP16 ? 1 : 0) + (p.q_vring ? 3 : 0);
-  return launch_dense(qm, km, sm, rm, p, num_parts, kind,
-                      reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? MLA_OK
-             : MLA_ERR_CUDA;
+  return launch_dense(qm, km, sm, rm, p, num_parts, kind, cs) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* d_split_offset, int n_units,
@@ -587,13 +599,16 @@ int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size
   p.lse = d_lse;
   p.status = d_status;
   CUtensorMap qm, km, sm, rm;
-  int rc = encode_q_map(&qm, d_q, units * h_q);
+  void* q16 = static_cast<char*>(d_workspace) + w.q16_off;  // the kernel reads an fp16 copy of Q
+  int rc = encode_q_map(&qm, q16, units * h_q);
   if (rc == MLA_OK) rc = encode_fp8_record_map(&km, records, static_cast<int>(pool_pages), 0);
   if (rc == MLA_OK) rc = encode_fp8_record_map(&sm, records, static_cast<int>(pool_pages), 1);
   if (rc == MLA_OK) rc = encode_fp8_record_map(&rm, records, static_cast<int>(pool_pages), 2);
   if (rc != MLA_OK) return rc;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_dense(qm, km, sm, rm, p, num_parts, 2, cs) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_q_fp16(d_q, q16, static_cast<size_t>(units) * h_q * MLA_D_QK, d.sms, cs) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (launch_dense(qm, km, sm, rm, p, num_parts, 5, cs) != cudaSuccess) return MLA_ERR_CUDA;
   return mla_combine(d_workspace, workspace_bytes, d_split_offset, static_cast<int>(units), h_q, num_parts, d_out,
                      0, d_lse, stream);
 }

@@ -42,7 +42,9 @@
 //    still-empty V ring.)
 //  * FP8 records (instance kFp8): the producers bring each box in as raw
 //    codes and scales, three converter warps turn them into fp16 boxes in
-//    place (Q and RoPE go bf16 -> fp16), and the rest is the fp16 path.
+//    place (RoPE goes bf16 -> fp16), and the rest is the fp16 path.  Q is
+//    turned into fp16 once per call, by a small kernel launched just before
+//    (q_fp16_kernel), rather than by every CTA pair that reads it.
 //  * One tile = nine 64-dim TMA boxes of one page.  The four boxes that are
 //    this CTA's V half go to a 3-slot "V" ring for every tile (P V reads
 //    them; for its own tiles Q K^T reads them too); the other five go to a
@@ -59,6 +61,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -124,8 +128,7 @@ enum : int {
   DRAIN,
   RAW_K,                      // +slot, FP8 records: the K slot's raw bytes have landed
   RAW_V = RAW_K + kKSlots,    // +slot, FP8 records: a V slot's raw bytes have landed
-  QB_READY = RAW_V + kVSlots, // +slot, FP8 records: a landed Q box has been turned into fp16
-  VQ_FULL = QB_READY + kQSmemBoxes,  // 16-bit KV: the first unit's Q boxes 0-5 have landed in the V ring
+  VQ_FULL = RAW_V + kVSlots,  // 16-bit KV: the first unit's Q boxes 0-5 have landed in the V ring
   VQ_EMPTY,                          // ... and have been copied into TMEM: the V ring is free
   kNumBars
 };
@@ -191,22 +194,24 @@ struct Cursor {
   bool valid;
 };
 
-// Keys of unit b.  kRec (FP8-record instance) also serves packed selections
-// (FlashMLA PR #200, "Packed attention specialization"): with packed_mask set,
-// a unit is one query token, its keys the first min(topk_length, topk) slots
-// (all topk when no lengths are given).
-template <bool kRec>
+// Keys of unit b.  The packed instance (kPacked: FlashMLA PR #200, "Packed
+// attention specialization") serves packed selections: a unit is one query
+// token, its keys the first min(topk_length, topk) packed slots (all topk when
+// no lengths are given).  (A separate instance: the cursor is inlined into
+// every role, and the dense FP8-record instance ran measurably slower with
+// both forms compiled in.)
+template <bool kPacked>
 __device__ __forceinline__ int unit_keys(const DecodeParams& p, int b) {
-  if constexpr (kRec) {
-    if (p.packed_mask != nullptr) return min(p.lengths != nullptr ? max(p.lengths[b], 0) : p.default_length, p.topk);
-  }
-  return max(p.lengths[b], 0);
+  if constexpr (kPacked)
+    return min(p.lengths != nullptr ? max(p.lengths[b], 0) : p.default_length, p.topk);
+  else
+    return max(p.lengths[b], 0);
 }
 
-template <bool kRec>
+template <bool kPacked>
 __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& P, Cursor& c, int from_b) {
   for (int b = from_b; unit_in_part(P, b, p.n_units); ++b) {
-    const int L = unit_keys<kRec>(p, b);
+    const int L = unit_keys<kPacked>(p, b);
     const int lo = (b == P.b0) ? P.t0 : 0;
     const int hi = (b == P.b1) ? P.t1 : num_tiles(L);
     if (hi > lo) {
@@ -222,22 +227,22 @@ __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& P
   c.valid = false;
 }
 
-template <bool kRec>
+template <bool kPacked>
 __device__ __forceinline__ void cursor_init(const DecodeParams& p, const Part& P, Cursor& c) {
   c.u = 0;
   c.t = 0;
-  cursor_seek<kRec>(p, P, c, P.b0);
+  cursor_seek<kPacked>(p, P, c, P.b0);
 }
 
 __device__ __forceinline__ bool cursor_first(const Cursor& c) { return c.k == c.lo; }
 __device__ __forceinline__ bool cursor_last(const Cursor& c) { return c.k == c.hi - 1; }
 
-template <bool kRec>
+template <bool kPacked>
 __device__ __forceinline__ void cursor_next(const DecodeParams& p, const Part& P, Cursor& c) {
   ++c.t;
   if (++c.k == c.hi) {
     ++c.u;
-    cursor_seek<kRec>(p, P, c, c.b + 1);
+    cursor_seek<kPacked>(p, P, c, c.b + 1);
   }
 }
 
@@ -263,14 +268,12 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
 
 // Page ids of 32 consecutive pages of unit c.b starting at `base`, one per lane
 // (0 past the partition's range; ids outside the pool are reported and read as 0).
-template <bool kRec>
+template <bool kPacked>
 __device__ __forceinline__ int load_page_window(const DecodeParams& p, const Cursor& c, int base, int lane) {
   const int kk = base + lane;
+  // packed selection: the unit's tiles are consecutive pages of the packed records
+  if constexpr (kPacked) return kk < c.hi ? c.b * ((p.topk + kT - 1) / kT) + kk : 0;
   int pg = 0;
-  if constexpr (kRec) {
-    // packed selection: the unit's tiles are consecutive pages of the packed records
-    if (p.packed_mask != nullptr) return kk < c.hi ? c.b * ((p.topk + kT - 1) / kT) + kk : 0;
-  }
   if (kk < c.hi) {
     pg = kk < p.max_pages ? p.block_table[static_cast<size_t>(c.b) * p.max_pages + kk] : -1;
     if (pg < 0 || pg >= p.num_pages) {
@@ -456,13 +459,14 @@ __device__ __forceinline__ float ref_alpha(float r_old, float r_new) {
 // turned into fp16 in shared memory (records: fp16(code * scale); Q and
 // RoPE: bf16 -> fp16).  Otherwise kv_map is the 16-bit pool and sc_map /
 // rope_map are unused.
-template <bool kHalf, bool kFp8, bool kQV>
+template <bool kHalf, bool kFp8, bool kQV, bool kPacked>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     dense_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
                         const __grid_constant__ CUtensorMap sc_map, const __grid_constant__ CUtensorMap rope_map,
                         const DecodeParams p) {
   static_assert(!kFp8 || kHalf, "FP8 records are converted to fp16");
   static_assert(!(kFp8 && kQV), "the V-ring Q stage is for 16-bit KV");
+  static_assert(!kPacked || kFp8, "packed selections are FP8 records");
   constexpr int kNThreads = kFp8 ? kThreadsFp8 : kThreads;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -499,7 +503,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     for (int i = 0; i < kQSmemBoxes; ++i) {
       mbar_init(&bars[QB_FULL + i], 1);
       mbar_init(&bars[QB_EMPTY + i], 1);
-      mbar_init(&bars[QB_READY + i], 1);
     }
     mbar_init(&bars[VQ_FULL], 1);
     mbar_init(&bars[VQ_EMPTY], 1);
@@ -576,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     const bool is_k = (warp == kWarpK);
     const uint64_t pol_kv = policy_evict_first();
     Cursor c;
-    cursor_init<kFp8>(p, P, c);
+    cursor_init<kPacked>(p, P, c);
     bool ok = true;
     uint32_t k_issued[kKSlots] = {}, v_issued[kVSlots] = {};
     uint32_t own_k = 0;
@@ -588,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         if (c.b != cur_b || c.k - page_base >= 32) {
           cur_b = c.b;
           page_base = c.k;
-          page_reg = load_page_window<kFp8>(p, c, page_base, lane);
+          page_reg = load_page_window<kPacked>(p, c, page_base, lane);
         }
         const int page = __shfl_sync(0xffffffffu, page_reg, c.k - page_base);
         if (lane == 0) {
@@ -655,7 +658,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       if (is_k && mine) ++own_k;
-      cursor_next<kFp8>(p, P, c);
+      cursor_next<kPacked>(p, P, c);
     }
     if (lane == 0) {
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
@@ -678,7 +681,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     if constexpr (kFp8) {
       const uint32_t cw = static_cast<uint32_t>(warp - kWarpConv);
       Cursor c;
-      cursor_init<kFp8>(p, P, c);
+      cursor_init<kPacked>(p, P, c);
       bool ok = true;
       uint32_t own_k = 0;
       while (ok && c.valid) {
@@ -718,7 +721,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[V_FULL + s]);
         }
-        cursor_next<kFp8>(p, P, c);
+        cursor_next<kPacked>(p, P, c);
       }
       if (!ok && lane == 0) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
     }
@@ -728,64 +731,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     // of the shared-memory Q buffer: box j goes to slot j % 3.  Boxes 0-5
     // (dims [0, 384)) are copied into TMEM by the Q K^T thread, which frees
     // the slot for box j + 3; boxes 6-8 stay until the unit's last Q K^T.
+    // FP8 records: Q is the fp16 copy written by q_fp16_kernel, the grid
+    // launched just before this one; it is complete once griddepcontrol.wait
+    // returns (every other role starts without it).
     if constexpr (kFp8) {
-      // FP8 records (h_kv = 1): the same nine boxes, but the whole warp turns
-      // each landed box into fp16 in place and then signals QB_READY; a slot
-      // is refilled with box j + 3 once the Q K^T thread has copied box j.
-      const uint64_t pol_q = policy_evict_last();
-      Cursor c;
-      cursor_init<kFp8>(p, P, c);
-      bool ok = true;
-      uint32_t qb_issued[kQSmemBoxes] = {};
-      const auto q_load = [&](int b, int j) {  // lane 0
-        const int sl = j % kQSmemBoxes;
-        mbar_arrive_expect_tx(&bars[QB_FULL + sl], q_box_bytes);
-        tma_load_2d(sQ + sl * kQBoxBytes, &q_map, &bars[QB_FULL + sl], 64 * j, b * p.rows + rb * kRowsPerBlock,
-                    pol_q);
-        ++qb_issued[sl];
-      };
-      while (ok && c.valid) {
-        if (lane == 0) {
-          if (c.u >= 1) ok = mbar_wait(&bars[Q_EMPTY], (c.u - 1) & 1, abort_flag);
-          if (ok)
-            for (int j = 0; j < kQSmemBoxes; ++j) q_load(c.b, j);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        for (int j = 0; ok && j < 9; ++j) {
-          const int sl = j % kQSmemBoxes;
-          ok = warp_wait(&bars[QB_FULL + sl], (3 * c.u + j / 3) & 1, abort_flag);
-          if (!ok) break;
-          bf16_box_to_fp16(sQ + sl * kQBoxBytes, static_cast<int>(q_box_bytes / 4), lane);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bars[QB_READY + sl]);
-            if (j + kQSmemBoxes < 9) {
-              ok = mbar_wait(&bars[QB_EMPTY + sl], (2 * c.u + j / 3) & 1, abort_flag);
-              if (ok) q_load(c.b, j + kQSmemBoxes);
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-        }
-        c.t += static_cast<uint32_t>(c.hi - c.k);
-        ++c.u;
-        cursor_seek<kFp8>(p, P, c, c.b + 1);
-        if (ok && c.valid && lane == 0)
-          for (int j = 0; j < 9; ++j) tma_prefetch_2d(&q_map, 64 * j, c.b * p.rows + rb * kRowsPerBlock);
-      }
-      if (lane == 0) {
-        if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
-        for (int sl = 0; sl < kQSmemBoxes; ++sl)
-          if (qb_issued[sl] > 0) mbar_wait(&bars[QB_FULL + sl], (qb_issued[sl] - 1) & 1, nullptr);
-      }
-    } else if (kQV && lane == 0) {
+      if (lane == 0) pdl_wait_prior_grid();
+    }
+    if (kQV && lane == 0) {
       // 16-bit KV, V-ring instance.  The first unit: boxes 0-5 go into the V
       // ring, still empty at the start (the Q K^T thread copies them into TMEM
       // and frees the ring for the V producer), boxes 6-8 into the Q slots,
       // all nine at once.  Later units: box j through slot j % 3 as below.
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
-      cursor_init<kFp8>(p, P, c);
+      cursor_init<kPacked>(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {}, vq_issued = 0;
       // box j of unit b into dst; into L2 only when bar is null
@@ -831,7 +790,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // on to the next unit; its Q into L2 while this one is worked on
         c.t += static_cast<uint32_t>(c.hi - c.k);
         ++c.u;
-        cursor_seek<kFp8>(p, P, c, c.b + 1);
+        cursor_seek<kPacked>(p, P, c, c.b + 1);
         if (ok && c.valid)
           for (int j = 0; j < 9; ++j) q_box(c.b, j, nullptr, nullptr);
       }
@@ -843,7 +802,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     } else if (lane == 0) {
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
-      cursor_init<kFp8>(p, P, c);
+      cursor_init<kPacked>(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {};
       // box j of unit b into slot j % 3; into L2 only when bar is null
@@ -880,7 +839,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // on to the next unit; its Q into L2 while this one is worked on
         c.t += static_cast<uint32_t>(c.hi - c.k);
         ++c.u;
-        cursor_seek<kFp8>(p, P, c, c.b + 1);
+        cursor_seek<kPacked>(p, P, c, c.b + 1);
         if (ok && c.valid)
           for (int j = 0; j < 9; ++j) q_box(c.b, j, nullptr);
       }
@@ -902,7 +861,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       const uint64_t precv_desc = sdesc_sw128(smem_u32(sPRecv), 16, 1024);
       const uint16_t peer_mask = static_cast<uint16_t>(1u << peer);
       Cursor cv;
-      cursor_init<kFp8>(p, P, cv);
+      cursor_init<kPacked>(p, P, cv);
       uint32_t pv_own = 0, pv_recv = 0;
       bool ok = true;
       uint64_t t_last = globaltimer_ns();
@@ -940,7 +899,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
             }
             if (cursor_last(cv)) umma_commit(&bars[O_FULL]);
             MLA_TRACE(16, cv.t);
-            cursor_next<kFp8>(p, P, cv);
+            cursor_next<kPacked>(p, P, cv);
             progressed = true;
           }
         }
@@ -972,7 +931,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       // issues at most one job: a landed Q box's copies into TMEM, else the
       // next Q K^T half.
       Cursor cq;
-      cursor_init<kFp8>(p, P, cq);
+      cursor_init<kPacked>(p, P, cq);
       uint32_t a_own = 0;
       int q_phase = 0;          // 0: next is QKa of cq, 1: next is QKb of cq
       uint32_t qb_seen = 0;     // Q boxes seen landed (nine per unit, in order)
@@ -990,7 +949,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
               if (qb_seen < 9u * static_cast<uint32_t>(cq.u + 1)) return false;
               umma_commit(&bars[Q_EMPTY]);
             }
-            cursor_next<kFp8>(p, P, cq);
+            cursor_next<kPacked>(p, P, cq);
             q_phase = 0;
             continue;
           }
@@ -1006,7 +965,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // completion of this box's slot barrier: three per unit, except one
         // (boxes 6-8) for a first unit staged in the V ring
         const uint32_t idx = !kQV ? 3u * uq + j / 3u : (uq == 0 ? 0u : 1u + 3u * (uq - 1u) + j / 3u);
-        if (!mbar_test_wait(&bars[(kFp8 ? QB_READY : QB_FULL) + sl], idx & 1u)) return false;
+        if (!mbar_test_wait(&bars[QB_FULL + sl], idx & 1u)) return false;
         if (j < 6u) {
           tc_fence_after();
 #pragma unroll
@@ -1112,7 +1071,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     const uint32_t peer_l_full = mapa_shared(smem_u32(&bars[L_FULL]), peer);
     const uint32_t peer_l_free = mapa_shared(smem_u32(&bars[L_FREE]), peer);
     Cursor c;
-    cursor_init<kFp8>(p, P, c);
+    cursor_init<kPacked>(p, P, c);
     bool ok = true;
     uint32_t own_i = 0, recv_i = 0, units = 0;
     float r_cur = -INFINITY;  // reference (log2 units) after the last tile seen
@@ -1131,10 +1090,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // ---- own tile: scores, reference, P
         const int jmax = p.causal ? (c.L - p.s_q + tok) : (c.L - 1);  // last visible key
         const int vis = jmax - c.k * kT;                                // keys 0..vis of this tile are visible
-        uint64_t pmask = ~0ull;  // packed selection: the tile's valid slots (read before the wait)
-        if constexpr (kFp8) {
-          if (p.packed_mask != nullptr) pmask = p.packed_mask[static_cast<size_t>(c.b) * ((p.topk + kT - 1) / kT) + c.k];
-        }
+        uint64_t keep = vis >= kT - 1 ? ~0ull : (vis < 0 ? 0ull : (~0ull >> (kT - 1 - vis)));
+        // packed selection: and the tile's valid slots (read before the wait)
+        if constexpr (kPacked) keep &= p.packed_mask[static_cast<size_t>(c.b) * ((p.topk + kT - 1) / kT) + c.k];
         ok = warp_wait(&bars[S_FULL], own_i & 1, abort_flag);
         if (!ok) break;
         if (tid == 0) MLA_TRACE(4, t);
@@ -1149,17 +1107,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         }
         tc_fence_before();
         mbar_arrive(&bars[S_FREE]);
-        // masked keys -> -inf; raw tile max (the scale is positive, so max commutes with it)
-        if (vis < kT - 1) {
+        // masked keys (past the last visible one, or unused packed slots) ->
+        // -inf; raw tile max (the scale is positive, so max commutes with it)
+        if (keep != ~0ull) {
+          const uint32_t klo = static_cast<uint32_t>(keep), khi = static_cast<uint32_t>(keep >> 32);
 #pragma unroll
-          for (int j = 0; j < kT; ++j)
-            if (j > vis) s[j] = -INFINITY;
-        }
-        if constexpr (kFp8) {
-          if (pmask != ~0ull) {
-#pragma unroll
-            for (int j = 0; j < kT; ++j)
-              if (!((pmask >> j) & 1ull)) s[j] = -INFINITY;
+          for (int j = 0; j < 32; ++j) {
+            if (!((klo >> j) & 1u)) s[j] = -INFINITY;
+            if (!((khi >> j) & 1u)) s[j + 32] = -INFINITY;
           }
         }
         float mx[8];
@@ -1251,7 +1206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         ++recv_i;
       }
       const int b_here = c.b, u_here = c.u;
-      cursor_next<kFp8>(p, P, c);
+      cursor_next<kPacked>(p, P, c);
       if (!last) continue;
       // ---- row sum of the unit: ours + the peer's, both relative to r_cur
       if (units >= 1) {
@@ -1368,48 +1323,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   }
 }
 
+// bf16 Q -> fp16 for the FP8-record instance, 8 values per thread and step
+// (the same rounding as the converter warps: bf16 -> fp32 exactly, then
+// round to nearest even).  It lets the dependent decode grid launch at once;
+// that grid's Q producer waits for this one to complete.
+__global__ void __launch_bounds__(256) q_fp16_kernel(const uint4* __restrict__ q, uint4* __restrict__ q16,
+                                                     size_t n_vec) {
+  pdl_launch_dependents();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_vec;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    uint4 x = q[i];
+    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+      w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    q16[i] = x;
+  }
+}
+
 }  // namespace dn
 
 int dense_smem_bytes() { return dn::kSmemBytes; }
 // kind 0: bf16, 1: fp16, 2: FP8 records (bf16 Q), 3: bf16 with the V-ring Q
-// stage, 4: fp16 with it
-int dense_threads(int kind) { return kind == 2 ? dn::kThreadsFp8 : dn::kThreads; }
+// stage, 4: fp16 with it, 5: packed FP8 records (bf16 Q)
+int dense_threads(int kind) { return kind == 2 || kind == 5 ? dn::kThreadsFp8 : dn::kThreads; }
 const void* dense_kernel_ptr(int kind) {
   switch (kind) {
-    case 1: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, false>);
-    case 2: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true, false>);
-    case 3: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, true>);
-    case 4: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, true>);
-    default: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, false>);
+    case 1: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, false, false>);
+    case 2: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true, false, false>);
+    case 3: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, true, false>);
+    case 4: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, true, false>);
+    case 5: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true, false, true>);
+    default: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, false, false>);
   }
 }
+
+namespace {
+
+template <bool kHalf, bool kFp8, bool kQV, bool kPacked>
+cudaError_t launch_instance(const CUtensorMap& q_map, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
+                            const CUtensorMap& rope_map, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kFp8 ? dn::kThreadsFp8 : dn::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = dn::kSmemBytes;
+  cfg.stream = stream;
+  // FP8 records: after q_fp16_kernel, as its programmatic dependent (the Q
+  // producer waits for it)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = kFp8 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, dn::dense_decode_kernel<kHalf, kFp8, kQV, kPacked>, q_map, kv_map, sc_map,
+                            rope_map, p);
+}
+
+}  // namespace
 
 cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
                          const CUtensorMap& rope_map, const DecodeParams& p, int num_parts, int kind,
                          cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
-  const int threads = dense_threads(kind);
   switch (kind) {
-    case 1:
-      dn::dense_decode_kernel<true, false, false><<<grid, threads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                           rope_map, p);
-      break;
-    case 2:
-      dn::dense_decode_kernel<true, true, false><<<grid, threads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                          rope_map, p);
-      break;
-    case 3:
-      dn::dense_decode_kernel<false, false, true><<<grid, threads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                           rope_map, p);
-      break;
-    case 4:
-      dn::dense_decode_kernel<true, false, true><<<grid, threads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                          rope_map, p);
-      break;
-    default:
-      dn::dense_decode_kernel<false, false, false><<<grid, threads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                            rope_map, p);
+    case 1: return launch_instance<true, false, false, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    case 2: return launch_instance<true, true, false, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    case 3: return launch_instance<false, false, true, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    case 4: return launch_instance<true, false, true, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    case 5: return launch_instance<true, true, false, true>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    default: return launch_instance<false, false, false, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
   }
+}
+
+cudaError_t launch_q_fp16(const void* q, void* q16, size_t elems, int sms, cudaStream_t stream) {
+  const size_t n_vec = elems / 8;  // rows of 576 values: whole vectors of 8
+  const size_t want = (n_vec + 4 * 256 - 1) / (4 * 256);
+  const int blocks = static_cast<int>(std::max<size_t>(1, std::min<size_t>(want, 2 * static_cast<size_t>(sms))));
+  dn::q_fp16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(q), static_cast<uint4*>(q16), n_vec);
   return cudaGetLastError();
 }
 

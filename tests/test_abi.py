@@ -63,7 +63,9 @@ def test_host_validation_without_gpu(lib_path):
     lib.mla_workspace_bytes.restype = ctypes.c_size_t
     lib.mla_workspace_bytes.argtypes = [ctypes.c_int] * 3
     # (n_units + num_parts) slots x rows x (512 + 1) fp32, 256-byte aligned pieces
-    assert lib.mla_workspace_bytes(64, 128, 76) == (64 + 76) * 128 * 512 * 4 + (64 + 76) * 128 * 4
+    # split slots (fp32 O, fp32 LSE), then the fp16 copy of Q: 36,771,840 + 9,437,184 bytes
+    assert lib.mla_workspace_bytes(64, 128, 76) == (64 + 76) * 128 * 512 * 4 + (64 + 76) * 128 * 4 + 64 * 128 * 576 * 2
+    assert lib.mla_workspace_bytes(1, 3, 1) == 2 * 3 * 2048 + 256 + 3 * 1152 + 128  # each region 256-aligned
     assert lib.mla_workspace_bytes(0, 0, 1) == 0
     null = ctypes.c_void_p(0)
     lib.mla_get_metadata.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
