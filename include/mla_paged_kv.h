@@ -228,7 +228,10 @@ int mla_decode_fwd_static_ws(const void* d_q, const void* d_kv, const int32_t* d
  *   d_out [n_units, rows_per_unit, 512] of out_type (MLA_DTYPE_BF16, _FP32 or
  *   _FP16), d_lse [n_units, rows].
  * Launched with programmatic dependent launch: it may start before the
- * previous kernel on the stream ends and waits for it on the device. */
+ * previous kernel on the stream ends and waits for it on the device before
+ * reading the workspace; d_split_offset it reads before that wait, so it
+ * must not be written by the kernel launched just before this call (the
+ * plan from mla_get_metadata is ready long before). */
 int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* d_split_offset, int n_units,
                 int rows_per_unit, int num_parts, void* d_out, int out_type, float* d_lse, mla_stream_t stream);
 

@@ -53,16 +53,19 @@ __device__ __forceinline__ void acc4(float4& a, float w, const float4& v) {
 // several times over; 1 -> a warp covers a 128-column quarter (a block = 1
 // row), 4x the warps for fewer rows.  Few rows with many splits per unit
 // (long context) go to combine_split_kernel instead.
-// Split weights are computed with the lanes spread over the splits and
-// broadcast by shuffle; the partial rows of kBatch splits are loaded before
-// any is summed.
+// Latency: split_offset comes from the plan (complete before the attention
+// grid started), so it is read before waiting for that grid.  After the wait
+// the split LSEs are loaded with the lanes spread over the splits; quarter-row
+// warps (kVec = 1) also load the partial rows of their first kBatch splits in
+// the same round trip (for whole-row warps that batch is 16 float4 a lane,
+// and the registers it takes cost more occupancy than the round trip saves).
 template <int kVec>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const float* __restrict__ o_accum, const float* __restrict__ lse_accum,
                    const int32_t* __restrict__ split_offset, int rows, void* __restrict__ out, int out_type,
                    float* __restrict__ lse) {
   constexpr int kBatch = kVec == 4 ? 4 : 8;
-  pdl_wait_prior_grid();
+  constexpr int kPre = kVec == 1 ? kBatch : 0;  // partial rows loaded with the LSEs
   const int unit = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = kVec == 4 ? blockIdx.x * kCombineWarps + warp : blockIdx.x;
@@ -70,12 +73,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   const int s0 = split_offset[unit];
   const int n = split_offset[unit + 1] - s0;
   if (n == 1) return;  // written directly by the attention kernel
+  pdl_wait_prior_grid();
   const size_t orow = static_cast<size_t>(unit) * rows + row;
   const size_t col = (kVec == 4 ? 0 : static_cast<size_t>(warp) * 128) + lane * 4;
   const bool writes_lse = kVec == 4 ? lane == 0 : (warp == 0 && lane == 0);
+  const size_t split_stride = static_cast<size_t>(rows) * kDv / 4;  // float4 between consecutive splits
+  const float4* src0 = reinterpret_cast<const float4*>(o_accum + (static_cast<size_t>(s0) * rows + row) * kDv + col);
 
-  float m = -INFINITY;
-  for (int s = lane; s < n; s += 32) m = fmaxf(m, lse_accum[static_cast<size_t>(s0 + s) * rows + row]);
+  // the first 32 LSEs (and the first kPre splits' rows), all in flight at once
+  const float l0 = lane < n ? lse_accum[static_cast<size_t>(s0 + lane) * rows + row] : -INFINITY;
+  const int first = min(n, kPre);
+  float4 v0[kPre > 0 ? kPre : 1][kVec];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i)
+#pragma unroll
+    for (int k = 0; k < kVec; ++k)
+      v0[i][k] = i < first ? __ldg(src0 + static_cast<size_t>(i) * split_stride + 32 * k)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+  float m = l0;
+  for (int s = 32 + lane; s < n; s += 32) m = fmaxf(m, lse_accum[static_cast<size_t>(s0 + s) * rows + row]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if (n <= 0 || m == -INFINITY) {
@@ -84,8 +100,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     if (writes_lse) lse[orow] = -INFINITY;
     return;
   }
-  float z = 0.f;
-  for (int s = lane; s < n; s += 32) {
+  float z = (l0 == -INFINITY) ? 0.f : expf(l0 - m);
+  for (int s = 32 + lane; s < n; s += 32) {
     const float l = lse_accum[static_cast<size_t>(s0 + s) * rows + row];
     z += (l == -INFINITY) ? 0.f : expf(l - m);
   }
@@ -93,17 +109,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
   const float inv_z = 1.f / z;
 
-  const size_t split_stride = static_cast<size_t>(rows) * kDv / 4;  // float4 between consecutive splits
   float4 acc[kVec];
 #pragma unroll
   for (int k = 0; k < kVec; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  {
+    const float w = (l0 == -INFINITY) ? 0.f : expf(l0 - m) * inv_z;
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+      const float wj = __shfl_sync(0xffffffffu, w, i);
+      if (i < first)
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) acc4(acc[k], wj, v0[i][k]);
+    }
+  }
   for (int c0 = 0; c0 < n; c0 += 32) {
     const int cnt = min(32, n - c0);
     const float l = lane < cnt ? lse_accum[static_cast<size_t>(s0 + c0 + lane) * rows + row] : -INFINITY;
     const float w = (l == -INFINITY) ? 0.f : expf(l - m) * inv_z;
-    const float4* src = reinterpret_cast<const float4*>(o_accum + (static_cast<size_t>(s0 + c0) * rows + row) * kDv +
-                                                        col);
-    int j = 0;
+    const float4* src = src0 + static_cast<size_t>(c0) * split_stride;
+    int j = c0 == 0 ? first : 0;  // the first batch is already summed
     for (; j + kBatch <= cnt; j += kBatch) {
       float4 v[kBatch][kVec];
 #pragma unroll
@@ -142,14 +166,14 @@ __global__ void __launch_bounds__(kSubsets * 32)
                          float* __restrict__ lse) {
   constexpr int kBatch = 4;
   __shared__ float4 part[kSubsets][32];
-  pdl_wait_prior_grid();
   const int unit = blockIdx.y;
   const int row = blockIdx.x >> 2, quarter = blockIdx.x & 3;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (row >= rows) return;  // uniform over the block
-  const int s0 = split_offset[unit];
+  const int s0 = split_offset[unit];  // from the plan: read before the wait
   const int n = split_offset[unit + 1] - s0;
   if (n == 1) return;  // written directly by the attention kernel
+  pdl_wait_prior_grid();
   const size_t orow = static_cast<size_t>(unit) * rows + row;
   const size_t col = static_cast<size_t>(quarter) * 128 + lane * 4;
 
