@@ -808,12 +808,24 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ k
   __syncthreads();
   if (tid == 0) masks[static_cast<size_t>(unit) * tiles + tile] = s_half[0] | (static_cast<uint64_t>(s_half[1]) << 32);
   uint4* dst = reinterpret_cast<uint4*>(packed + (static_cast<size_t>(unit) * tiles + tile) * kT * MLA_RECORD_BYTES);
-  for (int c = tid; c < kT * kChunks; c += 256) {
-    const int key = c / kChunks, part = c - kChunks * (c / kChunks);
-    const int idx = s_idx[key];
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (idx >= 0) v = __ldg(reinterpret_cast<const uint4*>(kv8 + static_cast<size_t>(idx) * MLA_RECORD_BYTES) + part);
-    dst[c] = v;
+  // every piece a thread moves is loaded before any is stored: one round trip
+  // to the pool per block rather than one per piece
+  constexpr int kPer = (kT * kChunks + 255) / 256;  // 11
+  uint4 v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int c = tid + 256 * i;
+    v[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (c < kT * kChunks) {
+      const int key = c / kChunks, part = c - kChunks * key;
+      const int idx = s_idx[key];
+      if (idx >= 0) v[i] = __ldg(reinterpret_cast<const uint4*>(kv8 + static_cast<size_t>(idx) * MLA_RECORD_BYTES) + part);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int c = tid + 256 * i;
+    if (c < kT * kChunks) dst[c] = v[i];
   }
 }
 
