@@ -107,9 +107,13 @@ size_t mla_workspace_bytes(int n_units, int rows_per_unit, int num_parts);
  *               (begin_unit, begin_tile, end_unit, end_tile, begin_split, 0,0,0)
  *               over 64-key tiles.
  *   d_split_offset int32 [n_units + 1] out: prefix sum of splits per unit.
- * The plan: cost(unit) = tiles + MLA_SPLIT_FIXED_COST; partitions take
- * consecutive (unit, tile) ranges of at most ceil(total/num_parts) +
- * MLA_SPLIT_FIXED_COST cost; the last one takes the rest.  One thread block. */
+ * The plan: cost(unit) = tiles + F (F = MLA_SPLIT_FIXED_COST); partitions
+ * take consecutive (unit, tile) ranges of at most `cap` cost (whole units
+ * while remaining + F fits, then budget - F tiles of the next one); the last
+ * one takes the rest.  With c0 = ceil(total cost / num_parts), cap is the
+ * smallest value in c0 .. c0 + F that leaves the last partition at most cap;
+ * c0 + F if none does, or when n_units > 4096 or num_parts > 128 (the
+ * candidates walk at once, one warp each).  One thread block. */
 int mla_get_metadata(const int32_t* d_lengths, int default_length, int n_units, int num_parts,
                      int32_t* d_sched, int32_t* d_split_offset, mla_stream_t stream);
 

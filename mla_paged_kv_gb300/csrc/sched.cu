@@ -6,9 +6,12 @@
 // the number of partitions by the CTAs that fit; every extra partition costs
 // a Q reload, a prologue/epilogue and a combine row.  This kernel implements
 // this library's plan (documented in include/mla_paged_kv.h):
-//   cost(unit) = tiles(unit) + F,  cap = ceil(sum cost / P) + F,
+//   cost(unit) = tiles(unit) + F,  c0 = ceil(sum cost / P),
 // partitions take consecutive (unit, tile) ranges within their cap, the last
-// partition takes what is left.
+// partition takes what is left; cap is the smallest value in c0 .. c0 + F
+// whose walk leaves the last partition at most cap (c0 + F if none does, or
+// for more than kSchedMaxSmemUnits units or kSchedSearchParts partitions).  c0 + F alone often finishes the
+// walk early and leaves the last partitions without work.
 //
 // One block.  The tile counts and the total cost come from all threads; the
 // greedy walk over the partitions is sequential (one thread, O(units +
@@ -21,6 +24,18 @@ namespace mla {
 
 constexpr int kSchedThreads = 256;
 constexpr int kSchedMaxSmemUnits = 4096;
+constexpr int kSchedSearchParts = 128;  // partitions the cap search handles (more: no search)
+constexpr int kSchedSearchCaps = MLA_SPLIT_FIXED_COST + 1;  // candidate caps c0 .. c0 + F, one warp each
+static_assert(kSchedSearchCaps <= kSchedThreads / 32, "one warp per candidate cap");
+
+// Shared memory of the cap search: each candidate's partition ends, the
+// chosen one's begins and last units, and each candidate's leftover cost.
+struct SchedSearch {
+  int2 end[kSchedSearchCaps * kSchedSearchParts];
+  int2 begin[kSchedSearchParts];
+  int last[kSchedSearchParts];
+  long long left[kSchedSearchCaps];
+};
 
 // Exclusive scan of one int per thread over the block; *total gets the sum.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
@@ -104,6 +119,50 @@ __device__ __forceinline__ void sched_walk(NtOf nt_of, int* diff, int n_units, i
   }
 }
 
+// The greedy walk with budget cap, recording where each partition ends,
+// (unit, tile), in end[p] (one thread; the same steps as sched_walk).  A
+// partition begins where the previous one ended, past units without tiles.
+// Returns the cost left for the last partition after partitions 0 .. P-2.
+__device__ __forceinline__ long long sched_walk_record(const int* nt_of, int n_units, int num_parts, int fixed_cost,
+                                                       int cap, int2* end) {
+  int b = 0, t = 0;
+  long long left = 0;
+  for (int p = 0; p < num_parts; ++p) {
+    while (b < n_units && nt_of[b] == 0) {
+      ++b;
+      t = 0;
+    }
+    if (p == num_parts - 1) {
+      for (int u = b; u < n_units; ++u)
+        if (nt_of[u] > 0) left += nt_of[u] - (u == b ? t : 0) + fixed_cost;
+      b = n_units;
+      t = 0;
+    } else {
+      int budget = cap;
+      while (b < n_units) {
+        const int nt = nt_of[b];
+        if (nt == 0) {
+          ++b;
+          t = 0;
+          continue;
+        }
+        const int rem = nt - t;
+        if (rem + fixed_cost <= budget) {
+          budget -= rem + fixed_cost;
+          ++b;
+          t = 0;
+        } else {
+          const int take = budget - fixed_cost;
+          if (take > 0) t += take;
+          break;
+        }
+      }
+    }
+    end[p] = make_int2(b, t);
+  }
+  return left;
+}
+
 // Tile count of unit u straight from the lengths (for the many-units path).
 struct NtFromLengths {
   const int32_t* lengths;
@@ -117,7 +176,7 @@ struct NtFromLengths {
 // the tile counts and the split-count difference array in shared memory.
 __device__ void plan_native(const int32_t* __restrict__ lengths, int default_length, int n_units, int num_parts,
                             int fixed_cost, int32_t* __restrict__ sched, int32_t* __restrict__ split_offset,
-                            int* s_nt, int* s_diff, long long* s_warp_cost, int* s_warp) {
+                            int* s_nt, int* s_diff, long long* s_warp_cost, int* s_warp, SchedSearch* s) {
   const bool in_smem = n_units <= kSchedMaxSmemUnits;
   // difference array of the per-unit split counts: shared memory, or the
   // output array itself when there are too many units
@@ -137,16 +196,66 @@ __device__ void plan_native(const int32_t* __restrict__ lengths, int default_len
   if ((threadIdx.x & 31) == 0) s_warp_cost[threadIdx.x >> 5] = part;
   __syncthreads();
 
-  if (threadIdx.x == 0) {
-    long long total = 0;
-    for (int w = 0; w < kSchedThreads / 32; ++w) total += s_warp_cost[w];
-    const long long cap = total > 0 ? (total + num_parts - 1) / num_parts + fixed_cost : 0;
-    if (in_smem && cap < (1LL << 30))
-      sched_walk<int, int*>(s_nt, s_diff, n_units, num_parts, fixed_cost, static_cast<int>(cap), sched);
-    else
-      sched_walk<long long>(nt_of, diff, n_units, num_parts, fixed_cost, cap, sched);
+  long long total_cost = 0;
+  for (int w = 0; w < kSchedThreads / 32; ++w) total_cost += s_warp_cost[w];
+  const long long c0 = total_cost > 0 ? (total_cost + num_parts - 1) / num_parts : 0;
+  // Cap search: candidate caps c0 .. c0 + F walk at once, one per warp, each
+  // recording its partition bounds; the smallest cap that leaves the last
+  // partition at most itself wins (else c0 + F), and the metadata is then
+  // filled in parallel from its bounds.  Needs the tile counts in shared
+  // memory, at most kSchedSearchParts partitions and F <= MLA_SPLIT_FIXED_COST.
+  const bool search = in_smem && total_cost > 0 && c0 + fixed_cost < (1LL << 30) && num_parts <= kSchedSearchParts &&
+                      fixed_cost + 1 <= kSchedSearchCaps;
+  if (!search) {
+    if (threadIdx.x == 0) {
+      const long long cap = total_cost > 0 ? c0 + fixed_cost : 0;
+      if (in_smem && cap < (1LL << 30))
+        sched_walk<int, int*>(s_nt, s_diff, n_units, num_parts, fixed_cost, static_cast<int>(cap), sched);
+      else
+        sched_walk<long long>(nt_of, diff, n_units, num_parts, fixed_cost, cap, sched);
+    }
+    __syncthreads();
+  } else {
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0 && warp <= fixed_cost)
+      s->left[warp] = sched_walk_record(s_nt, n_units, num_parts, fixed_cost, static_cast<int>(c0) + warp,
+                                        s->end + warp * kSchedSearchParts);
+    __syncthreads();
+    int w = fixed_cost;
+    for (int k = 0; k < fixed_cost; ++k)
+      if (s->left[k] <= c0 + k) {
+        w = k;
+        break;
+      }
+    const int2* end = s->end + w * kSchedSearchParts;
+    // each partition's begin and last unit (-1 when it is empty)
+    for (int p = threadIdx.x; p < num_parts; p += kSchedThreads) {
+      int b = p == 0 ? 0 : end[p - 1].x, t = p == 0 ? 0 : end[p - 1].y;
+      while (b < n_units && s_nt[b] == 0) {
+        ++b;
+        t = 0;
+      }
+      const int2 e = end[p];
+      s->begin[p] = make_int2(b, t);
+      s->last[p] = (b == e.x && t == e.y) ? -1 : min(e.y > 0 ? e.x : e.x - 1, n_units - 1);
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < num_parts; p += kSchedThreads) {
+      const int2 bg = s->begin[p], e = end[p];
+      // earlier non-empty partitions ending in this one's first unit
+      int begin_split = 0;
+      if (bg.x < n_units)
+        for (int q = 0; q < p; ++q) begin_split += s->last[q] == bg.x;
+      int4* out = reinterpret_cast<int4*>(sched + p * MLA_SCHED_INTS);
+      out[0] = make_int4(bg.x, bg.y, e.x, e.y);
+      out[1] = make_int4(begin_split, 0, 0, 0);
+      if (s->last[p] >= 0) {
+        atomicAdd(&diff[bg.x], 1);
+        atomicAdd(&diff[s->last[p] + 1], -1);
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   // each thread scans a contiguous chunk of units
   const int chunk = (n_units + kSchedThreads - 1) / kSchedThreads;
@@ -183,8 +292,9 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const int32_t* __r
   __shared__ int s_diff[kSchedMaxSmemUnits + 1];
   __shared__ long long s_warp_cost[kSchedThreads / 32];
   __shared__ int s_warp[kSchedThreads / 32];
+  __shared__ SchedSearch s_search;
   plan_native(lengths, default_length, n_units, num_parts, fixed_cost, sched, split_offset, s_nt, s_diff,
-              s_warp_cost, s_warp);
+              s_warp_cost, s_warp, &s_search);
 }
 
 // Request-local plan (FlashMLA PR #200, section "Scheduler policy", names a
@@ -208,6 +318,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_local_kernel(const int32_
   __shared__ long long s_rem[kSchedLocalMaxUnits];
   __shared__ long long s_sum[2];  // total tiles, parts given by the quotas
   __shared__ int s_active;
+  __shared__ SchedSearch s_search;
   if (n_units <= kSchedLocalMaxUnits) {
     long long tiles = 0;
     int act = 0;
@@ -243,7 +354,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_local_kernel(const int32_
   if (active == 0 || active > num_parts) {
     __syncthreads();
     plan_native(lengths, default_length, n_units, num_parts, fixed_cost, sched, split_offset, s_nt, s_diff,
-                s_warp_cost, s_warp);
+                s_warp_cost, s_warp, &s_search);
     return;
   }
   const long long total = s_sum[0];

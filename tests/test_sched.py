@@ -49,6 +49,61 @@ def test_plan_covers_every_tile_once(num_parts, F):
             assert (n == 0) == (nt[b] == 0)
 
 
+def _forced(L, num_parts, F, cap):
+    """The plan's walk with a given cap (the oracle's own walk, cap fixed)."""
+    saved = sp.choose_cap
+    sp.choose_cap = lambda nt, P, F_: cap
+    try:
+        return sp.plan(L, num_parts, F)
+    finally:
+        sp.choose_cap = saved
+
+
+@pytest.mark.parametrize("num_parts", [2, 7, 38, 76])
+def test_plan_cap_never_worse_than_the_plain_cap(num_parts):
+    """The chosen cap's plan has a largest part no costlier than the plan with
+    cap = c0 + F, and when a smaller cap is chosen the last part fits in it."""
+    rng = np.random.default_rng(num_parts + 300)
+    F = 4
+    for trial in range(30):
+        B = int(rng.integers(1, 70))
+        L = rng.integers(0, 5000, size=B).tolist()
+        nt = [-(-int(x) // 64) for x in L]
+        total = sum(n + F for n in nt if n > 0)
+        if total == 0:
+            continue
+        c0 = -(-total // num_parts)
+        cap = sp.choose_cap(nt, num_parts, F)
+        assert c0 <= cap <= c0 + F
+
+        def part_costs(sched):
+            return [cost_of(sp.part_ranges(e, L), F) for e in sched]
+        chosen = part_costs(sp.plan(L, num_parts, F)[0])
+        plain = part_costs(_forced(L, num_parts, F, c0 + F)[0])
+        assert max(chosen) <= max(plain)
+        if cap < c0 + F:
+            assert chosen[-1] <= cap
+            # and no smaller cap in the range would do: its last part overflows
+            for c in range(c0, cap):
+                assert part_costs(_forced(L, num_parts, F, c)[0])[-1] > c
+
+
+def test_plan_cap_by_hand():
+    """Requests of 2, 1, 1, 1 tiles, 4 parts, F = 4: costs 6, 5, 5, 5, total 21,
+    c0 = ceil(21 / 4) = 6.  Cap 6: part 0 takes request 0 (6, then 1 + 4 > 0
+    left), parts 1 and 2 one request each, the last part request 3 (5 <= 6):
+    cap 6 is chosen.  The plain cap c0 + F = 10 puts requests 1 and 2 in part 1
+    (5 + 5) and leaves the last part empty."""
+    L = [128, 64, 64, 64]
+    assert sp.choose_cap([2, 1, 1, 1], 4, 4) == 6
+    sched, off = sp.plan(L, 4, 4)
+    assert sched == [(0, 0, 1, 0, 0, 0, 0, 0), (1, 0, 2, 0, 0, 0, 0, 0), (2, 0, 3, 0, 0, 0, 0, 0),
+                     (3, 0, 4, 0, 0, 0, 0, 0)]
+    assert off == [0, 1, 2, 3, 4]
+    plain = _forced(L, 4, 4, 10)[0]
+    assert [cost_of(sp.part_ranges(e, L), 4) for e in plain] == [6, 10, 5, 0]
+
+
 def test_plan_single_request_long_context():
     sched, off = sp.plan([65536], 76, 4)
     rs = [sp.part_ranges(e, [65536]) for e in sched]
