@@ -63,6 +63,19 @@ def test_dense_splits_then_combine_entry_points():
     compare(out, lse, ro, rl)
 
 
+@pytest.mark.parametrize("h_q,lens", [(16, [65536] + [64] * 9),        # 160 rows: quarter-row combine
+                                        (128, [32768] + [64] * 63)])    # 8192 rows: whole-row combine
+def test_dense_combine_unit_with_many_splits(h_q, lens):
+    """One long request among short ones: its more than 32 splits go through the
+    combine's loop past the first 32 LSEs (and past the first batch of rows)."""
+    case = wl.dense_case(len(lens), 1, h_q, 0, seqlens=lens, seed=31 + h_q)
+    out, lse, pl = run_dense(case, num_parts=76)
+    so = pl.split_offset.cpu().tolist()
+    assert so[1] - so[0] > 32 and all(so[i + 1] - so[i] >= 1 for i in range(len(lens)))
+    ro, rl = dense_oracle(case)
+    compare(out, lse, ro, rl)
+
+
 @pytest.mark.parametrize("lens", [[1, 2], [64, 65], [300, 129]])
 def test_dense_causal_two_tokens(lens):
     case = wl.dense_case(len(lens), 2, 128, 0, seqlens=lens, causal=True, seed=11 + sum(lens))
