@@ -497,6 +497,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   const int grp = blk / p.blocks_per_group;  // KV head group (0 when h_kv = 1)
   const int rb = blk - grp * p.blocks_per_group;
 
+  // FP8 records: the partition, and for the producers of K, V and Q the
+  // first unit and its first 32 page ids (three dependent global reads), are
+  // read before the setup below so that their latency overlaps it.  (The
+  // 16-bit instances read them after the setup: the same change there
+  // perturbed their code and cost 3-5 us.)
+  Part P_first{};
+  Cursor c_first{};
+  int page_first = 0;
+  if constexpr (kFp8) {
+    P_first = load_part(p.sched, part_idx);
+    if (warp == kWarpK || warp == kWarpV || warp == kWarpQ) {
+      cursor_init<kPacked>(p, P_first, c_first);
+      if (warp != kWarpQ && c_first.valid) page_first = load_page_window<kPacked>(p, c_first, c_first.k, lane);
+    }
+  }
+
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(&bars[Q_EMPTY], 1);
@@ -570,7 +586,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
 
-  const Part P = load_part(p.sched, part_idx);
+  const Part P = kFp8 ? P_first : load_part(p.sched, part_idx);
   bool aborted = false;
   uint32_t r_seen = 0, l_seen = 0;  // reference / row-sum messages received (armed phases)
 
@@ -579,11 +595,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     const bool is_k = (warp == kWarpK);
     const uint64_t pol_kv = policy_evict_first();
     Cursor c;
-    cursor_init<kPacked>(p, P, c);
+    int page_reg = 0, page_base = -1, cur_b = -1;
+    if constexpr (kFp8) {
+      c = c_first;
+      page_reg = page_first;
+      page_base = c.k;
+      cur_b = c.valid ? c.b : -1;
+    } else {
+      cursor_init<kPacked>(p, P, c);
+    }
     bool ok = true;
     uint32_t k_issued[kKSlots] = {}, v_issued[kVSlots] = {};
     uint32_t own_k = 0;
-    int page_reg = 0, page_base = -1, cur_b = -1;
     while (ok && c.valid) {
       const bool mine = (c.t & 1u) == rank;
       if (!is_k || mine) {
@@ -744,7 +767,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       // all nine at once.  Later units: box j through slot j % 3 as below.
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
-      cursor_init<kPacked>(p, P, c);
+      if constexpr (kFp8)
+        c = c_first;
+      else
+        cursor_init<kPacked>(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {}, vq_issued = 0;
       // box j of unit b into dst; into L2 only when bar is null
@@ -802,7 +828,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     } else if (lane == 0) {
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
-      cursor_init<kPacked>(p, P, c);
+      if constexpr (kFp8)
+        c = c_first;
+      else
+        cursor_init<kPacked>(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {};
       // box j of unit b into slot j % 3; into L2 only when bar is null
