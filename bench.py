@@ -124,7 +124,9 @@ class ClockSampler:
 
     def __init__(self):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples; the JSON line carries their summary
+        self.path = os.path.join(os.environ.get("MLA_BENCH_OUT", os.path.join(ROOT, "bench_out")),
+                                 f"clocks_{os.getpid()}.csv")
 
     def start(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
