@@ -55,6 +55,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-other", action="store_true", help="skip timing the other named workloads")
+    ap.add_argument("--other", default="", help="comma-separated subset of the other named workloads to time")
     return ap.parse_args()
 
 
@@ -206,11 +207,11 @@ OTHER_WORKLOADS = ["dense_b1_hq16_sk256_fp32out", "dense_b1_hq64_sk65536", "dens
                    "sparse_fp8_b2_sq8_hq128_topk2048"]
 
 
-def time_other_workloads(mla, wl, timed, steps):
+def time_other_workloads(mla, wl, timed, steps, names=None):
     """µs per mla_decode_fwd / mla_sparse_fp8_decode_fwd call (L2 flushed before each) on the other workloads."""
     import torch
     res = {}
-    for name in OTHER_WORKLOADS:
+    for name in (names or OTHER_WORKLOADS):
         case = wl.make(name)
         sparse = name.startswith("sparse")
         fp8_dense = name.startswith("dense_fp8")
@@ -482,7 +483,11 @@ def main():
 
     other = None
     if world == 1 and not args.no_other:
-        other = time_other_workloads(mla, wl, timed, max(20, min(200, args.steps // 10)))
+        subset = [n for n in args.other.split(",") if n]
+        unknown = [n for n in subset if n not in OTHER_WORKLOADS]
+        if unknown:
+            raise SystemExit(f"--other: unknown workload(s) {unknown}; known: {OTHER_WORKLOADS}")
+        other = time_other_workloads(mla, wl, timed, max(20, min(200, args.steps // 10)), subset or None)
 
     if rank != 0:
         if dist is not None:
