@@ -55,17 +55,18 @@ __device__ __forceinline__ void acc4(float4& a, float w, const float4& v) {
 // (long context) go to combine_split_kernel instead.
 // Latency: split_offset comes from the plan (complete before the attention
 // grid started), so it is read before waiting for that grid.  After the wait
-// the split LSEs are loaded with the lanes spread over the splits; quarter-row
-// warps (kVec = 1) also load the partial rows of their first kBatch splits in
-// the same round trip (for whole-row warps that batch is 16 float4 a lane,
-// and the registers it takes cost more occupancy than the round trip saves).
+// the split LSEs are loaded with the lanes spread over the splits, and in the
+// same round trip the partial rows of the first kPre splits: kBatch for
+// quarter-row warps (kVec = 1), 2 for whole-row warps (the count most units
+// have when partitions slightly outnumber requests; a batch of 4 is 16 float4
+// a lane, and its registers cost more occupancy than the round trip saves).
 template <int kVec>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const float* __restrict__ o_accum, const float* __restrict__ lse_accum,
                    const int32_t* __restrict__ split_offset, int rows, void* __restrict__ out, int out_type,
                    float* __restrict__ lse) {
   constexpr int kBatch = kVec == 4 ? 4 : 8;
-  constexpr int kPre = kVec == 1 ? kBatch : 0;  // partial rows loaded with the LSEs
+  constexpr int kPre = kVec == 1 ? kBatch : 2;  // partial rows loaded with the LSEs
   const int unit = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = kVec == 4 ? blockIdx.x * kCombineWarps + warp : blockIdx.x;
