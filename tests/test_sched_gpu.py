@@ -44,6 +44,28 @@ def test_sched_kernel_matches_plan(seed, n, parts, lo, hi, zero_frac):
     assert off == ref_off
 
 
+def test_sched_kernel_cap_search_by_hand():
+    """Requests of 2, 1, 1, 1 tiles over 4 partitions (F = 4): the plan's cap is
+    c0 = 6, one request per partition (tests/test_sched.py works it out); the
+    plain cap c0 + F = 10 would leave the last partition empty."""
+    sched, off = _gpu_plan([128, 64, 64, 64], 4)
+    assert sched == [[0, 0, 1, 0, 0, 0, 0, 0], [1, 0, 2, 0, 0, 0, 0, 0], [2, 0, 3, 0, 0, 0, 0, 0],
+                     [3, 0, 4, 0, 0, 0, 0, 0]]
+    assert off == [0, 1, 2, 3, 4]
+
+
+@pytest.mark.parametrize("parts", [76, 128, 129])
+def test_sched_kernel_search_limit(parts):
+    """At most 128 partitions take the cap search; 129 take the single walk with
+    c0 + F.  Both sides apply the same limit."""
+    rng = np.random.default_rng(parts)
+    lens = rng.integers(1, 3000, size=40).tolist()
+    ref_sched, ref_off = mla_sched.plan(lens, parts, 4)
+    sched, off = _gpu_plan(lens, parts)
+    assert sched == [list(e) for e in ref_sched]
+    assert off == ref_off
+
+
 def test_sched_kernel_default_length():
     ref_sched, ref_off = mla_sched.plan([2048], 76, 4)
     sched, off = _gpu_plan(None, 76, default_length=2048)
