@@ -785,11 +785,21 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ k
                                                    const int32_t* __restrict__ indices, int topk,
                                                    const int32_t* __restrict__ topk_length, uint8_t* __restrict__ packed,
                                                    uint64_t* __restrict__ masks, int32_t* status) {
-  constexpr int kChunks = MLA_RECORD_BYTES / 16;  // 41
+  // The tile's 64 records are staged in shared memory: each valid one comes
+  // in by one bulk copy (656 bytes, 16-byte aligned at both ends), the others
+  // are zero-filled there, and the whole tile (41 984 contiguous bytes) goes
+  // out by one bulk store.
+  constexpr int kTileBytes = kT * MLA_RECORD_BYTES;
+  __shared__ __align__(128) uint8_t s_rec[kTileBytes];
+  __shared__ __align__(8) uint64_t s_bar;
   __shared__ int s_idx[kT];
   __shared__ uint32_t s_half[2];
   const int tiles = gridDim.x, tile = blockIdx.x, unit = blockIdx.y;
   const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    fence_mbar_init_cluster();
+  }
   if (tid < kT) {
     const int t = tile * kT + tid;
     const int L = topk_length != nullptr ? max(min(topk_length[unit], topk), 0) : topk;
@@ -806,26 +816,39 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ k
     if ((tid & 31) == 0) s_half[tid >> 5] = half;
   }
   __syncthreads();
-  if (tid == 0) masks[static_cast<size_t>(unit) * tiles + tile] = s_half[0] | (static_cast<uint64_t>(s_half[1]) << 32);
-  uint4* dst = reinterpret_cast<uint4*>(packed + (static_cast<size_t>(unit) * tiles + tile) * kT * MLA_RECORD_BYTES);
-  // every piece a thread moves is loaded before any is stored: one round trip
-  // to the pool per block rather than one per piece
-  constexpr int kPer = (kT * kChunks + 255) / 256;  // 11
-  uint4 v[kPer];
+  const uint64_t valid = s_half[0] | (static_cast<uint64_t>(s_half[1]) << 32);
+  if (tid == 0) masks[static_cast<size_t>(unit) * tiles + tile] = valid;
+  const uint32_t n_valid = static_cast<uint32_t>(__popcll(valid));
+  if (tid < 32) {
+    // warp 0: the transaction count first, then the copies (lanes k and k + 32)
+    if (tid == 0) mbar_arrive_expect_tx(&s_bar, n_valid * MLA_RECORD_BYTES);
+    __syncwarp();
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int c = tid + 256 * i;
-    v[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (c < kT * kChunks) {
-      const int key = c / kChunks, part = c - kChunks * key;
-      const int idx = s_idx[key];
-      if (idx >= 0) v[i] = __ldg(reinterpret_cast<const uint4*>(kv8 + static_cast<size_t>(idx) * MLA_RECORD_BYTES) + part);
+    for (int h = 0; h < 2; ++h) {
+      const int k = tid + 32 * h;
+      const int idx = s_idx[k];
+      if (idx >= 0)
+        bulk_load_g2s(smem_u32(s_rec + k * MLA_RECORD_BYTES), kv8 + static_cast<size_t>(idx) * MLA_RECORD_BYTES,
+                      MLA_RECORD_BYTES, &s_bar);
     }
   }
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int c = tid + 256 * i;
-    if (c < kT * kChunks) dst[c] = v[i];
+  // the unused slots' records are zeros (16-byte pieces, generic proxy)
+  for (int c = tid; c < kT * (MLA_RECORD_BYTES / 16); c += 256) {
+    const int key = c / (MLA_RECORD_BYTES / 16);
+    if (s_idx[key] < 0) reinterpret_cast<uint4*>(s_rec)[c] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_smem();  // the zeros are visible to the bulk store
+  __syncthreads();
+  if (tid == 0) {
+    bool ok = mbar_wait(&s_bar, 0, nullptr);
+    if (!ok) {
+      report(status, MLA_ERR_TIMEOUT);
+      ok = mbar_wait(&s_bar, 0, nullptr);  // the copies in flight, once more before leaving
+    }
+    if (ok) {
+      bulk_store_s2g(packed + (static_cast<size_t>(unit) * tiles + tile) * kTileBytes, smem_u32(s_rec), kTileBytes);
+      bulk_commit_and_wait_all();
+    }
   }
 }
 
