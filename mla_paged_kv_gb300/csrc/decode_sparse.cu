@@ -781,6 +781,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // gets its 656-byte record, every other slot 656 zero bytes; the tile's
 // 64-bit valid mask goes to `masks`.  An index outside [-1, pool) is reported
 // (MLA_ERR_BAD_INDEX) and packed as masked.
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory; completion is signalled as
+// transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_smem),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16, 16-byte aligned) from this CTA's shared
+// memory to global memory, in the thread's current bulk async-group.
+__device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(src_smem), "r"(bytes)
+               : "memory");
+}
+
+// Close the thread's bulk async-group, then wait until all its groups have
+// completed (the writes are done).
+__device__ __forceinline__ void bulk_commit_and_wait_all() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ kv8, int num_pages,
                                                    const int32_t* __restrict__ indices, int topk,
                                                    const int32_t* __restrict__ topk_length, uint8_t* __restrict__ packed,

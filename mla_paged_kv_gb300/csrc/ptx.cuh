@@ -205,31 +205,6 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint3
                : "memory");
 }
 
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
-// global memory into this CTA's shared memory; completion is signalled as
-// transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_load_g2s(uint32_t dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   dst_smem),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
-// Bulk copy of `bytes` (multiple of 16, 16-byte aligned) from this CTA's shared
-// memory to global memory, in the thread's current bulk async-group.
-__device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src_smem, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
-               "r"(src_smem), "r"(bytes)
-               : "memory");
-}
-
-// Close the thread's bulk async-group, then wait until all its groups have
-// completed (the writes are done).
-__device__ __forceinline__ void bulk_commit_and_wait_all() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
