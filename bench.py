@@ -97,6 +97,15 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bf16_peak_tflops():
+    """Burst cuBLAS bf16 TFLOP/s of MEASURED_PEAKS.json (a call is timed alone), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def source_sha():
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -200,6 +209,67 @@ def cpu_oracle_sample(case, budget_s, gpu_out=None, gpu_lse=None):
     return {"kv_bytes": kv_bytes, "seconds": t_total, "requests": done, "cores": cores, "errors": errs}
 
 
+def cpu_model():
+    """The host CPU's model name (/proc/cpuinfo; Arm hosts list an implementer/part instead)."""
+    try:
+        text = open("/proc/cpuinfo").read()
+    except OSError:
+        return None
+    for key in ("model name", "Model", "cpu model"):
+        m = re.search(rf"^{key}\s*:\s*(.+)$", text, flags=re.M)
+        if m:
+            return m.group(1).strip()
+    parts = sorted(set(re.findall(r"^CPU part\s*:\s*(\S+)", text, flags=re.M)))
+    impl = sorted(set(re.findall(r"^CPU implementer\s*:\s*(\S+)", text, flags=re.M)))
+    return f"implementer {','.join(impl)} part {','.join(parts)}" if parts else None
+
+
+_ONE_THREAD_SCRIPT = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+from mla_paged_kv_gb300 import workloads as wl
+from oracle import mla_oracle as orc
+spec = json.loads(sys.argv[2]); kind = spec.pop("kind")
+case = wl.dense_case(**spec)
+q, kv = case.q.double().numpy(), case.kv.float().numpy()
+bt, sl = case.block_table.numpy(), case.cache_seqlens.numpy()
+t0 = time.perf_counter(); n = 0; nbytes = 0
+while n < 1 or time.perf_counter() - t0 < float(sys.argv[3]):
+    b = n % case.batch
+    orc.dense_decode(q, kv, bt, sl, case.causal, case.scale, batches=[b])
+    nbytes += int(sl[b]) * 1152; n += 1
+print(json.dumps({"seconds": time.perf_counter() - t0, "kv_bytes": nbytes, "requests": n}))
+"""
+
+
+def cpu_oracle_one_thread(spec, budget_s):
+    """The same oracle in a child process with every BLAS/OpenMP pool held to one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               NUMEXPR_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    try:
+        res = subprocess.run([sys.executable, "-c", _ONE_THREAD_SCRIPT, ROOT, json.dumps(spec), str(budget_s)],
+                             capture_output=True, text=True, env=env, timeout=600)
+        r = json.loads(res.stdout.strip().splitlines()[-1])
+        return {"value": r["kv_bytes"] / r["seconds"] / 1e9, "unit": "GB/s", "cores": 1,
+                "sample": f"{r['requests']} requests, {r['seconds']:.1f} s"}
+    except Exception as e:  # the baseline is context; its absence must not stop the bench
+        return {"value": None, "error": str(e)[-200:]}
+
+
+def dense_flops(case):
+    """2 * (576 + 512) flops per (query row, visible key): Q K^T and P V."""
+    L = case.cache_seqlens.long()
+    s_q, h_q = case.s_q, case.h_q
+    vis = 0
+    for i in range(s_q):
+        vis += int((L - s_q + i + 1).clamp(min=0).sum()) if case.causal else int(L.sum())
+    return 2.0 * (576 + 512) * h_q * vis
+
+
+def stats_us(ms):
+    return {"mean": 1e3 * statistics.mean(ms), "median": 1e3 * statistics.median(ms), "min": 1e3 * min(ms)}
+
+
 OTHER_WORKLOADS = ["dense_b1_hq16_sk256_fp32out", "dense_b1_hq64_sk65536", "dense_b16_sq2causal_hq128_sk4096to8192",
                    "dense_b64_hq128_sk2048to4096_fp16", "dense_b32_hkv2_hq128_sk2048to4096",
                    "dense_fp8_b64_hq128_sk2048to4096",
@@ -249,10 +319,16 @@ def time_other_workloads(mla, wl, timed, steps, names=None):
         mla.check_status(status, name)
         us = 1e3 * statistics.mean(ms)
         nbytes = case.kv_bytes()
-        res[name] = {"us_per_call": us, "gb_per_s": nbytes / (us * 1e-6) / 1e9, "bytes_per_call": nbytes,
+        res[name] = {"us_per_call": us, "us_per_call_median": 1e3 * statistics.median(ms),
+                     "us_per_call_min": 1e3 * min(ms), "gb_per_s": nbytes / (us * 1e-6) / 1e9,
+                     "bytes_per_call": nbytes,
                      "bytes": ("valid records x 656" if sparse else "sum of cache_seqlens x 656" if fp8_dense
                                else "sum of cache_seqlens x 1152 x h_kv"),
                      "num_parts": pl.num_parts, "splits": int(pl.split_offset[-1].item())}
+        if not sparse:
+            fl = dense_flops(case)
+            res[name]["tflops"] = fl / (us * 1e-6) / 1e12
+            res[name]["pct_of_bf16_tensor_peak"] = 100.0 * res[name]["tflops"] / bf16_peak_tflops()
         if fp8_dense:
             # the exact-score path (the FP8 sparse kernel addressing the same cache by block table)
             ul = torch.empty(B * s_q, dtype=torch.int32, device="cuda")
@@ -514,11 +590,12 @@ def main():
                    "seqlen": "uniform[2048,4096]", "page_size": 64, "kv_bytes_per_step": kv_bytes,
                    "num_parts": pl.num_parts, "l2": "flushed before every timed step (512 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "us_per_call_stats": stats_us(ms),
         "kv_pct_of_hbm": 100.0 * (kv_bytes / (ms_step * 1e-3) / 1e9) / peak,
         "scheduler_us": 1e3 * sched_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_kind, "kernel": "dense_decode_kernel (split-KV attention)",
-                     "kernel_us": 1e3 * k_ms, "traffic": traffic},
+                     "kernel_us": 1e3 * k_ms, "kernel_us_stats": stats_us(ms_k), "traffic": traffic},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "e2e": e2e,
@@ -527,7 +604,9 @@ def main():
         line["workloads"] = other
     if cpu is not None:
         line["cpu_baseline"] = {"value": cpu["kv_bytes"] / cpu["seconds"] / 1e9, "unit": "GB/s",
-                                "cores": cpu["cores"], "kind": "oracle",
+                                "cores": cpu["cores"], "kind": "oracle", "cpu_model": cpu_model(),
+                                "one_thread": cpu_oracle_one_thread(dict(wl.WORKLOADS[WORKLOAD]),
+                                                                    min(10.0, args.cpu_seconds)),
                                 "sample": f"{len(cpu['requests'])} requests cycling over the {B} of the batch "
                                           f"({cpu['kv_bytes']} KV bytes), "
                                           f"fp64 numpy oracle, {cpu['seconds']:.1f} s",

@@ -25,8 +25,12 @@
  *  - Host-detectable errors are returned BEFORE anything is launched.
  *  - Errors found on the device (bad block-table entry, bad sparse index,
  *    a pipeline wait that timed out) are written to *d_status (int32, must
- *    be zeroed by the caller before the call; the first error wins).  The
- *    output of the affected request is then unspecified.
+ *    be zeroed by the caller before the call; the first error wins).  A
+ *    block-table entry or sparse index outside the pool masks the keys it
+ *    names (weight 0, as if absent) and the rest of the call is exact.
+ *    After MLA_ERR_TIMEOUT the kernel has given up part of its work: the
+ *    results of that call are unspecified and must not be used (the context
+ *    and the stream stay usable for later calls).
  *  - Layouts are row-major and contiguous.  A query "row" of request b is
  *    r = i * h_q + h for query token i < s_q and head h < h_q.
  *  - Every d_* pointer must be 16-byte aligned.
@@ -138,7 +142,10 @@ int mla_get_metadata_request_local(const int32_t* d_lengths, int default_length,
  *   d_q            [batch, s_q, h_q, 576], element type `dtype`
  *   d_kv           [num_pages, 64, h_kv, 576] paged latent cache, type `dtype`
  *                  (h_kv = 1: [num_pages, 64, 576])
- *   d_block_table  int32 [batch, max_pages]: logical page -> physical page
+ *   d_block_table  int32 [batch, max_pages]: logical page -> physical page.
+ *                  An entry outside [0, num_pages) at a position the request
+ *                  reads masks that page's 64 keys and is reported
+ *                  (MLA_ERR_BAD_INDEX).
  *   d_cache_seqlens int32 [batch]: keys of request b, including its s_q new
  *                  tokens.  Key j of request b is row j%64 of page
  *                  block_table[b][j/64].
@@ -292,10 +299,28 @@ size_t mla_packed_kv_workspace_bytes(int n_units, int topk);
  *   d_packed      16-byte aligned, >= mla_packed_kv_workspace_bytes(n_units,
  *                 topk) bytes; every byte of that size is written.
  * An index outside [-1, num_pages*64) is packed as masked and reported in
- * *d_status as MLA_ERR_BAD_INDEX (stream-ordered). */
+ * *d_status as MLA_ERR_BAD_INDEX (stream-ordered).  A tile whose record
+ * copies do not land within the wait budget is reported as MLA_ERR_TIMEOUT
+ * and gets a zero mask (its records are not written); the results of a call
+ * that reports it must not be used.
+ * MLA_ERR_UNSUPPORTED (before any launch) when num_pages * 64 exceeds
+ * 2^31 - 1 (slot indices are int32). */
 int mla_pack_selected_kv(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int topk,
                          const int32_t* d_topk_length, int n_units, void* d_packed, size_t packed_bytes,
                          int32_t* d_status, mla_stream_t stream);
+
+/* Test hook for the device timeout path (no counterpart on the pages: it
+ * exists so that a test can make a bounded wait run out on a real GPU
+ * without faulting or hanging it).  Same arguments and checks as
+ * mla_pack_selected_kv, but every block of its pack kernel withholds the
+ * arrival that completes its bulk-copy barrier: the block's 200 us bounded
+ * wait runs out, it writes MLA_ERR_TIMEOUT to *d_status and a zero mask for
+ * its tile, then makes the withheld arrival, waits (bounded) until its own
+ * copies have landed and exits without storing records.  The context and
+ * the stream stay usable; the records region is left as it was. */
+int mla_test_pack_timeout(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int topk,
+                          const int32_t* d_topk_length, int n_units, void* d_packed, size_t packed_bytes,
+                          int32_t* d_status, mla_stream_t stream);
 
 /* Sparse FP8 decode over a packed workspace (FlashMLA PR #200, "Packed
  * attention specialization"): attention of each query token over the
@@ -307,7 +332,8 @@ int mla_pack_selected_kv(const uint8_t* d_kv8, int num_pages, const int32_t* d_i
  * MLA_DTYPE_FP8_RECORD: a score moves by at most
  * scale * (2^-11 + 2^-20) * sum_d |q_d k_d| from the exact one, where
  * mla_sparse_fp8_decode_fwd keeps the scores exact.  d_topk_length must be
- * the one given to the pack (it counts the tiles each unit schedules); the
+ * the one given to the pack (it counts the tiles each unit schedules;
+ * entries above topk are allowed, only the first topk slots exist); the
  * plan comes from mla_get_metadata exactly as for the native call (the
  * pages' H=128 packed path keeps the native scheduler).  h_q <= 128.  Other
  * arguments as for mla_sparse_fp8_decode_fwd. */
@@ -351,7 +377,9 @@ int mla_dense_fp8_unit_lengths(const int32_t* d_cache_seqlens, int batch, int s_
  * k[d] = fp32(e4m3[d]) * scale[d/128] as one fp32 round-to-nearest-even
  * multiply (d < 512), k[512+e] = fp32(bf16 rope[e]).  Index -1 or an index
  * outside the pool gives a zero row (the latter also MLA_ERR_BAD_INDEX).
- *   d_indices int32 [n], d_k_out fp32 [n, 576]. */
+ *   d_indices int32 [n], d_k_out fp32 [n, 576].
+ * MLA_ERR_UNSUPPORTED (before any launch) when num_pages * 64 exceeds
+ * 2^31 - 1. */
 int mla_sparse_fp8_unpack(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int n, float* d_k_out,
                           int32_t* d_status, mla_stream_t stream);
 

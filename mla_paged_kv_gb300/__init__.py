@@ -27,7 +27,7 @@ __all__ = [
     "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws",
     "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd",
     "mla_get_metadata_request_local", "mla_num_parts_dense", "mla_dense_fp8_decode_fwd",
-    "mla_dense_fp8_unit_lengths", "plan", "decode", "dense_fp8_decode",
+    "mla_dense_fp8_unit_lengths", "mla_test_pack_timeout", "plan", "decode", "dense_fp8_decode",
     "sparse_decode", "pack_selected_kv", "packed_sparse_decode",
     "EXPORTED_SYMBOLS",
 ]
@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack",
     "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv",
     "mla_sparse_fp8_packed_decode_fwd", "mla_get_metadata_request_local", "mla_num_parts_dense",
-    "mla_dense_fp8_decode_fwd", "mla_dense_fp8_unit_lengths",
+    "mla_dense_fp8_decode_fwd", "mla_dense_fp8_unit_lengths", "mla_test_pack_timeout",
 )
 
 _P = ctypes.c_void_p
@@ -66,6 +66,7 @@ _SIGS = {
                                       _P, _P, _P]),
     "mla_packed_kv_workspace_bytes": (_SZ, [_I, _I]),
     "mla_pack_selected_kv": (_I, [_P, _I, _P, _I, _P, _I, _P, _SZ, _P, _P]),
+    "mla_test_pack_timeout": (_I, [_P, _I, _P, _I, _P, _I, _P, _SZ, _P, _P]),
     "mla_sparse_fp8_packed_decode_fwd": (_I, [_P, _P, _SZ, _I, _P, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _P, _P,
                                               _P]),
 }
@@ -286,16 +287,24 @@ def mla_packed_kv_workspace_bytes(n_units: int, topk: int) -> int:
     return int(load_library().mla_packed_kv_workspace_bytes(int(n_units), int(topk)))
 
 
-def mla_pack_selected_kv(kv8, indices, topk_length, packed, status, stream=None):
+def _pack(name, kv8, indices, topk_length, packed, status, stream):
     _need(kv8, torch.uint8, "kv8", 3)
     _need(indices, torch.int32, "indices", 3)
     if topk_length is not None:
         _need(topk_length, torch.int32, "topk_length", 2)
     _need(packed, torch.uint8, "packed")
     B, s_q, topk = indices.shape
-    _check(load_library().mla_pack_selected_kv(_ptr(kv8), kv8.shape[0], _ptr(indices), topk, _ptr(topk_length),
-                                               B * s_q, _ptr(packed), packed.numel(), _ptr(status),
-                                               _stream(stream)), "mla_pack_selected_kv")
+    _check(getattr(load_library(), name)(_ptr(kv8), kv8.shape[0], _ptr(indices), topk, _ptr(topk_length), B * s_q,
+                                         _ptr(packed), packed.numel(), _ptr(status), _stream(stream)), name)
+
+
+def mla_pack_selected_kv(kv8, indices, topk_length, packed, status, stream=None):
+    _pack("mla_pack_selected_kv", kv8, indices, topk_length, packed, status, stream)
+
+
+def mla_test_pack_timeout(kv8, indices, topk_length, packed, status, stream=None):
+    """Test hook: the pack with every block's bounded wait made to run out (MLA_ERR_TIMEOUT)."""
+    _pack("mla_test_pack_timeout", kv8, indices, topk_length, packed, status, stream)
 
 
 def mla_sparse_fp8_packed_decode_fwd(q, packed, topk, topk_length, sched, split_offset, num_parts, workspace, out,

@@ -28,7 +28,7 @@ const void* sparse_kernel_ptr();
 cudaError_t launch_unpack(const uint8_t*, int, const int32_t*, int, float*, int32_t*, cudaStream_t);
 cudaError_t launch_unit_lengths(const int32_t*, int, int, int, int32_t*, cudaStream_t);
 cudaError_t launch_pack(const uint8_t*, int, const int32_t*, int, const int32_t*, int, uint8_t*, uint64_t*,
-                        int32_t*, cudaStream_t);
+                        int32_t*, int, cudaStream_t);
 }  // namespace mla
 
 using namespace mla;
@@ -161,18 +161,24 @@ int encode_q_map(CUtensorMap* m, const void* q, long long rows) {
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
-// Dense KV pool as [num_pages][64][h_kv][576] (16-bit elements), dims listed
-// innermost first: (576, h_kv, 64, num_pages).  One box = 64 dims x 64 tokens
-// of one page and one KV head.
-int encode_kv_map(CUtensorMap* m, const void* kv, int num_pages, int h_kv) {
+// Dense KV pool as [num_pages][64][h_kv][576] (16-bit elements), viewed as
+// five dims, innermost first: (64 dims of a slice, 64 tokens, 9 slices of 64
+// dims, h_kv, num_pages).  One box = `slices` consecutive 64-dim slices of
+// the 64 tokens of one page and one KV head; it lands as `slices` 8 KB
+// 128-byte-swizzled boxes of 64 tokens x 64 dims one after another, the
+// layout the MMA descriptors read, in one TMA instruction (the TMA engine's
+// time goes mostly per instruction, so whole slice ranges per instruction
+// move several times the bytes per second of one 8 KB box each).
+int encode_kv_map(CUtensorMap* m, const void* kv, int num_pages, int h_kv, int slices) {
   auto fn = encode_fn();
   if (fn == nullptr) return MLA_ERR_CUDA;
   const cuuint64_t row = static_cast<cuuint64_t>(MLA_D_QK) * 2;
-  cuuint64_t dims[4] = {MLA_D_QK, static_cast<cuuint64_t>(h_kv), MLA_PAGE_SIZE, static_cast<cuuint64_t>(num_pages)};
-  cuuint64_t strides[3] = {row, row * h_kv, row * h_kv * MLA_PAGE_SIZE};
-  cuuint32_t box[4] = {64, 1, MLA_PAGE_SIZE, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(kv), dims, strides, box, es,
+  cuuint64_t dims[5] = {64, MLA_PAGE_SIZE, MLA_D_QK / 64, static_cast<cuuint64_t>(h_kv),
+                        static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[4] = {row * h_kv, 128, row, row * h_kv * MLA_PAGE_SIZE};
+  cuuint32_t box[5] = {64, MLA_PAGE_SIZE, static_cast<cuuint32_t>(slices), 1, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(kv), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
@@ -263,9 +269,12 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
     if (rc == MLA_OK) rc = encode_fp8_record_map(sc_map, kv, num_pages, 1);
     if (rc == MLA_OK) rc = encode_fp8_record_map(rope_map, kv, num_pages, 2);
   } else {
-    rc = encode_kv_map(kv_map, kv, num_pages, h_kv);
-    *sc_map = *kv_map;  // unused
-    *rope_map = *kv_map;
+    // 16-bit KV: the three box widths the producers load (a value half: 4
+    // slices; rank 0's K slot: slices 4-8; rank 1's RoPE slice), passed in the
+    // kernel's kv / sc / rope map parameters
+    rc = encode_kv_map(kv_map, kv, num_pages, h_kv, 4);
+    if (rc == MLA_OK) rc = encode_kv_map(sc_map, kv, num_pages, h_kv, 5);
+    if (rc == MLA_OK) rc = encode_kv_map(rope_map, kv, num_pages, h_kv, 1);
   }
   if (rc != MLA_OK) return rc;
   *p = DecodeParams{};
@@ -523,12 +532,16 @@ size_t mla_packed_kv_workspace_bytes(int n_units, int topk) {
   return static_cast<size_t>(packed_layout(n_units, topk).total);
 }
 
-int mla_pack_selected_kv(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int topk,
-                         const int32_t* d_topk_length, int n_units, void* d_packed, size_t packed_bytes,
-                         int32_t* d_status, mla_stream_t stream) {
+namespace {
+
+int pack_selected(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int topk,
+                  const int32_t* d_topk_length, int n_units, void* d_packed, size_t packed_bytes, int32_t* d_status,
+                  int stall_test, mla_stream_t stream) {
   if (!d_kv8 || !d_indices || !d_packed || !d_status) return MLA_ERR_INVALID_ARG;
   if (num_pages < 1 || topk < 1 || n_units < 0) return MLA_ERR_INVALID_ARG;
   if (n_units > 65535) return MLA_ERR_UNSUPPORTED;
+  // slot indices are 32-bit: the pool's slots must fit
+  if (static_cast<long long>(num_pages) * MLA_PAGE_SIZE > (1LL << 31) - 1) return MLA_ERR_UNSUPPORTED;
   if (!aligned16(d_kv8) || !aligned16(d_packed)) return MLA_ERR_INVALID_ARG;
   const PackedLayout l = packed_layout(n_units, topk);
   if (packed_bytes < static_cast<size_t>(l.total)) return MLA_ERR_INVALID_ARG;
@@ -536,9 +549,25 @@ int mla_pack_selected_kv(const uint8_t* d_kv8, int num_pages, const int32_t* d_i
   uint8_t* records = static_cast<uint8_t*>(d_packed);
   uint64_t* masks = reinterpret_cast<uint64_t*>(records + l.records_bytes);
   return launch_pack(d_kv8, num_pages, d_indices, topk, d_topk_length, n_units, records, masks, d_status,
-                     reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+                     stall_test, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+int mla_pack_selected_kv(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int topk,
+                         const int32_t* d_topk_length, int n_units, void* d_packed, size_t packed_bytes,
+                         int32_t* d_status, mla_stream_t stream) {
+  return pack_selected(d_kv8, num_pages, d_indices, topk, d_topk_length, n_units, d_packed, packed_bytes, d_status,
+                       0, stream);
+}
+
+int mla_test_pack_timeout(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int topk,
+                          const int32_t* d_topk_length, int n_units, void* d_packed, size_t packed_bytes,
+                          int32_t* d_status, mla_stream_t stream) {
+  return pack_selected(d_kv8, num_pages, d_indices, topk, d_topk_length, n_units, d_packed, packed_bytes, d_status,
+                       1, stream);
 }
 
 int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size_t packed_bytes, int topk,
@@ -643,6 +672,7 @@ int mla_dense_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, const int32_
 int mla_sparse_fp8_unpack(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int n, float* d_k_out,
                           int32_t* d_status, mla_stream_t stream) {
   if (!d_kv8 || !d_indices || !d_k_out || !d_status || num_pages < 1 || n < 0) return MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_pages) * MLA_PAGE_SIZE > (1LL << 31) - 1) return MLA_ERR_UNSUPPORTED;
   if (!aligned16(d_kv8) || !aligned16(d_k_out)) return MLA_ERR_INVALID_ARG;
   if (n == 0) return MLA_OK;
   return launch_unpack(d_kv8, num_pages, d_indices, n, d_k_out, d_status, reinterpret_cast<cudaStream_t>(stream)) ==

@@ -20,12 +20,14 @@
 //    is computed once; only P crosses between the SMs.
 //  * Both halves of O must use the same softmax reference.  The reference
 //    after tile t is R_t = the running max (log2 units), raised only when a
-//    tile's max exceeds it by more than 2^8 (lazy rescale).  The owner of t
-//    needs R_{t-1} from the other CTA: it arrives as 128 floats in a small
-//    mailbox in distributed shared memory (a 128-byte bulk copy per warp),
-//    sent as soon as that tile's row max is known, long before its P.  When
-//    R changes, both CTAs rescale their O half in TMEM before that tile's
-//    P V.  Each CTA keeps the row sum l of its own tiles only (rescaled on
+//    tile's max exceeds it by more than 2^8 (lazy rescale).  Each CTA derives
+//    every R_t itself, by that rule, from the raw row maxima of all tiles in
+//    order: its own tiles' and the other CTA's, which arrive as 128 floats in
+//    a small mailbox in distributed shared memory (a 128-byte bulk copy per
+//    warp), sent as soon as the owner has read the tile's scores, long
+//    before its P.  The same fp32 comparisons in the same order give both
+//    CTAs the same references.  When R changes, both CTAs rescale their O
+//    half in TMEM before that tile's P V.  Each CTA keeps the row sum l of its own tiles only (rescaled on
 //    every reference change); the two are added once per unit, before the
 //    epilogue, through a second mailbox.
 //  * The P V of a received tile waits only for its P to land (the P V thread
@@ -45,10 +47,14 @@
 //    place (RoPE goes bf16 -> fp16), and the rest is the fp16 path.  Q is
 //    turned into fp16 once per call, by a small kernel launched just before
 //    (q_fp16_kernel), rather than by every CTA pair that reads it.
-//  * One tile = nine 64-dim TMA boxes of one page.  The four boxes that are
-//    this CTA's V half go to a 3-slot "V" ring for every tile (P V reads
-//    them; for its own tiles Q K^T reads them too); the other five go to a
-//    "K" slot, for own tiles only, released as soon as Q K^T has read them.
+//  * One tile = nine 64-dim slices (8 KB swizzled boxes) of one page.  The
+//    four that are this CTA's V half go to a 3-slot "V" ring for every tile
+//    (P V reads them; for its own tiles Q K^T reads them too); the other five
+//    go to a "K" slot, for own tiles only, released as soon as Q K^T has read
+//    them.  16-bit KV: each range of consecutive slices comes in ONE TMA
+//    instruction (a 5-D box of four or five slices; rank 1's K slot takes
+//    two): the TMA engine's time goes mostly per instruction, so that moves
+//    the same bytes with a third of the engine time of 8 KB boxes.
 //  * tcgen05.mma M=128: S (N=64) and O (N=256) accumulate in TMEM; each
 //    group of MMAs is one fully unrolled block of compile-time descriptors.
 // Roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane),
@@ -194,26 +200,32 @@ struct Cursor {
   bool valid;
 };
 
-// Keys of unit b.  The packed instance (kPacked: FlashMLA PR #200, "Packed
-// attention specialization") serves packed selections: a unit is one query
-// token, its keys the first min(topk_length, topk) packed slots (all topk when
-// no lengths are given).  (A separate instance: the cursor is inlined into
-// every role, and the dense FP8-record instance ran measurably slower with
-// both forms compiled in.)
+// Keys of unit b as the partition plan counted them (its tile ranges).  The
+// packed instance (kPacked: FlashMLA PR #200, "Packed attention
+// specialization") serves packed selections: a unit is one query token and
+// the plan counts topk_length as given (all topk when no lengths are given),
+// while only the first min(topk_length, topk) packed slots exist; tiles past
+// them are walked with every key masked.  (A separate instance: the cursor is
+// inlined into every role, and the dense FP8-record instance ran measurably
+// slower with both forms compiled in.)
 template <bool kPacked>
-__device__ __forceinline__ int unit_keys(const DecodeParams& p, int b) {
+__device__ __forceinline__ int unit_plan_keys(const DecodeParams& p, int b) {
   if constexpr (kPacked)
-    return min(p.lengths != nullptr ? max(p.lengths[b], 0) : p.default_length, p.topk);
+    return p.lengths != nullptr ? max(p.lengths[b], 0) : p.default_length;
   else
     return max(p.lengths[b], 0);
 }
 
+// Packed selections: packed pages (tiles) per unit.
+__device__ __forceinline__ int packed_tiles(const DecodeParams& p) { return (p.topk + kTile - 1) / kTile; }
+
 template <bool kPacked>
 __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& P, Cursor& c, int from_b) {
   for (int b = from_b; unit_in_part(P, b, p.n_units); ++b) {
-    const int L = unit_keys<kPacked>(p, b);
+    const int Lp = unit_plan_keys<kPacked>(p, b);
+    const int L = kPacked ? min(Lp, p.topk) : Lp;  // keys that exist
     const int lo = (b == P.b0) ? P.t0 : 0;
-    const int hi = (b == P.b1) ? P.t1 : num_tiles(L);
+    const int hi = (b == P.b1) ? P.t1 : num_tiles(Lp);
     if (hi > lo) {
       c.b = b;
       c.L = L;
@@ -267,18 +279,24 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
 }
 
 // Page ids of 32 consecutive pages of unit c.b starting at `base`, one per lane
-// (0 past the partition's range; ids outside the pool are reported and read as 0).
+// (0 past the partition's range; ids outside the pool are reported and read
+// as page 0, whose keys the softmax then masks).
 template <bool kPacked>
 __device__ __forceinline__ int load_page_window(const DecodeParams& p, const Cursor& c, int base, int lane) {
   const int kk = base + lane;
-  // packed selection: the unit's tiles are consecutive pages of the packed records
-  if constexpr (kPacked) return kk < c.hi ? c.b * ((p.topk + kT - 1) / kT) + kk : 0;
+  // packed selection: the unit's tiles are consecutive pages of the packed
+  // records; a tile past them (topk_length > topk) reads the unit's last one,
+  // every key masked
+  if constexpr (kPacked) {
+    const int tiles = packed_tiles(p);
+    return kk < c.hi ? c.b * tiles + min(kk, tiles - 1) : 0;
+  }
   int pg = 0;
   if (kk < c.hi) {
     pg = kk < p.max_pages ? p.block_table[static_cast<size_t>(c.b) * p.max_pages + kk] : -1;
     if (pg < 0 || pg >= p.num_pages) {
       report(p.status, MLA_ERR_BAD_INDEX);
-      pg = 0;
+      pg = -1;
     }
   }
   return pg;
@@ -457,8 +475,8 @@ __device__ __forceinline__ float ref_alpha(float r_old, float r_new) {
 // a pool of FP8 records (kv_map = their codes in 64-byte boxes, sc_map =
 // scales, rope_map = RoPE as a swizzled bf16 box) and Q is bf16; both are
 // turned into fp16 in shared memory (records: fp16(code * scale); Q and
-// RoPE: bf16 -> fp16).  Otherwise kv_map is the 16-bit pool and sc_map /
-// rope_map are unused.
+// RoPE: bf16 -> fp16).  Otherwise the three maps view the 16-bit pool with
+// boxes of 4, 5 and 1 consecutive 64-dim slices (kv_map, sc_map, rope_map).
 template <bool kHalf, bool kFp8, bool kQV, bool kPacked>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     dense_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
@@ -483,6 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  volatile int* sBad = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);  // [2]: own tile's page outside the pool
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -616,13 +635,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
           page_base = c.k;
           page_reg = load_page_window<kPacked>(p, c, page_base, lane);
         }
-        const int page = __shfl_sync(0xffffffffu, page_reg, c.k - page_base);
+        const int page_raw = __shfl_sync(0xffffffffu, page_reg, c.k - page_base);
+        const int page = max(page_raw, 0);  // a page outside the pool (-1) reads page 0
         if (lane == 0) {
           if (is_k) {
             const uint32_t n = own_k / kKSlots;
             const int s = static_cast<int>(own_k % kKSlots);
             if (n >= 1) ok = mbar_wait(&bars[K_EMPTY + s], (n - 1) & 1, abort_flag);
             if (ok) {
+              // the softmax masks this own tile's keys if its page was outside
+              // the pool; written once the previous own tile's Q K^T has read
+              // the K slot, hence after the softmax read the entry's last use
+              // (that Q K^T waited for the scores two own tiles back to be read)
+              sBad[own_k & 1] = page_raw < 0 ? 1 : 0;
+              __threadfence_block();
               MLA_TRACE(9, c.t);
               uint8_t* dst = sK + s * kKSlotBytes;
               if constexpr (kFp8) {
@@ -639,10 +665,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
                 tma_load_2d(dst + 4 * kBoxBytes, &rope_map, bar, 528, page * kT, pol_kv);
               } else {
                 mbar_arrive_expect_tx(&bars[K_FULL + s], kKSlotBytes);
-#pragma unroll
-                for (int j = 0; j < kKBoxes; ++j) {
-                  const int g = rank == 0 ? k_box<0>(j) : k_box<1>(j);
-                  tma_load_4d(dst + j * kBoxBytes, &kv_map, &bars[K_FULL + s], 64 * g, grp, 0, page, pol_kv);
+                if (rank == 0) {
+                  tma_load_5d(dst, &sc_map, &bars[K_FULL + s], 0, 0, k_box<0>(0), grp, page, pol_kv);
+                } else {
+                  tma_load_5d(dst, &kv_map, &bars[K_FULL + s], 0, 0, k_box<1>(0), grp, page, pol_kv);
+                  tma_load_5d(dst + 4 * kBoxBytes, &rope_map, &bars[K_FULL + s], 0, 0, k_box<1>(4), grp, page,
+                              pol_kv);
                 }
               }
               ++k_issued[s];
@@ -669,10 +697,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
                 }
               } else {
                 mbar_arrive_expect_tx(&bars[V_FULL + s], kVSlotBytes);
-#pragma unroll
-                for (int j = 0; j < kVBoxes; ++j)
-                  tma_load_4d(dst + j * kBoxBytes, &kv_map, &bars[V_FULL + s],
-                              64 * (4 * static_cast<int>(rank) + j), grp, 0, page, pol_kv);
+                tma_load_5d(dst, &kv_map, &bars[V_FULL + s], 0, 0, 4 * static_cast<int>(rank), grp, page, pol_kv);
               }
               ++v_issued[s];
             }
@@ -1101,6 +1126,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     const uint32_t peer_l_free = mapa_shared(smem_u32(&bars[L_FREE]), peer);
     Cursor c;
     cursor_init<kPacked>(p, P, c);
+    // Packed selection: the next own tile's valid-slot bits, read a whole
+    // received tile ahead (when the cursor reaches the received tile before
+    // it), so that the load is done long before the scores are; only an own
+    // tile that starts a unit reads its bits one step ahead.
+    auto tile_mask = [&](int b, int k) -> uint64_t {
+      const int tiles = packed_tiles(p);
+      return k < tiles ? p.packed_mask[static_cast<size_t>(b) * tiles + k] : 0ull;
+    };
+    uint64_t mask_own = ~0ull;
+    auto prefetch_mask = [&]() {
+      if (!kPacked || !c.valid) return;
+      if ((c.t & 1u) != rank) {
+        if (!cursor_last(c)) mask_own = tile_mask(c.b, c.k + 1);
+      } else if (cursor_first(c) || c.t == 0) {
+        mask_own = tile_mask(c.b, c.k);
+      }
+    };
+    prefetch_mask();
     bool ok = true;
     uint32_t own_i = 0, recv_i = 0, units = 0;
     float r_cur = -INFINITY;  // reference (log2 units) after the last tile seen
@@ -1119,13 +1162,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // ---- own tile: scores, reference, P
         const int jmax = p.causal ? (c.L - p.s_q + tok) : (c.L - 1);  // last visible key
         const int vis = jmax - c.k * kT;                                // keys 0..vis of this tile are visible
-        uint64_t keep = vis >= kT - 1 ? ~0ull : (vis < 0 ? 0ull : (~0ull >> (kT - 1 - vis)));
-        // packed selection: and the tile's valid slots (read before the wait)
-        if constexpr (kPacked) keep &= p.packed_mask[static_cast<size_t>(c.b) * ((p.topk + kT - 1) / kT) + c.k];
+        uint64_t keep = (vis >= kT - 1 ? ~0ull : (vis < 0 ? 0ull : (~0ull >> (kT - 1 - vis))));
+        if constexpr (kPacked) keep &= mask_own;
         ok = warp_wait(&bars[S_FULL], own_i & 1, abort_flag);
         if (!ok) break;
         if (tid == 0) MLA_TRACE(4, t);
         tc_fence_after();
+        // a page outside the pool (the K producer's flag): every key masked.
+        // Read before S_FREE: the producer rewrites the entry only after that.
+        // (Read from shared memory, not the block table: a global load here
+        // sat on every own tile's critical path and cost 4-9 us per call.)
+        if (!kPacked && sBad[own_i & 1]) keep = 0ull;
         float s[kT];
         {
           uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
@@ -1156,17 +1203,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float mt = mraw * c_log2;  // -inf stays -inf
-        const float r_t = (mt > r_cur + kTau) ? mt : r_cur;
-        // the peer needs this tile's reference for its next tile and its O
+        // the peer derives this tile's reference from its raw maximum, as we
+        // do: it is sent at once and waits for nothing of the peer's
         if (own_i >= 1) {
           ok = warp_wait_cluster(&bars[R_FREE], (own_i - 1) & 1, abort_flag);
           if (!ok) break;
         }
-        sRefOut[r] = r_t;
+        sRefOut[r] = mt;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) bulk_copy_to_cluster(peer_ref, smem_u32(sRefOut + 32 * warp), 32 * 4, peer_r_full);
         if (tid == 0) MLA_TRACE(13, t);
+        const float r_t = (mt > r_cur + kTau) ? mt : r_cur;
         const float mref = (r_t == -INFINITY) ? 0.f : r_t;
         uint32_t pk[kT / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1199,15 +1247,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         l_own = l_own * alpha + rowsum;
         r_cur = r_t;
       } else {
-        // ---- received tile: apply its reference now; its P V runs when its P lands
+        // ---- received tile: its reference from the owner's raw maximum, by the
+        // same rule the owner applies; its P V runs when its P lands
         ok = warp_wait_cluster(&bars[R_FULL], recv_i & 1, abort_flag);
         if (!ok) break;
         if (tid == 0) mbar_arrive_expect_tx(&bars[R_FULL], kVecBytes);  // armed for the next message
         // read (and use, so the load has completed) before the mailbox is released
-        const float r_t = __shfl_sync(0xffffffffu, sRefIn[r], lane);
+        const float m_in = __shfl_sync(0xffffffffu, sRefIn[r], lane);
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(peer_r_free);
         if (tid == 0) MLA_TRACE(10, t);
+        const float r_t = (m_in > r_cur + kTau) ? m_in : r_cur;
         alpha = ref_alpha(r_cur, r_t);
         l_own *= alpha;
         r_cur = r_t;
@@ -1236,6 +1286,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       }
       const int b_here = c.b, u_here = c.u;
       cursor_next<kPacked>(p, P, c);
+      prefetch_mask();
       if (!last) continue;
       // ---- row sum of the unit: ours + the peer's, both relative to r_cur
       if (units >= 1) {

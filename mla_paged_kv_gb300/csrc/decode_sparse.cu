@@ -806,6 +806,18 @@ __device__ __forceinline__ void bulk_commit_and_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Wait budget of the stall-test instance (below): short, so that the test
+// ends quickly; the real instance keeps the 2 s budget of every other wait.
+constexpr uint64_t kStallTestWaitNs = 200000;  // 200 us
+
+// kStallTest: the test instance of the timeout path.  Thread 0 withholds the
+// arrival (with the transaction count) that completes its tile's bulk-copy
+// barrier, so its bounded wait runs out as if a copy had never landed; it
+// reports MLA_ERR_TIMEOUT, zeroes the tile's mask, then makes the arrival
+// after all, waits (bounded) until its copies have landed, and leaves without
+// storing.  (A barrier's transaction count may go below zero before the
+// arrival that raises it: the copies' completions are simply counted first.)
+template <bool kStallTest>
 __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ kv8, int num_pages,
                                                    const int32_t* __restrict__ indices, int topk,
                                                    const int32_t* __restrict__ topk_length, uint8_t* __restrict__ packed,
@@ -846,7 +858,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ k
   const uint32_t n_valid = static_cast<uint32_t>(__popcll(valid));
   if (tid < 32) {
     // warp 0: the transaction count first, then the copies (lanes k and k + 32)
-    if (tid == 0) mbar_arrive_expect_tx(&s_bar, n_valid * MLA_RECORD_BYTES);
+    if (tid == 0 && !kStallTest) mbar_arrive_expect_tx(&s_bar, n_valid * MLA_RECORD_BYTES);
     __syncwarp();
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -865,14 +877,16 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ k
   fence_proxy_async_smem();  // the zeros are visible to the bulk store
   __syncthreads();
   if (tid == 0) {
-    bool ok = mbar_wait(&s_bar, 0, nullptr);
-    if (!ok) {
-      report(status, MLA_ERR_TIMEOUT);
-      ok = mbar_wait(&s_bar, 0, nullptr);  // the copies in flight, once more before leaving
-    }
-    if (ok) {
+    if (mbar_wait(&s_bar, 0, nullptr, kStallTest ? kStallTestWaitNs : MLA_WAIT_LIMIT_NS)) {
       bulk_store_s2g(packed + (static_cast<size_t>(unit) * tiles + tile) * kTileBytes, smem_u32(s_rec), kTileBytes);
       bulk_commit_and_wait_all();
+    } else {
+      // the tile's records are not stored: its mask says no slot is valid, so
+      // the attention ignores whatever the workspace holds there
+      report(status, MLA_ERR_TIMEOUT);
+      masks[static_cast<size_t>(unit) * tiles + tile] = 0ull;
+      if (kStallTest) mbar_arrive_expect_tx(&s_bar, n_valid * MLA_RECORD_BYTES);  // the withheld arrival
+      mbar_wait(&s_bar, 0, nullptr);  // no copy may still be landing when the block exits
     }
   }
 }
@@ -942,9 +956,14 @@ cudaError_t launch_sparse(const CUtensorMap& q_map, const DecodeParams& p, int n
 
 cudaError_t launch_pack(const uint8_t* kv8, int num_pages, const int32_t* indices, int topk,
                         const int32_t* topk_length, int n_units, uint8_t* packed, uint64_t* masks, int32_t* status,
-                        cudaStream_t stream) {
+                        int stall_test, cudaStream_t stream) {
   const dim3 grid((topk + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE, n_units);
-  sp::pack_kernel<<<grid, 256, 0, stream>>>(kv8, num_pages, indices, topk, topk_length, packed, masks, status);
+  if (stall_test)
+    sp::pack_kernel<true><<<grid, 256, 0, stream>>>(kv8, num_pages, indices, topk, topk_length, packed, masks,
+                                                    status);
+  else
+    sp::pack_kernel<false><<<grid, 256, 0, stream>>>(kv8, num_pages, indices, topk, topk_length, packed, masks,
+                                                     status);
   return cudaGetLastError();
 }
 

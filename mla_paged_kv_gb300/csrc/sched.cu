@@ -13,12 +13,15 @@
 // for more than kSchedMaxSmemUnits units or kSchedSearchParts partitions).  c0 + F alone often finishes the
 // walk early and leaves the last partitions without work.
 //
-// One block.  The tile counts and the total cost come from all threads; the
-// greedy walk over the partitions is sequential (one thread, O(units +
-// partitions) steps, shared memory only); the per-unit split counts come from
-// a difference array written by the walk, and both prefix sums (counts, then
-// split offsets) are block-wide scans.
+// One block.  The tile counts and the total cost come from all threads; each
+// candidate cap's greedy walk is sequential (one thread per candidate, one
+// step per unit with a closed form for the partitions a unit spans, shared
+// memory only); the metadata is then filled in parallel from the chosen
+// walk's partition ends, the per-unit split counts come from a difference
+// array, and both prefix sums (counts, then split offsets) are block-wide
+// scans.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace mla {
 
@@ -120,46 +123,70 @@ __device__ __forceinline__ void sched_walk(NtOf nt_of, int* diff, int n_units, i
 }
 
 // The greedy walk with budget cap, recording where each partition ends,
-// (unit, tile), in end[p] (one thread; the same steps as sched_walk).  A
-// partition begins where the previous one ended, past units without tiles.
-// Returns the cost left for the last partition after partitions 0 .. P-2.
+// (unit, tile), in end[p].  The same partitions as sched_walk, reached one
+// unit at a time instead of one partition at a time: a unit that fits the
+// budget left is taken whole; otherwise the current partition takes
+// budget - F of its tiles (none if that is not positive) and ends, the
+// following partitions take full chunks of w = cap - F tiles while the rest
+// does not fit with its F, and the rest opens the next partition with
+// cap - rest - F left.  Partitions that never end inside a unit end past the
+// last one.  The last partition takes everything left; returns its cost.
+// One warp, every lane running the same walk (lane 0 stores): the tile
+// counts come 32 at a time, one per lane, and reach the walk by shuffle, so
+// that only the budget arithmetic is serial.
 __device__ __forceinline__ long long sched_walk_record(const int* nt_of, int n_units, int num_parts, int fixed_cost,
                                                        int cap, int2* end) {
-  int b = 0, t = 0;
+  const int lane = threadIdx.x & 31;
+  const int last_p = num_parts - 1;
+  const int w = cap - fixed_cost;  // tiles a partition takes from a unit it starts on and cannot finish
+  const float inv_w = w > 0 ? 1.f / static_cast<float>(w) : 0.f;
+  int p = 0, budget = cap;
   long long left = 0;
-  for (int p = 0; p < num_parts; ++p) {
-    while (b < n_units && nt_of[b] == 0) {
-      ++b;
-      t = 0;
-    }
-    if (p == num_parts - 1) {
-      for (int u = b; u < n_units; ++u)
-        if (nt_of[u] > 0) left += nt_of[u] - (u == b ? t : 0) + fixed_cost;
-      b = n_units;
-      t = 0;
-    } else {
-      int budget = cap;
-      while (b < n_units) {
-        const int nt = nt_of[b];
-        if (nt == 0) {
-          ++b;
-          t = 0;
-          continue;
-        }
-        const int rem = nt - t;
-        if (rem + fixed_cost <= budget) {
-          budget -= rem + fixed_cost;
-          ++b;
-          t = 0;
+  for (int base = 0; base < n_units; base += 32) {
+    const int mine = base + lane < n_units ? nt_of[base + lane] : 0;
+    const int cnt = min(32, n_units - base);
+    for (int j = 0; j < cnt; ++j) {
+      const int x = __shfl_sync(0xffffffffu, mine, j);
+      if (x == 0) continue;
+      const int u = base + j;
+      if (p == last_p) {
+        left += x + fixed_cost;
+        continue;
+      }
+      if (x + fixed_cost <= budget) {
+        budget -= x + fixed_cost;
+        continue;
+      }
+      int t = max(budget - fixed_cost, 0);
+      if (lane == 0) end[p] = make_int2(u, t);
+      ++p;
+      int r = x - t;
+      if (p < last_p && r + fixed_cost > cap) {
+        if (w <= 0) {
+          // nothing fits: every partition up to the last ends here, empty
+          for (; p < last_p; ++p)
+            if (lane == 0) end[p] = make_int2(u, t);
         } else {
-          const int take = budget - fixed_cost;
-          if (take > 0) t += take;
-          break;
+          // full chunks while r > w: k = (r - 1) / w, from a float estimate
+          int k = __float2int_rz(static_cast<float>(r - 1) * inv_w);
+          while (k > 0 && k * w > r - 1) --k;
+          while ((k + 1) * w <= r - 1) ++k;
+          k = min(k, last_p - p);
+          for (int i = 1; i <= k; ++i)
+            if (lane == 0) end[p + i - 1] = make_int2(u, t + i * w);
+          p += k;
+          t += k * w;
+          r -= k * w;
         }
       }
+      if (p == last_p)
+        left += r + fixed_cost;
+      else
+        budget = cap - r - fixed_cost;
     }
-    end[p] = make_int2(b, t);
   }
+  if (lane == 0)
+    for (int q = p; q < num_parts; ++q) end[q] = make_int2(n_units, 0);
   return left;
 }
 
@@ -217,9 +244,11 @@ __device__ void plan_native(const int32_t* __restrict__ lengths, int default_len
     __syncthreads();
   } else {
     const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0 && warp <= fixed_cost)
-      s->left[warp] = sched_walk_record(s_nt, n_units, num_parts, fixed_cost, static_cast<int>(c0) + warp,
-                                        s->end + warp * kSchedSearchParts);
+    if (warp <= fixed_cost) {
+      const long long left = sched_walk_record(s_nt, n_units, num_parts, fixed_cost, static_cast<int>(c0) + warp,
+                                               s->end + warp * kSchedSearchParts);
+      if ((threadIdx.x & 31) == 0) s->left[warp] = left;
+    }
     __syncthreads();
     int w = fixed_cost;
     for (int k = 0; k < fixed_cost; ++k)
@@ -293,6 +322,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_kernel(const int32_t* __r
   __shared__ long long s_warp_cost[kSchedThreads / 32];
   __shared__ int s_warp[kSchedThreads / 32];
   __shared__ SchedSearch s_search;
+  pdl_wait_prior_grid();  // launched early (programmatic dependent launch): the lengths may come from the grid before
   plan_native(lengths, default_length, n_units, num_parts, fixed_cost, sched, split_offset, s_nt, s_diff,
               s_warp_cost, s_warp, &s_search);
 }
@@ -319,6 +349,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_local_kernel(const int32_
   __shared__ long long s_sum[2];  // total tiles, parts given by the quotas
   __shared__ int s_active;
   __shared__ SchedSearch s_search;
+  pdl_wait_prior_grid();  // launched early (programmatic dependent launch): the lengths may come from the grid before
   if (n_units <= kSchedLocalMaxUnits) {
     long long tiles = 0;
     int act = 0;
@@ -420,13 +451,24 @@ __global__ void __launch_bounds__(kSchedThreads) sched_local_kernel(const int32_
 
 cudaError_t launch_sched(const int32_t* lengths, int default_length, int n_units, int num_parts,
                          int32_t* sched, int32_t* split_offset, int request_local, cudaStream_t stream) {
+  // A programmatic dependent of whatever runs before it on the stream: the
+  // block starts while that grid drains and waits for it on the device
+  // (griddepcontrol.wait) before it reads the lengths.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(kSchedThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (request_local)
-    sched_local_kernel<<<1, kSchedThreads, 0, stream>>>(lengths, default_length, n_units, num_parts,
-                                                        MLA_SPLIT_FIXED_COST, sched, split_offset);
-  else
-    sched_kernel<<<1, kSchedThreads, 0, stream>>>(lengths, default_length, n_units, num_parts, MLA_SPLIT_FIXED_COST,
-                                                  sched, split_offset);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, sched_local_kernel, lengths, default_length, n_units, num_parts,
+                              static_cast<int>(MLA_SPLIT_FIXED_COST), sched, split_offset);
+  return cudaLaunchKernelEx(&cfg, sched_kernel, lengths, default_length, n_units, num_parts,
+                            static_cast<int>(MLA_SPLIT_FIXED_COST), sched, split_offset);
 }
 
 }  // namespace mla

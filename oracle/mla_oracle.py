@@ -38,6 +38,8 @@ Readings taken where the pages are silent (each is listed in the design doc):
   * Sparse: index -1 is masked anywhere; entries at or past topk_length are
     masked; a duplicated index counts as two keys; an index outside
     [0, num_pages*64) is masked and reported.
+  * Dense: a block-table entry outside [0, num_pages) masks the 64 keys of
+    that logical page (the same reading as an out-of-pool sparse index).
   * Record bytes are contiguous in the order the page lists them:
     [0,512) E4M3 codes, [512,528) four little-endian fp32 scales,
     [528,656) 64 little-endian bf16.  Element d < 512 uses scale d // 128.
@@ -106,18 +108,22 @@ def _le_u16(byte_block: np.ndarray) -> np.ndarray:
 # Key gathering
 # --------------------------------------------------------------------------
 
-def dense_keys(kv: np.ndarray, block_table: np.ndarray, b: int, L: int) -> np.ndarray:
+def dense_keys(kv: np.ndarray, block_table: np.ndarray, b: int, L: int):
     """Latent rows of request b in logical order 0..L-1, read through the block table.
 
     Logical token j lives in physical page block_table[b][j // 64] at slot
     j % 64 (PR #183: 64-token pages; the block table maps logical to
-    physical pages).
+    physical pages).  Returns (rows [L, 576], present [L]): a token whose
+    page entry lies outside [0, num_pages) is absent (zero row, masked).
     """
-    rows = np.empty((L, D_QK), dtype=np.float64)
+    rows = np.zeros((L, D_QK), dtype=np.float64)
+    present = np.zeros(L, dtype=bool)
     for j in range(L):
         page = int(block_table[b, j // PAGE_SIZE])
-        rows[j] = kv[page, j % PAGE_SIZE]
-    return rows
+        if 0 <= page < kv.shape[0]:
+            rows[j] = kv[page, j % PAGE_SIZE]
+            present[j] = True
+    return rows, present
 
 
 def decode_record(rec: np.ndarray) -> np.ndarray:
@@ -239,10 +245,10 @@ def dense_decode(q, kv, block_table, cache_seqlens, causal, scale, batches=None)
     for b in (range(B) if batches is None else batches):
         L = int(cache_seqlens[b])
         for g in range(h_kv):
-            keys = dense_keys(kv[:, :, g, :], block_table, b, L)
+            keys, present = dense_keys(kv[:, :, g, :], block_table, b, L)
             heads = slice(g * G, (g + 1) * G)
             qrows = q[b][:, heads, :].reshape(s_q * G, D_QK)
-            o, l = attend(qrows, keys, scale, causal_mask(s_q, G, L, causal))
+            o, l = attend(qrows, keys, scale, causal_mask(s_q, G, L, causal) & present[None, :])
             out[b][:, heads] = o.reshape(s_q, G, D_V)
             lse[b][:, heads] = l.reshape(s_q, G)
     return out, lse
@@ -266,11 +272,15 @@ def dense_fp8_decode(q, kv8, block_table, cache_seqlens, causal, scale, batches=
     lse = np.full((B, s_q, h_q), -np.inf, dtype=np.float64)
     for b in (range(B) if batches is None else batches):
         L = int(cache_seqlens[b])
-        keys = np.empty((L, D_QK), dtype=np.float64)
+        keys = np.zeros((L, D_QK), dtype=np.float64)
+        present = np.zeros(L, dtype=bool)          # out-of-pool page entries mask their keys
         for j in range(L):
-            keys[j] = decode_record(kv8[int(block_table[b, j // PAGE_SIZE]), j % PAGE_SIZE])
+            page = int(block_table[b, j // PAGE_SIZE])
+            if 0 <= page < kv8.shape[0]:
+                keys[j] = decode_record(kv8[page, j % PAGE_SIZE])
+                present[j] = True
         qrows = q[b].reshape(s_q * h_q, D_QK)
-        o, l = attend(qrows, keys, scale, causal_mask(s_q, h_q, L, causal))
+        o, l = attend(qrows, keys, scale, causal_mask(s_q, h_q, L, causal) & present[None, :])
         out[b] = o.reshape(s_q, h_q, D_V)
         lse[b] = l.reshape(s_q, h_q)
     return out, lse

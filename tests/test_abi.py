@@ -36,7 +36,7 @@ def test_header_declares_the_boundary():
                             "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes",
                             "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd",
                             "mla_get_metadata_request_local", "mla_num_parts_dense", "mla_dense_fp8_decode_fwd",
-                            "mla_dense_fp8_unit_lengths"])
+                            "mla_dense_fp8_unit_lengths", "mla_test_pack_timeout"])
 
 
 def test_library_exports_every_declared_symbol(lib_path):
@@ -96,3 +96,11 @@ def test_host_validation_without_gpu(lib_path):
     # a workspace smaller than the layout is refused before any launch
     p16 = ctypes.c_void_p(256)
     assert lib.mla_pack_selected_kv(p16, 1, p16, 64, null, 1, p16, 64 * 656, p16, null) == 1
+
+    # pools whose slot count does not fit int32 are refused before any launch (pack, test hook, unpack)
+    big = (1 << 31) // 64
+    assert lib.mla_pack_selected_kv(p16, big, p16, 64, null, 1, p16, 1 << 20, p16, null) == 2   # UNSUPPORTED
+    lib.mla_test_pack_timeout.argtypes = lib.mla_pack_selected_kv.argtypes
+    assert lib.mla_test_pack_timeout(p16, big, p16, 64, null, 1, p16, 1 << 20, p16, null) == 2
+    assert lib.mla_test_pack_timeout(null, 1, null, 64, null, 1, null, 0, null, null) == 1
+    assert lib.mla_sparse_fp8_unpack(p16, big, p16, 4, p16, p16, null) == 2

@@ -172,14 +172,15 @@ def test_dense_fp8_records_agree_with_the_exact_score_path():
     compare(out_r, lse_r, out_e.double().cpu().numpy(), lse_e.double().cpu().numpy())
 
 
-def test_dense_fp8_records_bad_page_is_reported():
+def test_dense_fp8_records_bad_page_is_reported_and_masked():
     case = wl.dense_fp8_case(2, 1, 64, 0, seqlens=[300, 200], seed=195)
     bt = case.block_table.clone()
     bt[0, 2] = case.kv8.shape[0] + 5                 # keys 128..191 of request 0 point outside the pool
     out, lse, st = run_records(case, block_table=bt)
     assert st == 5                                   # MLA_ERR_BAD_INDEX
-    ro, rl = oracle(case)
-    compare(out[1:], lse[1:], ro[1:], rl[1:])        # the other request is untouched
+    ro, rl = orc.dense_fp8_decode(case.q.double().numpy(), case.kv8.numpy(), bt.numpy(),
+                                  case.cache_seqlens.numpy(), case.causal, case.scale)   # those keys masked
+    compare(out, lse, ro, rl)
 
 
 def test_dense_fp8_records_decode_helper():

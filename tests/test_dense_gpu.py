@@ -204,3 +204,32 @@ def test_num_parts_dense_counts_row_blocks():
     assert mla.mla_num_parts_dense(1, 128, 2) == max(base // 2, 1)      # two head groups of 64 heads
     assert mla.mla_num_parts_dense(3, 96, 3) == max(base // 3, 1)       # 3 groups, each one block of 3 tokens x 32 heads
     assert mla.mla_num_parts_dense(5, 64, 2) == max(base // 4, 1)       # 2 groups of 32 heads x 2 blocks (4 + 1 tokens)
+
+
+# ---------------------------------------------------------------- block-table entries outside the pool
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("num_parts", [2, 76])      # 76 parts per 2 requests: the instance staging Q in the V ring
+@pytest.mark.parametrize("bad_entry", [-7, 10 ** 6])
+def test_dense_out_of_pool_page_is_masked_and_reported(dtype, num_parts, bad_entry):
+    """A block-table entry outside [0, num_pages) masks the 64 keys of its
+    page (the oracle's reading) and sets MLA_ERR_BAD_INDEX; both requests
+    still match the oracle, the untouched one bit for bit against a clean run."""
+    case = wl.dense_case(2, 2, 128, 0, seqlens=[700, 333], causal=True, dtype=dtype, seed=81)
+    bt = case.block_table.clone()
+    bt[0, 3] = bad_entry                               # keys 192..255 of request 0
+    bad = wl.DenseCase(q=case.q, kv=case.kv, block_table=bt, cache_seqlens=case.cache_seqlens, causal=True,
+                       scale=case.scale, out_fp32=False)
+    c = to_dev(bad)
+    pl = mla.plan(c.cache_seqlens, 2, 256, num_parts=num_parts)
+    out = torch.full((2, 2, 128, 512), float("nan"), device="cuda", dtype=dtype)
+    lse = torch.full((2, 2, 128), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_decode_fwd(c.q, c.kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset, pl.num_parts,
+                       pl.workspace, out, lse, status, True, case.scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5                     # MLA_ERR_BAD_INDEX
+    ro, rl = dense_oracle(bad)
+    compare(out, lse, ro, rl)
+    clean_o, clean_l, _ = run_dense(case, num_parts=num_parts)
+    assert torch.equal(out[1], clean_o[1]) and torch.equal(lse[1], clean_l[1])

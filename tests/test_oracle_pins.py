@@ -542,3 +542,50 @@ def test_dense_fp8_equals_sparse_over_every_slot():
     o1, l1 = orc.dense_fp8_decode(f64(case.q), case.kv8.numpy(), bt, L, False, case.scale)
     o2, l2, bad = orc.sparse_decode(f64(case.q), case.kv8.numpy(), ind, None, case.scale)
     assert bad == 0 and np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------- out-of-pool block-table entries
+
+@pytest.mark.parametrize("bad_entry", [-3, 10 ** 6])
+def test_dense_out_of_pool_page_masks_its_keys(bad_entry):
+    """A block-table entry outside [0, num_pages) removes that logical page's
+    64 keys: torch SDPA over the remaining keys (gathered by torch indexing,
+    the page dropped by position) gives the same rows; other requests are
+    untouched."""
+    case = wl.dense_case(2, 2, 8, 0, seqlens=[300, 150], causal=True, seed=61)
+    bt = case.block_table.clone()
+    bt[0, 2] = bad_entry                              # keys 128..191 of request 0
+    out, lse = orc.dense_decode(f64(case.q), f64(case.kv), bt.numpy(), case.cache_seqlens.numpy(), True,
+                                case.scale)
+    L = 300
+    j = torch.arange(L)
+    keep = (j // 64) != 2
+    slot = case.block_table[0].long()[j // 64] * 64 + (j % 64)
+    K = case.kv.double().reshape(-1, 576)[slot[keep]]
+    q = case.q[0].double().reshape(16, 576)
+    tok = torch.arange(16) // 8
+    allowed = j[keep][None, :] <= (L - 2 + tok[:, None])
+    bias = torch.zeros(16, int(keep.sum()), dtype=torch.float64).masked_fill(~allowed, float("-inf"))
+    ro = torch.nn.functional.scaled_dot_product_attention(q[None], K[None], K[None, :, :512], attn_mask=bias[None],
+                                                          scale=case.scale)[0]
+    rl = torch.logsumexp(q @ K.T * case.scale + bias, dim=-1)
+    assert np.abs(out[0].reshape(16, 512) - ro.numpy()).max() < TOL
+    assert np.abs(lse[0].reshape(16) - rl.numpy()).max() < TOL
+    good_o, good_l = orc.dense_decode(f64(case.q), f64(case.kv), case.block_table.numpy(),
+                                      case.cache_seqlens.numpy(), True, case.scale)
+    assert np.array_equal(out[1], good_o[1]) and np.array_equal(lse[1], good_l[1])
+
+
+def test_dense_fp8_out_of_pool_page_equals_sparse_with_those_slots_masked():
+    case = wl.dense_fp8_case(2, 1, 4, 0, seqlens=[200, 64], seed=85)
+    bt = case.block_table.numpy().copy()
+    L = case.cache_seqlens.numpy()
+    ind = np.full((2, 1, 256), -1, dtype=np.int64)
+    for b in range(2):
+        j = np.arange(L[b])
+        ind[b, 0, :L[b]] = bt[b, j // 64] * 64 + j % 64
+    bt[0, 1] = case.kv8.shape[0]                      # keys 64..127 of request 0: one past the pool
+    ind[0, 0, 64:128] = -1
+    o1, l1 = orc.dense_fp8_decode(f64(case.q), case.kv8.numpy(), bt, L, False, case.scale)
+    o2, l2, bad = orc.sparse_decode(f64(case.q), case.kv8.numpy(), ind, None, case.scale)
+    assert bad == 0 and np.array_equal(o1, o2) and np.array_equal(l1, l2)

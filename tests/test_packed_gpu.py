@@ -112,3 +112,24 @@ def test_packed_full_size_workload():
     assert bad == 0 and np.array_equal(packed.cpu().numpy(), ref)
     ro, rl = orc.packed_decode(case.q.double().numpy(), ref, 2048, case.topk_length.numpy(), case.scale)
     compare(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("where", ["middle", "last"])
+def test_packed_topk_length_above_topk(where):
+    """topk_length may exceed topk: the plan counts tiles from the lengths as
+    given, only the first topk slots exist.  The walked tiles past them carry
+    no key (no read past the unit's records or masks), and every split the
+    plan counts is written, so the result equals the oracle's (which takes
+    min(topk_length, topk))."""
+    topk = 192
+    lengths = [[topk], [topk], [topk]]
+    case, ind = case_with_holes(3, 1, 128, topk, 16, lengths, seed=77)
+    tl = case.topk_length.clone()
+    tl[1 if where == "middle" else 2, 0] = topk + 300  # five phantom tiles past the unit's three
+    case.topk_length = tl
+    packed, _ = orc.pack_selected(case.kv8.numpy(), ind.numpy(), tl.numpy())
+    for num_parts in (5, 23):                           # partitions beginning inside the phantom tiles
+        out, lse, st, pl = run_packed(case, packed, topk, num_parts=num_parts)
+        assert st == 0
+        ro, rl = orc.packed_decode(case.q.double().numpy(), packed, topk, tl.numpy(), case.scale)
+        compare(out, lse, ro, rl)

@@ -1,0 +1,43 @@
+"""The device timeout path on a real GPU, in a form that faults and hangs
+nothing: the test instance of the pack kernel withholds the arrival that
+completes each block's bulk-copy barrier, so that block's bounded wait
+(200 us) runs out.  The block must report MLA_ERR_TIMEOUT, give its tile a
+zero mask, make the withheld arrival, wait for its own copies and exit
+without storing; the context and the stream must stay usable, which the
+normal pack right after it checks byte for byte against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import mla_paged_kv_gb300 as mla
+from mla_paged_kv_gb300 import workloads as wl
+from oracle import mla_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+MLA_ERR_TIMEOUT = 4
+
+
+def test_pack_wait_runs_out_reports_timeout_and_the_next_call_is_exact():
+    case = wl.sparse_case(2, 1, 16, topk=192, pages_per_req=8, topk_lengths=[[192], [70]], seed=99)
+    kv8, ind, tl = case.kv8.cuda(), case.indices.cuda(), case.topk_length.cuda()
+    n_bytes = mla.mla_packed_kv_workspace_bytes(2, 192)
+    rec_bytes = 2 * 3 * 64 * 656
+    packed = torch.full((n_bytes,), 0xAB, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_test_pack_timeout(kv8, ind, tl, packed, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == MLA_ERR_TIMEOUT
+    got = packed.cpu().numpy()
+    assert not got[rec_bytes:].any()                  # every tile's mask is zero
+    assert (got[:rec_bytes] == 0xAB).all()            # no record was stored
+
+    # same process, same stream: the normal pack is unaffected
+    packed.fill_(0xAB)
+    status.zero_()
+    mla.mla_pack_selected_kv(kv8, ind, tl, packed, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref, bad = orc.pack_selected(case.kv8.numpy(), case.indices.numpy(), case.topk_length.numpy())
+    assert bad == 0 and np.array_equal(packed.cpu().numpy(), ref)

@@ -44,15 +44,19 @@ def test_static_ws_refuses_oversize_before_any_device_call():
 def _run(case, num_parts, static):
     c = to_dev(case)
     B, s_q, h_q = case.batch, case.s_q, case.h_q
+    kv = c.kv8 if hasattr(c, "kv8") else c.kv          # FP8 records, or the 16-bit cache (h_kv >= 1)
+    h_kv = 1 if kv.dim() == 3 else kv.shape[2]
+    if num_parts is None:
+        num_parts = mla.mla_num_parts_dense(s_q, h_q, h_kv)
     pl = mla.plan(c.cache_seqlens, B, s_q * h_q, num_parts=num_parts)
-    out = torch.full((B, s_q, h_q, 512), float("nan"), device="cuda", dtype=torch.bfloat16)
+    out = torch.full((B, s_q, h_q, 512), float("nan"), device="cuda", dtype=case.q.dtype)
     lse = torch.full((B, s_q, h_q), float("nan"), device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     if static:
-        mla.mla_decode_fwd_static_ws(c.q, c.kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset,
+        mla.mla_decode_fwd_static_ws(c.q, kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset,
                                      pl.num_parts, out, lse, status, case.causal, case.scale)
     else:
-        mla.mla_decode_fwd(c.q, c.kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset, pl.num_parts,
+        mla.mla_decode_fwd(c.q, kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset, pl.num_parts,
                            pl.workspace, out, lse, status, case.causal, case.scale)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, mla.mla_status_string(int(status.item()))
@@ -69,4 +73,39 @@ def test_static_ws_matches_caller_workspace_on_consecutive_calls():
     for name, case, parts in (("a", a, None), ("b", b, 40), ("a", a, None)):
         out, lse = _run(case, parts, static=True)
         ro, rl = ref[name]
+        compare(out, lse, ro.double().cpu().numpy(), rl.double().cpu().numpy())
+
+
+# The other cache types go through the same array: fp16, two latent KV heads,
+# and FP8 records, whose fp16 copy of Q sits in the array behind the partials.
+KINDS = {
+    "fp16": lambda: wl.dense_case(3, 1, 128, 0, seqlens=[2500, 90, 1300], dtype=torch.float16, seed=73),
+    "hkv2": lambda: wl.dense_case(3, 2, 128, 0, seqlens=[700, 2200, 64], causal=True, h_kv=2, seed=74),
+    "fp8_records": lambda: wl.dense_fp8_case(3, 1, 128, 0, seqlens=[1800, 5, 900], seed=75),
+}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", sorted(KINDS))
+def test_static_ws_other_cache_types_on_consecutive_calls(kind):
+    case = KINDS[kind]()
+    ro, rl = _run(case, None, static=False)
+    for _ in range(2):
+        out, lse = _run(case, None, static=True)
+        compare(out, lse, ro.double().cpu().numpy(), rl.double().cpu().numpy())
+
+
+@pytest.mark.gpu
+def test_static_ws_fp8_records_just_under_the_limit():
+    """The largest FP8-record batch whose workspace (partials, LSEs, then the
+    fp16 copy of Q) still fits the array: the Q copy ends inside it."""
+    parts = mla.mla_num_parts_dense(1, 128, 1)
+    B = 1
+    while mla.mla_workspace_bytes(B + 1, 128, parts) <= STATIC_WORKSPACE_BYTES:
+        B += 1
+    assert STATIC_WORKSPACE_BYTES - mla.mla_workspace_bytes(B, 128, parts) < 128 * (2052 + 1152) + 512
+    case = wl.dense_fp8_case(B, 1, 128, 64, 320, seed=76)
+    ro, rl = _run(case, parts, static=False)
+    for _ in range(2):
+        out, lse = _run(case, parts, static=True)
         compare(out, lse, ro.double().cpu().numpy(), rl.double().cpu().numpy())
