@@ -384,11 +384,22 @@ def check_status(status: torch.Tensor, where: str):
 
 
 def decode(q, kv, block_table, cache_seqlens, causal=False, softmax_scale=None, out_fp32=False, pl=None,
-           check=True):
-    """Dense decode with freshly allocated outputs; returns (out, lse)."""
+           check=True, fast_fp8=False):
+    """Dense decode with freshly allocated outputs; returns (out, lse).
+
+    A cache of FP8 records (uint8 [pages, 64, 656]) goes, by default, through
+    the path whose scores are exact in the codes and scales
+    (mla_dense_fp8_decode_fwd, bf16 output).  fast_fp8=True selects the dense
+    kernel's FP8-record instance instead (mla_decode_fwd with
+    MLA_DTYPE_FP8_RECORD): faster, with each key value rounded once to fp16
+    (the bound is in the header)."""
     B, s_q, h_q, _ = q.shape
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(576)
+    if kv.dtype == torch.uint8 and not fast_fp8:
+        if out_fp32:
+            raise ValueError("the exact FP8-record path writes bf16; fast_fp8=True gives an fp32 output")
+        return dense_fp8_decode(q, kv, block_table, cache_seqlens, causal, softmax_scale, pl=pl, check=check)
     if pl is None:
         h_kv = 1 if kv.dim() == 3 else kv.shape[2]
         pl = plan(cache_seqlens, B, s_q * h_q, num_parts=mla_num_parts_dense(s_q, h_q, h_kv))

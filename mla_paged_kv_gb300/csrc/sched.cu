@@ -131,63 +131,64 @@ __device__ __forceinline__ void sched_walk(NtOf nt_of, int* diff, int n_units, i
 // does not fit with its F, and the rest opens the next partition with
 // cap - rest - F left.  Partitions that never end inside a unit end past the
 // last one.  The last partition takes everything left; returns its cost.
-// One warp, every lane running the same walk (lane 0 stores): the tile
-// counts come 32 at a time, one per lane, and reach the walk by shuffle, so
-// that only the budget arithmetic is serial.
+// One warp, every lane running the same walk (lane 0 stores): the tile counts
+// come 32 at a time, one per lane, by shuffle.  Each step is selects on the
+// budget and the partition index (a branch per step stalled the warp ~400
+// cycles a unit); the chunk count is a division by the constant w done as a
+// 64-bit multiply and one correction.  Once the last partition is reached the
+// rest of the units' cost is a warp sum.
 __device__ __forceinline__ long long sched_walk_record(const int* nt_of, int n_units, int num_parts, int fixed_cost,
                                                        int cap, int2* end) {
   const int lane = threadIdx.x & 31;
   const int last_p = num_parts - 1;
   const int w = cap - fixed_cost;  // tiles a partition takes from a unit it starts on and cannot finish
-  const float inv_w = w > 0 ? 1.f / static_cast<float>(w) : 0.f;
+  const int wc = max(w, 0);
+  const unsigned long long inv_w = w > 0 ? (1ull << 32) / static_cast<unsigned long long>(w) + 1ull : 0ull;
   int p = 0, budget = cap;
+  int u_stop = n_units;  // the unit in which the last partition begins (its rest is in `left`)
   long long left = 0;
-  for (int base = 0; base < n_units; base += 32) {
+  for (int base = 0; base < n_units && p < last_p; base += 32) {
     const int mine = base + lane < n_units ? nt_of[base + lane] : 0;
     const int cnt = min(32, n_units - base);
-    for (int j = 0; j < cnt; ++j) {
+    for (int j = 0; j < cnt && p < last_p; ++j) {
       const int x = __shfl_sync(0xffffffffu, mine, j);
-      if (x == 0) continue;
-      const int u = base + j;
-      if (p == last_p) {
-        left += x + fixed_cost;
-        continue;
+      const bool fits = x + fixed_cost <= budget;
+      const int t = max(budget - fixed_cost, 0);
+      const int r = x - t;  // >= 1 when the unit does not fit
+      // full chunks while the rest does not fit: (r - 1) / w (w > 0), else every partition
+      const unsigned int n1 = static_cast<unsigned int>(max(r - 1, 0));
+      int q = static_cast<int>((static_cast<unsigned long long>(n1) * inv_w) >> 32);
+      q -= (static_cast<long long>(q) * w > n1) ? 1 : 0;
+      q += (static_cast<long long>(q + 1) * w <= n1) ? 1 : 0;
+      const int k = (r + fixed_cost > cap) ? (w > 0 ? q : last_p) : 0;
+      const int kk = min(k, last_p - p - 1);  // chunk partitions before the last one
+      const bool split = !fits && x > 0;
+      if (split && lane == 0) {
+        end[p] = make_int2(base + j, t);
+        for (int i = 1; i <= kk; ++i) end[p + i] = make_int2(base + j, t + i * wc);
       }
-      if (x + fixed_cost <= budget) {
-        budget -= x + fixed_cost;
-        continue;
+      const int rem = r - kk * wc;
+      const int p_new = split ? p + 1 + kk : p;
+      if (split && p_new == last_p) {
+        left = rem + fixed_cost;
+        u_stop = base + j;
       }
-      int t = max(budget - fixed_cost, 0);
-      if (lane == 0) end[p] = make_int2(u, t);
-      ++p;
-      int r = x - t;
-      if (p < last_p && r + fixed_cost > cap) {
-        if (w <= 0) {
-          // nothing fits: every partition up to the last ends here, empty
-          for (; p < last_p; ++p)
-            if (lane == 0) end[p] = make_int2(u, t);
-        } else {
-          // full chunks while r > w: k = (r - 1) / w, from a float estimate
-          int k = __float2int_rz(static_cast<float>(r - 1) * inv_w);
-          while (k > 0 && k * w > r - 1) --k;
-          while ((k + 1) * w <= r - 1) ++k;
-          k = min(k, last_p - p);
-          for (int i = 1; i <= k; ++i)
-            if (lane == 0) end[p + i - 1] = make_int2(u, t + i * w);
-          p += k;
-          t += k * w;
-          r -= k * w;
-        }
-      }
-      if (p == last_p)
-        left += r + fixed_cost;
-      else
-        budget = cap - r - fixed_cost;
+      budget = split ? cap - rem - fixed_cost : (x > 0 ? budget - x - fixed_cost : budget);
+      p = p_new;
     }
   }
+  if (p == last_p && u_stop == n_units) u_stop = -1;  // one partition: it takes every unit
+  // the units after u_stop go to the last partition whole
+  long long rest = 0;
+  for (int u = u_stop + 1 + lane; u < n_units; u += 32) {
+    const int x = nt_of[u];
+    if (x > 0) rest += x + fixed_cost;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) rest += __shfl_xor_sync(0xffffffffu, rest, o);
   if (lane == 0)
-    for (int q = p; q < num_parts; ++q) end[q] = make_int2(n_units, 0);
-  return left;
+    for (int q2 = p; q2 < num_parts; ++q2) end[q2] = make_int2(n_units, 0);
+  return left + rest;
 }
 
 // Tile count of unit u straight from the lengths (for the many-units path).

@@ -183,10 +183,22 @@ def test_dense_fp8_records_bad_page_is_reported_and_masked():
     compare(out, lse, ro, rl)
 
 
-def test_dense_fp8_records_decode_helper():
-    case = wl.dense_fp8_case(2, 2, 64, 0, seqlens=[400, 90], causal=True, seed=196)
+@pytest.mark.parametrize("q_scale", [1.0, 8.0])
+def test_dense_fp8_decode_helper_default_is_exact(q_scale):
+    """mla.decode on an FP8-record cache takes the exact-score path by
+    default: the plain bars hold even for peaky queries (q x 8)."""
+    case = wl.dense_fp8_case(2, 2, 64, 0, seqlens=[400, 90], causal=True, q_scale=q_scale, seed=196)
     out, lse = mla.decode(case.q.cuda(), case.kv8.cuda(), case.block_table.cuda(), case.cache_seqlens.cuda(),
                           causal=True, softmax_scale=case.scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle(case)
+    compare(out, lse, ro, rl)
+
+
+def test_dense_fp8_decode_helper_fast_option():
+    case = wl.dense_fp8_case(2, 2, 64, 0, seqlens=[400, 90], causal=True, seed=198)
+    out, lse = mla.decode(case.q.cuda(), case.kv8.cuda(), case.block_table.cuda(), case.cache_seqlens.cuda(),
+                          causal=True, softmax_scale=case.scale, fast_fp8=True)
     torch.cuda.synchronize()
     ro, rl = oracle(case)
     compare(out, lse, ro, rl)

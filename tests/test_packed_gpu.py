@@ -133,3 +133,40 @@ def test_packed_topk_length_above_topk(where):
         assert st == 0
         ro, rl = orc.packed_decode(case.q.double().numpy(), packed, topk, tl.numpy(), case.scale)
         compare(out, lse, ro, rl)
+
+
+def test_packed_and_native_with_peaky_queries():
+    """q x 8.  The native sparse call keeps scores exact in codes and scales:
+    the plain bars hold.  The packed attention rounds each key value once to
+    fp16 (relative <= 2^-11 + 2^-20, the header's statement): its output meets
+    the plain O bars and each LSE stays within scale * (2^-11 + 2^-20) *
+    max_j sum_d |q_d k_jd| (+ fp32 slack) of the oracle's."""
+    topk = 256
+    case, ind = case_with_holes(2, 1, 128, topk, 16, [[topk], [150]], seed=88)
+    case.q = case.q * 8
+    packed, _ = orc.pack_selected(case.kv8.numpy(), ind.numpy(), case.topk_length.numpy())
+    out, lse, st, pl = run_packed(case, packed, topk)
+    assert st == 0
+    ro, rl = orc.packed_decode(case.q.double().numpy(), packed, topk, case.topk_length.numpy(), case.scale)
+    o = out.double().cpu().numpy()
+    assert np.abs(o - ro).max() <= 2e-2
+    assert np.linalg.norm(o - ro) / np.linalg.norm(ro) <= 5e-3
+    q = np.abs(case.q.double().numpy())
+    bound = np.zeros(q.shape[:3])
+    for b in range(2):
+        L = int(case.topk_length[b, 0])
+        sel = [int(i) for i in ind[b, 0, :L] if i >= 0]
+        k = np.abs(np.stack([orc.decode_record(case.kv8.numpy().reshape(-1, 656)[i]) for i in sel]))
+        dots = np.einsum("hd,jd->hj", q[b, 0], k)
+        bound[b, 0] = case.scale * (2.0 ** -11 + 2.0 ** -20) * dots.max(-1) + 1e-5
+    assert (np.abs(lse.double().cpu().numpy() - rl) <= bound).all()
+    out_n = torch.empty_like(out)
+    lse_n = torch.empty_like(lse)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_sparse_fp8_decode_fwd(case.q.cuda(), case.kv8.cuda(), ind.cuda(), case.topk_length.cuda(), pl.sched,
+                                  pl.split_offset, pl.num_parts, pl.workspace, out_n, lse_n, status, case.scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rn, rln, _ = orc.sparse_decode(case.q.double().numpy(), case.kv8.numpy(), ind.numpy(),
+                                   case.topk_length.numpy(), case.scale)
+    compare(out_n, lse_n, rn, rln)
