@@ -323,20 +323,19 @@ int mla_test_pack_timeout(const uint8_t* d_kv8, int num_pages, const int32_t* d_
                           int32_t* d_status, mla_stream_t stream);
 
 /* Sparse FP8 decode over a packed workspace (FlashMLA PR #200, "Packed
- * attention specialization"): attention of each query token over the
- * records that were packed for it.  The packed records are contiguous pages,
- * so the dense decode kernel runs over them (its FP8-record instance: page
- * u * tiles + t is tile t of unit u, the per-tile masks hide the slots whose
- * index was -1).  Each NoPE value enters the MMAs as fp16(code * scale) and
- * q and the RoPE dims as fp16, as for mla_decode_fwd with
- * MLA_DTYPE_FP8_RECORD: a score moves by at most
- * scale * (2^-11 + 2^-20) * sum_d |q_d k_d| from the exact one, where
- * mla_sparse_fp8_decode_fwd keeps the scores exact.  d_topk_length must be
- * the one given to the pack (it counts the tiles each unit schedules;
- * entries above topk are allowed, only the first topk slots exist); the
- * plan comes from mla_get_metadata exactly as for the native call (the
- * pages' H=128 packed path keeps the native scheduler).  h_q <= 128.  Other
- * arguments as for mla_sparse_fp8_decode_fwd. */
+ * attention specialization": the packed attention reuses the native
+ * dequantisation, softmax, split and combine pipeline and only replaces the
+ * index/page/gather loader with direct loads of the packed tiles).  The same
+ * kernel as mla_sparse_fp8_decode_fwd runs with slot t of unit u read from
+ * packed record u * tiles * 64 + t and masked by its mask bit: the scores stay
+ * exact in codes and scales, and under the same plan the result equals the
+ * native call's on the same selection bit for bit.  d_topk_length must be
+ * the one given to the pack (the plan counts each unit's tiles from it;
+ * entries above topk are allowed, only the first topk slots exist); the plan
+ * comes from mla_get_metadata exactly as for the native call (the pages'
+ * H=128 packed path keeps the native scheduler).  h_q <= 128.  A bad index
+ * was reported by the pack; this call reports none.  Other arguments as for
+ * mla_sparse_fp8_decode_fwd. */
 int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size_t packed_bytes, int topk,
                                      const int32_t* d_topk_length, int batch, int s_q, int h_q, float softmax_scale,
                                      const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,

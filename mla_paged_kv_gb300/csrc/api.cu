@@ -108,8 +108,6 @@ const DeviceInfo& device_info() {
           cudaSuccess ||
       cudaFuncSetAttribute(dense_kernel_ptr(4), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
           cudaSuccess ||
-      cudaFuncSetAttribute(dense_kernel_ptr(5), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
-          cudaSuccess ||
       cudaFuncSetAttribute(sparse_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            sparse_smem_bytes()) != cudaSuccess) {
     cudaGetLastError();
@@ -581,65 +579,16 @@ int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size
   const PackedLayout l = packed_layout(units, topk);
   if (packed_bytes < static_cast<size_t>(l.total)) return MLA_ERR_INVALID_ARG;
   const uint8_t* records = static_cast<const uint8_t*>(d_packed);
-  const uint64_t* masks = reinterpret_cast<const uint64_t*>(records + l.records_bytes);
   // the packed records form a pool of units * tiles pages of 64 records,
-  // unit u's tiles being pages u * tiles .. u * tiles + tiles - 1
+  // unit u's tiles being pages u * tiles .. u * tiles + tiles - 1; slot t of
+  // unit u is record u * tiles * 64 + t, live when its mask bit is set
   const long long pool_pages = units * l.tiles;
-  if (pool_pages > (1LL << 31) / MLA_PAGE_SIZE) return MLA_ERR_UNSUPPORTED;
-  if (!d_q || !d_sched || !d_split_offset || !d_workspace || !d_out || !d_lse || !d_status || h_q < 1 ||
-      num_parts < 1)
-    return MLA_ERR_INVALID_ARG;
-  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
-  if (h_q > MLA_ROWS_PER_BLOCK) return MLA_ERR_UNSUPPORTED;
-  if (!aligned16(d_q) || !aligned16(d_packed) || !aligned16(d_workspace) || !aligned16(d_out))
-    return MLA_ERR_INVALID_ARG;
-  const WorkspaceLayout w = ws_layout(static_cast<int>(units), h_q, num_parts);
-  if (workspace_bytes < w.total) return MLA_ERR_INVALID_ARG;
-  const DeviceInfo& d = device_info();
-  if (d.status != MLA_OK) return d.status;
-  // The dense kernel's FP8-record instance attends over the packed pages: a
-  // unit is one query token (its h_q rows), its keys the first
-  // min(topk_length, topk) packed slots, the per-tile masks hiding the
-  // slots whose index was -1 (their records are zero).
-  DecodeParams p{};
-  p.lengths = d_topk_length;
-  p.default_length = topk;
-  p.topk = topk;
-  p.packed_mask = masks;
-  p.n_units = static_cast<int>(units);
-  p.rows = h_q;
-  p.row_blocks = 1;
-  p.h_q = h_q;
-  p.s_q = 1;
-  p.h_kv = 1;
-  p.group_heads = h_q;
-  p.block_tokens = 0;
-  p.blocks_per_group = 1;
-  p.causal = 0;
-  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
-  p.num_pages = static_cast<int>(pool_pages);
-  p.sched = d_sched;
-  p.split_offset = d_split_offset;
-  p.num_parts = num_parts;
-  p.o_accum = static_cast<float*>(d_workspace);
-  p.lse_accum = reinterpret_cast<float*>(static_cast<char*>(d_workspace) + w.lse_off);
-  p.out = d_out;
-  p.out_type = MLA_DTYPE_BF16;
-  p.lse = d_lse;
-  p.status = d_status;
-  CUtensorMap qm, km, sm, rm;
-  void* q16 = static_cast<char*>(d_workspace) + w.q16_off;  // the kernel reads an fp16 copy of Q
-  int rc = encode_q_map(&qm, q16, units * h_q);
-  if (rc == MLA_OK) rc = encode_fp8_record_map(&km, records, static_cast<int>(pool_pages), 0);
-  if (rc == MLA_OK) rc = encode_fp8_record_map(&sm, records, static_cast<int>(pool_pages), 1);
-  if (rc == MLA_OK) rc = encode_fp8_record_map(&rm, records, static_cast<int>(pool_pages), 2);
-  if (rc != MLA_OK) return rc;
-  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_q_fp16(d_q, q16, static_cast<size_t>(units) * h_q * MLA_D_QK, d.sms, cs) != cudaSuccess)
-    return MLA_ERR_CUDA;
-  if (launch_dense(qm, km, sm, rm, p, num_parts, 5, cs) != cudaSuccess) return MLA_ERR_CUDA;
-  return mla_combine(d_workspace, workspace_bytes, d_split_offset, static_cast<int>(units), h_q, num_parts, d_out,
-                     0, d_lse, stream);
+  if (pool_pages * MLA_PAGE_SIZE > (1LL << 31) - 1) return MLA_ERR_UNSUPPORTED;
+  SlotSource src;
+  src.masks = reinterpret_cast<const uint64_t*>(records + l.records_bytes);
+  return sparse_decode(d_q, records, static_cast<int>(pool_pages), src, topk, d_topk_length, batch, s_q, h_q,
+                       softmax_scale, d_sched, d_split_offset, num_parts, d_workspace, workspace_bytes, d_out, d_lse,
+                       d_status, stream);
 }
 
 int mla_dense_fp8_unit_lengths(const int32_t* d_cache_seqlens, int batch, int s_q, int causal,

@@ -200,32 +200,11 @@ struct Cursor {
   bool valid;
 };
 
-// Keys of unit b as the partition plan counted them (its tile ranges).  The
-// packed instance (kPacked: FlashMLA PR #200, "Packed attention
-// specialization") serves packed selections: a unit is one query token and
-// the plan counts topk_length as given (all topk when no lengths are given),
-// while only the first min(topk_length, topk) packed slots exist; tiles past
-// them are walked with every key masked.  (A separate instance: the cursor is
-// inlined into every role, and the dense FP8-record instance ran measurably
-// slower with both forms compiled in.)
-template <bool kPacked>
-__device__ __forceinline__ int unit_plan_keys(const DecodeParams& p, int b) {
-  if constexpr (kPacked)
-    return p.lengths != nullptr ? max(p.lengths[b], 0) : p.default_length;
-  else
-    return max(p.lengths[b], 0);
-}
-
-// Packed selections: packed pages (tiles) per unit.
-__device__ __forceinline__ int packed_tiles(const DecodeParams& p) { return (p.topk + kTile - 1) / kTile; }
-
-template <bool kPacked>
 __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& P, Cursor& c, int from_b) {
   for (int b = from_b; unit_in_part(P, b, p.n_units); ++b) {
-    const int Lp = unit_plan_keys<kPacked>(p, b);
-    const int L = kPacked ? min(Lp, p.topk) : Lp;  // keys that exist
+    const int L = max(p.lengths[b], 0);
     const int lo = (b == P.b0) ? P.t0 : 0;
-    const int hi = (b == P.b1) ? P.t1 : num_tiles(Lp);
+    const int hi = (b == P.b1) ? P.t1 : num_tiles(L);
     if (hi > lo) {
       c.b = b;
       c.L = L;
@@ -239,22 +218,20 @@ __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& P
   c.valid = false;
 }
 
-template <bool kPacked>
 __device__ __forceinline__ void cursor_init(const DecodeParams& p, const Part& P, Cursor& c) {
   c.u = 0;
   c.t = 0;
-  cursor_seek<kPacked>(p, P, c, P.b0);
+  cursor_seek(p, P, c, P.b0);
 }
 
 __device__ __forceinline__ bool cursor_first(const Cursor& c) { return c.k == c.lo; }
 __device__ __forceinline__ bool cursor_last(const Cursor& c) { return c.k == c.hi - 1; }
 
-template <bool kPacked>
 __device__ __forceinline__ void cursor_next(const DecodeParams& p, const Part& P, Cursor& c) {
   ++c.t;
   if (++c.k == c.hi) {
     ++c.u;
-    cursor_seek<kPacked>(p, P, c, c.b + 1);
+    cursor_seek(p, P, c, c.b + 1);
   }
 }
 
@@ -281,16 +258,8 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
 // Page ids of 32 consecutive pages of unit c.b starting at `base`, one per lane
 // (0 past the partition's range; ids outside the pool are reported and read
 // as page 0, whose keys the softmax then masks).
-template <bool kPacked>
 __device__ __forceinline__ int load_page_window(const DecodeParams& p, const Cursor& c, int base, int lane) {
   const int kk = base + lane;
-  // packed selection: the unit's tiles are consecutive pages of the packed
-  // records; a tile past them (topk_length > topk) reads the unit's last one,
-  // every key masked
-  if constexpr (kPacked) {
-    const int tiles = packed_tiles(p);
-    return kk < c.hi ? c.b * tiles + min(kk, tiles - 1) : 0;
-  }
   int pg = 0;
   if (kk < c.hi) {
     pg = kk < p.max_pages ? p.block_table[static_cast<size_t>(c.b) * p.max_pages + kk] : -1;
@@ -477,14 +446,13 @@ __device__ __forceinline__ float ref_alpha(float r_old, float r_new) {
 // turned into fp16 in shared memory (records: fp16(code * scale); Q and
 // RoPE: bf16 -> fp16).  Otherwise the three maps view the 16-bit pool with
 // boxes of 4, 5 and 1 consecutive 64-dim slices (kv_map, sc_map, rope_map).
-template <bool kHalf, bool kFp8, bool kQV, bool kPacked>
+template <bool kHalf, bool kFp8, bool kQV>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     dense_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
                         const __grid_constant__ CUtensorMap sc_map, const __grid_constant__ CUtensorMap rope_map,
                         const DecodeParams p) {
   static_assert(!kFp8 || kHalf, "FP8 records are converted to fp16");
   static_assert(!(kFp8 && kQV), "the V-ring Q stage is for 16-bit KV");
-  static_assert(!kPacked || kFp8, "packed selections are FP8 records");
   constexpr int kNThreads = kFp8 ? kThreadsFp8 : kThreads;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -527,8 +495,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   if constexpr (kFp8) {
     P_first = load_part(p.sched, part_idx);
     if (warp == kWarpK || warp == kWarpV || warp == kWarpQ) {
-      cursor_init<kPacked>(p, P_first, c_first);
-      if (warp != kWarpQ && c_first.valid) page_first = load_page_window<kPacked>(p, c_first, c_first.k, lane);
+      cursor_init(p, P_first, c_first);
+      if (warp != kWarpQ && c_first.valid) page_first = load_page_window(p, c_first, c_first.k, lane);
     }
   }
 
@@ -621,7 +589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       page_base = c.k;
       cur_b = c.valid ? c.b : -1;
     } else {
-      cursor_init<kPacked>(p, P, c);
+      cursor_init(p, P, c);
     }
     bool ok = true;
     uint32_t k_issued[kKSlots] = {}, v_issued[kVSlots] = {};
@@ -633,7 +601,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         if (c.b != cur_b || c.k - page_base >= 32) {
           cur_b = c.b;
           page_base = c.k;
-          page_reg = load_page_window<kPacked>(p, c, page_base, lane);
+          page_reg = load_page_window(p, c, page_base, lane);
         }
         const int page_raw = __shfl_sync(0xffffffffu, page_reg, c.k - page_base);
         const int page = max(page_raw, 0);  // a page outside the pool (-1) reads page 0
@@ -706,7 +674,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       if (is_k && mine) ++own_k;
-      cursor_next<kPacked>(p, P, c);
+      cursor_next(p, P, c);
     }
     if (lane == 0) {
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
@@ -729,7 +697,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     if constexpr (kFp8) {
       const uint32_t cw = static_cast<uint32_t>(warp - kWarpConv);
       Cursor c;
-      cursor_init<kPacked>(p, P, c);
+      cursor_init(p, P, c);
       bool ok = true;
       uint32_t own_k = 0;
       while (ok && c.valid) {
@@ -769,7 +737,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[V_FULL + s]);
         }
-        cursor_next<kPacked>(p, P, c);
+        cursor_next(p, P, c);
       }
       if (!ok && lane == 0) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
     }
@@ -795,7 +763,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       if constexpr (kFp8)
         c = c_first;
       else
-        cursor_init<kPacked>(p, P, c);
+        cursor_init(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {}, vq_issued = 0;
       // box j of unit b into dst; into L2 only when bar is null
@@ -841,7 +809,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // on to the next unit; its Q into L2 while this one is worked on
         c.t += static_cast<uint32_t>(c.hi - c.k);
         ++c.u;
-        cursor_seek<kPacked>(p, P, c, c.b + 1);
+        cursor_seek(p, P, c, c.b + 1);
         if (ok && c.valid)
           for (int j = 0; j < 9; ++j) q_box(c.b, j, nullptr, nullptr);
       }
@@ -856,7 +824,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       if constexpr (kFp8)
         c = c_first;
       else
-        cursor_init<kPacked>(p, P, c);
+        cursor_init(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {};
       // box j of unit b into slot j % 3; into L2 only when bar is null
@@ -893,7 +861,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // on to the next unit; its Q into L2 while this one is worked on
         c.t += static_cast<uint32_t>(c.hi - c.k);
         ++c.u;
-        cursor_seek<kPacked>(p, P, c, c.b + 1);
+        cursor_seek(p, P, c, c.b + 1);
         if (ok && c.valid)
           for (int j = 0; j < 9; ++j) q_box(c.b, j, nullptr);
       }
@@ -915,7 +883,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       const uint64_t precv_desc = sdesc_sw128(smem_u32(sPRecv), 16, 1024);
       const uint16_t peer_mask = static_cast<uint16_t>(1u << peer);
       Cursor cv;
-      cursor_init<kPacked>(p, P, cv);
+      cursor_init(p, P, cv);
       uint32_t pv_own = 0, pv_recv = 0;
       bool ok = true;
       uint64_t t_last = globaltimer_ns();
@@ -953,7 +921,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
             }
             if (cursor_last(cv)) umma_commit(&bars[O_FULL]);
             MLA_TRACE(16, cv.t);
-            cursor_next<kPacked>(p, P, cv);
+            cursor_next(p, P, cv);
             progressed = true;
           }
         }
@@ -985,7 +953,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       // issues at most one job: a landed Q box's copies into TMEM, else the
       // next Q K^T half.
       Cursor cq;
-      cursor_init<kPacked>(p, P, cq);
+      cursor_init(p, P, cq);
       uint32_t a_own = 0;
       int q_phase = 0;          // 0: next is QKa of cq, 1: next is QKb of cq
       uint32_t qb_seen = 0;     // Q boxes seen landed (nine per unit, in order)
@@ -1003,7 +971,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
               if (qb_seen < 9u * static_cast<uint32_t>(cq.u + 1)) return false;
               umma_commit(&bars[Q_EMPTY]);
             }
-            cursor_next<kPacked>(p, P, cq);
+            cursor_next(p, P, cq);
             q_phase = 0;
             continue;
           }
@@ -1125,25 +1093,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     const uint32_t peer_l_full = mapa_shared(smem_u32(&bars[L_FULL]), peer);
     const uint32_t peer_l_free = mapa_shared(smem_u32(&bars[L_FREE]), peer);
     Cursor c;
-    cursor_init<kPacked>(p, P, c);
-    // Packed selection: the next own tile's valid-slot bits, read a whole
-    // received tile ahead (when the cursor reaches the received tile before
-    // it), so that the load is done long before the scores are; only an own
-    // tile that starts a unit reads its bits one step ahead.
-    auto tile_mask = [&](int b, int k) -> uint64_t {
-      const int tiles = packed_tiles(p);
-      return k < tiles ? p.packed_mask[static_cast<size_t>(b) * tiles + k] : 0ull;
-    };
-    uint64_t mask_own = ~0ull;
-    auto prefetch_mask = [&]() {
-      if (!kPacked || !c.valid) return;
-      if ((c.t & 1u) != rank) {
-        if (!cursor_last(c)) mask_own = tile_mask(c.b, c.k + 1);
-      } else if (cursor_first(c) || c.t == 0) {
-        mask_own = tile_mask(c.b, c.k);
-      }
-    };
-    prefetch_mask();
+    cursor_init(p, P, c);
     bool ok = true;
     uint32_t own_i = 0, recv_i = 0, units = 0;
     float r_cur = -INFINITY;  // reference (log2 units) after the last tile seen
@@ -1163,7 +1113,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         const int jmax = p.causal ? (c.L - p.s_q + tok) : (c.L - 1);  // last visible key
         const int vis = jmax - c.k * kT;                                // keys 0..vis of this tile are visible
         uint64_t keep = (vis >= kT - 1 ? ~0ull : (vis < 0 ? 0ull : (~0ull >> (kT - 1 - vis))));
-        if constexpr (kPacked) keep &= mask_own;
         ok = warp_wait(&bars[S_FULL], own_i & 1, abort_flag);
         if (!ok) break;
         if (tid == 0) MLA_TRACE(4, t);
@@ -1172,7 +1121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         // Read before S_FREE: the producer rewrites the entry only after that.
         // (Read from shared memory, not the block table: a global load here
         // sat on every own tile's critical path and cost 4-9 us per call.)
-        if (!kPacked && sBad[own_i & 1]) keep = 0ull;
+        if (sBad[own_i & 1]) keep = 0ull;
         float s[kT];
         {
           uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
@@ -1183,7 +1132,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         }
         tc_fence_before();
         mbar_arrive(&bars[S_FREE]);
-        // masked keys (past the last visible one, or unused packed slots) ->
+        // masked keys (past the last visible one, or on a page outside the pool) ->
         // -inf; raw tile max (the scale is positive, so max commutes with it)
         if (keep != ~0ull) {
           const uint32_t klo = static_cast<uint32_t>(keep), khi = static_cast<uint32_t>(keep >> 32);
@@ -1285,8 +1234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
         ++recv_i;
       }
       const int b_here = c.b, u_here = c.u;
-      cursor_next<kPacked>(p, P, c);
-      prefetch_mask();
+      cursor_next(p, P, c);
       if (!last) continue;
       // ---- row sum of the unit: ours + the peer's, both relative to r_cur
       if (units >= 1) {
@@ -1427,22 +1375,21 @@ __global__ void __launch_bounds__(256) q_fp16_kernel(const uint4* __restrict__ q
 
 int dense_smem_bytes() { return dn::kSmemBytes; }
 // kind 0: bf16, 1: fp16, 2: FP8 records (bf16 Q), 3: bf16 with the V-ring Q
-// stage, 4: fp16 with it, 5: packed FP8 records (bf16 Q)
-int dense_threads(int kind) { return kind == 2 || kind == 5 ? dn::kThreadsFp8 : dn::kThreads; }
+// stage, 4: fp16 with it
+int dense_threads(int kind) { return kind == 2 ? dn::kThreadsFp8 : dn::kThreads; }
 const void* dense_kernel_ptr(int kind) {
   switch (kind) {
-    case 1: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, false, false>);
-    case 2: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true, false, false>);
-    case 3: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, true, false>);
-    case 4: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, true, false>);
-    case 5: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true, false, true>);
-    default: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, false, false>);
+    case 1: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, false>);
+    case 2: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true, false>);
+    case 3: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, true>);
+    case 4: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, true>);
+    default: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, false>);
   }
 }
 
 namespace {
 
-template <bool kHalf, bool kFp8, bool kQV, bool kPacked>
+template <bool kHalf, bool kFp8, bool kQV>
 cudaError_t launch_instance(const CUtensorMap& q_map, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
                             const CUtensorMap& rope_map, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -1457,7 +1404,7 @@ cudaError_t launch_instance(const CUtensorMap& q_map, const CUtensorMap& kv_map,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = kFp8 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, dn::dense_decode_kernel<kHalf, kFp8, kQV, kPacked>, q_map, kv_map, sc_map,
+  return cudaLaunchKernelEx(&cfg, dn::dense_decode_kernel<kHalf, kFp8, kQV>, q_map, kv_map, sc_map,
                             rope_map, p);
 }
 
@@ -1468,12 +1415,11 @@ cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, co
                          cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
   switch (kind) {
-    case 1: return launch_instance<true, false, false, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
-    case 2: return launch_instance<true, true, false, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
-    case 3: return launch_instance<false, false, true, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
-    case 4: return launch_instance<true, false, true, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
-    case 5: return launch_instance<true, true, false, true>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
-    default: return launch_instance<false, false, false, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    case 1: return launch_instance<true, false, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    case 2: return launch_instance<true, true, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    case 3: return launch_instance<false, false, true>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    case 4: return launch_instance<true, false, true>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    default: return launch_instance<false, false, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
   }
 }
 
