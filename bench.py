@@ -299,7 +299,8 @@ def time_other_workloads(mla, wl, timed, steps, names=None):
                 mla.mla_sparse_fp8_decode_fwd(q, kv8, ind, tl, pl.sched, pl.split_offset, pl.num_parts,
                                               pl.workspace, out, lse, status, case.scale)
         elif fp8_dense:
-            # the dense kernel over the FP8 record cache (dtype FP8_RECORD)
+            # the FP8 record cache through mla_decode_fwd (dtype FP8_RECORD: the
+            # sparse kernel with the block table as its slot source, dense plan)
             kv8, bt, sl = case.kv8.cuda(), case.block_table.cuda(), case.cache_seqlens.cuda()
             pl = mla.plan(sl, B, s_q * h_q, num_parts=mla.mla_num_parts_dense(s_q, h_q, 1))
 
@@ -329,22 +330,6 @@ def time_other_workloads(mla, wl, timed, steps, names=None):
             fl = dense_flops(case)
             res[name]["tflops"] = fl / (us * 1e-6) / 1e12
             res[name]["pct_of_bf16_tensor_peak"] = 100.0 * res[name]["tflops"] / bf16_peak_tflops()
-        if fp8_dense:
-            # the exact-score path (the FP8 sparse kernel addressing the same cache by block table)
-            ul = torch.empty(B * s_q, dtype=torch.int32, device="cuda")
-            mla.mla_dense_fp8_unit_lengths(sl, s_q, case.causal, ul)
-            pl_x = mla.plan(ul, B * s_q, h_q, sparse=True)
-
-            def fn_x():
-                mla.mla_dense_fp8_decode_fwd(q, kv8, bt, ul, pl_x.sched, pl_x.split_offset, pl_x.num_parts,
-                                             pl_x.workspace, out, lse, status, case.scale)
-            for _ in range(5):
-                fn_x()
-            us_x = 1e3 * statistics.mean(timed(fn_x, steps))
-            mla.check_status(status, name + " exact-score path")
-            res[name + "_exact_scores"] = {"us_per_call": us_x, "gb_per_s": nbytes / (us_x * 1e-6) / 1e9,
-                                           "path": "mla_dense_fp8_decode_fwd (FP8 sparse kernel, scores exact in "
-                                                   "codes and scales)"}
         if sparse:
             res[name + "_packed"] = time_packed(mla, case, q, kv8, ind, tl, pl, out, lse, status, timed, steps)
             # the same call under the request-local partition plan

@@ -158,16 +158,17 @@ int mla_get_metadata_request_local(const int32_t* d_lengths, int default_length,
  *                  format": 512 E4M3 NoPE codes, four fp32 scales, one per
  *                  128 dims, 64 bf16 RoPE dims), q is bf16, h_kv must be 1.
  *                  Token j of request b is record j%64 of page
- *                  block_table[b][j/64].  The kernel turns each NoPE value
- *                  into fp16(code * scale) (relative error <= 2^-11 + 2^-20
- *                  inside fp16's normal range) and q and the RoPE dims into
- *                  fp16 (exact inside that range; q's fp16 copy is written
- *                  to the workspace by a kernel launched just before the
- *                  decode), then runs the fp16 path:
- *                  a score moves by at most scale * (2^-11 + 2^-20) *
- *                  sum_d |q_d k_d|.  Values must lie inside fp16's range.
- *                  mla_dense_fp8_decode_fwd keeps the scores exact in the
- *                  codes and scales instead (slower).
+ *                  block_table[b][j/64], decoded as for
+ *                  mla_sparse_fp8_decode_fwd (FlashMLA PR #183, "Limitations
+ *                  / future work", names an FP8 cache as missing from its
+ *                  dense kernel without giving a format; PR #200's record is
+ *                  the FP8 format the pages define).  This dtype runs the
+ *                  sparse kernel with the block table as its slot source and
+ *                  a whole request as its unit, under the same plan and
+ *                  workspace as the 16-bit caches: the scores stay exact in
+ *                  codes and scales (a per-group fp32 accumulator each, the
+ *                  scales applied in fp32), the value scale is folded into
+ *                  P (rounded to bf16).
  *   causal         1: query token i sees keys j <= L_b - s_q + i.
  *   softmax_scale  multiplies q.k (e.g. 1/sqrt(576)); must be finite and > 0.
  *   d_sched, d_split_offset, num_parts: from mla_get_metadata (or its
@@ -341,36 +342,6 @@ int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size
                                      const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
                                      void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
                                      int32_t* d_status, mla_stream_t stream);
-
-/* Dense decode over a paged cache of FP8 records.  FlashMLA PR #183
- * (Limitations / future work) names an FP8 KV cache as missing from its SM80
- * dense kernel without a format; the FP8 format the pages define is PR #200's
- * 656-byte record, so that is the cache format here: d_kv8 [num_pages, 64,
- * 656], token j of request b is record j%64 of page block_table[b][j/64], and
- * its key/value decode exactly as for mla_sparse_fp8_decode_fwd.  Every token
- * is a key (no selection); the sparse kernel runs with block-table addressing.
- *   d_q            bf16 [batch, s_q, h_q, 576], h_q <= 128
- *   d_block_table  int32 [batch, max_pages]; a page outside [0, num_pages) at
- *                  a position the unit reads is masked and reported
- *                  (MLA_ERR_BAD_INDEX).
- *   d_unit_lengths int32 [batch * s_q]: keys each query token sees, from
- *                  mla_dense_fp8_unit_lengths (causal alignment as for
- *                  mla_decode_fwd); also the d_lengths of the plan:
- *                  mla_get_metadata(d_unit_lengths, -1, batch*s_q, num_parts,
- *                  ...) with num_parts = mla_num_parts(h_q, 1).
- *   d_workspace    >= mla_workspace_bytes(batch*s_q, h_q, num_parts)
- *   d_out bf16 [batch, s_q, h_q, 512], d_lse fp32 [batch, s_q, h_q]. */
-int mla_dense_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, const int32_t* d_block_table, int max_pages,
-                             int num_pages, const int32_t* d_unit_lengths, int batch, int s_q, int h_q,
-                             float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
-                             int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
-                             int32_t* d_status, mla_stream_t stream);
-
-/* Keys seen by each query token of a dense cache: unit b*s_q + i gets
- * max(L_b - s_q + i + 1, 0) when causal, else L_b (d_cache_seqlens int32
- * [batch] -> d_unit_lengths int32 [batch * s_q]). */
-int mla_dense_fp8_unit_lengths(const int32_t* d_cache_seqlens, int batch, int s_q, int causal,
-                               int32_t* d_unit_lengths, mla_stream_t stream);
 
 /* Gather + unpack of selected records to fp32 key rows, bit-exact:
  * k[d] = fp32(e4m3[d]) * scale[d/128] as one fp32 round-to-nearest-even

@@ -26,8 +26,7 @@ __all__ = [
     "mla_get_metadata", "mla_decode_fwd", "mla_decode_splits", "mla_combine",
     "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws",
     "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd",
-    "mla_get_metadata_request_local", "mla_num_parts_dense", "mla_dense_fp8_decode_fwd",
-    "mla_dense_fp8_unit_lengths", "mla_test_pack_timeout", "plan", "decode", "dense_fp8_decode",
+    "mla_get_metadata_request_local", "mla_num_parts_dense", "mla_test_pack_timeout", "plan", "decode",
     "sparse_decode", "pack_selected_kv", "packed_sparse_decode",
     "EXPORTED_SYMBOLS",
 ]
@@ -37,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack",
     "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv",
     "mla_sparse_fp8_packed_decode_fwd", "mla_get_metadata_request_local", "mla_num_parts_dense",
-    "mla_dense_fp8_decode_fwd", "mla_dense_fp8_unit_lengths", "mla_test_pack_timeout",
+    "mla_test_pack_timeout",
 )
 
 _P = ctypes.c_void_p
@@ -49,8 +48,6 @@ _SIGS = {
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_num_parts": (_I, [_I, _I]),
     "mla_num_parts_dense": (_I, [_I, _I, _I]),
-    "mla_dense_fp8_decode_fwd": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _P, _P, _P]),
-    "mla_dense_fp8_unit_lengths": (_I, [_P, _I, _I, _I, _P, _P]),
     "mla_workspace_bytes": (_SZ, [_I, _I, _I]),
     "mla_get_metadata": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "mla_get_metadata_request_local": (_I, [_P, _I, _I, _I, _P, _P, _P]),
@@ -217,8 +214,9 @@ def _dense_args(q, kv, block_table, cache_seqlens, sched, split_offset, num_part
 
 def mla_decode_fwd(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse, status,
                    causal=False, softmax_scale=1.0 / 24.0, stream=None):
-    """Dense decode.  q/kv bf16 or fp16 (same type); kv [pages, 64, 576] or
-    [pages, 64, h_kv, 576]; out bf16, fp16 or fp32."""
+    """Dense decode.  q/kv bf16 or fp16 (same type), kv [pages, 64, 576] or
+    [pages, 64, h_kv, 576]; or a bf16 q over FP8 records, kv uint8
+    [pages, 64, 656].  out bf16, fp16 or fp32."""
     args = _dense_args(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse,
                        status, causal, softmax_scale, stream)
     _check(load_library().mla_decode_fwd(*args), "mla_decode_fwd")
@@ -323,32 +321,6 @@ def mla_sparse_fp8_packed_decode_fwd(q, packed, topk, topk_length, sched, split_
         _ptr(status), _stream(stream)), "mla_sparse_fp8_packed_decode_fwd")
 
 
-def mla_dense_fp8_unit_lengths(cache_seqlens, s_q, causal, unit_lengths, stream=None):
-    _need(cache_seqlens, torch.int32, "cache_seqlens", 1)
-    _need(unit_lengths, torch.int32, "unit_lengths")
-    if unit_lengths.numel() < cache_seqlens.shape[0] * s_q:
-        raise ValueError("unit_lengths too small")
-    _check(load_library().mla_dense_fp8_unit_lengths(_ptr(cache_seqlens), cache_seqlens.shape[0], int(s_q),
-                                                     int(bool(causal)), _ptr(unit_lengths), _stream(stream)),
-           "mla_dense_fp8_unit_lengths")
-
-
-def mla_dense_fp8_decode_fwd(q, kv8, block_table, unit_lengths, sched, split_offset, num_parts, workspace, out, lse,
-                             status, softmax_scale=1.0 / 24.0, stream=None):
-    _need(q, torch.bfloat16, "q", 4)
-    _need(kv8, torch.uint8, "kv8", 3)
-    _need(block_table, torch.int32, "block_table", 2)
-    _need(unit_lengths, torch.int32, "unit_lengths")
-    _need(out, torch.bfloat16, "out", 4)
-    B, s_q, h_q, d = q.shape
-    if d != 576 or kv8.shape[1:] != (64, 656) or block_table.shape[0] != B:
-        raise ValueError("q must be [B, s_q, h_q, 576], kv8 [pages, 64, 656], block_table [B, max_pages]")
-    _check(load_library().mla_dense_fp8_decode_fwd(
-        _ptr(q), _ptr(kv8), _ptr(block_table), block_table.shape[1], kv8.shape[0], _ptr(unit_lengths), B, s_q, h_q,
-        float(softmax_scale), _ptr(sched), _ptr(split_offset), int(num_parts), _ptr(workspace), workspace.numel(),
-        _ptr(out), _ptr(lse), _ptr(status), _stream(stream)), "mla_dense_fp8_decode_fwd")
-
-
 # ---------------------------------------------------------------- helpers
 
 
@@ -384,22 +356,13 @@ def check_status(status: torch.Tensor, where: str):
 
 
 def decode(q, kv, block_table, cache_seqlens, causal=False, softmax_scale=None, out_fp32=False, pl=None,
-           check=True, fast_fp8=False):
-    """Dense decode with freshly allocated outputs; returns (out, lse).
-
-    A cache of FP8 records (uint8 [pages, 64, 656]) goes, by default, through
-    the path whose scores are exact in the codes and scales
-    (mla_dense_fp8_decode_fwd, bf16 output).  fast_fp8=True selects the dense
-    kernel's FP8-record instance instead (mla_decode_fwd with
-    MLA_DTYPE_FP8_RECORD): faster, with each key value rounded once to fp16
-    (the bound is in the header)."""
+           check=True):
+    """Dense decode with freshly allocated outputs; returns (out, lse).  The
+    cache is bf16 or fp16 latent rows, or FP8 records (uint8 [pages, 64, 656],
+    bf16 q)."""
     B, s_q, h_q, _ = q.shape
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(576)
-    if kv.dtype == torch.uint8 and not fast_fp8:
-        if out_fp32:
-            raise ValueError("the exact FP8-record path writes bf16; fast_fp8=True gives an fp32 output")
-        return dense_fp8_decode(q, kv, block_table, cache_seqlens, causal, softmax_scale, pl=pl, check=check)
     if pl is None:
         h_kv = 1 if kv.dim() == 3 else kv.shape[2]
         pl = plan(cache_seqlens, B, s_q * h_q, num_parts=mla_num_parts_dense(s_q, h_q, h_kv))
@@ -458,23 +421,4 @@ def packed_sparse_decode(q, packed, topk, topk_length=None, softmax_scale=None, 
                                      pl.workspace, out, lse, status, softmax_scale)
     if check:
         check_status(status, "mla_sparse_fp8_packed_decode_fwd")
-    return out, lse
-
-
-def dense_fp8_decode(q, kv8, block_table, cache_seqlens, causal=False, softmax_scale=None, pl=None, check=True):
-    """Dense decode over a paged FP8 record cache with freshly allocated outputs; returns (out, lse)."""
-    B, s_q, h_q, _ = q.shape
-    if softmax_scale is None:
-        softmax_scale = 1.0 / math.sqrt(576)
-    unit_lengths = torch.empty(B * s_q, dtype=torch.int32, device=q.device)
-    mla_dense_fp8_unit_lengths(cache_seqlens, s_q, causal, unit_lengths)
-    if pl is None:
-        pl = plan(unit_lengths, B * s_q, h_q, sparse=True, device=q.device)
-    out = torch.empty(B, s_q, h_q, 512, dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty(B, s_q, h_q, dtype=torch.float32, device=q.device)
-    status = torch.zeros(1, dtype=torch.int32, device=q.device)
-    mla_dense_fp8_decode_fwd(q, kv8, block_table, unit_lengths, pl.sched, pl.split_offset, pl.num_parts,
-                             pl.workspace, out, lse, status, softmax_scale)
-    if check:
-        check_status(status, "mla_dense_fp8_decode_fwd")
     return out, lse

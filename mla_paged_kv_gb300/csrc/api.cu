@@ -15,7 +15,6 @@
 namespace mla {
 cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, int, cudaStream_t);
 cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, int, void*, int, float*, cudaStream_t);
-cudaError_t launch_q_fp16(const void*, void*, size_t, int, cudaStream_t);
 cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                          const DecodeParams&, int, int, cudaStream_t);
 int dense_smem_bytes();
@@ -26,7 +25,6 @@ int sparse_smem_bytes();
 int sparse_threads();
 const void* sparse_kernel_ptr();
 cudaError_t launch_unpack(const uint8_t*, int, const int32_t*, int, float*, int32_t*, cudaStream_t);
-cudaError_t launch_unit_lengths(const int32_t*, int, int, int, int32_t*, cudaStream_t);
 cudaError_t launch_pack(const uint8_t*, int, const int32_t*, int, const int32_t*, int, uint8_t*, uint64_t*,
                         int32_t*, int, cudaStream_t);
 }  // namespace mla
@@ -98,25 +96,20 @@ const DeviceInfo& device_info() {
     d.ready = true;
     return d;
   }
-  if (cudaFuncSetAttribute(dense_kernel_ptr(0), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(dense_kernel_ptr(1), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(dense_kernel_ptr(2), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(dense_kernel_ptr(3), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(dense_kernel_ptr(4), cudaFuncAttributeMaxDynamicSharedMemorySize, dense_smem_bytes()) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(sparse_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           sparse_smem_bytes()) != cudaSuccess) {
+  bool attr_ok = cudaFuncSetAttribute(sparse_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      sparse_smem_bytes()) == cudaSuccess;
+  for (int kind = 0; kind < 4; ++kind)
+    attr_ok = attr_ok && cudaFuncSetAttribute(dense_kernel_ptr(kind), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              dense_smem_bytes()) == cudaSuccess;
+  if (!attr_ok) {
     cudaGetLastError();
     d.status = MLA_ERR_CUDA;
     d.ready = true;
     return d;
   }
+  // the dense plan also sizes the FP8-record calls, which run the sparse kernel
   d.dense_clusters = std::min(max_clusters(dense_kernel_ptr(0), dense_threads(0), dense_smem_bytes()),
-                              max_clusters(dense_kernel_ptr(2), dense_threads(2), dense_smem_bytes()));
+                              max_clusters(sparse_kernel_ptr(), sparse_threads(), sparse_smem_bytes()));
   d.sparse_clusters = max_clusters(sparse_kernel_ptr(), sparse_threads(), sparse_smem_bytes());
   cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
   if (d.dense_clusters <= 0 || d.sparse_clusters <= 0 || d.sms <= 0) {
@@ -132,7 +125,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WorkspaceLayout {
-  size_t o_bytes, lse_off, q16_off, total;
+  size_t o_bytes, lse_off, total;
 };
 
 WorkspaceLayout ws_layout(int n_units, int rows, int num_parts) {
@@ -140,9 +133,7 @@ WorkspaceLayout ws_layout(int n_units, int rows, int num_parts) {
   WorkspaceLayout w;
   w.o_bytes = slots * rows * MLA_D_V * sizeof(float);
   w.lse_off = align_up(w.o_bytes, 256);
-  // then the fp16 copy of Q that the FP8-record calls make once per call
-  w.q16_off = align_up(w.lse_off + slots * rows * sizeof(float), 256);
-  w.total = align_up(w.q16_off + static_cast<size_t>(n_units) * rows * MLA_D_QK * 2, 256);
+  w.total = align_up(w.lse_off + slots * rows * sizeof(float), 256);
   return w;
 }
 
@@ -182,25 +173,6 @@ int encode_kv_map(CUtensorMap* m, const void* kv, int num_pages, int h_kv, int s
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
 }
 
-// Pool of FP8 records [num_pages][64][656] as a 2-D byte tensor (656, rows =
-// num_pages * 64); one box covers the 64 records of a page.  kind 0: the
-// E4M3 codes of one 128-dim scale group (128 B per record, unswizzled, 8 KB);
-// 1: the four fp32 scales (16 B per record, 1 KB); 2: the 64 bf16 RoPE dims
-// (128 B per record, 128-byte swizzle: lands as the 16-bit box an MMA reads).
-int encode_fp8_record_map(CUtensorMap* m, const void* kv8, int num_pages, int kind) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return MLA_ERR_CUDA;
-  cuuint64_t dims[2] = {656, static_cast<cuuint64_t>(num_pages) * MLA_PAGE_SIZE};
-  cuuint64_t strides[1] = {656};
-  const cuuint32_t inner = kind == 1 ? 16 : 128;
-  cuuint32_t box[2] = {inner, MLA_PAGE_SIZE};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv8), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, kind == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARG;
-}
-
 // Dense Q with h_kv > 1 as [tokens = batch*s_q][h_kv][group_heads][576], dims
 // innermost first: (576, group_heads, h_kv, tokens).  One box = 64 dims x
 // group_heads heads x block_tokens tokens of one head group.
@@ -224,15 +196,13 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
                   const int32_t* seqlens, int batch, int s_q, int h_q, int h_kv, int dtype, int causal, float scale,
                   const int32_t* sched, const int32_t* split_offset, int num_parts, void* workspace,
                   size_t workspace_bytes, void* out, int out_type, float* lse, int32_t* status, DecodeParams* p,
-                  CUtensorMap* q_map, CUtensorMap* kv_map, CUtensorMap* sc_map, CUtensorMap* rope_map,
-                  void** q16) {
+                  CUtensorMap* q_map, CUtensorMap* kv_map, CUtensorMap* sc_map, CUtensorMap* rope_map) {
   if (!q || !kv || !block_table || !seqlens || !sched || !split_offset || !workspace || !out || !lse || !status)
     return MLA_ERR_INVALID_ARG;
   if (batch < 1 || s_q < 1 || h_q < 1 || h_kv < 1 || max_pages < 1 || num_pages < 1 || num_parts < 1)
     return MLA_ERR_INVALID_ARG;
   if (h_q % h_kv != 0) return MLA_ERR_INVALID_ARG;
-  if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_FP16 && dtype != MLA_DTYPE_FP8_RECORD) return MLA_ERR_INVALID_ARG;
-  if (dtype == MLA_DTYPE_FP8_RECORD && h_kv != 1) return MLA_ERR_UNSUPPORTED;
+  if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_FP16) return MLA_ERR_INVALID_ARG;
   if (out_type != MLA_DTYPE_BF16 && out_type != MLA_DTYPE_FP32 && out_type != MLA_DTYPE_FP16)
     return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return MLA_ERR_INVALID_ARG;
@@ -255,25 +225,16 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
   if (2LL * num_parts * row_blocks > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
   const DeviceInfo& d = device_info();
   if (d.status != MLA_OK) return d.status;
-  // FP8 records: the kernel reads the fp16 copy of Q in the workspace
-  *q16 = dtype == MLA_DTYPE_FP8_RECORD ? static_cast<char*>(workspace) + w.q16_off : nullptr;
-  int rc = h_kv == 1 ? encode_q_map(q_map, *q16 ? *q16 : q, static_cast<long long>(batch) * rows)
+  int rc = h_kv == 1 ? encode_q_map(q_map, q, static_cast<long long>(batch) * rows)
                      : encode_q_map_groups(q_map, q, static_cast<long long>(batch) * s_q, h_kv, group_heads,
                                            block_tokens);
   if (rc != MLA_OK) return rc;
-  if (dtype == MLA_DTYPE_FP8_RECORD) {
-    if (static_cast<long long>(num_pages) * MLA_PAGE_SIZE > (1LL << 31) - 1) return MLA_ERR_UNSUPPORTED;
-    rc = encode_fp8_record_map(kv_map, kv, num_pages, 0);
-    if (rc == MLA_OK) rc = encode_fp8_record_map(sc_map, kv, num_pages, 1);
-    if (rc == MLA_OK) rc = encode_fp8_record_map(rope_map, kv, num_pages, 2);
-  } else {
-    // 16-bit KV: the three box widths the producers load (a value half: 4
-    // slices; rank 0's K slot: slices 4-8; rank 1's RoPE slice), passed in the
-    // kernel's kv / sc / rope map parameters
-    rc = encode_kv_map(kv_map, kv, num_pages, h_kv, 4);
-    if (rc == MLA_OK) rc = encode_kv_map(sc_map, kv, num_pages, h_kv, 5);
-    if (rc == MLA_OK) rc = encode_kv_map(rope_map, kv, num_pages, h_kv, 1);
-  }
+  // the three box widths the producers load (a value half: 4 slices; rank
+  // 0's K slot: slices 4-8; rank 1's RoPE slice), passed in the kernel's kv /
+  // sc / rope map parameters
+  rc = encode_kv_map(kv_map, kv, num_pages, h_kv, 4);
+  if (rc == MLA_OK) rc = encode_kv_map(sc_map, kv, num_pages, h_kv, 5);
+  if (rc == MLA_OK) rc = encode_kv_map(rope_map, kv, num_pages, h_kv, 1);
   if (rc != MLA_OK) return rc;
   *p = DecodeParams{};
   p->lengths = seqlens;
@@ -307,6 +268,98 @@ int dense_prepare(const void* q, const void* kv, const int32_t* block_table, int
   p->lse = lse;
   p->status = status;
   return MLA_OK;
+}
+
+// How a unit's slots address the record pool: an index list (native
+// sparse), per-tile masks over packed records, or a block table (dense FP8).
+struct SlotSource {
+  const int32_t* indices = nullptr;
+  const uint64_t* masks = nullptr;
+  const int32_t* block_table = nullptr;
+  int max_pages = 0;
+};
+
+// One launch of the sparse kernel over a record pool, and its combine.  A
+// unit is one query token (native and packed selections: rows = h_q <= 128)
+// or one request (a dense FP8 cache under the dense plan: rows = s_q * h_q
+// in row blocks of 128, token-major, with the causal alignment per row).
+struct SparseCall {
+  const void* q = nullptr;
+  const uint8_t* kv8 = nullptr;
+  int num_pages = 0;
+  SlotSource src;
+  int topk = 0;                      // slots per unit that may exist
+  const int32_t* lengths = nullptr;  // keys (slots) per unit, or NULL: topk
+  int n_units = 0, rows = 0, s_q = 1, h_q = 0, causal = 0, unit_request_div = 1;
+  float scale = 0.f;
+  const int32_t* sched = nullptr;
+  const int32_t* split_offset = nullptr;
+  int num_parts = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  void* out = nullptr;
+  int out_type = MLA_DTYPE_BF16;
+  float* lse = nullptr;
+  int32_t* status = nullptr;
+  mla_stream_t stream = nullptr;
+};
+
+int sparse_run(const SparseCall& c, bool combine) {
+  if (!c.q || !c.kv8 || (!c.src.indices && !c.src.masks && !c.src.block_table) || !c.sched || !c.split_offset ||
+      !c.ws || !c.out || !c.lse || !c.status)
+    return MLA_ERR_INVALID_ARG;
+  if (c.n_units < 1 || c.rows < 1 || c.h_q < 1 || c.num_pages < 1 || c.topk < 1 || c.num_parts < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (c.out_type != MLA_DTYPE_BF16 && c.out_type != MLA_DTYPE_FP32 && c.out_type != MLA_DTYPE_FP16)
+    return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(c.scale) || !(c.scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (c.n_units > 65535) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c.n_units) * c.rows > (1LL << 31) - 1) return MLA_ERR_UNSUPPORTED;
+  // record ordinals are 32-bit
+  if (static_cast<long long>(c.num_pages) * MLA_PAGE_SIZE > (1LL << 31) - 1) return MLA_ERR_UNSUPPORTED;
+  if (!aligned16(c.q) || !aligned16(c.kv8) || !aligned16(c.ws) || !aligned16(c.out)) return MLA_ERR_INVALID_ARG;
+  const WorkspaceLayout w = ws_layout(c.n_units, c.rows, c.num_parts);
+  if (c.ws_bytes < w.total) return MLA_ERR_INVALID_ARG;
+  const int row_blocks = (c.rows + MLA_ROWS_PER_BLOCK - 1) / MLA_ROWS_PER_BLOCK;
+  if (2LL * c.num_parts * row_blocks > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
+  const DeviceInfo& d = device_info();
+  if (d.status != MLA_OK) return d.status;
+  DecodeParams p{};
+  p.lengths = c.lengths;
+  p.default_length = c.topk;
+  p.n_units = c.n_units;
+  p.rows = c.rows;
+  p.row_blocks = row_blocks;
+  p.h_q = c.h_q;
+  p.s_q = c.s_q;
+  p.h_kv = 1;
+  p.causal = c.causal;
+  p.scale_log2 = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634);
+  p.num_pages = c.num_pages;
+  p.indices = c.src.indices;
+  p.packed_mask = c.src.masks;
+  p.block_table = c.src.block_table;
+  p.max_pages = c.src.max_pages;
+  p.unit_request_div = c.unit_request_div;
+  p.topk = c.topk;
+  p.kv8 = c.kv8;
+  p.sched = c.sched;
+  p.split_offset = c.split_offset;
+  p.num_parts = c.num_parts;
+  p.o_accum = static_cast<float*>(c.ws);
+  p.lse_accum = reinterpret_cast<float*>(static_cast<char*>(c.ws) + w.lse_off);
+  p.out = c.out;
+  p.out_type = c.out_type;
+  p.lse = c.lse;
+  p.status = c.status;
+  CUtensorMap qm;
+  const int rc = encode_q_map(&qm, c.q, static_cast<long long>(c.n_units) * c.rows);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(c.stream);
+  if (launch_sparse(qm, p, c.num_parts, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (!combine) return MLA_OK;
+  return mla_combine(c.ws, c.ws_bytes, c.split_offset, c.n_units, c.rows, c.num_parts, c.out, c.out_type, c.lse,
+                     c.stream);
 }
 
 }  // namespace
@@ -386,18 +439,51 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
                       int dtype, int causal, float softmax_scale, const int32_t* d_sched,
                       const int32_t* d_split_offset, int num_parts, void* d_workspace, size_t workspace_bytes,
                       void* d_out, int out_type, float* d_lse, int32_t* d_status, mla_stream_t stream) {
+  if (dtype == MLA_DTYPE_FP8_RECORD) {
+    // A cache of FP8 records runs the sparse kernel (exact scores in codes
+    // and scales) with the block table as the slot source and a whole
+    // request as the unit, under the same plan as the 16-bit caches.
+    if (!d_block_table || !d_cache_seqlens || max_pages < 1 || batch < 1 || s_q < 1 || h_q < 1)
+      return MLA_ERR_INVALID_ARG;
+    if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
+    const long long rows = static_cast<long long>(s_q) * h_q;
+    if (rows > (1 << 20) || static_cast<long long>(max_pages) * MLA_PAGE_SIZE > (1LL << 31) - 1)
+      return MLA_ERR_UNSUPPORTED;
+    SparseCall c;
+    c.q = d_q;
+    c.kv8 = static_cast<const uint8_t*>(d_kv);
+    c.num_pages = num_pages;
+    c.src.block_table = d_block_table;
+    c.src.max_pages = max_pages;
+    c.topk = max_pages * MLA_PAGE_SIZE;
+    c.lengths = d_cache_seqlens;
+    c.n_units = batch;
+    c.rows = static_cast<int>(rows);
+    c.s_q = s_q;
+    c.h_q = h_q;
+    c.causal = causal ? 1 : 0;
+    c.unit_request_div = 1;
+    c.scale = softmax_scale;
+    c.sched = d_sched;
+    c.split_offset = d_split_offset;
+    c.num_parts = num_parts;
+    c.ws = d_workspace;
+    c.ws_bytes = workspace_bytes;
+    c.out = d_out;
+    c.out_type = out_type;
+    c.lse = d_lse;
+    c.status = d_status;
+    c.stream = stream;
+    return sparse_run(c, false);
+  }
   DecodeParams p;
   CUtensorMap qm, km, sm, rm;
-  void* q16 = nullptr;
   const int rc = dense_prepare(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q,
                                h_kv, dtype, causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
-                               workspace_bytes, d_out, out_type, d_lse, d_status, &p, &qm, &km, &sm, &rm, &q16);
+                               workspace_bytes, d_out, out_type, d_lse, d_status, &p, &qm, &km, &sm, &rm);
   if (rc != MLA_OK) return rc;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (q16 != nullptr &&
-      launch_q_fp16(d_q, q16, static_cast<size_t>(batch) * p.rows * MLA_D_QK, device_info().sms, cs) != cudaSuccess)
-    return MLA_ERR_CUDA;
-  const int kind = dtype == MLA_DTYPE_FP8_RECORD ? 2 : (dtype == MLA_DTYPE_FP16 ? 1 : 0) + (p.q_vring ? 3 : 0);
+  const int kind = (dtype == MLA_DTYPE_FP16 ? 1 : 0) + (p.q_vring ? 2 : 0);
   return launch_dense(qm, km, sm, rm, p, num_parts, kind, cs) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -434,68 +520,36 @@ int mla_decode_fwd(const void* d_q, const void* d_kv, const int32_t* d_block_tab
 
 namespace {
 
-// Sparse attention over a record pool: the native selection (indices into
-// the paged pool) or a packed one (masks over the packed records).
-// How a unit's slots address the record pool: an index list (native
-// sparse), per-tile masks over packed records, or a block table (dense FP8).
-struct SlotSource {
-  const int32_t* indices = nullptr;
-  const uint64_t* masks = nullptr;
-  const int32_t* block_table = nullptr;
-  int max_pages = 0;
-};
-
+// A selection (native or packed): one unit per query token, h_q <= 128 rows.
 int sparse_decode(const void* d_q, const uint8_t* d_kv8, int num_pages, SlotSource src, int topk,
                   const int32_t* d_topk_length, int batch, int s_q, int h_q, float softmax_scale,
                   const int32_t* d_sched, const int32_t* d_split_offset, int num_parts, void* d_workspace,
                   size_t workspace_bytes, void* d_out, float* d_lse, int32_t* d_status, mla_stream_t stream) {
-  if (!d_q || !d_kv8 || (!src.indices && !src.masks && !src.block_table) || !d_sched || !d_split_offset || !d_workspace || !d_out || !d_lse || !d_status)
-    return MLA_ERR_INVALID_ARG;
-  if (batch < 1 || s_q < 1 || h_q < 1 || num_pages < 1 || topk < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
-  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (batch < 1 || s_q < 1 || h_q < 1) return MLA_ERR_INVALID_ARG;
   if (h_q > MLA_ROWS_PER_BLOCK) return MLA_ERR_UNSUPPORTED;
   const long long units = static_cast<long long>(batch) * s_q;
   if (units > 65535) return MLA_ERR_UNSUPPORTED;
-  if (!aligned16(d_q) || !aligned16(d_kv8) || !aligned16(d_workspace) || !aligned16(d_out))
-    return MLA_ERR_INVALID_ARG;
-  const WorkspaceLayout w = ws_layout(static_cast<int>(units), h_q, num_parts);
-  if (workspace_bytes < w.total) return MLA_ERR_INVALID_ARG;
-  const DeviceInfo& d = device_info();
-  if (d.status != MLA_OK) return d.status;
-  DecodeParams p{};
-  p.lengths = d_topk_length;
-  p.default_length = topk;
-  p.n_units = static_cast<int>(units);
-  p.rows = h_q;
-  p.row_blocks = 1;
-  p.h_q = h_q;
-  p.s_q = src.block_table != nullptr ? s_q : 1;  // dense FP8: unit u is token u % s_q of request u / s_q
-  p.causal = 0;
-  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
-  p.num_pages = num_pages;
-  p.indices = src.indices;
-  p.packed_mask = src.masks;
-  p.block_table = src.block_table;
-  p.max_pages = src.max_pages;
-  p.topk = topk;
-  p.kv8 = d_kv8;
-  p.sched = d_sched;
-  p.split_offset = d_split_offset;
-  p.num_parts = num_parts;
-  p.o_accum = static_cast<float*>(d_workspace);
-  p.lse_accum = reinterpret_cast<float*>(static_cast<char*>(d_workspace) + w.lse_off);
-  p.out = d_out;
-  p.out_type = MLA_DTYPE_BF16;
-  p.h_kv = 1;
-  p.lse = d_lse;
-  p.status = d_status;
-  CUtensorMap qm;
-  const int rc = encode_q_map(&qm, d_q, units * h_q);
-  if (rc != MLA_OK) return rc;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_sparse(qm, p, num_parts, s) != cudaSuccess) return MLA_ERR_CUDA;
-  return mla_combine(d_workspace, workspace_bytes, d_split_offset, static_cast<int>(units), h_q, num_parts, d_out,
-                     0, d_lse, stream);
+  SparseCall c;
+  c.q = d_q;
+  c.kv8 = d_kv8;
+  c.num_pages = num_pages;
+  c.src = src;
+  c.topk = topk;
+  c.lengths = d_topk_length;
+  c.n_units = static_cast<int>(units);
+  c.rows = h_q;
+  c.h_q = h_q;
+  c.scale = softmax_scale;
+  c.sched = d_sched;
+  c.split_offset = d_split_offset;
+  c.num_parts = num_parts;
+  c.ws = d_workspace;
+  c.ws_bytes = workspace_bytes;
+  c.out = d_out;
+  c.lse = d_lse;
+  c.status = d_status;
+  c.stream = stream;
+  return sparse_run(c, true);
 }
 
 // Packed workspace layout: records, then one 64-bit mask per (unit, tile).
@@ -591,32 +645,6 @@ int mla_sparse_fp8_packed_decode_fwd(const void* d_q, const void* d_packed, size
                        d_status, stream);
 }
 
-int mla_dense_fp8_unit_lengths(const int32_t* d_cache_seqlens, int batch, int s_q, int causal,
-                               int32_t* d_unit_lengths, mla_stream_t stream) {
-  if (!d_cache_seqlens || !d_unit_lengths || batch < 1 || s_q < 1) return MLA_ERR_INVALID_ARG;
-  if (static_cast<long long>(batch) * s_q > 65535) return MLA_ERR_UNSUPPORTED;
-  return launch_unit_lengths(d_cache_seqlens, batch, s_q, causal ? 1 : 0, d_unit_lengths,
-                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? MLA_OK
-             : MLA_ERR_CUDA;
-}
-
-int mla_dense_fp8_decode_fwd(const void* d_q, const uint8_t* d_kv8, const int32_t* d_block_table, int max_pages,
-                             int num_pages, const int32_t* d_unit_lengths, int batch, int s_q, int h_q,
-                             float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset,
-                             int num_parts, void* d_workspace, size_t workspace_bytes, void* d_out, float* d_lse,
-                             int32_t* d_status, mla_stream_t stream) {
-  if (!d_block_table || !d_unit_lengths || max_pages < 1) return MLA_ERR_INVALID_ARG;
-  if (static_cast<long long>(max_pages) * MLA_PAGE_SIZE > (1LL << 30) ||
-      static_cast<long long>(num_pages) * MLA_PAGE_SIZE > (1LL << 30))
-    return MLA_ERR_UNSUPPORTED;
-  SlotSource src;
-  src.block_table = d_block_table;
-  src.max_pages = max_pages;
-  return sparse_decode(d_q, d_kv8, num_pages, src, max_pages * MLA_PAGE_SIZE, d_unit_lengths, batch, s_q, h_q,
-                       softmax_scale, d_sched, d_split_offset, num_parts, d_workspace, workspace_bytes, d_out, d_lse,
-                       d_status, stream);
-}
 
 int mla_sparse_fp8_unpack(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int n, float* d_k_out,
                           int32_t* d_status, mla_stream_t stream) {

@@ -38,7 +38,7 @@ struct DecodeParams {
   int group_heads;          // h_q / h_kv
   int block_tokens;         // h_kv > 1: tokens per row block (group_heads * block_tokens <= 128)
   int blocks_per_group;     // row blocks per head group
-  int s_q;                  // dense: tokens per unit (causal alignment); sparse: 1
+  int s_q;                  // query tokens per request (causal alignment)
   int causal;
   float scale_log2;         // softmax_scale * log2(e)
   // dense
@@ -51,6 +51,10 @@ struct DecodeParams {
   int topk;
   const uint8_t* kv8;       // [num_pages, 64, 656]; packed: the packed records
   const uint64_t* packed_mask;  // packed: [n_units, ceil(topk/64)] valid-slot bits, else NULL
+  // sparse kernel over a dense FP8 cache (block_table set): unit b reads
+  // block-table row b / unit_request_div (s_q when a unit is one query token
+  // of a request, 1 when it is the whole request)
+  int unit_request_div;
   // schedule
   const int32_t* sched;
   const int32_t* split_offset;

@@ -5,8 +5,8 @@
 // of a request (all heads share one latent KV head), over the keys of one
 // split: S = Q K^T on 576 dims, online softmax, O = P V with V = the first
 // 512 dims of the same latent rows; then O / l and the split's LSE.  Keys
-// come from 64-token pages (bf16 or fp16, one or more latent KV heads, or
-// FlashMLA PR #200's 656-byte FP8 records) through the block table.
+// come from 64-token pages (bf16 or fp16, one or more latent KV heads)
+// through the block table.
 //
 // How (GB300 design, not the page's SM80 one):
 //  * TMEM holds 512 fp32 columns per SM, exactly one 128 x 512 accumulator,
@@ -42,16 +42,11 @@
 //    the softmax warps write the epilogue while Q streams in.  (Instance
 //    kQV: the first unit's nine boxes load at once, boxes 0-5 staged in the
 //    still-empty V ring.)
-//  * FP8 records (instance kFp8): the producers bring each box in as raw
-//    codes and scales, three converter warps turn them into fp16 boxes in
-//    place (RoPE goes bf16 -> fp16), and the rest is the fp16 path.  Q is
-//    turned into fp16 once per call, by a small kernel launched just before
-//    (q_fp16_kernel), rather than by every CTA pair that reads it.
 //  * One tile = nine 64-dim slices (8 KB swizzled boxes) of one page.  The
 //    four that are this CTA's V half go to a 3-slot "V" ring for every tile
 //    (P V reads them; for its own tiles Q K^T reads them too); the other five
 //    go to a "K" slot, for own tiles only, released as soon as Q K^T has read
-//    them.  16-bit KV: each range of consecutive slices comes in ONE TMA
+//    them.  Each range of consecutive slices comes in ONE TMA
 //    instruction (a 5-D box of four or five slices; rank 1's K slot takes
 //    two): the TMA engine's time goes mostly per instruction, so that moves
 //    the same bytes with a third of the engine time of 8 KB boxes.
@@ -60,7 +55,7 @@
 // Roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane),
 //        warp 4 K-slot producer, warp 5 V-ring producer,
 //        warp 6 Q K^T issuer (and Q copies into TMEM) and TMEM owner,
-//        warp 7 Q producer, warp 8 P V issuer (warps 9-11: FP8 converters).
+//        warp 7 Q producer, warp 8 P V issuer.
 //        Q K^T and P V come from two threads so that a ready P V does not
 //        wait for a Q K^T block to finish issuing; they touch different TMEM
 //        accumulators.
@@ -132,10 +127,8 @@ enum : int {
   O_FULL = PV_DONE + 2,
   O_FREE,
   DRAIN,
-  RAW_K,                      // +slot, FP8 records: the K slot's raw bytes have landed
-  RAW_V = RAW_K + kKSlots,    // +slot, FP8 records: a V slot's raw bytes have landed
-  VQ_FULL = RAW_V + kVSlots,  // 16-bit KV: the first unit's Q boxes 0-5 have landed in the V ring
-  VQ_EMPTY,                          // ... and have been copied into TMEM: the V ring is free
+  VQ_FULL,   // V-ring Q stage: the first unit's Q boxes 0-5 have landed in the V ring
+  VQ_EMPTY,  // ... and have been copied into TMEM: the V ring is free
   kNumBars
 };
 
@@ -149,22 +142,8 @@ static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffPOwn % 1024 == 0 && 
 static_assert(kOffRefOut % 16 == 0 && kOffRefIn % 16 == 0 && kOffLOut % 16 == 0 && kOffLIn % 16 == 0,
               "bulk copies need 16-byte alignment");
 
-constexpr int kThreads = 288;      // bf16 / fp16 KV
-constexpr int kThreadsFp8 = 384;   // FP8 record KV: three more warps convert the records
+constexpr int kThreads = 288;
 constexpr int kWarpK = 4, kWarpV = 5, kWarpMma = 6, kWarpQ = 7, kWarpPV = 8;
-constexpr int kWarpConv = 9, kConvWarps = 3;  // FP8 record converters: warps 9-11
-// FP8 records (FlashMLA PR #200, section "FP8 KV cache format"): 656 bytes =
-// 512 E4M3 NoPE codes, four fp32 scales (one per 128 dims), 64 bf16 RoPE.
-constexpr int kRecBytes = 656;
-static_assert(512 + 16 + 128 == kRecBytes, "record layout");
-// Raw bytes of a pair of 64-dim NoPE boxes (one 128-dim scale group): the
-// codes as one box of 64 records x 128 B (8 KB, unswizzled), landing in the
-// pair's second box, and the page's scales (64 x 16 B), landing at the start
-// of the pair's first box.
-constexpr int kFp8PairCodeBytes = kT * 128;
-constexpr int kFp8ScaleBytes = kT * 16;
-constexpr int kFp8KSlotTx = 2 * (kFp8PairCodeBytes + kFp8ScaleBytes) + kBoxBytes;  // two pairs + RoPE
-constexpr int kFp8VSlotTx = 2 * (kFp8PairCodeBytes + kFp8ScaleBytes);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
 constexpr uint32_t kTmemS = 256;  // S: [256, 320)
@@ -306,88 +285,6 @@ __device__ __forceinline__ void issue_qk_v(uint32_t d, uint32_t tmem, uint64_t q
   qk_box<kHalf, 4 * kRank + 3>(d, tmem, q_desc0, vslot + ((3 * kBoxBytes) >> 4), false);
 }
 
-// A pair of 64-dim NoPE boxes of a page of FP8 records, in place: the raw
-// codes of both (64 records x 128 B, record-major, in `hi`) and the page's
-// 64 x 4 fp32 scales (at the start of `lo`) become the two 64 x 64 fp16 boxes
-// (8 KB each, 128-byte swizzle) that the MMAs read, value = code * scale
-// rounded to fp16.  Per value pair: one conversion (two E4M3 codes -> two
-// exact fp16) and three fp16x2 ops.  The record's scale s is split as
-// s = 2^e * (s_hi + s_lo), s_hi = fp16(s / 2^e) with s / 2^e in [1, 2) and
-// s_lo = fp16(s / 2^e - s_hi); then v = fma(c, s_hi, c * s_lo) is c * s / 2^e
-// rounded once up to a relative 2^-21, and v * 2^e is exact (a power of two)
-// unless it falls below fp16's normal range.  So each value carries a
-// relative error <= 2^-11 + 2^-20 inside fp16's normal range.  `sg` = the
-// pair's scale group.
-// One warp, compact code (the kernel is large; instruction fetch matters).
-// Each lane first takes the scales of records lane and lane + 32 into
-// registers (the scale bytes are overwritten later).  Then, group by group,
-// the 8 records 8k..8k+7: their 1 KB of raw codes is read, and the same
-// bytes of `hi` (its rows 8k..8k+7) and rows 8k..8k+7 of `lo` are written.
-__device__ __forceinline__ void convert_fp8_pair(uint8_t* lo, uint8_t* hi, int sg, int lane) {
-  const float* scales = reinterpret_cast<const float*>(lo);
-  const float sc0 = scales[lane * 4 + sg], sc1 = scales[(lane + 32) * 4 + sg];
-  __syncwarp();
-#pragma unroll 1
-  for (int k = 0; k < 8; ++k) {
-    // lane L: 16 codes at raw bytes 16L and 512 + 16L of the group: records
-    // 8k + L/8 and 8k + 4 + L/8, dims 16 * (L % 8) .. of the pair's 128
-    const uint4 c0 = reinterpret_cast<const uint4*>(hi + 1024 * k)[lane];
-    const uint4 c1 = reinterpret_cast<const uint4*>(hi + 1024 * k)[32 + lane];
-    const int r0 = 8 * k + (lane >> 3), r1 = r0 + 4;
-    const uint32_t sb0 = __float_as_uint(__shfl_sync(0xffffffffu, k < 4 ? sc0 : sc1, r0 & 31));
-    const uint32_t sb1 = __float_as_uint(__shfl_sync(0xffffffffu, k < 4 ? sc0 : sc1, r1 & 31));
-    __syncwarp();  // the group's raw bytes are all read before any lane writes them
-    const int d = lane & 7;                 // 16-code chunk of the pair's 128 dims
-    uint8_t* box = d < 4 ? lo : hi;          // dims 0-63 -> lo, 64-127 -> hi
-    const uint32_t cc = 2u * static_cast<uint32_t>(d & 3);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t sb = h ? sb1 : sb0;
-      const uint4 code = h ? c1 : c0;
-      const int row = h ? r1 : r0;
-      const float sm = __uint_as_float((sb & 0x807FFFFFu) | (127u << 23));  // s / 2^e in [1, 2) (sign kept)
-      const __half shi = __float2half_rn(sm);
-      const __half2 s_hi = __half2half2(shi);
-      const __half2 s_lo = __half2half2(__float2half_rn(sm - __half2float(shi)));
-      const __half2 s_pow = __half2half2(__float2half_rn(__uint_as_float(sb & 0x7F800000u)));  // 2^e
-      const uint32_t in[4] = {code.x, code.y, code.z, code.w};
-      uint32_t w[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const __half2_raw hr =
-            __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((in[i >> 1] >> (16 * (i & 1))) & 0xFFFFu),
-                                       __NV_E4M3);
-        const __half2 cv = *reinterpret_cast<const __half2*>(&hr);
-        const __half2 v = __hmul2(__hfma2(cv, s_hi, __hmul2(cv, s_lo)), s_pow);
-        w[i] = *reinterpret_cast<const uint32_t*>(&v);
-      }
-      uint8_t* rowp = box + row * 128;
-      const uint32_t sw = static_cast<uint32_t>(row & 7);
-      *reinterpret_cast<uint4*>(rowp + ((cc ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(rowp + (((cc + 1u) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-    }
-  }
-}
-
-// A box of `words` 32-bit words of bf16 pairs -> fp16 pairs, in place, by
-// one warp (elementwise, so any swizzle is kept).  bf16 -> f32 is exact and
-// f32 -> fp16 rounds to nearest even: exact for values inside fp16's normal
-// range (bf16 carries 8 significant bits, fp16 11).
-__device__ __forceinline__ void bf16_box_to_fp16(uint8_t* box, int words, int lane) {
-  uint4* v = reinterpret_cast<uint4*>(box);
-#pragma unroll 2
-  for (int i = lane; i < words / 4; i += 32) {
-    uint4 x = v[i];
-    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
-      w[k] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    v[i] = x;
-  }
-}
-
 // Two fp32 -> one packed pair of 16-bit floats (round to nearest even).
 template <bool kHalf>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -440,20 +337,14 @@ __device__ __forceinline__ float ref_alpha(float r_old, float r_new) {
 // and all nine boxes load at once (a separate instance, chosen when many
 // partitions share each request, so that the other instances keep their
 // code unchanged).
-// kHalf: the MMAs take fp16 operands (else bf16).  kFp8 (with kHalf): KV is
-// a pool of FP8 records (kv_map = their codes in 64-byte boxes, sc_map =
-// scales, rope_map = RoPE as a swizzled bf16 box) and Q is bf16; both are
-// turned into fp16 in shared memory (records: fp16(code * scale); Q and
-// RoPE: bf16 -> fp16).  Otherwise the three maps view the 16-bit pool with
-// boxes of 4, 5 and 1 consecutive 64-dim slices (kv_map, sc_map, rope_map).
-template <bool kHalf, bool kFp8, bool kQV>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
+// kHalf: Q and KV are fp16 (else bf16).  The three maps view the 16-bit
+// pool with boxes of 4, 5 and 1 consecutive 64-dim slices (kv_map, sc_map,
+// rope_map).
+template <bool kHalf, bool kQV>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     dense_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
                         const __grid_constant__ CUtensorMap sc_map, const __grid_constant__ CUtensorMap rope_map,
                         const DecodeParams p) {
-  static_assert(!kFp8 || kHalf, "FP8 records are converted to fp16");
-  static_assert(!(kFp8 && kQV), "the V-ring Q stage is for 16-bit KV");
-  constexpr int kNThreads = kFp8 ? kThreadsFp8 : kThreads;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -484,22 +375,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   const int grp = blk / p.blocks_per_group;  // KV head group (0 when h_kv = 1)
   const int rb = blk - grp * p.blocks_per_group;
 
-  // FP8 records: the partition, and for the producers of K, V and Q the
-  // first unit and its first 32 page ids (three dependent global reads), are
-  // read before the setup below so that their latency overlaps it.  (The
-  // 16-bit instances read them after the setup: the same change there
-  // perturbed their code and cost 3-5 us.)
-  Part P_first{};
-  Cursor c_first{};
-  int page_first = 0;
-  if constexpr (kFp8) {
-    P_first = load_part(p.sched, part_idx);
-    if (warp == kWarpK || warp == kWarpV || warp == kWarpQ) {
-      cursor_init(p, P_first, c_first);
-      if (warp != kWarpQ && c_first.valid) page_first = load_page_window(p, c_first, c_first.k, lane);
-    }
-  }
-
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(&bars[Q_EMPTY], 1);
@@ -510,17 +385,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     mbar_init(&bars[VQ_FULL], 1);
     mbar_init(&bars[VQ_EMPTY], 1);
     for (int i = 0; i < kKSlots; ++i) {
-      mbar_init(&bars[K_FULL + i], kFp8 ? kConvWarps : 1);
+      mbar_init(&bars[K_FULL + i], 1);
       mbar_init(&bars[K_EMPTY + i], 1);
     }
-    // FP8 records: a slot is full when the converter warps are done with it
-    // rather than when its TMA bytes land
     for (int i = 0; i < kVSlots; ++i) {
-      mbar_init(&bars[V_FULL + i], kFp8 ? kConvWarps : 1);
+      mbar_init(&bars[V_FULL + i], 1);
       mbar_init(&bars[V_EMPTY + i], 1);
     }
-    for (int i = 0; i < kKSlots; ++i) mbar_init(&bars[RAW_K + i], 1);
-    for (int i = 0; i < kVSlots; ++i) mbar_init(&bars[RAW_V + i], 1);
     mbar_init(&bars[S_FULL], 1);
     mbar_init(&bars[S_FREE], 128);
     mbar_init(&bars[OWN_GO], 128);
@@ -546,10 +417,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   if (q_box_bytes < static_cast<uint32_t>(kQBoxBytes)) {
     // Q boxes of a head group cover fewer than 128 rows: the rows past them stay
     // zero (in the Q buffer, and in the V ring where the first unit's Q lands)
-    for (int i = tid; i < kQSmemBoxes * kQBoxBytes / 16; i += kNThreads)
+    for (int i = tid; i < kQSmemBoxes * kQBoxBytes / 16; i += kThreads)
       reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (kQV)
-      for (int i = tid; i < 6 * kQBoxBytes / 16; i += kNThreads)
+      for (int i = tid; i < 6 * kQBoxBytes / 16; i += kThreads)
         reinterpret_cast<uint4*>(sV)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
@@ -558,13 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     tmem_relinquish();
   }
   if (warp == kWarpQ && lane == 0) prefetch_tmap(&q_map);
-  if (warp == kWarpK && lane == 0) {
-    prefetch_tmap(&kv_map);
-    if constexpr (kFp8) {
-      prefetch_tmap(&sc_map);
-      prefetch_tmap(&rope_map);
-    }
-  }
+  if (warp == kWarpK && lane == 0) prefetch_tmap(&kv_map);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -573,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
 
-  const Part P = kFp8 ? P_first : load_part(p.sched, part_idx);
+  const Part P = load_part(p.sched, part_idx);
   bool aborted = false;
   uint32_t r_seen = 0, l_seen = 0;  // reference / row-sum messages received (armed phases)
 
@@ -583,14 +448,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     const uint64_t pol_kv = policy_evict_first();
     Cursor c;
     int page_reg = 0, page_base = -1, cur_b = -1;
-    if constexpr (kFp8) {
-      c = c_first;
-      page_reg = page_first;
-      page_base = c.k;
-      cur_b = c.valid ? c.b : -1;
-    } else {
-      cursor_init(p, P, c);
-    }
+    cursor_init(p, P, c);
     bool ok = true;
     uint32_t k_issued[kKSlots] = {}, v_issued[kVSlots] = {};
     uint32_t own_k = 0;
@@ -619,27 +477,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
               __threadfence_block();
               MLA_TRACE(9, c.t);
               uint8_t* dst = sK + s * kKSlotBytes;
-              if constexpr (kFp8) {
-                // raw bytes (the other value half as two code pairs + scales, and
-                // the RoPE box); the converters make the fp16 boxes and fill K_FULL
-                uint64_t* bar = &bars[RAW_K + s];
-                mbar_arrive_expect_tx(bar, kFp8KSlotTx);
-                const int x0 = 256 * (1 - static_cast<int>(rank));
-#pragma unroll
-                for (int pr = 0; pr < 2; ++pr) {
-                  tma_load_2d(dst + (2 * pr + 1) * kBoxBytes, &kv_map, bar, x0 + 128 * pr, page * kT, pol_kv);
-                  tma_load_2d(dst + (2 * pr) * kBoxBytes, &sc_map, bar, 512, page * kT, pol_kv);
-                }
-                tma_load_2d(dst + 4 * kBoxBytes, &rope_map, bar, 528, page * kT, pol_kv);
+              mbar_arrive_expect_tx(&bars[K_FULL + s], kKSlotBytes);
+              if (rank == 0) {
+                tma_load_5d(dst, &sc_map, &bars[K_FULL + s], 0, 0, k_box<0>(0), grp, page, pol_kv);
               } else {
-                mbar_arrive_expect_tx(&bars[K_FULL + s], kKSlotBytes);
-                if (rank == 0) {
-                  tma_load_5d(dst, &sc_map, &bars[K_FULL + s], 0, 0, k_box<0>(0), grp, page, pol_kv);
-                } else {
-                  tma_load_5d(dst, &kv_map, &bars[K_FULL + s], 0, 0, k_box<1>(0), grp, page, pol_kv);
-                  tma_load_5d(dst + 4 * kBoxBytes, &rope_map, &bars[K_FULL + s], 0, 0, k_box<1>(4), grp, page,
-                              pol_kv);
-                }
+                tma_load_5d(dst, &kv_map, &bars[K_FULL + s], 0, 0, k_box<1>(0), grp, page, pol_kv);
+                tma_load_5d(dst + 4 * kBoxBytes, &rope_map, &bars[K_FULL + s], 0, 0, k_box<1>(4), grp, page,
+                            pol_kv);
               }
               ++k_issued[s];
             }
@@ -647,26 +491,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
             const uint32_t n = c.t / kVSlots;
             const int s = static_cast<int>(c.t % kVSlots);
             if (n >= 1) ok = mbar_wait(&bars[V_EMPTY + s], (n - 1) & 1, abort_flag);
-            // 16-bit KV: the ring holds the first unit's Q until it is in TMEM
+            // V-ring Q stage: the ring holds the first unit's Q until it is in TMEM
             if constexpr (kQV) {
               if (c.t == 0 && ok) ok = mbar_wait(&bars[VQ_EMPTY], 0, abort_flag);
             }
             if (ok) {
               MLA_TRACE(7, c.t);
               uint8_t* dst = sV + s * kVSlotBytes;
-              if constexpr (kFp8) {
-                uint64_t* bar = &bars[RAW_V + s];
-                mbar_arrive_expect_tx(bar, kFp8VSlotTx);
-                const int x0 = 256 * static_cast<int>(rank);
-#pragma unroll
-                for (int pr = 0; pr < 2; ++pr) {
-                  tma_load_2d(dst + (2 * pr + 1) * kBoxBytes, &kv_map, bar, x0 + 128 * pr, page * kT, pol_kv);
-                  tma_load_2d(dst + (2 * pr) * kBoxBytes, &sc_map, bar, 512, page * kT, pol_kv);
-                }
-              } else {
-                mbar_arrive_expect_tx(&bars[V_FULL + s], kVSlotBytes);
-                tma_load_5d(dst, &kv_map, &bars[V_FULL + s], 0, 0, 4 * static_cast<int>(rank), grp, page, pol_kv);
-              }
+              mbar_arrive_expect_tx(&bars[V_FULL + s], kVSlotBytes);
+              tma_load_5d(dst, &kv_map, &bars[V_FULL + s], 0, 0, 4 * static_cast<int>(rank), grp, page, pol_kv);
               ++v_issued[s];
             }
           }
@@ -680,90 +513,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // no TMA write may land after this CTA exits
       for (int s = 0; s < kKSlots; ++s)
-        if (k_issued[s] > 0) mbar_wait(&bars[(kFp8 ? RAW_K : K_FULL) + s], (k_issued[s] - 1) & 1, nullptr);
+        if (k_issued[s] > 0) mbar_wait(&bars[K_FULL + s], (k_issued[s] - 1) & 1, nullptr);
       for (int s = 0; s < kVSlots; ++s)
-        if (v_issued[s] > 0) mbar_wait(&bars[(kFp8 ? RAW_V : V_FULL) + s], (v_issued[s] - 1) & 1, nullptr);
+        if (v_issued[s] > 0) mbar_wait(&bars[V_FULL + s], (v_issued[s] - 1) & 1, nullptr);
     }
     __syncwarp();
-  } else if (warp >= kWarpConv) {
-    // ------------------------------------------------------------ FP8 record converters
-    // (FP8 instance only.)  A tile's conversion jobs are shared round-robin by
-    // the three converter warps, rotating with the tile: an own tile's K slot
-    // first (jobs 0, 1: the other value half's two box pairs; job 2: the RoPE
-    // box, bf16 -> fp16), then its V slot (jobs 3, 4: this CTA's value half's
-    // two box pairs).  Each warp waits for the slot's raw bytes, converts its
-    // jobs in place, makes its writes visible to the tensor cores and arrives
-    // on the slot's FULL (every warp once per slot use).
-    if constexpr (kFp8) {
-      const uint32_t cw = static_cast<uint32_t>(warp - kWarpConv);
-      Cursor c;
-      cursor_init(p, P, c);
-      bool ok = true;
-      uint32_t own_k = 0;
-      while (ok && c.valid) {
-        const bool mine = (c.t & 1u) == rank;
-        const uint32_t rot = c.t % kConvWarps;
-        if (mine) {
-          const int s = static_cast<int>(own_k % kKSlots);
-          ok = warp_wait(&bars[RAW_K + s], (own_k / kKSlots) & 1, abort_flag);
-          if (!ok) break;
-          uint8_t* slot = sK + s * kKSlotBytes;
-#pragma unroll 1
-          for (int j = 0; j < 3; ++j) {
-            if ((static_cast<uint32_t>(j) + rot) % kConvWarps != cw) continue;
-            if (j < 2)
-              convert_fp8_pair(slot + 2 * j * kBoxBytes, slot + (2 * j + 1) * kBoxBytes,
-                               2 * (1 - static_cast<int>(rank)) + j, lane);
-            else
-              bf16_box_to_fp16(slot + 4 * kBoxBytes, kBoxBytes / 4, lane);  // RoPE
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[K_FULL + s]);
-          ++own_k;
-        }
-        {
-          const int s = static_cast<int>(c.t % kVSlots);
-          ok = warp_wait(&bars[RAW_V + s], (c.t / kVSlots) & 1, abort_flag);
-          if (!ok) break;
-          uint8_t* slot = sV + s * kVSlotBytes;
-#pragma unroll 1
-          for (int j = 0; j < 2; ++j) {
-            if ((static_cast<uint32_t>(j + 3) + rot) % kConvWarps != cw) continue;
-            convert_fp8_pair(slot + 2 * j * kBoxBytes, slot + (2 * j + 1) * kBoxBytes,
-                             2 * static_cast<int>(rank) + j, lane);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[V_FULL + s]);
-        }
-        cursor_next(p, P, c);
-      }
-      if (!ok && lane == 0) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
-    }
   } else if (warp == kWarpQ) {
     // ------------------------------------------------------------ Q producer
     // Per unit, the nine 64-dim boxes of Q in order through the three slots
     // of the shared-memory Q buffer: box j goes to slot j % 3.  Boxes 0-5
     // (dims [0, 384)) are copied into TMEM by the Q K^T thread, which frees
     // the slot for box j + 3; boxes 6-8 stay until the unit's last Q K^T.
-    // FP8 records: Q is the fp16 copy written by q_fp16_kernel, the grid
-    // launched just before this one; it is complete once griddepcontrol.wait
-    // returns (every other role starts without it).
-    if constexpr (kFp8) {
-      if (lane == 0) pdl_wait_prior_grid();
-    }
     if (kQV && lane == 0) {
-      // 16-bit KV, V-ring instance.  The first unit: boxes 0-5 go into the V
+      // V-ring instance.  The first unit: boxes 0-5 go into the V
       // ring, still empty at the start (the Q K^T thread copies them into TMEM
       // and frees the ring for the V producer), boxes 6-8 into the Q slots,
       // all nine at once.  Later units: box j through slot j % 3 as below.
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
-      if constexpr (kFp8)
-        c = c_first;
-      else
-        cursor_init(p, P, c);
+      cursor_init(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {}, vq_issued = 0;
       // box j of unit b into dst; into L2 only when bar is null
@@ -821,10 +589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     } else if (lane == 0) {
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
-      if constexpr (kFp8)
-        c = c_first;
-      else
-        cursor_init(p, P, c);
+      cursor_init(p, P, c);
       bool ok = true;
       uint32_t qb_issued[kQSmemBoxes] = {};
       // box j of unit b into slot j % 3; into L2 only when bar is null
@@ -1351,83 +1116,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   }
 }
 
-// bf16 Q -> fp16 for the FP8-record instance, 8 values per thread and step
-// (the same rounding as the converter warps: bf16 -> fp32 exactly, then
-// round to nearest even).  It lets the dependent decode grid launch at once;
-// that grid's Q producer waits for this one to complete.
-__global__ void __launch_bounds__(256) q_fp16_kernel(const uint4* __restrict__ q, uint4* __restrict__ q16,
-                                                     size_t n_vec) {
-  pdl_launch_dependents();
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_vec;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    uint4 x = q[i];
-    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
-      w[k] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    q16[i] = x;
-  }
-}
-
 }  // namespace dn
 
 int dense_smem_bytes() { return dn::kSmemBytes; }
-// kind 0: bf16, 1: fp16, 2: FP8 records (bf16 Q), 3: bf16 with the V-ring Q
-// stage, 4: fp16 with it
-int dense_threads(int kind) { return kind == 2 ? dn::kThreadsFp8 : dn::kThreads; }
+// kind 0: bf16, 1: fp16, 2: bf16 with the V-ring Q stage, 3: fp16 with it
+int dense_threads(int) { return dn::kThreads; }
 const void* dense_kernel_ptr(int kind) {
   switch (kind) {
-    case 1: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, false>);
-    case 2: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true, false>);
-    case 3: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, true>);
-    case 4: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, true>);
-    default: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, false>);
+    case 1: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false>);
+    case 2: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, true>);
+    case 3: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true>);
+    default: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false>);
   }
 }
-
-namespace {
-
-template <bool kHalf, bool kFp8, bool kQV>
-cudaError_t launch_instance(const CUtensorMap& q_map, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
-                            const CUtensorMap& rope_map, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kFp8 ? dn::kThreadsFp8 : dn::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = dn::kSmemBytes;
-  cfg.stream = stream;
-  // FP8 records: after q_fp16_kernel, as its programmatic dependent (the Q
-  // producer waits for it)
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = kFp8 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, dn::dense_decode_kernel<kHalf, kFp8, kQV>, q_map, kv_map, sc_map,
-                            rope_map, p);
-}
-
-}  // namespace
 
 cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, const CUtensorMap& sc_map,
                          const CUtensorMap& rope_map, const DecodeParams& p, int num_parts, int kind,
                          cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
   switch (kind) {
-    case 1: return launch_instance<true, false, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
-    case 2: return launch_instance<true, true, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
-    case 3: return launch_instance<false, false, true>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
-    case 4: return launch_instance<true, false, true>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
-    default: return launch_instance<false, false, false>(q_map, kv_map, sc_map, rope_map, p, grid, stream);
+    case 1:
+      dn::dense_decode_kernel<true, false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                            rope_map, p);
+      break;
+    case 2:
+      dn::dense_decode_kernel<false, true><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                            rope_map, p);
+      break;
+    case 3:
+      dn::dense_decode_kernel<true, true><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                           rope_map, p);
+      break;
+    default:
+      dn::dense_decode_kernel<false, false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
+                                                                                             rope_map, p);
   }
-}
-
-cudaError_t launch_q_fp16(const void* q, void* q16, size_t elems, int sms, cudaStream_t stream) {
-  const size_t n_vec = elems / 8;  // rows of 576 values: whole vectors of 8
-  const size_t want = (n_vec + 4 * 256 - 1) / (4 * 256);
-  const int blocks = static_cast<int>(std::max<size_t>(1, std::min<size_t>(want, 2 * static_cast<size_t>(sms))));
-  dn::q_fp16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(q), static_cast<uint4*>(q16), n_vec);
   return cudaGetLastError();
 }
 

@@ -10,7 +10,12 @@
 // fp32 scales (one per 128-dim group) and 64 bf16 RoPE values; the key is
 // code * scale (NoPE) followed by the RoPE values, the value is the NoPE
 // part.  Per split: S = Q K^T over 576 dims, online softmax, O = P V, then
-// O / l and the split's LSE; the combine kernel merges the splits.
+// O / l and the split's LSE; the combine kernel merges the splits.  The same
+// kernel serves two other slot sources: packed selections (slot t of unit
+// u is packed record u * tiles * 64 + t, live when its mask bit is set) and
+// a dense cache of FP8 records read through the block table, a unit then
+// being a whole request (its s_q * h_q rows in row blocks of 128, each row
+// masked at its token's causal limit).
 //
 // How (GB300 design):
 //  * One 2-CTA cluster per (partition, row block of 128 heads).  The pair
@@ -218,15 +223,15 @@ __device__ __forceinline__ uint4 codes_to_bf16(uint2 codes) {
 // Selection entry t of unit b as stored (no check yet); -1 past the list.
 // Packed selection: the record of slot t sits at ordinal b * tiles * 64 + t
 // of the packed records when its bit in the tile's valid mask is set.
-// Dense FP8 cache: every token is a key; slot t of unit b (query token
-// b % s_q of request b / s_q) is record t % 64 of page block_table[b/s_q][t/64];
-// a page outside the pool comes back as -2 (reported, masked).
+// Dense FP8 cache: every token is a key; slot t of unit b is record t % 64
+// of page block_table[b / unit_request_div][t / 64] (a unit is a whole
+// request); a page outside the pool comes back as -2 (reported, masked).
 __device__ __forceinline__ int load_slot(const DecodeParams& p, int b, int t, int L) {
   if (t >= L) return -1;
   if (p.block_table != nullptr) {
     const int pg = t / kT;
     const int page =
-        pg < p.max_pages ? __ldg(p.block_table + static_cast<size_t>(b / p.s_q) * p.max_pages + pg) : -1;
+        pg < p.max_pages ? __ldg(p.block_table + static_cast<size_t>(b / p.unit_request_div) * p.max_pages + pg) : -1;
     return (page < 0 || page >= p.num_pages) ? -2 : page * kT + (t - pg * kT);
   }
   if (p.packed_mask != nullptr) {
@@ -569,6 +574,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (hi <= lo) continue;
       const int row = rb * kRowsPerBlock + r;
       const bool row_ok = row < p.rows;
+      // last key this row sees: with the causal mask, query token i of a
+      // request with L keys ends at key L - s_q + i (rows are token-major)
+      const int row_last = p.causal ? L - p.s_q + row / p.h_q : L - 1;
       float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and fp32 row sum
       for (int k = lo; ok && k < hi; ++k, ++t) {
         const int st = t & 1;
@@ -576,8 +584,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = warp_wait(&bars[KV_FULL + st], (t >> 1) & 1, abort_flag);
         if (!ok) break;
         // which of the tile's 64 slots are valid (the same for every row)
-        const uint64_t vis_mask = static_cast<uint64_t>(sVis[(t & (kVisSlots - 1)) * 2]) |
-                                  (static_cast<uint64_t>(sVis[(t & (kVisSlots - 1)) * 2 + 1]) << 32);
+        const int lim = row_last - k * kT;  // keys 0..lim of this tile are visible to the row
+        const uint64_t vis_mask = (static_cast<uint64_t>(sVis[(t & (kVisSlots - 1)) * 2]) |
+                                   (static_cast<uint64_t>(sVis[(t & (kVisSlots - 1)) * 2 + 1]) << 32)) &
+                                  (lim >= kT - 1 ? ~0ull : (lim < 0 ? 0ull : (~0ull >> (kT - 1 - lim))));
         ok = warp_wait(&bars[S_FULL], t & 1, abort_flag);
         if (!ok) break;
         if (tid == 0) MLA_TRACE(4, t);
@@ -722,16 +732,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         if (!row_ok) continue;
         const size_t col = 256u * rank + c0;
-        if (direct && p.out_type == MLA_DTYPE_BF16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * kDv + col);
+        if (direct && p.out_type != MLA_DTYPE_FP32) {
+          // 16-bit output: bf16 or fp16 (same size, same layout)
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kDv + col);
+          const bool half = p.out_type == MLA_DTYPE_FP16;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[8 * c + 2 * i]) * inv_l,
-                                                             __uint_as_float(v[8 * c + 2 * i + 1]) * inv_l);
-              w[i] = *reinterpret_cast<const uint32_t*>(&h);
+              const float x0 = __uint_as_float(v[8 * c + 2 * i]) * inv_l;
+              const float x1 = __uint_as_float(v[8 * c + 2 * i + 1]) * inv_l;
+              if (half) {
+                const __half2 h = __floats2half2_rn(x0, x1);
+                w[i] = *reinterpret_cast<const uint32_t*>(&h);
+              } else {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                w[i] = *reinterpret_cast<const uint32_t*>(&h);
+              }
             }
             dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
           }
@@ -891,17 +909,6 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t* __restrict__ k
   }
 }
 
-// Keys each query token sees in a dense cache: token i of request b sees the
-// first L_b - s_q + i + 1 keys when causal (bottom-right alignment), all L_b otherwise.
-__global__ void unit_lengths_kernel(const int32_t* __restrict__ seqlens, int batch, int s_q, int causal,
-                                    int32_t* __restrict__ unit_len) {
-  const int u = blockIdx.x * blockDim.x + threadIdx.x;
-  if (u >= batch * s_q) return;
-  const int b = u / s_q, i = u - b * s_q;
-  const int L = max(seqlens[b], 0);
-  unit_len[u] = causal ? max(L - s_q + i + 1, 0) : L;
-}
-
 // Bit-exact record unpack: one thread per (record, 8-dim chunk).
 __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__ kv8, int num_pages,
                                                      const int32_t* __restrict__ indices, int n,
@@ -964,13 +971,6 @@ cudaError_t launch_pack(const uint8_t* kv8, int num_pages, const int32_t* indice
   else
     sp::pack_kernel<false><<<grid, 256, 0, stream>>>(kv8, num_pages, indices, topk, topk_length, packed, masks,
                                                      status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_unit_lengths(const int32_t* seqlens, int batch, int s_q, int causal, int32_t* unit_len,
-                                cudaStream_t stream) {
-  const int n = batch * s_q;
-  sp::unit_lengths_kernel<<<(n + 255) / 256, 256, 0, stream>>>(seqlens, batch, s_q, causal, unit_len);
   return cudaGetLastError();
 }
 

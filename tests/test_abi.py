@@ -35,8 +35,7 @@ def test_header_declares_the_boundary():
                             "mla_decode_fwd", "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd",
                             "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes",
                             "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd",
-                            "mla_get_metadata_request_local", "mla_num_parts_dense", "mla_dense_fp8_decode_fwd",
-                            "mla_dense_fp8_unit_lengths", "mla_test_pack_timeout"])
+                            "mla_get_metadata_request_local", "mla_num_parts_dense", "mla_test_pack_timeout"])
 
 
 def test_library_exports_every_declared_symbol(lib_path):
@@ -62,10 +61,10 @@ def test_host_validation_without_gpu(lib_path):
     assert b"unknown" in lib.mla_status_string(99)
     lib.mla_workspace_bytes.restype = ctypes.c_size_t
     lib.mla_workspace_bytes.argtypes = [ctypes.c_int] * 3
-    # (n_units + num_parts) slots x rows x (512 + 1) fp32, 256-byte aligned pieces
-    # split slots (fp32 O, fp32 LSE), then the fp16 copy of Q: 36,771,840 + 9,437,184 bytes
-    assert lib.mla_workspace_bytes(64, 128, 76) == (64 + 76) * 128 * 512 * 4 + (64 + 76) * 128 * 4 + 64 * 128 * 576 * 2
-    assert lib.mla_workspace_bytes(1, 3, 1) == 2 * 3 * 2048 + 256 + 3 * 1152 + 128  # each region 256-aligned
+    # (n_units + num_parts) slots x rows x (512 + 1) fp32: fp32 O, then fp32 LSE,
+    # each region 256-byte aligned (36,771,840 bytes at 64 x 128 rows, 76 parts)
+    assert lib.mla_workspace_bytes(64, 128, 76) == (64 + 76) * 128 * 512 * 4 + (64 + 76) * 128 * 4
+    assert lib.mla_workspace_bytes(1, 3, 1) == 2 * 3 * 2048 + 256
     assert lib.mla_workspace_bytes(0, 0, 1) == 0
     null = ctypes.c_void_p(0)
     lib.mla_get_metadata.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,

@@ -77,7 +77,7 @@ def test_static_ws_matches_caller_workspace_on_consecutive_calls():
 
 
 # The other cache types go through the same array: fp16, two latent KV heads,
-# and FP8 records, whose fp16 copy of Q sits in the array behind the partials.
+# and FP8 records (the sparse kernel under the dense plan, same partials).
 KINDS = {
     "fp16": lambda: wl.dense_case(3, 1, 128, 0, seqlens=[2500, 90, 1300], dtype=torch.float16, seed=73),
     "hkv2": lambda: wl.dense_case(3, 2, 128, 0, seqlens=[700, 2200, 64], causal=True, h_kv=2, seed=74),
@@ -97,13 +97,13 @@ def test_static_ws_other_cache_types_on_consecutive_calls(kind):
 
 @pytest.mark.gpu
 def test_static_ws_fp8_records_just_under_the_limit():
-    """The largest FP8-record batch whose workspace (partials, LSEs, then the
-    fp16 copy of Q) still fits the array: the Q copy ends inside it."""
+    """The largest FP8-record batch whose workspace (partials, then LSEs)
+    still fits the array: the last LSE ends inside it."""
     parts = mla.mla_num_parts_dense(1, 128, 1)
     B = 1
     while mla.mla_workspace_bytes(B + 1, 128, parts) <= STATIC_WORKSPACE_BYTES:
         B += 1
-    assert STATIC_WORKSPACE_BYTES - mla.mla_workspace_bytes(B, 128, parts) < 128 * (2052 + 1152) + 512
+    assert STATIC_WORKSPACE_BYTES - mla.mla_workspace_bytes(B, 128, parts) < 128 * 2052 + 512
     case = wl.dense_fp8_case(B, 1, 128, 64, 320, seed=76)
     ro, rl = _run(case, parts, static=False)
     for _ in range(2):
