@@ -67,6 +67,8 @@ constexpr int kStageBytes = kMaxBoxes * kBoxBytes;
 constexpr int kScaleStageBytes = 2 * kT * 4;      // the rank's two group scales of 64 keys
 constexpr int kXBytes = kRowsPerBlock * kT * 4;   // the peer's partial scores
 constexpr int kPGroupBytes = kRowsPerBlock * kT * 2;
+constexpr uint32_t kHalfX = kXBytes / 2;          // scores 32-63 of the mailbox rows
+static_assert(kHalfX == kPGroupBytes && kXBytes == 2 * kPGroupBytes, "the partial is staged in the P buffer");
 
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kMaxBoxes * kQBoxBytes;
@@ -124,6 +126,10 @@ __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 struct Part {
@@ -557,8 +563,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax + epilogue
     const int r = tid;  // row of the block == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
-    const uint32_t x_local = smem_u32(sX) + r * 256;
-    const uint32_t x_remote = mapa_shared(x_local, peer);
+    // Partial-score mailbox (and the staging of this rank's partial in the P
+    // buffer, same layout): scores 0-31 of row r at r * 128, scores 32-63 at
+    // 16 KB + r * 128, 16-byte chunks swizzled by r & 7.  A warp's rows then
+    // occupy the same two 4 KB pieces as its rows of P (group 0, group 1).
+    const uint32_t x_local = smem_u32(sX) + r * 128;
+    const uint32_t x_stage = smem_u32(sP) + r * 128;
+    const uint32_t x_stage_warp = smem_u32(sP) + warp * (32 * 128);
+    const uint32_t x_remote_warp = mapa_shared(smem_u32(sX) + warp * (32 * 128), peer);
     const uint32_t xfull_remote = mapa_shared(smem_u32(&bars[X_FULL + warp]), peer);
     const uint32_t xfree_remote = mapa_shared(smem_u32(&bars[X_FREE + warp]), peer);
     const uint32_t swz = static_cast<uint32_t>(r & 7);
@@ -621,16 +633,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&bars[S_FREE]);
-        // swap partial scores with the peer CTA
+        // Swap partial scores with the peer CTA.  The rank's partial goes to
+        // the P buffer (free once P V of the previous tile is done: its P has
+        // been read), in the layout of the peer's mailbox, and each warp's
+        // 8 KB leaves in one bulk copy into the peer's mailbox, completing the
+        // peer's X_FULL.
+        if (t >= 1) {
+          ok = warp_wait(&bars[P_FREE], (t - 1) & 1, abort_flag);
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          st_shared_v4(x_stage + (c >> 3) * kHalfX + (((static_cast<uint32_t>(c) & 7u) ^ swz) << 4), s[4 * c],
+                       s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        // the peer has read our previous partial (so that copy is complete)
         if (t >= 1) {
           ok = warp_wait_cluster(&bars[X_FREE + warp], (t - 1) & 1, abort_flag);
           if (!ok) break;
         }
-        // asynchronous remote stores; their bytes complete the peer's X_FULL
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_async_v4(x_remote + ((static_cast<uint32_t>(c) ^ swz) << 4), s[4 * c], s[4 * c + 1], s[4 * c + 2],
-                      s[4 * c + 3], xfull_remote);
+        if (lane == 0) {
+          bulk_copy_to_cluster(x_remote_warp, x_stage_warp, 32 * 128, xfull_remote);
+          bulk_copy_to_cluster(x_remote_warp + kHalfX, x_stage_warp + kHalfX, 32 * 128, xfull_remote);
+        }
         if (tid == 0) MLA_TRACE(5, t);
         ok = warp_wait_cluster(&bars[X_FULL + warp], t & 1, abort_flag);
         if (!ok) break;
@@ -639,7 +665,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // full score = own partial + peer's partial (one fp32 add: the same bits on both ranks)
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float4 o = ld_shared_v4(x_local + ((static_cast<uint32_t>(c) ^ swz) << 4));
+          const float4 o = ld_shared_v4(x_local + (c >> 3) * kHalfX + (((static_cast<uint32_t>(c) & 7u) ^ swz) << 4));
           s[4 * c + 0] += o.x;
           s[4 * c + 1] += o.y;
           s[4 * c + 2] += o.z;
@@ -670,11 +696,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ls[j & 3] += s[j];
         }
         l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        // P of the previous tile has been consumed (and O holds its PV)
-        if (t >= 1) {
-          ok = warp_wait(&bars[P_FREE], (t - 1) & 1, abort_flag);
-          if (!ok) break;
-        }
+        // our partial has left the P buffer (the peer has read it) before P is written there
+        ok = warp_wait_cluster(&bars[X_FREE + warp], t & 1, abort_flag);
+        if (!ok) break;
         if (__any_sync(0xffffffffu, rescale)) {
           tc_fence_after();
 #pragma unroll 1
