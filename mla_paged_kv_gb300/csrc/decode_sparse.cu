@@ -38,8 +38,9 @@
 //    Q comes by TMA.  One elected thread issues every tcgen05.mma.
 //  * Online softmax in the log2 domain with a lazy rescale of O (only when
 //    the running max grows by more than 2^8).
-// Roles: warps 0-3 softmax + epilogue (thread = row = TMEM lane), warps 4-6
-// gather producer, warp 7 MMA issuer and TMEM owner.
+// Roles: warps 0-7 softmax + epilogue (two warps per TMEM lane quarter, a
+// thread per row and half of the tile's scores), warps 8-10 gather producer,
+// warp 11 MMA issuer and TMEM owner.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -89,9 +90,16 @@ static_assert(kOffKV % 1024 == 0 && kOffX % 1024 == 0 && kOffP % 1024 == 0, "swi
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O half: columns [0, 256)
 constexpr uint32_t kTmemS = 256;  // score accumulators: A_{2c}, A_{2c+1}, RoPE (rank 0), 64 columns each
+// [448, 452): where the two softmax threads of a row swap their halves' row
+// maximum (448 + h) and row sum (450 + h): the two warps of a lane quarter
+// reach the same TMEM lanes
+constexpr uint32_t kTmemX = 448;
 
+constexpr int kSoftmaxWarps = 8;
+// named barriers: 1-4 pair the two softmax warps of a TMEM lane quarter
+constexpr uint32_t kBarProdSync = 5, kBarProdOr = 6;
 constexpr int kProducerWarps = 3;
-constexpr int kMmaWarp = 4 + kProducerWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + kProducerWarps;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
 
 enum : int {
@@ -335,11 +343,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bars[KV_EMPTY + i], 1);
     }
     mbar_init(&bars[S_FULL], 1);
-    mbar_init(&bars[S_FREE], 128);
-    mbar_init(&bars[P_FULL], 128);
+    mbar_init(&bars[S_FREE], 32 * kSoftmaxWarps);
+    mbar_init(&bars[P_FULL], 32 * kSoftmaxWarps);
     mbar_init(&bars[P_FREE], 1);
     mbar_init(&bars[O_FULL], 1);
-    mbar_init(&bars[O_FREE], 128);
+    mbar_init(&bars[O_FREE], 32 * kSoftmaxWarps);
     for (int w = 0; w < 4; ++w) {
       mbar_init(&bars[X_FULL + w], 1);
       mbar_init(&bars[X_FREE + w], 1);
@@ -364,15 +372,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const Part P = load_part(p.sched, part_idx);
 
-  if (warp >= 4 && warp < kMmaWarp) {
+  if (warp >= kSoftmaxWarps && warp < kMmaWarp) {
     // ------------------------------------------------------------ producer
-    const int ptid = tid - 128;  // 0 .. 32 * kProducerWarps - 1
+    const int ptid = tid - 32 * kSoftmaxWarps;  // 0 .. 32 * kProducerWarps - 1
     const uint64_t pol_q = policy_evict_last();
-    // 16-byte chunks per key: 16 NoPE chunks (16 E4M3 codes each) of the
-    // rank's two groups, plus 8 RoPE chunks (8 bf16 each) on rank 0
-    const int nck = rank == 0 ? 24 : 16;
+    // Per key: 16 NoPE chunks of 16 bytes (16 E4M3 codes each) of the rank's
+    // two groups, loaded into registers a tile ahead and converted; the two
+    // group scales (threads 0-63, one key each), also a tile ahead; on rank
+    // 0 the 8 RoPE chunks (8 bf16 each), copied into the stage by cp.async
+    // once it is free (they need no conversion).
     const int nope0 = 256 * static_cast<int>(rank);
-    constexpr int kPerMax = (kT * 24 + 32 * kProducerWarps - 1) / (32 * kProducerWarps);  // 16
+    constexpr int kPerMax = (kT * 16 + 32 * kProducerWarps - 1) / (32 * kProducerWarps);  // 11
+    constexpr int kRopePer = (kT * 8 + 32 * kProducerWarps - 1) / (32 * kProducerWarps);   // 6
     uint32_t t = 0;
     int u = 0;
     bool ok = true;
@@ -393,7 +404,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ++q_issued;
         }
       }
-      if (named_bar_or(2, 32 * kProducerWarps, !ok)) {
+      if (named_bar_or(kBarProdOr, 32 * kProducerWarps, !ok)) {
         ok = false;
         break;
       }
@@ -401,31 +412,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // are issued before tile k is converted, so two tiles' scattered record
       // loads are in flight while one is being written.
       uint4 raw[kPerMax];
-      float sc[kPerMax];
+      float sc[2];
       // phase 1 for tile tt: its 64 slot entries (loaded earlier, see below)
       // -> record index or -1, and the tile's valid-slot mask for the softmax
       auto publish_indices = [&](int entry, uint32_t tt) {
-        named_bar_sync(1, 32 * kProducerWarps);  // the slot's previous tile is no longer read
+        named_bar_sync(kBarProdSync, 32 * kProducerWarps);  // the slot's previous tile is no longer read
         if (ptid < kT) {
           const int idx = resolve_slot(p, entry);
           sIdx[(tt & 1) * kT + ptid] = idx;
           const uint32_t half = __ballot_sync(0xffffffffu, idx >= 0);
           if (lane == 0) sVis[(tt & (kVisSlots - 1)) * 2 + (ptid >> 5)] = half;
         }
-        named_bar_sync(1, 32 * kProducerWarps);
+        named_bar_sync(kBarProdSync, 32 * kProducerWarps);
       };
-      // phase 2 for tile tt: every chunk's loads (a masked slot reads record 0)
-      auto issue_loads = [&](uint32_t tt, uint4 (&rr)[kPerMax], float (&ss)[kPerMax]) {
+      // phase 2 for tile tt: the NoPE chunks' loads (a masked slot reads
+      // record 0) and, on threads 0-63, the key's two group scales
+      auto issue_loads = [&](uint32_t tt, uint4 (&rr)[kPerMax], float (&ss)[2]) {
         const int* idx_t = sIdx + (tt & 1) * kT;
 #pragma unroll
         for (int i = 0; i < kPerMax; ++i) {
-          const int q = ptid + 32 * kProducerWarps * i;
-          const int key = min(q / nck, kT - 1), c = q - nck * (q / nck);
-          const int idx = idx_t[key];
+          const int qq = min(ptid + 32 * kProducerWarps * i, kT * 16 - 1);
+          const int idx = idx_t[qq >> 4];
           const uint8_t* rec = p.kv8 + static_cast<size_t>(max(idx, 0)) * MLA_RECORD_BYTES;
-          const int off = c < 16 ? nope0 + 16 * c : 528 + 16 * (c - 16);
-          rr[i] = __ldg(reinterpret_cast<const uint4*>(rec + off));
-          ss[i] = __ldg(reinterpret_cast<const float*>(rec + 512) + ((nope0 + 16 * min(c, 15)) >> 7));
+          rr[i] = __ldg(reinterpret_cast<const uint4*>(rec + nope0 + 16 * (qq & 15)));
+        }
+        if (ptid < kT) {
+          const uint8_t* rec = p.kv8 + static_cast<size_t>(max(idx_t[ptid], 0)) * MLA_RECORD_BYTES;
+          const float2 f = __ldg(reinterpret_cast<const float2*>(rec + 512 + 8 * static_cast<int>(rank)));
+          ss[0] = f.x;
+          ss[1] = f.y;
         }
       };
       // slot entries are loaded two tiles ahead of their records, so that no
@@ -437,7 +452,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int k = lo; ok && k < hi; ++k, ++t) {
         const int st = t & 1;
         uint4 raw_n[kPerMax];
-        float sc_n[kPerMax];
+        float sc_n[2];
         if (k + 1 < hi) {
           publish_indices(entry_n, t + 1);
           entry_n = (ptid < kT && k + 2 < hi) ? load_slot(p, b, (k + 2) * kT + ptid, L) : -1;
@@ -446,7 +461,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool failed = false;
         if (t >= 2) failed = !mbar_wait(&bars[KV_EMPTY + st], ((t - 2) >> 1) & 1, abort_flag);
         // one decision for the whole producer group: its named barriers need every thread
-        if (named_bar_or(2, 32 * kProducerWarps, failed)) {
+        if (named_bar_or(kBarProdOr, 32 * kProducerWarps, failed)) {
           ok = false;
           break;
         }
@@ -454,35 +469,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int* idx_t = sIdx + (t & 1) * kT;
         uint8_t* stage = sKV + st * kStageBytes;
         float* scale_st = sScale + st * (2 * kT);
+        if (rank == 0) {
+          // RoPE: straight into the stage's fifth box (zero for a masked slot)
 #pragma unroll
-        for (int i = 0; i < kPerMax; ++i) {
-          const int q = ptid + 32 * kProducerWarps * i;
-          const int key = q / nck, c = q - nck * (q / nck);
-          if (key < kT) {
-            const bool live = idx_t[key] >= 0;
-            const uint4 w = live ? raw[i] : make_uint4(0u, 0u, 0u, 0u);
-            uint8_t* row = stage + key * 128;
-            const uint32_t swz = static_cast<uint32_t>(key & 7);
-            if (c < 16) {
-              // 16 codes -> 16 bf16: two 16-byte pieces of box c/4, columns 2(c%4), 2(c%4)+1
-              uint8_t* box = row + (c >> 2) * kBoxBytes;
-              const uint32_t cc = 2u * static_cast<uint32_t>(c & 3);
-              *reinterpret_cast<uint4*>(box + ((cc ^ swz) << 4)) = codes_to_bf16(make_uint2(w.x, w.y));
-              *reinterpret_cast<uint4*>(box + (((cc + 1u) ^ swz) << 4)) = codes_to_bf16(make_uint2(w.z, w.w));
-              if ((c & 7) == 0) scale_st[(c >> 3) * kT + key] = live ? sc[i] : 0.f;
-            } else {
-              *reinterpret_cast<uint4*>(row + 4 * kBoxBytes + ((static_cast<uint32_t>(c - 16) ^ swz) << 4)) = w;
+          for (int j = 0; j < kRopePer; ++j) {
+            const int qq = ptid + 32 * kProducerWarps * j;
+            if (qq < kT * 8) {
+              const int key = qq >> 3, c = qq & 7;
+              const int idx = idx_t[key];
+              uint8_t* dst = stage + 4 * kBoxBytes + key * 128 + ((static_cast<uint32_t>(c) ^ (key & 7)) << 4);
+              if (idx >= 0)
+                cp_async16(smem_u32(dst), p.kv8 + static_cast<size_t>(idx) * MLA_RECORD_BYTES + 528 + 16 * c);
+              else
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
             }
           }
         }
+        if (ptid < kT) {
+          const bool live = idx_t[ptid] >= 0;
+          scale_st[ptid] = live ? sc[0] : 0.f;
+          scale_st[kT + ptid] = live ? sc[1] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kPerMax; ++i) {
+          const int qq = ptid + 32 * kProducerWarps * i;
+          if (qq < kT * 16) {
+            const int key = qq >> 4, c = qq & 15;
+            const uint4 w = idx_t[key] >= 0 ? raw[i] : make_uint4(0u, 0u, 0u, 0u);
+            // 16 codes -> 16 bf16: two 16-byte pieces of box c/4, columns 2(c%4), 2(c%4)+1
+            uint8_t* box = stage + (c >> 2) * kBoxBytes + key * 128;
+            const uint32_t swz = static_cast<uint32_t>(key & 7);
+            const uint32_t cc = 2u * static_cast<uint32_t>(c & 3);
+            *reinterpret_cast<uint4*>(box + ((cc ^ swz) << 4)) = codes_to_bf16(make_uint2(w.x, w.y));
+            *reinterpret_cast<uint4*>(box + (((cc + 1u) ^ swz) << 4)) = codes_to_bf16(make_uint2(w.z, w.w));
+          }
+        }
+        if (rank == 0) cp_async_wait_all();
         fence_proxy_async_smem();
         mbar_arrive(&bars[KV_FULL + st]);
         if (ptid == 0) MLA_TRACE(1, t);
 #pragma unroll
-        for (int i = 0; i < kPerMax; ++i) {
-          raw[i] = raw_n[i];
-          sc[i] = sc_n[i];
-        }
+        for (int i = 0; i < kPerMax; ++i) raw[i] = raw_n[i];
+        sc[0] = sc_n[0];
+        sc[1] = sc_n[1];
       }
       ++u;
     }
@@ -562,19 +591,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int r = tid;  // row of the block == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
-    // Partial-score mailbox (and the staging of this rank's partial in the P
-    // buffer, same layout): scores 0-31 of row r at r * 128, scores 32-63 at
-    // 16 KB + r * 128, 16-byte chunks swizzled by r & 7.  A warp's rows then
-    // occupy the same two 4 KB pieces as its rows of P (group 0, group 1).
-    const uint32_t x_local = smem_u32(sX) + r * 128;
-    const uint32_t x_stage = smem_u32(sP) + r * 128;
-    const uint32_t x_stage_warp = smem_u32(sP) + warp * (32 * 128);
-    const uint32_t x_remote_warp = mapa_shared(smem_u32(sX) + warp * (32 * 128), peer);
-    const uint32_t xfull_remote = mapa_shared(smem_u32(&bars[X_FULL + warp]), peer);
-    const uint32_t xfree_remote = mapa_shared(smem_u32(&bars[X_FREE + warp]), peer);
+    // Eight warps: warp w takes the rows of TMEM lane quarter q = w % 4
+    // (rows 32q .. 32q+31, one per thread) and scores 32h .. 32h+31 (h = w / 4)
+    // of every tile; for O (rescale, epilogue) it takes columns 128h .. 128h+127
+    // of the rank's half.  The two warps of a quarter meet at a named barrier
+    // (bar.red.or, so that they leave the loop together) to send the
+    // quarter's partial scores, to combine the row maxima and the row sums.
+    const int q = warp & 3, h = warp >> 2;
+    const int r = 32 * q + lane;  // row of the block == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const uint32_t pair_bar = 1 + q, pair_n = 64;
+    const bool sender = h == 0 && lane == 0;  // sends, re-arms and frees the quarter's mailbox
     const uint32_t swz = static_cast<uint32_t>(r & 7);
+    // A row's 64 partial scores travel in the row's P footprint (two groups x
+    // 128 bytes, 16-byte chunks c at position c ^ (r & 7)): scores
+    // 32h + 4k .. 32h + 4k + 3 (k = 0..7) sit in group k >> 2, chunk
+    // 4h + (k & 3), exactly where this thread later writes its P.  The peer's
+    // mailbox sX has the same layout, so a quarter's partials are two 4 KB
+    // pieces (group 0 rows, group 1 rows) on both sides.
+    auto chunk_off = [&](int k) -> uint32_t {
+      return static_cast<uint32_t>(k >> 2) * kPGroupBytes + r * 128u +
+             (((4u * h + static_cast<uint32_t>(k & 3)) ^ swz) << 4);
+    };
+    const uint32_t x_local = smem_u32(sX), x_stage = smem_u32(sP);
+    const uint32_t q_off = static_cast<uint32_t>(32 * q) * 128u;
+    const uint32_t x_remote_q = mapa_shared(smem_u32(sX) + q_off, peer);
+    const uint32_t xfull_remote = mapa_shared(smem_u32(&bars[X_FULL + q]), peer);
+    const uint32_t xfree_remote = mapa_shared(smem_u32(&bars[X_FREE + q]), peer);
     const int n_acc = rank == 0 ? 3 : 2;
     uint32_t t = 0;
     int u = 0;
@@ -590,137 +633,150 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // last key this row sees: with the causal mask, query token i of a
       // request with L keys ends at key L - s_q + i (rows are token-major)
       const int row_last = p.causal ? L - p.s_q + row / p.h_q : L - 1;
-      float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and fp32 row sum
-      for (int k = lo; ok && k < hi; ++k, ++t) {
+      // running max (log2 units), the same in both threads of a row, and
+      // this thread's part of the fp32 row sum
+      float m_used = -INFINITY, l_part = 0.f;
+      for (int k = lo; k < hi; ++k, ++t) {
         const int st = t & 1;
-        // the tile's valid-slot mask and scales: visible once its KV_FULL phase has completed
-        ok = warp_wait(&bars[KV_FULL + st], (t >> 1) & 1, abort_flag);
-        if (!ok) break;
-        // which of the tile's 64 slots are valid (the same for every row)
-        const int lim = row_last - k * kT;  // keys 0..lim of this tile are visible to the row
-        const uint64_t vis_mask = (static_cast<uint64_t>(sVis[(t & (kVisSlots - 1)) * 2]) |
-                                   (static_cast<uint64_t>(sVis[(t & (kVisSlots - 1)) * 2 + 1]) << 32)) &
-                                  (lim >= kT - 1 ? ~0ull : (lim < 0 ? 0ull : (~0ull >> (kT - 1 - lim))));
-        ok = warp_wait(&bars[S_FULL], t & 1, abort_flag);
-        if (!ok) break;
-        if (tid == 0) MLA_TRACE(4, t);
-        tc_fence_after();
-        const uint32_t sc_base = smem_u32(sScale + st * (2 * kT));
-        // partial score of this rank: sum over its groups of scale_g[j] * A_g[j] (+ RoPE)
-        float s[kT];
+        // ---- phase 1: this thread's 32 partial scores, staged for the peer
+        if (ok) ok = warp_wait(&bars[KV_FULL + st], (t >> 1) & 1, abort_flag);
+        // which of this thread's 32 slots are valid and visible to the row
+        const int lim = row_last - k * kT - 32 * h;
+        const uint32_t vis = (ok ? sVis[(t & (kVisSlots - 1)) * 2 + h] : 0u) &
+                             (lim >= 31 ? 0xffffffffu : (lim < 0 ? 0u : (0xffffffffu >> (31 - lim))));
+        if (ok) ok = warp_wait(&bars[S_FULL], t & 1, abort_flag);
+        float s[32];
 #pragma unroll
-        for (int j = 0; j < kT; ++j) s[j] = 0.f;
+        for (int j = 0; j < 32; ++j) s[j] = 0.f;
+        if (ok) {
+          if (tid == 0) MLA_TRACE(4, t);
+          tc_fence_after();
+          const uint32_t sc_base = smem_u32(sScale + st * (2 * kT)) + 128u * h;
 #pragma unroll 1
-        for (int a = 0; a < n_acc; ++a) {
-          uint32_t va[2][32];
-          tmem_ld32(tmem + lane_base + kTmemS + 64u * a, va[0]);
-          tmem_ld32(tmem + lane_base + kTmemS + 64u * a + 32u, va[1]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t (&v)[32] = va[h];
+          for (int a = 0; a < n_acc; ++a) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + kTmemS + 64u * a + 32u * h, v);
+            tmem_wait_ld();
             if (a < 2) {
 #pragma unroll
               for (int j4 = 0; j4 < 8; ++j4) {
-                const float4 sc = ld_shared_v4(sc_base + (a * kT + 32 * h + 4 * j4) * 4);
-                s[32 * h + 4 * j4 + 0] = fmaf(sc.x, __uint_as_float(v[4 * j4 + 0]), s[32 * h + 4 * j4 + 0]);
-                s[32 * h + 4 * j4 + 1] = fmaf(sc.y, __uint_as_float(v[4 * j4 + 1]), s[32 * h + 4 * j4 + 1]);
-                s[32 * h + 4 * j4 + 2] = fmaf(sc.z, __uint_as_float(v[4 * j4 + 2]), s[32 * h + 4 * j4 + 2]);
-                s[32 * h + 4 * j4 + 3] = fmaf(sc.w, __uint_as_float(v[4 * j4 + 3]), s[32 * h + 4 * j4 + 3]);
+                const float4 sc = ld_shared_v4(sc_base + (a * kT + 4 * j4) * 4);
+                s[4 * j4 + 0] = fmaf(sc.x, __uint_as_float(v[4 * j4 + 0]), s[4 * j4 + 0]);
+                s[4 * j4 + 1] = fmaf(sc.y, __uint_as_float(v[4 * j4 + 1]), s[4 * j4 + 1]);
+                s[4 * j4 + 2] = fmaf(sc.z, __uint_as_float(v[4 * j4 + 2]), s[4 * j4 + 2]);
+                s[4 * j4 + 3] = fmaf(sc.w, __uint_as_float(v[4 * j4 + 3]), s[4 * j4 + 3]);
               }
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) s[32 * h + j] += __uint_as_float(v[j]);
+              for (int j = 0; j < 32; ++j) s[j] += __uint_as_float(v[j]);
             }
           }
+          tc_fence_before();
+          mbar_arrive(&bars[S_FREE]);
+          // the P buffer is free once P V of the previous tile is done
+          if (t >= 1) ok = warp_wait(&bars[P_FREE], (t - 1) & 1, abort_flag);
         }
-        tc_fence_before();
-        mbar_arrive(&bars[S_FREE]);
-        // Swap partial scores with the peer CTA.  The rank's partial goes to
-        // the P buffer (free once P V of the previous tile is done: its P has
-        // been read), in the layout of the peer's mailbox, and each warp's
-        // 8 KB leaves in one bulk copy into the peer's mailbox, completing the
-        // peer's X_FULL.
-        if (t >= 1) {
-          ok = warp_wait(&bars[P_FREE], (t - 1) & 1, abort_flag);
-          if (!ok) break;
-        }
+        if (ok) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_shared_v4(x_stage + (c >> 3) * kHalfX + (((static_cast<uint32_t>(c) & 7u) ^ swz) << 4), s[4 * c],
-                       s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        // the peer has read our previous partial (so that copy is complete)
-        if (t >= 1) {
-          ok = warp_wait_cluster(&bars[X_FREE + warp], (t - 1) & 1, abort_flag);
-          if (!ok) break;
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(x_stage + chunk_off(c), s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+          fence_proxy_async_smem();
         }
-        if (lane == 0) {
-          bulk_copy_to_cluster(x_remote_warp, x_stage_warp, 32 * 128, xfull_remote);
-          bulk_copy_to_cluster(x_remote_warp + kHalfX, x_stage_warp + kHalfX, 32 * 128, xfull_remote);
+        if (named_bar_or(pair_bar, pair_n, !ok)) {
+          ok = false;
+          break;
+        }
+        // ---- phase 2: send the quarter's partials, receive the peer's, row max
+        if (sender) {
+          // the peer has read our previous partials (so that copy is complete)
+          bool sent = t == 0 || mbar_wait<true>(&bars[X_FREE + q], (t - 1) & 1, abort_flag);
+          if (sent) {
+            bulk_copy_to_cluster(x_remote_q, x_stage + q_off, 32 * 128, xfull_remote);
+            bulk_copy_to_cluster(x_remote_q + kPGroupBytes, x_stage + kPGroupBytes + q_off, 32 * 128, xfull_remote);
+          } else {
+            set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+          }
         }
         if (tid == 0) MLA_TRACE(5, t);
-        ok = warp_wait_cluster(&bars[X_FULL + warp], t & 1, abort_flag);
-        if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(&bars[X_FULL + warp], 32 * kT * 4);  // armed for the next tile
-        if (tid == 0) MLA_TRACE(6, t);
-        // full score = own partial + peer's partial (one fp32 add: the same bits on both ranks)
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 o = ld_shared_v4(x_local + (c >> 3) * kHalfX + (((static_cast<uint32_t>(c) & 7u) ^ swz) << 4));
-          s[4 * c + 0] += o.x;
-          s[4 * c + 1] += o.y;
-          s[4 * c + 2] += o.z;
-          s[4 * c + 3] += o.w;
-        }
-        __syncwarp();  // every lane has consumed its row (the adds above used the loads)
-        if (lane == 0) mbar_arrive_remote(xfree_remote);
-        // mask, scale into the log2 domain, tile max
+        ok = warp_wait_cluster(&bars[X_FULL + q], t & 1, abort_flag);
         float mt = -INFINITY;
+        if (ok) {
+          if (tid == 0) MLA_TRACE(6, t);
+          // full score = own partial + peer's partial (one fp32 add: the same bits on both ranks)
 #pragma unroll
-        for (int j = 0; j < kT; ++j) {
-          s[j] = ((vis_mask >> j) & 1ull) ? s[j] * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, s[j]);
+          for (int c = 0; c < 8; ++c) {
+            const float4 o = ld_shared_v4(x_local + chunk_off(c));
+            s[4 * c + 0] += o.x;
+            s[4 * c + 1] += o.y;
+            s[4 * c + 2] += o.z;
+            s[4 * c + 3] += o.w;
+          }
+          // mask, scale into the log2 domain, maximum of this thread's 32
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            s[j] = ((vis >> j) & 1u) ? s[j] * p.scale_log2 : -INFINITY;
+            m4[j & 3] = fmaxf(m4[j & 3], s[j]);
+          }
+          mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          tmem_st1(tmem + lane_base + kTmemX + h, __float_as_uint(mt));
+          tmem_wait_st();
         }
+        tc_fence_before();
+        if (named_bar_or(pair_bar, pair_n, !ok)) {
+          ok = false;
+          break;
+        }
+        // both warps have read the mailbox: arm it for the next tile, free it for the peer
+        if (sender) {
+          mbar_arrive_expect_tx(&bars[X_FULL + q], 2 * 32 * 128);
+          mbar_arrive_remote(xfree_remote);
+        }
+        // ---- phase 3: the row's tile max, reference, exponentials, P
+        tc_fence_after();
+        mt = fmaxf(mt, __uint_as_float(tmem_ld1(tmem + lane_base + kTmemX + 1 - h)));
+        tmem_wait_ld();
         bool rescale = false;
         float alpha = 1.f;
         if (mt > m_used + kTau) {
           alpha = ex2(m_used - mt);  // 0 when m_used == -inf
           rescale = k > lo;
-          l_sum *= alpha;
+          l_part *= alpha;
           m_used = mt;
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < kT; ++j) {
+        for (int j = 0; j < 32; ++j) {
           s[j] = ex2(s[j] - mref);
           ls[j & 3] += s[j];
         }
-        l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        // our partial has left the P buffer (the peer has read it) before P is written there
-        ok = warp_wait_cluster(&bars[X_FREE + warp], t & 1, abort_flag);
-        if (!ok) break;
+        l_part += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // our partials have left the P buffer (the peer has read them) before P is written there
+        ok = warp_wait_cluster(&bars[X_FREE + q], t & 1, abort_flag);
+        if (!ok) {
+          set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
+          continue;  // the next pair barrier takes both warps out
+        }
         if (__any_sync(0xffffffffu, rescale)) {
           tc_fence_after();
 #pragma unroll 1
-          for (uint32_t c0 = 0; c0 < 256; c0 += 16) {
+          for (uint32_t c0 = 0; c0 < 128; c0 += 16) {
             uint32_t v[16];
-            tmem_ld16(tmem + lane_base + kTmemO + c0, v);
+            tmem_ld16(tmem + lane_base + kTmemO + 128u * h + c0, v);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-            tmem_st16(tmem + lane_base + kTmemO + c0, v);
+            tmem_st16(tmem + lane_base + kTmemO + 128u * h + c0, v);
           }
           tmem_wait_st();
         }
         // P_g[j] = p[j] * scale_g[j] for the rank's two groups, bf16, swizzled rows
+        const uint32_t sc_base = smem_u32(sScale + st * (2 * kT)) + 128u * h;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
-          uint8_t* prow = sP + g * kPGroupBytes + r * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < 4; ++c) {
             const float4 sa = ld_shared_v4(sc_base + (g * kT + 8 * c) * 4);
             const float4 sb = ld_shared_v4(sc_base + (g * kT + 8 * c + 4) * 4);
             const float w[8] = {s[8 * c] * sa.x,     s[8 * c + 1] * sa.y, s[8 * c + 2] * sa.z, s[8 * c + 3] * sa.w,
@@ -731,7 +787,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const __nv_bfloat162 hv = __floats2bfloat162_rn(w[2 * i], w[2 * i + 1]);
               pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
             }
-            *reinterpret_cast<uint4*>(prow + ((static_cast<uint32_t>(c) ^ swz) << 4)) =
+            *reinterpret_cast<uint4*>(sP + g * kPGroupBytes + r * 128 + (((4u * h + c) ^ swz) << 4)) =
                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
@@ -740,10 +796,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars[P_FULL]);
         if (tid == 0) MLA_TRACE(7, t);
       }
-      if (!ok) break;
-      // ---- epilogue of this (unit, split)
+      if (named_bar_or(pair_bar, pair_n, !ok)) {
+        ok = false;
+        break;
+      }
+      // ---- epilogue of this (unit, split): the row sum of both threads
+      tmem_st1(tmem + lane_base + kTmemX + 2 + h, __float_as_uint(l_part));
+      tmem_wait_st();
+      tc_fence_before();
+      named_bar_sync(pair_bar, pair_n);
+      tc_fence_after();
+      const uint32_t l_other = tmem_ld1(tmem + lane_base + kTmemX + 3 - h);
+      tmem_wait_ld();
+      const float l_sum = l_part + __uint_as_float(l_other);
       ok = warp_wait(&bars[O_FULL], u & 1, abort_flag);
-      if (!ok) break;
+      if (named_bar_or(pair_bar, pair_n, !ok)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const int s_begin = p.split_offset[b];
       const int nsplit = p.split_offset[b + 1] - s_begin;
@@ -753,12 +823,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const size_t arow = static_cast<size_t>(slot) * p.rows + row;
       const bool direct = (nsplit == 1);
 #pragma unroll 1
-      for (uint32_t c0 = 0; c0 < 256; c0 += 32) {
+      for (uint32_t c0 = 0; c0 < 128; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kTmemO + c0, v);
+        tmem_ld32(tmem + lane_base + kTmemO + 128u * h + c0, v);
         tmem_wait_ld();
         if (!row_ok) continue;
-        const size_t col = 256u * rank + c0;
+        const size_t col = 256u * rank + 128u * h + c0;
         if (direct && p.out_type != MLA_DTYPE_FP32) {
           // 16-bit output: bf16 or fp16 (same size, same layout)
           uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kDv + col);
@@ -771,11 +841,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const float x0 = __uint_as_float(v[8 * c + 2 * i]) * inv_l;
               const float x1 = __uint_as_float(v[8 * c + 2 * i + 1]) * inv_l;
               if (half) {
-                const __half2 h = __floats2half2_rn(x0, x1);
-                w[i] = *reinterpret_cast<const uint32_t*>(&h);
+                const __half2 hh = __floats2half2_rn(x0, x1);
+                w[i] = *reinterpret_cast<const uint32_t*>(&hh);
               } else {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-                w[i] = *reinterpret_cast<const uint32_t*>(&h);
+                const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
+                w[i] = *reinterpret_cast<const uint32_t*>(&hh);
               }
             }
             dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -791,7 +861,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&bars[O_FREE]);
-      if (rank == 0 && row_ok) {
+      if (rank == 0 && h == 0 && row_ok) {
         const float lse = l_sum > 0.f ? (m_used + __log2f(l_sum)) * kLn2 : -INFINITY;
         if (direct)
           p.lse[orow] = lse;
@@ -800,10 +870,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       ++u;
     }
-    if (!ok && lane == 0) {
+    if (!ok && sender) {
       set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // partial scores the peer already sent may still be landing here
-      mbar_wait<true>(&bars[X_FULL + warp], t & 1, nullptr);
+      mbar_wait<true>(&bars[X_FULL + q], t & 1, nullptr);
     }
   }
 
