@@ -472,12 +472,15 @@ def main():
         if dist is not None:
             dist.barrier()
 
+    # the clock sampler starts first (it sleeps while nvidia-smi comes up, and
+    # an idle GPU lowers its clocks), then the warm-up steps bring the clocks
+    # back before the timed ones
+    sampler = ClockSampler()
+    sampler.start()
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
     barrier()
-    sampler = ClockSampler()
-    sampler.start()
     ms = timed(step, args.steps)
     barrier()
     bus = getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None)
