@@ -156,17 +156,22 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 
 // Few rows, many splits (long context: one unit, dozens of splits): one
 // block per (row, 128-column quarter); its kSubsets warps take every
-// kSubsets-th split each, so a warp's loop is n / kSubsets long, and the
-// warps' sums are added through shared memory.  The split weights are the
-// same as above (every warp computes m and Z over all splits).
+// kSubsets-th split each.  A warp loads the LSEs and partial rows of up to
+// kBatch of its splits in one round of loads and merges them into its own
+// (max, sum, weighted row) with the LSE rule, rescaling what it has when a
+// later round raises its max; the warps' triples are then merged the same
+// way through shared memory.  So the whole combine is one round of global
+// latency for up to kSubsets * kBatch splits, instead of one round for the
+// maximum, one for the sum and one per batch of rows.
 constexpr int kSubsets = 8;
 
 __global__ void __launch_bounds__(kSubsets * 32)
     combine_split_kernel(const float* __restrict__ o_accum, const float* __restrict__ lse_accum,
                          const int32_t* __restrict__ split_offset, int rows, void* __restrict__ out, int out_type,
                          float* __restrict__ lse) {
-  constexpr int kBatch = 4;
+  constexpr int kBatch = 12;
   __shared__ float4 part[kSubsets][32];
+  __shared__ float part_m[kSubsets], part_z[kSubsets];
   const int unit = blockIdx.y;
   const int row = blockIdx.x >> 2, quarter = blockIdx.x & 3;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -177,56 +182,66 @@ __global__ void __launch_bounds__(kSubsets * 32)
   pdl_wait_prior_grid();
   const size_t orow = static_cast<size_t>(unit) * rows + row;
   const size_t col = static_cast<size_t>(quarter) * 128 + lane * 4;
-
-  float m = -INFINITY;
-  for (int s = lane; s < n; s += 32) m = fmaxf(m, lse_accum[static_cast<size_t>(s0 + s) * rows + row]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (n <= 0 || m == -INFINITY) {
-    if (warp == 0) {
-      store_row4(out, out_type, orow * kDv + col, 0.f, 0.f, 0.f, 0.f);
-      if (quarter == 0 && lane == 0) lse[orow] = -INFINITY;
-    }
-    return;
-  }
-  float z = 0.f;
-  for (int s = lane; s < n; s += 32) {
-    const float l = lse_accum[static_cast<size_t>(s0 + s) * rows + row];
-    z += (l == -INFINITY) ? 0.f : expf(l - m);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  const float inv_z = 1.f / z;
-
   const size_t split_stride = static_cast<size_t>(rows) * kDv / 4;  // float4 between consecutive splits
   const float4* src = reinterpret_cast<const float4*>(o_accum + (static_cast<size_t>(s0) * rows + row) * kDv + col);
+
+  // this warp's splits: max m, sum z of exp(lse - m), row acc of exp(lse - m) * O
+  float m = -INFINITY, z = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s = warp; s < n; s += kSubsets * kBatch) {
     float4 v[kBatch];
-    float w[kBatch];
+    float l[kBatch];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int si = s + i * kSubsets;
-      const float l = si < n ? lse_accum[static_cast<size_t>(s0 + si) * rows + row] : -INFINITY;
-      w[i] = (l == -INFINITY) ? 0.f : expf(l - m) * inv_z;
+      l[i] = si < n ? lse_accum[static_cast<size_t>(s0 + si) * rows + row] : -INFINITY;
       v[i] = si < n ? __ldg(src + static_cast<size_t>(si) * split_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    float mb = m;
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) acc4(acc, w[i], v[i]);
+    for (int i = 0; i < kBatch; ++i) mb = fmaxf(mb, l[i]);
+    if (mb == -INFINITY) continue;  // nothing but empty splits so far
+    const float r = (m == -INFINITY) ? 0.f : expf(m - mb);
+    z *= r;
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
+    m = mb;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const float w = (l[i] == -INFINITY) ? 0.f : expf(l[i] - m);
+      z += w;
+      acc4(acc, w, v[i]);
+    }
   }
   part[warp][lane] = acc;
+  if (lane == 0) {
+    part_m[warp] = m;
+    part_z[warp] = z;
+  }
   __syncthreads();
   if (warp == 0) {
-    float4 t = part[0][lane];
+    float M = -INFINITY;
 #pragma unroll
-    for (int k = 1; k < kSubsets; ++k) {
-      t.x += part[k][lane].x;
-      t.y += part[k][lane].y;
-      t.z += part[k][lane].z;
-      t.w += part[k][lane].w;
+    for (int k = 0; k < kSubsets; ++k) M = fmaxf(M, part_m[k]);
+    if (M == -INFINITY) {  // every split empty
+      store_row4(out, out_type, orow * kDv + col, 0.f, 0.f, 0.f, 0.f);
+      if (quarter == 0 && lane == 0) lse[orow] = -INFINITY;
+      return;
     }
-    store_row4(out, out_type, orow * kDv + col, t.x, t.y, t.z, t.w);
-    if (quarter == 0 && lane == 0) lse[orow] = m + logf(z);
+    float Z = 0.f;
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kSubsets; ++k) {
+      const float mk = part_m[k];
+      const float r = (mk == -INFINITY) ? 0.f : expf(mk - M);
+      Z = fmaf(part_z[k], r, Z);
+      acc4(t, r, part[k][lane]);
+    }
+    const float inv_z = 1.f / Z;
+    store_row4(out, out_type, orow * kDv + col, t.x * inv_z, t.y * inv_z, t.z * inv_z, t.w * inv_z);
+    if (quarter == 0 && lane == 0) lse[orow] = M + logf(Z);
   }
 }
 
