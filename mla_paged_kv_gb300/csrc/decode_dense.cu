@@ -23,13 +23,14 @@
 //    tile's max exceeds it by more than 2^8 (lazy rescale).  Each CTA derives
 //    every R_t itself, by that rule, from the raw row maxima of all tiles in
 //    order: its own tiles' and the other CTA's, which arrive as 128 floats in
-//    a small mailbox in distributed shared memory (a 128-byte bulk copy per
-//    warp), sent as soon as the owner has read the tile's scores, long
-//    before its P.  The same fp32 comparisons in the same order give both
-//    CTAs the same references.  When R changes, both CTAs rescale their O
-//    half in TMEM before that tile's P V.  Each CTA keeps the row sum l of its own tiles only (rescaled on
-//    every reference change); the two are added once per unit, before the
-//    epilogue, through a second mailbox.
+//    a small mailbox in distributed shared memory (one 4-byte remote store
+//    per row, which takes no TMA instruction), sent as soon as the owner has
+//    read the tile's scores, long before its P.  The same fp32 comparisons
+//    in the same order give both CTAs the same references.  When R changes,
+//    both CTAs rescale their O half in TMEM before that tile's P V.  Each CTA
+//    keeps the row sum l of its own tiles only (rescaled on every reference
+//    change); the two are added once per unit, before the epilogue, through
+//    a second mailbox.
 //  * The P V of a received tile waits only for its P to land (the P V thread
 //    watches the copy's barrier) and for the softmax threads' go, given as
 //    soon as the tile's reference is known.
@@ -99,8 +100,7 @@ constexpr int kOffK = kOffQ + kQSmemBoxes * kQBoxBytes;
 constexpr int kOffV = kOffK + kKSlots * kKSlotBytes;
 constexpr int kOffPOwn = kOffV + kVSlots * kVSlotBytes;
 constexpr int kOffPRecv = kOffPOwn + kPBytes;
-constexpr int kOffRefOut = kOffPRecv + kPBytes;   // this CTA's references, staged for the copy
-constexpr int kOffRefIn = kOffRefOut + kVecBytes;  // mailbox: the peer's references
+constexpr int kOffRefIn = kOffPRecv + kPBytes;     // mailbox: the peer's raw tile maxima
 constexpr int kOffLOut = kOffRefIn + kVecBytes;    // this CTA's row sums, staged
 constexpr int kOffLIn = kOffLOut + kVecBytes;      // mailbox: the peer's row sums
 constexpr int kOffBar = kOffLIn + kVecBytes;
@@ -119,7 +119,7 @@ enum : int {
   OWN_FREE,   // own P buffer reusable: own P V done + the peer's P V done (its multicast commit)
   RECV_FULL,  // the peer's P has landed (bulk-copy bytes); watched and re-armed by the P V thread
   RECV_GO,    // softmax -> P V thread: received tile's reference applied (O rescaled if it changed)
-  R_FULL,     // reference mailbox filled (bulk-copy bytes)
+  R_FULL,     // raw-maximum mailbox filled (remote-store bytes)
   R_FREE,     // the peer has read our last references (one remote arrival per warp)
   L_FULL,     // row-sum mailbox filled (bulk-copy bytes)
   L_FREE,     // the peer has read our last row sums (one remote arrival per warp)
@@ -139,7 +139,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffPOwn % 1024 == 0 && kOffPRecv % 1024 == 0 &&
                   kKSlotBytes % 1024 == 0 && kVSlotBytes % 1024 == 0,
               "swizzle atoms need 1024-byte alignment");
-static_assert(kOffRefOut % 16 == 0 && kOffRefIn % 16 == 0 && kOffLOut % 16 == 0 && kOffLIn % 16 == 0,
+static_assert(kOffRefIn % 16 == 0 && kOffLOut % 16 == 0 && kOffLIn % 16 == 0,
               "bulk copies need 16-byte alignment");
 
 constexpr int kThreads = 288;
@@ -353,7 +353,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sV = smem + kOffV;
   uint8_t* sPOwn = smem + kOffPOwn;
   uint8_t* sPRecv = smem + kOffPRecv;
-  float* sRefOut = reinterpret_cast<float*>(smem + kOffRefOut);
   float* sRefIn = reinterpret_cast<float*>(smem + kOffRefIn);
   float* sLOut = reinterpret_cast<float*>(smem + kOffLOut);
   float* sLIn = reinterpret_cast<float*>(smem + kOffLIn);
@@ -923,10 +922,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = warp_wait_cluster(&bars[R_FREE], (own_i - 1) & 1, abort_flag);
           if (!ok) break;
         }
-        sRefOut[r] = mt;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) bulk_copy_to_cluster(peer_ref, smem_u32(sRefOut + 32 * warp), 32 * 4, peer_r_full);
+        // one 4-byte remote store per row (no TMA instruction: the TMA engine's
+        // time goes per instruction, and it also carries the KV loads and P)
+        st_async_f32(peer_ref + 4u * static_cast<uint32_t>(lane), mt, peer_r_full);
         if (tid == 0) MLA_TRACE(13, t);
         const float r_t = (mt > r_cur + kTau) ? mt : r_cur;
         const float mref = (r_t == -INFINITY) ? 0.f : r_t;

@@ -195,6 +195,14 @@ __device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, float a, float
                : "memory");
 }
 
+// One 32-bit remote store into another CTA's shared memory, completing 4
+// transaction bytes on that CTA's mbarrier (addresses from mapa).
+__device__ __forceinline__ void st_async_f32(uint32_t dst_cluster, float a, uint32_t mbar_cluster) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst_cluster),
+               "f"(a), "r"(mbar_cluster)
+               : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // this CTA's shared memory to another CTA's (dst and its mbarrier from mapa);
 // completion is signalled as transaction bytes on that CTA's mbarrier.
