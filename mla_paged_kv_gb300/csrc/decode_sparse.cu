@@ -822,17 +822,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const size_t orow = static_cast<size_t>(b) * p.rows + row;
       const size_t arow = static_cast<size_t>(slot) * p.rows + row;
       const bool direct = (nsplit == 1);
+      const bool out16 = direct && p.out_type != MLA_DTYPE_FP32;
+      const bool half = p.out_type == MLA_DTYPE_FP16;
+      // Through a 4 KB stage per warp (its own rows' bytes of the P buffer,
+      // free once the last P V is done): each thread writes its row's 32
+      // values, then the warp stores whole row segments, so that a store
+      // instruction covers four (fp32) or eight (16-bit) rows' contiguous
+      // bytes instead of 32 rows' 16 bytes each.
+      uint8_t* stage = sP + warp * (32 * 128);
+      const int row_base = rb * kRowsPerBlock + 32 * q;  // the warp's first row
 #pragma unroll 1
       for (uint32_t c0 = 0; c0 < 128; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kTmemO + 128u * h + c0, v);
         tmem_wait_ld();
-        if (!row_ok) continue;
-        const size_t col = 256u * rank + 128u * h + c0;
-        if (direct && p.out_type != MLA_DTYPE_FP32) {
-          // 16-bit output: bf16 or fp16 (same size, same layout)
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * kDv + col);
-          const bool half = p.out_type == MLA_DTYPE_FP16;
+        uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
+        if (out16) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t w[4];
@@ -848,17 +853,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 w[i] = *reinterpret_cast<const uint32_t*>(&hh);
               }
             }
-            dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+            srow[c ^ (lane & 7)] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         } else {
-          float* dst = direct ? static_cast<float*>(p.out) + orow * kDv + col : p.o_accum + arow * kDv + col;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            reinterpret_cast<float4*>(dst)[c] =
-                make_float4(__uint_as_float(v[4 * c]) * inv_l, __uint_as_float(v[4 * c + 1]) * inv_l,
-                            __uint_as_float(v[4 * c + 2]) * inv_l, __uint_as_float(v[4 * c + 3]) * inv_l);
+            srow[c ^ (lane & 7)] =
+                make_uint4(__float_as_uint(__uint_as_float(v[4 * c]) * inv_l),
+                           __float_as_uint(__uint_as_float(v[4 * c + 1]) * inv_l),
+                           __float_as_uint(__uint_as_float(v[4 * c + 2]) * inv_l),
+                           __float_as_uint(__uint_as_float(v[4 * c + 3]) * inv_l));
         }
+        __syncwarp();
+        // 16-byte pieces per row: 4 (16-bit output) or 8 (fp32)
+        const int pieces = out16 ? 4 : 8;
+        const size_t col = 256u * rank + 128u * h + c0;
+#pragma unroll 1
+        for (int i = lane; i < 32 * pieces; i += 32) {
+          const int rl = i / pieces, pc = i - rl * pieces;
+          const int row_g = row_base + rl;
+          if (row_g < p.rows) {
+            const uint4 val = reinterpret_cast<const uint4*>(stage + rl * 128)[pc ^ (rl & 7)];
+            if (out16) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                    (static_cast<size_t>(b) * p.rows + row_g) * kDv + col);
+              dst[pc] = val;
+            } else {
+              float* base = direct ? static_cast<float*>(p.out) + (static_cast<size_t>(b) * p.rows + row_g) * kDv
+                                   : p.o_accum + (static_cast<size_t>(slot) * p.rows + row_g) * kDv;
+              reinterpret_cast<uint4*>(base + col)[pc] = val;
+            }
+          }
+        }
+        __syncwarp();
       }
+      // the other warp of the pair has read its stage too before either writes
+      // the next unit's partial scores into these bytes
+      named_bar_sync(pair_bar, pair_n);
       tc_fence_before();
       mbar_arrive(&bars[O_FREE]);
       if (rank == 0 && h == 0 && row_ok) {
