@@ -239,13 +239,17 @@ int mla_decode_fwd_static_ws(const void* d_q, const void* d_kv, const int32_t* d
  *   d_workspace as filled by mla_decode_splits / the sparse kernel.
  *   d_out [n_units, rows_per_unit, 512] of out_type (MLA_DTYPE_BF16, _FP32 or
  *   _FP16), d_lse [n_units, rows].
+ *   d_status      int32 (may be NULL): MLA_ERR_TIMEOUT if a wait of the
+ *                 kernel for its own bulk copies ran out (the rows it had
+ *                 not finished are then unspecified).
  * Launched with programmatic dependent launch: it may start before the
  * previous kernel on the stream ends and waits for it on the device before
  * reading the workspace; d_split_offset it reads before that wait, so it
  * must not be written by the kernel launched just before this call (the
  * plan from mla_get_metadata is ready long before). */
 int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* d_split_offset, int n_units,
-                int rows_per_unit, int num_parts, void* d_out, int out_type, float* d_lse, mla_stream_t stream);
+                int rows_per_unit, int num_parts, void* d_out, int out_type, float* d_lse, int32_t* d_status,
+                mla_stream_t stream);
 
 /* Sparse FP8 MLA decode (FlashMLA PR #200).  Query token (b, i) attends to
  * the records selected by d_indices[b][i][0 .. topk_length[b][i]); entry t
@@ -254,8 +258,11 @@ int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* 
  * [0, num_pages*64) is masked and reported as MLA_ERR_BAD_INDEX.
  * Record layout (656 B): [0,512) E4M3 codes, [512,528) four fp32 scales,
  * [528,656) 64 bf16 RoPE values; key[d] = e4m3[d] * scale[d/128] (d < 512),
- * key[512+e] = rope[e]; value = key[0..512).  In the kernel each NoPE value
- * is rounded to bf16 after the fp32 multiply before the tensor-core product.
+ * key[512+e] = rope[e]; value = key[0..512).  In the kernel the scores are
+ * exact in codes and scales: each 128-dim group's codes (exact in bf16) meet
+ * Q on the tensor cores with fp32 accumulation, and the group's scale
+ * multiplies that product in fp32; for the values, the softmax weight times
+ * the group's scale is rounded to bf16 and meets the unscaled codes.
  *   d_q           bf16 [batch, s_q, h_q, 576]
  *   d_kv8         uint8 [num_pages, 64, 656]
  *   d_indices     int32 [batch, s_q, topk]

@@ -55,7 +55,7 @@ _SIGS = {
                             _P, _P]),
     "mla_decode_splits": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _I,
                                _P, _P, _P]),
-    "mla_combine": (_I, [_P, _SZ, _P, _I, _I, _I, _P, _I, _P, _P]),
+    "mla_combine": (_I, [_P, _SZ, _P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "mla_sparse_fp8_decode_fwd": (_I, [_P, _P, _I, _P, _I, _P, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _P, _P,
                                        _P]),
     "mla_sparse_fp8_unpack": (_I, [_P, _I, _P, _I, _P, _P, _P]),
@@ -244,11 +244,11 @@ def mla_decode_fwd_static_ws(q, kv, block_table, cache_seqlens, sched, split_off
     _check(rc, "mla_decode_fwd_static_ws")
 
 
-def mla_combine(workspace, split_offset, n_units, rows_per_unit, num_parts, out, lse, stream=None):
+def mla_combine(workspace, split_offset, n_units, rows_per_unit, num_parts, out, lse, status=None, stream=None):
     _need(workspace, torch.uint8, "workspace")
     _check(load_library().mla_combine(_ptr(workspace), workspace.numel(), _ptr(split_offset), int(n_units),
                                       int(rows_per_unit), int(num_parts), _ptr(out),
-                                      _DTYPE_CODE[out.dtype], _ptr(lse), _stream(stream)), "mla_combine")
+                                      _DTYPE_CODE[out.dtype], _ptr(lse), _ptr(status), _stream(stream)), "mla_combine")
 
 
 def mla_sparse_fp8_decode_fwd(q, kv8, indices, topk_length, sched, split_offset, num_parts, workspace, out, lse,

@@ -14,7 +14,10 @@
 
 namespace mla {
 cudaError_t launch_sched(const int32_t*, int, int, int, int32_t*, int32_t*, int, cudaStream_t);
-cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, int, void*, int, float*, cudaStream_t);
+cudaError_t launch_combine(const float*, const float*, const int32_t*, int, int, int, void*, int, float*, int32_t*, int,
+                           cudaStream_t);
+const void* combine_stream_kernel_ptr();
+int combine_stream_smem_bytes();
 cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                          const DecodeParams&, int, int, cudaStream_t);
 int dense_smem_bytes();
@@ -101,6 +104,8 @@ const DeviceInfo& device_info() {
   for (int kind = 0; kind < 4; ++kind)
     attr_ok = attr_ok && cudaFuncSetAttribute(dense_kernel_ptr(kind), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               dense_smem_bytes()) == cudaSuccess;
+  attr_ok = attr_ok && cudaFuncSetAttribute(combine_stream_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            combine_stream_smem_bytes()) == cudaSuccess;
   if (!attr_ok) {
     cudaGetLastError();
     d.status = MLA_ERR_CUDA;
@@ -359,7 +364,7 @@ int sparse_run(const SparseCall& c, bool combine) {
   if (launch_sparse(qm, p, c.num_parts, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (!combine) return MLA_OK;
   return mla_combine(c.ws, c.ws_bytes, c.split_offset, c.n_units, c.rows, c.num_parts, c.out, c.out_type, c.lse,
-                     c.stream);
+                     c.status, c.stream);
 }
 
 }  // namespace
@@ -488,7 +493,8 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
 }
 
 int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* d_split_offset, int n_units,
-                int rows_per_unit, int num_parts, void* d_out, int out_type, float* d_lse, mla_stream_t stream) {
+                int rows_per_unit, int num_parts, void* d_out, int out_type, float* d_lse, int32_t* d_status,
+                mla_stream_t stream) {
   if (!d_workspace || !d_split_offset || !d_out || !d_lse) return MLA_ERR_INVALID_ARG;
   if (n_units < 1 || n_units > 65535 || rows_per_unit < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
   if (out_type != MLA_DTYPE_BF16 && out_type != MLA_DTYPE_FP32 && out_type != MLA_DTYPE_FP16)
@@ -496,10 +502,12 @@ int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* 
   if (!aligned16(d_workspace) || !aligned16(d_out)) return MLA_ERR_INVALID_ARG;
   const WorkspaceLayout w = ws_layout(n_units, rows_per_unit, num_parts);
   if (workspace_bytes < w.total) return MLA_ERR_INVALID_ARG;
+  const DeviceInfo& d = device_info();
+  if (d.status != MLA_OK) return d.status;
   const float* o = static_cast<const float*>(d_workspace);
   const float* l = reinterpret_cast<const float*>(static_cast<const char*>(d_workspace) + w.lse_off);
-  return launch_combine(o, l, d_split_offset, n_units, rows_per_unit, num_parts, d_out, out_type, d_lse,
-                        reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  return launch_combine(o, l, d_split_offset, n_units, rows_per_unit, num_parts, d_out, out_type, d_lse, d_status,
+                        d.sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
 }
@@ -515,7 +523,7 @@ int mla_decode_fwd(const void* d_q, const void* d_kv, const int32_t* d_block_tab
                              workspace_bytes, d_out, out_type, d_lse, d_status, stream);
   if (rc != MLA_OK) return rc;
   return mla_combine(d_workspace, workspace_bytes, d_split_offset, batch, s_q * h_q, num_parts, d_out, out_type,
-                     d_lse, stream);
+                     d_lse, d_status, stream);
 }
 
 namespace {

@@ -26,7 +26,7 @@ def run_dense(case, num_parts=None, split_path=False, out_dtype=None):
     if split_path:
         mla.mla_decode_splits(c.q, c.kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset, pl.num_parts,
                               pl.workspace, out, lse, status, case.causal, case.scale)
-        mla.mla_combine(pl.workspace, pl.split_offset, B, s_q * h_q, pl.num_parts, out, lse)
+        mla.mla_combine(pl.workspace, pl.split_offset, B, s_q * h_q, pl.num_parts, out, lse, status)
     else:
         mla.mla_decode_fwd(c.q, c.kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset, pl.num_parts,
                            pl.workspace, out, lse, status, case.causal, case.scale)
