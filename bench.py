@@ -221,7 +221,14 @@ def cpu_model():
             return m.group(1).strip()
     parts = sorted(set(re.findall(r"^CPU part\s*:\s*(\S+)", text, flags=re.M)))
     impl = sorted(set(re.findall(r"^CPU implementer\s*:\s*(\S+)", text, flags=re.M)))
-    return f"implementer {','.join(impl)} part {','.join(parts)}" if parts else None
+    if not parts:
+        return None
+    # Arm's published part numbers for the cores these hosts carry (implementer 0x41 = Arm)
+    arm_parts = {"0xd4f": "Neoverse V2", "0xd40": "Neoverse V1", "0xd0c": "Neoverse N1", "0xd49": "Neoverse N2",
+                 "0xd84": "Neoverse V3"}
+    names = [arm_parts[p] for p in parts if impl == ["0x41"] and p in arm_parts]
+    raw = f"implementer {','.join(impl)} part {','.join(parts)}"
+    return f"{', '.join(names)} ({raw})" if names else raw
 
 
 _ONE_THREAD_SCRIPT = r"""
