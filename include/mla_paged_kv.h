@@ -330,6 +330,23 @@ int mla_test_pack_timeout(const uint8_t* d_kv8, int num_pages, const int32_t* d_
                           const int32_t* d_topk_length, int n_units, void* d_packed, size_t packed_bytes,
                           int32_t* d_status, mla_stream_t stream);
 
+/* Test hook for the dense decode kernel's timeout and unwind path (no
+ * counterpart on the pages).  Same arguments and checks as
+ * mla_decode_splits, bf16 only (else MLA_ERR_UNSUPPORTED before any
+ * launch).  It runs an instance of the dense kernel whose K producer never
+ * loads the first own tile of each CTA and whose waits have a 200 us budget:
+ * the Q K^T thread's wait for that tile runs out, the CTA writes
+ * MLA_ERR_TIMEOUT to *d_status and unwinds (every role leaves its loop, the
+ * copies it issued land, the MMAs it issued complete, TMEM is released),
+ * its peer CTA's waits for messages that never come run out the same way,
+ * and the grid ends.  The context and the stream stay usable; out, lse and
+ * the workspace are unspecified. */
+int mla_test_decode_timeout(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
+                            int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int h_kv,
+                            int dtype, int causal, float softmax_scale, const int32_t* d_sched,
+                            const int32_t* d_split_offset, int num_parts, void* d_workspace, size_t workspace_bytes,
+                            void* d_out, int out_type, float* d_lse, int32_t* d_status, mla_stream_t stream);
+
 /* Sparse FP8 decode over a packed workspace (FlashMLA PR #200, "Packed
  * attention specialization": the packed attention reuses the native
  * dequantisation, softmax, split and combine pipeline and only replaces the

@@ -26,7 +26,8 @@ __all__ = [
     "mla_get_metadata", "mla_decode_fwd", "mla_decode_splits", "mla_combine",
     "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws",
     "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd",
-    "mla_get_metadata_request_local", "mla_num_parts_dense", "mla_test_pack_timeout", "plan", "decode",
+    "mla_get_metadata_request_local", "mla_num_parts_dense", "mla_test_pack_timeout", "mla_test_decode_timeout", "plan",
+    "decode",
     "sparse_decode", "pack_selected_kv", "packed_sparse_decode",
     "EXPORTED_SYMBOLS",
 ]
@@ -36,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd", "mla_sparse_fp8_unpack",
     "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes", "mla_pack_selected_kv",
     "mla_sparse_fp8_packed_decode_fwd", "mla_get_metadata_request_local", "mla_num_parts_dense",
-    "mla_test_pack_timeout",
+    "mla_test_pack_timeout", "mla_test_decode_timeout",
 )
 
 _P = ctypes.c_void_p
@@ -64,6 +65,8 @@ _SIGS = {
     "mla_packed_kv_workspace_bytes": (_SZ, [_I, _I]),
     "mla_pack_selected_kv": (_I, [_P, _I, _P, _I, _P, _I, _P, _SZ, _P, _P]),
     "mla_test_pack_timeout": (_I, [_P, _I, _P, _I, _P, _I, _P, _SZ, _P, _P]),
+    "mla_test_decode_timeout": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P,
+                                     _I, _P, _P, _P]),
     "mla_sparse_fp8_packed_decode_fwd": (_I, [_P, _P, _SZ, _I, _P, _I, _I, _I, _F, _P, _P, _I, _P, _SZ, _P, _P, _P,
                                               _P]),
 }
@@ -227,6 +230,15 @@ def mla_decode_splits(q, kv, block_table, cache_seqlens, sched, split_offset, nu
     args = _dense_args(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse,
                        status, causal, softmax_scale, stream)
     _check(load_library().mla_decode_splits(*args), "mla_decode_splits")
+
+
+def mla_test_decode_timeout(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse,
+                            status, causal=False, softmax_scale=1.0 / 24.0, stream=None):
+    """Test hook: the dense kernel instance whose first own K tile never
+    loads, so that a bounded wait runs out (*status = MLA_ERR_TIMEOUT)."""
+    args = _dense_args(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, workspace, out, lse,
+                       status, causal, softmax_scale, stream)
+    _check(load_library().mla_test_decode_timeout(*args), "mla_test_decode_timeout")
 
 
 def mla_decode_fwd_static_ws(q, kv, block_table, cache_seqlens, sched, split_offset, num_parts, out, lse, status,

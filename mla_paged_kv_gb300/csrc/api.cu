@@ -101,7 +101,7 @@ const DeviceInfo& device_info() {
   }
   bool attr_ok = cudaFuncSetAttribute(sparse_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       sparse_smem_bytes()) == cudaSuccess;
-  for (int kind = 0; kind < 4; ++kind)
+  for (int kind = 0; kind < 5; ++kind)
     attr_ok = attr_ok && cudaFuncSetAttribute(dense_kernel_ptr(kind), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               dense_smem_bytes()) == cudaSuccess;
   attr_ok = attr_ok && cudaFuncSetAttribute(combine_stream_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -621,6 +621,23 @@ int mla_pack_selected_kv(const uint8_t* d_kv8, int num_pages, const int32_t* d_i
                          int32_t* d_status, mla_stream_t stream) {
   return pack_selected(d_kv8, num_pages, d_indices, topk, d_topk_length, n_units, d_packed, packed_bytes, d_status,
                        0, stream);
+}
+
+int mla_test_decode_timeout(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
+                            int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int h_kv,
+                            int dtype, int causal, float softmax_scale, const int32_t* d_sched,
+                            const int32_t* d_split_offset, int num_parts, void* d_workspace, size_t workspace_bytes,
+                            void* d_out, int out_type, float* d_lse, int32_t* d_status, mla_stream_t stream) {
+  if (dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED;
+  DecodeParams p;
+  CUtensorMap qm, km, sm, rm;
+  const int rc = dense_prepare(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q,
+                               h_kv, dtype, causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace,
+                               workspace_bytes, d_out, out_type, d_lse, d_status, &p, &qm, &km, &sm, &rm);
+  if (rc != MLA_OK) return rc;
+  return launch_dense(qm, km, sm, rm, p, num_parts, 4, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 int mla_test_pack_timeout(const uint8_t* d_kv8, int num_pages, const int32_t* d_indices, int topk,

@@ -221,17 +221,23 @@ __host__ __device__ constexpr int k_box(int j) {
   return kRank == 0 ? 4 + j : (j < 4 ? j : 8);
 }
 
+// Wait budget of the stall-test instance (kStall): short, so that its test
+// ends quickly; the other instances keep the 2 s budget of every wait.
+constexpr uint64_t kStallWaitNs = 200000;  // 200 us
+
 __device__ __forceinline__ void set_abort(volatile int* abort_flag, int32_t* status, int code) {
   *abort_flag = 1;
   report(status, code);
 }
 
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, limit_ns));
 }
 
-__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  return __all_sync(0xffffffffu, mbar_wait<true>(bar, parity, abort_flag));
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait<true>(bar, parity, abort_flag, limit_ns));
 }
 
 // Page ids of 32 consecutive pages of unit c.b starting at `base`, one per lane
@@ -340,11 +346,12 @@ __device__ __forceinline__ float ref_alpha(float r_old, float r_new) {
 // kHalf: Q and KV are fp16 (else bf16).  The three maps view the 16-bit
 // pool with boxes of 4, 5 and 1 consecutive 64-dim slices (kv_map, sc_map,
 // rope_map).
-template <bool kHalf, bool kQV>
+template <bool kHalf, bool kQV, bool kStall>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     dense_decode_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
                         const __grid_constant__ CUtensorMap sc_map, const __grid_constant__ CUtensorMap rope_map,
                         const DecodeParams p) {
+  constexpr uint64_t kWaitNs = kStall ? kStallWaitNs : MLA_WAIT_LIMIT_NS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -466,8 +473,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (is_k) {
             const uint32_t n = own_k / kKSlots;
             const int s = static_cast<int>(own_k % kKSlots);
-            if (n >= 1) ok = mbar_wait(&bars[K_EMPTY + s], (n - 1) & 1, abort_flag);
-            if (ok) {
+            if (n >= 1) ok = mbar_wait(&bars[K_EMPTY + s], (n - 1) & 1, abort_flag, kWaitNs);
+            // the stall-test instance never loads its first own tile's K slot
+            if (kStall && own_k == 0) {
+              // nothing issued: the Q K^T thread's wait for this slot runs out
+            } else if (ok) {
               // the softmax masks this own tile's keys if its page was outside
               // the pool; written once the previous own tile's Q K^T has read
               // the K slot, hence after the softmax read the entry's last use
@@ -489,10 +499,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           } else {
             const uint32_t n = c.t / kVSlots;
             const int s = static_cast<int>(c.t % kVSlots);
-            if (n >= 1) ok = mbar_wait(&bars[V_EMPTY + s], (n - 1) & 1, abort_flag);
+            if (n >= 1) ok = mbar_wait(&bars[V_EMPTY + s], (n - 1) & 1, abort_flag, kWaitNs);
             // V-ring Q stage: the ring holds the first unit's Q until it is in TMEM
             if constexpr (kQV) {
-              if (c.t == 0 && ok) ok = mbar_wait(&bars[VQ_EMPTY], 0, abort_flag);
+              if (c.t == 0 && ok) ok = mbar_wait(&bars[VQ_EMPTY], 0, abort_flag, kWaitNs);
             }
             if (ok) {
               MLA_TRACE(7, c.t);
@@ -512,9 +522,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // no TMA write may land after this CTA exits
       for (int s = 0; s < kKSlots; ++s)
-        if (k_issued[s] > 0) mbar_wait(&bars[K_FULL + s], (k_issued[s] - 1) & 1, nullptr);
+        if (k_issued[s] > 0) mbar_wait(&bars[K_FULL + s], (k_issued[s] - 1) & 1, nullptr, kWaitNs);
       for (int s = 0; s < kVSlots; ++s)
-        if (v_issued[s] > 0) mbar_wait(&bars[V_FULL + s], (v_issued[s] - 1) & 1, nullptr);
+        if (v_issued[s] > 0) mbar_wait(&bars[V_FULL + s], (v_issued[s] - 1) & 1, nullptr, kWaitNs);
     }
     __syncwarp();
   } else if (warp == kWarpQ) {
@@ -562,11 +572,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         } else {
           const int us = c.u - 1;  // units streamed through the slots before this one
-          ok = mbar_wait(&bars[Q_EMPTY], (c.u - 1) & 1, abort_flag);
+          ok = mbar_wait(&bars[Q_EMPTY], (c.u - 1) & 1, abort_flag, kWaitNs);
           for (int j = 0; ok && j < 9; ++j) {
             const int sl = j % kQSmemBoxes;
             // the slot's previous box (j - 3) has been copied into TMEM (two copies a slot per streamed unit)
-            if (j >= kQSmemBoxes) ok = mbar_wait(&bars[QB_EMPTY + sl], (2 * us + j / 3 - 1) & 1, abort_flag);
+            if (j >= kQSmemBoxes) ok = mbar_wait(&bars[QB_EMPTY + sl], (2 * us + j / 3 - 1) & 1, abort_flag, kWaitNs);
             if (!ok) break;
             mbar_arrive_expect_tx(&bars[QB_FULL + sl], q_box_bytes);
             q_box(c.b, j, sQ + sl * kQBoxBytes, &bars[QB_FULL + sl]);
@@ -582,9 +592,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // no TMA write may land after this CTA exits
-      if (vq_issued > 0) mbar_wait(&bars[VQ_FULL], 0, nullptr);
+      if (vq_issued > 0) mbar_wait(&bars[VQ_FULL], 0, nullptr, kWaitNs);
       for (int sl = 0; sl < kQSmemBoxes; ++sl)
-        if (qb_issued[sl] > 0) mbar_wait(&bars[QB_FULL + sl], (qb_issued[sl] - 1) & 1, nullptr);
+        if (qb_issued[sl] > 0) mbar_wait(&bars[QB_FULL + sl], (qb_issued[sl] - 1) & 1, nullptr, kWaitNs);
     } else if (lane == 0) {
       const uint64_t pol_q = policy_evict_last();
       Cursor c;
@@ -612,11 +622,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (c.valid)
         for (int j = 3; j < 9; ++j) q_box(c.b, j, nullptr);
       while (ok && c.valid) {
-        if (c.u >= 1) ok = mbar_wait(&bars[Q_EMPTY], (c.u - 1) & 1, abort_flag);
+        if (c.u >= 1) ok = mbar_wait(&bars[Q_EMPTY], (c.u - 1) & 1, abort_flag, kWaitNs);
         for (int j = 0; ok && j < 9; ++j) {
           const int sl = j % kQSmemBoxes;
           // the slot's previous box (j - 3) has been copied into TMEM
-          if (j >= kQSmemBoxes) ok = mbar_wait(&bars[QB_EMPTY + sl], (2 * c.u + j / 3 - 1) & 1, abort_flag);
+          if (j >= kQSmemBoxes) ok = mbar_wait(&bars[QB_EMPTY + sl], (2 * c.u + j / 3 - 1) & 1, abort_flag, kWaitNs);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars[QB_FULL + sl], q_box_bytes);
           q_box(c.b, j, &bars[QB_FULL + sl]);
@@ -632,7 +642,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // no TMA write may land after this CTA exits
       for (int sl = 0; sl < kQSmemBoxes; ++sl)
-        if (qb_issued[sl] > 0) mbar_wait(&bars[QB_FULL + sl], (qb_issued[sl] - 1) & 1, nullptr);
+        if (qb_issued[sl] > 0) mbar_wait(&bars[QB_FULL + sl], (qb_issued[sl] - 1) & 1, nullptr, kWaitNs);
     }
     __syncwarp();
   } else if (warp == kWarpPV) {
@@ -691,7 +701,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (progressed) {
           t_last = globaltimer_ns();
-        } else if (*abort_flag || globaltimer_ns() - t_last > MLA_WAIT_LIMIT_NS) {
+        } else if (*abort_flag || globaltimer_ns() - t_last > kWaitNs) {
           ok = false;
           break;
         }
@@ -699,7 +709,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) {
         set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
         // a P the peer already sent may still be landing in our receive buffer
-        mbar_wait<true>(&bars[RECV_FULL], pv_recv & 1, nullptr);
+        mbar_wait<true>(&bars[RECV_FULL], pv_recv & 1, nullptr, kWaitNs);
       }
       umma_commit(&bars[DRAIN]);
     }
@@ -766,7 +776,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (kQV && cq.valid) {
         // the first unit's boxes 0-5, staged in the V ring: into TMEM (once,
         // before the issue loop), then the ring goes to the V producer
-        ok = mbar_wait(&bars[VQ_FULL], 0, abort_flag);
+        ok = mbar_wait(&bars[VQ_FULL], 0, abort_flag, kWaitNs);
         if (ok) {
           tc_fence_after();
           const uint64_t vq_desc0 = sdesc_sw128(smem_u32(sV), 16, 1024);
@@ -825,7 +835,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           t_last = globaltimer_ns();
         } else {
           // spin: a sleeping issuer reacts to a ready job far later than the job takes
-          if (*abort_flag || globaltimer_ns() - t_last > MLA_WAIT_LIMIT_NS) {
+          if (*abort_flag || globaltimer_ns() - t_last > kWaitNs) {
             ok = false;
             break;
           }
@@ -834,7 +844,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // every MMA (of both issuers) has completed before TMEM is released
       umma_commit(&bars[DRAIN]);
-      mbar_wait(&bars[DRAIN], 0, nullptr);
+      mbar_wait(&bars[DRAIN], 0, nullptr, kWaitNs);
     }
     __syncwarp();
   } else {
@@ -877,7 +887,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int jmax = p.causal ? (c.L - p.s_q + tok) : (c.L - 1);  // last visible key
         const int vis = jmax - c.k * kT;                                // keys 0..vis of this tile are visible
         uint64_t keep = (vis >= kT - 1 ? ~0ull : (vis < 0 ? 0ull : (~0ull >> (kT - 1 - vis))));
-        ok = warp_wait(&bars[S_FULL], own_i & 1, abort_flag);
+        ok = warp_wait(&bars[S_FULL], own_i & 1, abort_flag, kWaitNs);
         if (!ok) break;
         if (tid == 0) MLA_TRACE(4, t);
         tc_fence_after();
@@ -919,7 +929,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // the peer derives this tile's reference from its raw maximum, as we
         // do: it is sent at once and waits for nothing of the peer's
         if (own_i >= 1) {
-          ok = warp_wait_cluster(&bars[R_FREE], (own_i - 1) & 1, abort_flag);
+          ok = warp_wait_cluster(&bars[R_FREE], (own_i - 1) & 1, abort_flag, kWaitNs);
           if (!ok) break;
         }
         // one 4-byte remote store per row (no TMA instruction: the TMA engine's
@@ -941,7 +951,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // the own P buffer is free once our P V and the peer's P V of the
         // previous own tile are done (the latter also means our copy landed)
         if (own_i >= 1) {
-          ok = warp_wait_cluster(&bars[OWN_FREE], (own_i - 1) & 1, abort_flag);
+          ok = warp_wait_cluster(&bars[OWN_FREE], (own_i - 1) & 1, abort_flag, kWaitNs);
           if (!ok) break;
         }
         if (tid == 0) MLA_TRACE(14, t);
@@ -961,7 +971,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       } else {
         // ---- received tile: its reference from the owner's raw maximum, by the
         // same rule the owner applies; its P V runs when its P lands
-        ok = warp_wait_cluster(&bars[R_FULL], recv_i & 1, abort_flag);
+        ok = warp_wait_cluster(&bars[R_FULL], recv_i & 1, abort_flag, kWaitNs);
         if (!ok) break;
         if (tid == 0) mbar_arrive_expect_tx(&bars[R_FULL], kVecBytes);  // armed for the next message
         // read (and use, so the load has completed) before the mailbox is released
@@ -981,7 +991,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // it), so the parity wait cannot pass on an older completion.  (With one
       // barrier for all tiles it could, while P V t-2 was still in flight.)
       if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
-        ok = warp_wait(&bars[PV_DONE + ((t - 1) & 1)], ((t - 1) >> 1) & 1, abort_flag);
+        ok = warp_wait(&bars[PV_DONE + ((t - 1) & 1)], ((t - 1) >> 1) & 1, abort_flag, kWaitNs);
         if (!ok) break;
         tc_fence_after();
         rescale_o(taddr, alpha);
@@ -1001,14 +1011,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!last) continue;
       // ---- row sum of the unit: ours + the peer's, both relative to r_cur
       if (units >= 1) {
-        ok = warp_wait_cluster(&bars[L_FREE], (units - 1) & 1, abort_flag);
+        ok = warp_wait_cluster(&bars[L_FREE], (units - 1) & 1, abort_flag, kWaitNs);
         if (!ok) break;
       }
       sLOut[r] = l_own;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) bulk_copy_to_cluster(peer_l, smem_u32(sLOut + 32 * warp), 32 * 4, peer_l_full);
-      ok = warp_wait_cluster(&bars[L_FULL], units & 1, abort_flag);
+      ok = warp_wait_cluster(&bars[L_FULL], units & 1, abort_flag, kWaitNs);
       if (!ok) break;
       if (tid == 0) mbar_arrive_expect_tx(&bars[L_FULL], kVecBytes);
       const float l_peer = __shfl_sync(0xffffffffu, sLIn[r], lane);
@@ -1018,8 +1028,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ++units;
       // ---- epilogue of this (unit, split)
       // staging buffer: the own P buffer, free once both P V of our last own tile are done
-      ok = warp_wait(&bars[O_FULL], u_here & 1, abort_flag);
-      if (ok && own_i >= 1) ok = warp_wait_cluster(&bars[OWN_FREE], (own_i - 1) & 1, abort_flag);
+      ok = warp_wait(&bars[O_FULL], u_here & 1, abort_flag, kWaitNs);
+      if (ok && own_i >= 1) ok = warp_wait_cluster(&bars[OWN_FREE], (own_i - 1) & 1, abort_flag, kWaitNs);
       if (!ok) break;
       tc_fence_after();
       const int s_begin = p.split_offset[b_here];
@@ -1101,8 +1111,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // After a timeout the peer may still have a mailbox copy in flight to us:
   // give the armed ones (bounded) time to land before the cluster can exit.
   if (tid == 0 && (aborted || *abort_flag)) {
-    mbar_wait<true>(&bars[R_FULL], r_seen & 1, nullptr);
-    mbar_wait<true>(&bars[L_FULL], l_seen & 1, nullptr);
+    mbar_wait<true>(&bars[R_FULL], r_seen & 1, nullptr, kWaitNs);
+    mbar_wait<true>(&bars[L_FULL], l_seen & 1, nullptr, kWaitNs);
   }
   tc_fence_before();
   __syncthreads();
@@ -1117,14 +1127,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace dn
 
 int dense_smem_bytes() { return dn::kSmemBytes; }
-// kind 0: bf16, 1: fp16, 2: bf16 with the V-ring Q stage, 3: fp16 with it
+// kind 0: bf16, 1: fp16, 2: bf16 with the V-ring Q stage, 3: fp16 with it,
+// 4: the bf16 stall-test instance (its first own tile's K slot is never
+// loaded, so a wait runs out and the kernel reports MLA_ERR_TIMEOUT)
 int dense_threads(int) { return dn::kThreads; }
 const void* dense_kernel_ptr(int kind) {
   switch (kind) {
-    case 1: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false>);
-    case 2: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, true>);
-    case 3: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true>);
-    default: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false>);
+    case 1: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, false, false>);
+    case 2: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, true, false>);
+    case 3: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<true, true, false>);
+    case 4: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, true>);
+    default: return reinterpret_cast<const void*>(&dn::dense_decode_kernel<false, false, false>);
   }
 }
 
@@ -1134,20 +1147,24 @@ cudaError_t launch_dense(const CUtensorMap& q_map, const CUtensorMap& kv_map, co
   const dim3 grid(2 * num_parts * p.row_blocks);
   switch (kind) {
     case 1:
-      dn::dense_decode_kernel<true, false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                            rope_map, p);
+      dn::dense_decode_kernel<true, false, false>
+          <<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map, rope_map, p);
       break;
     case 2:
-      dn::dense_decode_kernel<false, true><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                            rope_map, p);
+      dn::dense_decode_kernel<false, true, false>
+          <<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map, rope_map, p);
       break;
     case 3:
-      dn::dense_decode_kernel<true, true><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                           rope_map, p);
+      dn::dense_decode_kernel<true, true, false>
+          <<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map, rope_map, p);
+      break;
+    case 4:
+      dn::dense_decode_kernel<false, false, true>
+          <<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map, rope_map, p);
       break;
     default:
-      dn::dense_decode_kernel<false, false><<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map,
-                                                                                             rope_map, p);
+      dn::dense_decode_kernel<false, false, false>
+          <<<grid, dn::kThreads, dn::kSmemBytes, stream>>>(q_map, kv_map, sc_map, rope_map, p);
   }
   return cudaGetLastError();
 }

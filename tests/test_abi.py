@@ -35,7 +35,8 @@ def test_header_declares_the_boundary():
                             "mla_decode_fwd", "mla_decode_splits", "mla_combine", "mla_sparse_fp8_decode_fwd",
                             "mla_sparse_fp8_unpack", "mla_decode_fwd_static_ws", "mla_packed_kv_workspace_bytes",
                             "mla_pack_selected_kv", "mla_sparse_fp8_packed_decode_fwd",
-                            "mla_get_metadata_request_local", "mla_num_parts_dense", "mla_test_pack_timeout"])
+                            "mla_get_metadata_request_local", "mla_num_parts_dense", "mla_test_pack_timeout",
+                            "mla_test_decode_timeout"])
 
 
 def test_library_exports_every_declared_symbol(lib_path):
