@@ -332,15 +332,18 @@ int mla_test_pack_timeout(const uint8_t* d_kv8, int num_pages, const int32_t* d_
 
 /* Test hook for the dense decode kernel's timeout and unwind path (no
  * counterpart on the pages).  Same arguments and checks as
- * mla_decode_splits, bf16 only (else MLA_ERR_UNSUPPORTED before any
- * launch).  It runs an instance of the dense kernel whose K producer never
- * loads the first own tile of each CTA and whose waits have a 200 us budget:
- * the Q K^T thread's wait for that tile runs out, the CTA writes
- * MLA_ERR_TIMEOUT to *d_status and unwinds (every role leaves its loop, the
- * copies it issued land, the MMAs it issued complete, TMEM is released),
- * its peer CTA's waits for messages that never come run out the same way,
- * and the grid ends.  The context and the stream stay usable; out, lse and
- * the workspace are unspecified. */
+ * mla_decode_splits, for a bf16 cache or a cache of FP8 records (else
+ * MLA_ERR_UNSUPPORTED before any launch).  bf16: an instance of the dense
+ * kernel whose K producer never loads the first own tile of each CTA and
+ * whose waits have a 200 us budget: the Q K^T thread's wait for that tile
+ * runs out, the CTA writes MLA_ERR_TIMEOUT to *d_status and unwinds (every
+ * role leaves its loop, the copies it issued land, the MMAs it issued
+ * complete, TMEM is released), its peer CTA's waits for messages that never
+ * come run out the same way, and the grid ends.  FP8 records: an instance
+ * of the sparse kernel (the one such a cache runs) that never computes the
+ * first tile's scores, with the same 200 us budgets and the same unwinding.
+ * The context and the stream stay usable; out, lse and the workspace are
+ * unspecified. */
 int mla_test_decode_timeout(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages,
                             int num_pages, const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int h_kv,
                             int dtype, int causal, float softmax_scale, const int32_t* d_sched,

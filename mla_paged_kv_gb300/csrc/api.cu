@@ -23,10 +23,10 @@ cudaError_t launch_dense(const CUtensorMap&, const CUtensorMap&, const CUtensorM
 int dense_smem_bytes();
 int dense_threads(int kind);
 const void* dense_kernel_ptr(int kind);
-cudaError_t launch_sparse(const CUtensorMap&, const DecodeParams&, int, cudaStream_t);
+cudaError_t launch_sparse(const CUtensorMap&, const DecodeParams&, int, int, cudaStream_t);
 int sparse_smem_bytes();
 int sparse_threads();
-const void* sparse_kernel_ptr();
+const void* sparse_kernel_ptr(int stall);
 cudaError_t launch_unpack(const uint8_t*, int, const int32_t*, int, float*, int32_t*, cudaStream_t);
 cudaError_t launch_pack(const uint8_t*, int, const int32_t*, int, const int32_t*, int, uint8_t*, uint64_t*,
                         int32_t*, int, cudaStream_t);
@@ -99,8 +99,10 @@ const DeviceInfo& device_info() {
     d.ready = true;
     return d;
   }
-  bool attr_ok = cudaFuncSetAttribute(sparse_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      sparse_smem_bytes()) == cudaSuccess;
+  bool attr_ok = true;
+  for (int stall = 0; stall < 2; ++stall)
+    attr_ok = attr_ok && cudaFuncSetAttribute(sparse_kernel_ptr(stall), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              sparse_smem_bytes()) == cudaSuccess;
   for (int kind = 0; kind < 5; ++kind)
     attr_ok = attr_ok && cudaFuncSetAttribute(dense_kernel_ptr(kind), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               dense_smem_bytes()) == cudaSuccess;
@@ -114,8 +116,8 @@ const DeviceInfo& device_info() {
   }
   // the dense plan also sizes the FP8-record calls, which run the sparse kernel
   d.dense_clusters = std::min(max_clusters(dense_kernel_ptr(0), dense_threads(0), dense_smem_bytes()),
-                              max_clusters(sparse_kernel_ptr(), sparse_threads(), sparse_smem_bytes()));
-  d.sparse_clusters = max_clusters(sparse_kernel_ptr(), sparse_threads(), sparse_smem_bytes());
+                              max_clusters(sparse_kernel_ptr(0), sparse_threads(), sparse_smem_bytes()));
+  d.sparse_clusters = max_clusters(sparse_kernel_ptr(0), sparse_threads(), sparse_smem_bytes());
   cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
   if (d.dense_clusters <= 0 || d.sparse_clusters <= 0 || d.sms <= 0) {
     cudaGetLastError();
@@ -307,6 +309,7 @@ struct SparseCall {
   float* lse = nullptr;
   int32_t* status = nullptr;
   mla_stream_t stream = nullptr;
+  int stall = 0;  // 1: the kernel's stall-test instance (mla_test_decode_timeout)
 };
 
 int sparse_run(const SparseCall& c, bool combine) {
@@ -361,10 +364,53 @@ int sparse_run(const SparseCall& c, bool combine) {
   const int rc = encode_q_map(&qm, c.q, static_cast<long long>(c.n_units) * c.rows);
   if (rc != MLA_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(c.stream);
-  if (launch_sparse(qm, p, c.num_parts, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_sparse(qm, p, c.num_parts, c.stall, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (!combine) return MLA_OK;
   return mla_combine(c.ws, c.ws_bytes, c.split_offset, c.n_units, c.rows, c.num_parts, c.out, c.out_type, c.lse,
                      c.status, c.stream);
+}
+
+// A cache of FP8 records runs the sparse kernel (exact scores in codes and
+// scales) with the block table as the slot source and a whole request as
+// the unit, under the same plan as the 16-bit caches.
+int fp8_record_splits(const void* d_q, const void* d_kv, const int32_t* d_block_table, int max_pages, int num_pages,
+                      const int32_t* d_cache_seqlens, int batch, int s_q, int h_q, int h_kv, int causal,
+                      float softmax_scale, const int32_t* d_sched, const int32_t* d_split_offset, int num_parts,
+                      void* d_workspace, size_t workspace_bytes, void* d_out, int out_type, float* d_lse,
+                      int32_t* d_status, mla_stream_t stream, int stall) {
+  if (!d_block_table || !d_cache_seqlens || max_pages < 1 || batch < 1 || s_q < 1 || h_q < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(s_q) * h_q;
+  if (rows > (1 << 20) || static_cast<long long>(max_pages) * MLA_PAGE_SIZE > (1LL << 31) - 1)
+    return MLA_ERR_UNSUPPORTED;
+  SparseCall c;
+  c.q = d_q;
+  c.kv8 = static_cast<const uint8_t*>(d_kv);
+  c.num_pages = num_pages;
+  c.src.block_table = d_block_table;
+  c.src.max_pages = max_pages;
+  c.topk = max_pages * MLA_PAGE_SIZE;
+  c.lengths = d_cache_seqlens;
+  c.n_units = batch;
+  c.rows = static_cast<int>(rows);
+  c.s_q = s_q;
+  c.h_q = h_q;
+  c.causal = causal ? 1 : 0;
+  c.unit_request_div = 1;
+  c.scale = softmax_scale;
+  c.sched = d_sched;
+  c.split_offset = d_split_offset;
+  c.num_parts = num_parts;
+  c.ws = d_workspace;
+  c.ws_bytes = workspace_bytes;
+  c.out = d_out;
+  c.out_type = out_type;
+  c.lse = d_lse;
+  c.status = d_status;
+  c.stream = stream;
+  c.stall = stall;
+  return sparse_run(c, false);
 }
 
 }  // namespace
@@ -444,43 +490,10 @@ int mla_decode_splits(const void* d_q, const void* d_kv, const int32_t* d_block_
                       int dtype, int causal, float softmax_scale, const int32_t* d_sched,
                       const int32_t* d_split_offset, int num_parts, void* d_workspace, size_t workspace_bytes,
                       void* d_out, int out_type, float* d_lse, int32_t* d_status, mla_stream_t stream) {
-  if (dtype == MLA_DTYPE_FP8_RECORD) {
-    // A cache of FP8 records runs the sparse kernel (exact scores in codes
-    // and scales) with the block table as the slot source and a whole
-    // request as the unit, under the same plan as the 16-bit caches.
-    if (!d_block_table || !d_cache_seqlens || max_pages < 1 || batch < 1 || s_q < 1 || h_q < 1)
-      return MLA_ERR_INVALID_ARG;
-    if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
-    const long long rows = static_cast<long long>(s_q) * h_q;
-    if (rows > (1 << 20) || static_cast<long long>(max_pages) * MLA_PAGE_SIZE > (1LL << 31) - 1)
-      return MLA_ERR_UNSUPPORTED;
-    SparseCall c;
-    c.q = d_q;
-    c.kv8 = static_cast<const uint8_t*>(d_kv);
-    c.num_pages = num_pages;
-    c.src.block_table = d_block_table;
-    c.src.max_pages = max_pages;
-    c.topk = max_pages * MLA_PAGE_SIZE;
-    c.lengths = d_cache_seqlens;
-    c.n_units = batch;
-    c.rows = static_cast<int>(rows);
-    c.s_q = s_q;
-    c.h_q = h_q;
-    c.causal = causal ? 1 : 0;
-    c.unit_request_div = 1;
-    c.scale = softmax_scale;
-    c.sched = d_sched;
-    c.split_offset = d_split_offset;
-    c.num_parts = num_parts;
-    c.ws = d_workspace;
-    c.ws_bytes = workspace_bytes;
-    c.out = d_out;
-    c.out_type = out_type;
-    c.lse = d_lse;
-    c.status = d_status;
-    c.stream = stream;
-    return sparse_run(c, false);
-  }
+  if (dtype == MLA_DTYPE_FP8_RECORD)
+    return fp8_record_splits(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q, h_kv,
+                             causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace, workspace_bytes,
+                             d_out, out_type, d_lse, d_status, stream, 0);
   DecodeParams p;
   CUtensorMap qm, km, sm, rm;
   const int rc = dense_prepare(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q,
@@ -628,6 +641,10 @@ int mla_test_decode_timeout(const void* d_q, const void* d_kv, const int32_t* d_
                             int dtype, int causal, float softmax_scale, const int32_t* d_sched,
                             const int32_t* d_split_offset, int num_parts, void* d_workspace, size_t workspace_bytes,
                             void* d_out, int out_type, float* d_lse, int32_t* d_status, mla_stream_t stream) {
+  if (dtype == MLA_DTYPE_FP8_RECORD)
+    return fp8_record_splits(d_q, d_kv, d_block_table, max_pages, num_pages, d_cache_seqlens, batch, s_q, h_q, h_kv,
+                             causal, softmax_scale, d_sched, d_split_offset, num_parts, d_workspace, workspace_bytes,
+                             d_out, out_type, d_lse, d_status, stream, 1);
   if (dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED;
   DecodeParams p;
   CUtensorMap qm, km, sm, rm;

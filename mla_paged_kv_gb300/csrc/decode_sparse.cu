@@ -210,13 +210,20 @@ __device__ __forceinline__ void set_abort(volatile int* abort_flag, int32_t* sta
   report(status, code);
 }
 
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, limit_ns));
 }
 
-__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  return __all_sync(0xffffffffu, mbar_wait<true>(bar, parity, abort_flag));
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait<true>(bar, parity, abort_flag, limit_ns));
 }
+
+// Wait budget of the stall-test instance of the decode kernel (kStall):
+// short, so that its test ends quickly; the other instance keeps the 2 s
+// budget of every wait.
+constexpr uint64_t kDecodeStallWaitNs = 200000;  // 200 us
 
 // Two E4M3 codes (bytes 0 and 1 of `pair`) -> two bf16 of the same values
 // (low half = byte 0): E4M3 -> f16 -> f32 -> bf16 is exact at every step
@@ -309,8 +316,10 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint64_t p_desc0, uint64
   }
 }
 
+template <bool kStall>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     sparse_decode_kernel(const __grid_constant__ CUtensorMap q_map, const DecodeParams p) {
+  constexpr uint64_t kWaitNs = kStall ? kDecodeStallWaitNs : MLA_WAIT_LIMIT_NS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -395,7 +404,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       unit_tiles(P, b, nt, lo, hi);
       if (hi <= lo) continue;
       if (ptid == 0) {
-        if (u >= 1) ok = mbar_wait(&bars[Q_EMPTY], (u - 1) & 1, abort_flag);
+        if (u >= 1) ok = mbar_wait(&bars[Q_EMPTY], (u - 1) & 1, abort_flag, kWaitNs);
         if (ok) {
           mbar_arrive_expect_tx(&bars[Q_FULL], n_boxes * kQBoxBytes);
           const int row0 = b * p.rows + rb * kRowsPerBlock;
@@ -459,7 +468,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           issue_loads(t + 1, raw_n, sc_n);
         }
         bool failed = false;
-        if (t >= 2) failed = !mbar_wait(&bars[KV_EMPTY + st], ((t - 2) >> 1) & 1, abort_flag);
+        if (t >= 2) failed = !mbar_wait(&bars[KV_EMPTY + st], ((t - 2) >> 1) & 1, abort_flag, kWaitNs);
         // one decision for the whole producer group: its named barriers need every thread
         if (named_bar_or(kBarProdOr, 32 * kProducerWarps, failed)) {
           ok = false;
@@ -517,7 +526,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
     // no TMA write may land after this CTA exits
-    if (ptid == 0 && q_issued > 0) mbar_wait(&bars[Q_FULL], (q_issued - 1) & 1, nullptr);
+    if (ptid == 0 && q_issued > 0) mbar_wait(&bars[Q_FULL], (q_issued - 1) & 1, nullptr, kWaitNs);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -563,11 +572,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             MLA_TRACE(3, cq.t);
             const uint64_t kvs = kv_desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
-            if (rank == 0)
-              issue_qk<3>(tmem, q_desc0, kvs, idesc_qk);
-            else
-              issue_qk<2>(tmem, q_desc0, kvs, idesc_qk);
-            umma_commit(&bars[S_FULL]);
+            // the stall-test instance never computes its first tile's scores
+            // (the softmax's wait for them runs out)
+            if (!(kStall && cq.t == 0)) {
+              if (rank == 0)
+                issue_qk<3>(tmem, q_desc0, kvs, idesc_qk);
+              else
+                issue_qk<2>(tmem, q_desc0, kvs, idesc_qk);
+              umma_commit(&bars[S_FULL]);
+            }
             if (cq.k == cq.hi - 1) umma_commit(&bars[Q_EMPTY]);
             cursor_next(p, P, cq);
             progressed = true;
@@ -576,7 +589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (progressed) {
           t_last = globaltimer_ns();
         } else {
-          if (*abort_flag || globaltimer_ns() - t_last > MLA_WAIT_LIMIT_NS) {
+          if (*abort_flag || globaltimer_ns() - t_last > kWaitNs) {
             ok = false;
             break;
           }
@@ -586,7 +599,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // every MMA has completed before TMEM is released
       umma_commit(&bars[DRAIN]);
-      mbar_wait(&bars[DRAIN], 0, nullptr);
+      mbar_wait(&bars[DRAIN], 0, nullptr, kWaitNs);
     }
     __syncwarp();
   } else {
@@ -639,12 +652,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int k = lo; k < hi; ++k, ++t) {
         const int st = t & 1;
         // ---- phase 1: this thread's 32 partial scores, staged for the peer
-        if (ok) ok = warp_wait(&bars[KV_FULL + st], (t >> 1) & 1, abort_flag);
+        if (ok) ok = warp_wait(&bars[KV_FULL + st], (t >> 1) & 1, abort_flag, kWaitNs);
         // which of this thread's 32 slots are valid and visible to the row
         const int lim = row_last - k * kT - 32 * h;
         const uint32_t vis = (ok ? sVis[(t & (kVisSlots - 1)) * 2 + h] : 0u) &
                              (lim >= 31 ? 0xffffffffu : (lim < 0 ? 0u : (0xffffffffu >> (31 - lim))));
-        if (ok) ok = warp_wait(&bars[S_FULL], t & 1, abort_flag);
+        if (ok) ok = warp_wait(&bars[S_FULL], t & 1, abort_flag, kWaitNs);
         float s[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) s[j] = 0.f;
@@ -674,7 +687,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(&bars[S_FREE]);
           // the P buffer is free once P V of the previous tile is done
-          if (t >= 1) ok = warp_wait(&bars[P_FREE], (t - 1) & 1, abort_flag);
+          if (t >= 1) ok = warp_wait(&bars[P_FREE], (t - 1) & 1, abort_flag, kWaitNs);
         }
         if (ok) {
 #pragma unroll
@@ -689,7 +702,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---- phase 2: send the quarter's partials, receive the peer's, row max
         if (sender) {
           // the peer has read our previous partials (so that copy is complete)
-          bool sent = t == 0 || mbar_wait<true>(&bars[X_FREE + q], (t - 1) & 1, abort_flag);
+          bool sent = t == 0 || mbar_wait<true>(&bars[X_FREE + q], (t - 1) & 1, abort_flag, kWaitNs);
           if (sent) {
             bulk_copy_to_cluster(x_remote_q, x_stage + q_off, 32 * 128, xfull_remote);
             bulk_copy_to_cluster(x_remote_q + kPGroupBytes, x_stage + kPGroupBytes + q_off, 32 * 128, xfull_remote);
@@ -698,7 +711,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (tid == 0) MLA_TRACE(5, t);
-        ok = warp_wait_cluster(&bars[X_FULL + q], t & 1, abort_flag);
+        ok = warp_wait_cluster(&bars[X_FULL + q], t & 1, abort_flag, kWaitNs);
         float mt = -INFINITY;
         if (ok) {
           if (tid == 0) MLA_TRACE(6, t);
@@ -753,7 +766,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         l_part += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         // our partials have left the P buffer (the peer has read them) before P is written there
-        ok = warp_wait_cluster(&bars[X_FREE + q], t & 1, abort_flag);
+        ok = warp_wait_cluster(&bars[X_FREE + q], t & 1, abort_flag, kWaitNs);
         if (!ok) {
           set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
           continue;  // the next pair barrier takes both warps out
@@ -809,7 +822,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t l_other = tmem_ld1(tmem + lane_base + kTmemX + 3 - h);
       tmem_wait_ld();
       const float l_sum = l_part + __uint_as_float(l_other);
-      ok = warp_wait(&bars[O_FULL], u & 1, abort_flag);
+      ok = warp_wait(&bars[O_FULL], u & 1, abort_flag, kWaitNs);
       if (named_bar_or(pair_bar, pair_n, !ok)) {
         ok = false;
         break;
@@ -904,7 +917,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (!ok && sender) {
       set_abort(abort_flag, p.status, MLA_ERR_TIMEOUT);
       // partial scores the peer already sent may still be landing here
-      mbar_wait<true>(&bars[X_FULL + q], t & 1, nullptr);
+      mbar_wait<true>(&bars[X_FULL + q], t & 1, nullptr, kWaitNs);
     }
   }
 
@@ -1081,11 +1094,19 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
 
 int sparse_smem_bytes() { return sp::kSmemBytes; }
 int sparse_threads() { return sp::kThreads; }
-const void* sparse_kernel_ptr() { return reinterpret_cast<const void*>(&sp::sparse_decode_kernel); }
+// stall 1: the test instance whose first tile's scores are never computed
+const void* sparse_kernel_ptr(int stall) {
+  return stall ? reinterpret_cast<const void*>(&sp::sparse_decode_kernel<true>)
+               : reinterpret_cast<const void*>(&sp::sparse_decode_kernel<false>);
+}
 
-cudaError_t launch_sparse(const CUtensorMap& q_map, const DecodeParams& p, int num_parts, cudaStream_t stream) {
+cudaError_t launch_sparse(const CUtensorMap& q_map, const DecodeParams& p, int num_parts, int stall,
+                          cudaStream_t stream) {
   const dim3 grid(2 * num_parts * p.row_blocks);
-  sp::sparse_decode_kernel<<<grid, sp::kThreads, sp::kSmemBytes, stream>>>(q_map, p);
+  if (stall)
+    sp::sparse_decode_kernel<true><<<grid, sp::kThreads, sp::kSmemBytes, stream>>>(q_map, p);
+  else
+    sp::sparse_decode_kernel<false><<<grid, sp::kThreads, sp::kSmemBytes, stream>>>(q_map, p);
   return cudaGetLastError();
 }
 
