@@ -262,7 +262,11 @@ int mla_combine(const void* d_workspace, size_t workspace_bytes, const int32_t* 
  * exact in codes and scales: each 128-dim group's codes (exact in bf16) meet
  * Q on the tensor cores with fp32 accumulation, and the group's scale
  * multiplies that product in fp32; for the values, the softmax weight times
- * the group's scale is rounded to bf16 and meets the unscaled codes.
+ * the group's scale is rounded to bf16 and meets the unscaled codes, and each
+ * group's output is divided by the sum of the weights so rounded (the LSE
+ * keeps the exact sum), so that a row with one or a few dominant keys
+ * carries no rounding of its scales into the output.  A scale below the
+ * smallest normal fp32 counts as 0.
  *   d_q           bf16 [batch, s_q, h_q, 576]
  *   d_kv8         uint8 [num_pages, 64, 656]
  *   d_indices     int32 [batch, s_q, topk]

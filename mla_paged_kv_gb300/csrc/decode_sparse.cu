@@ -220,6 +220,15 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
   return __all_sync(0xffffffffu, mbar_wait<true>(bar, parity, abort_flag, limit_ns));
 }
 
+// 1 / x within 5.1% for a normal positive x below 2^126: one integer
+// subtract from the bit pattern negates the exponent and takes the
+// mantissa's reciprocal to first order.  Used only to rescale the rounding
+// residual (relative size <= 2^-9) of a product p * x, so the result is
+// within 2^-13 of p of the exact quotient.  The producer stores scales
+// below the smallest normal fp32 as 0; for x = 0 the residual it scales is
+// 0 (so is the product), and the term is 0.
+__device__ __forceinline__ float approx_inv(float x) { return __int_as_float(0x7EF311C7 - __float_as_int(x)); }
+
 // Wait budget of the stall-test instance of the decode kernel (kStall):
 // short, so that its test ends quickly; the other instance keeps the 2 s
 // budget of every wait.
@@ -495,9 +504,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (ptid < kT) {
+          // a masked slot, and a scale below the smallest normal fp32 (its
+          // products with the codes are below 2^-117 and are lost in fp32
+          // rounding of any score or value that matters), count as 0; the
+          // weights' rounding correction then needs no guard for them
           const bool live = idx_t[ptid] >= 0;
-          scale_st[ptid] = live ? sc[0] : 0.f;
-          scale_st[kT + ptid] = live ? sc[1] : 0.f;
+          scale_st[ptid] = live && fabsf(sc[0]) >= 1.17549435e-38f ? sc[0] : 0.f;
+          scale_st[kT + ptid] = live && fabsf(sc[1]) >= 1.17549435e-38f ? sc[1] : 0.f;
         }
 #pragma unroll
         for (int i = 0; i < kPerMax; ++i) {
@@ -649,6 +662,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // running max (log2 units), the same in both threads of a row, and
       // this thread's part of the fp32 row sum
       float m_used = -INFINITY, l_part = 0.f;
+      // per group of this rank, the P V weights' rounding: sum over this
+      // thread's keys of (bf16(p * scale) - p * scale) / scale, so that each
+      // group's O columns are divided by the weights the MMA actually used
+      float corr0 = 0.f, corr1 = 0.f;
       for (int k = lo; k < hi; ++k, ++t) {
         const int st = t & 1;
         // ---- phase 1: this thread's 32 partial scores, staged for the peer
@@ -755,6 +772,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           alpha = ex2(m_used - mt);  // 0 when m_used == -inf
           rescale = k > lo;
           l_part *= alpha;
+          corr0 *= alpha;
+          corr1 *= alpha;
           m_used = mt;
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
@@ -788,21 +807,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t sc_base = smem_u32(sScale + st * (2 * kT)) + 128u * h;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
+          uint64_t corr2 = 0;  // (even keys, odd keys) as an f32x2 pair
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float4 sa = ld_shared_v4(sc_base + (g * kT + 8 * c) * 4);
             const float4 sb = ld_shared_v4(sc_base + (g * kT + 8 * c + 4) * 4);
             const float w[8] = {s[8 * c] * sa.x,     s[8 * c + 1] * sa.y, s[8 * c + 2] * sa.z, s[8 * c + 3] * sa.w,
                                 s[8 * c + 4] * sb.x, s[8 * c + 5] * sb.y, s[8 * c + 6] * sb.z, s[8 * c + 7] * sb.w};
+            const float sc8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
             uint32_t pk[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const __nv_bfloat162 hv = __floats2bfloat162_rn(w[2 * i], w[2 * i + 1]);
               pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
+              // the rounding of each weight (an exact difference), in units of
+              // p: divided by the key's scale through an approximate inverse
+              uint64_t fr, wr, ir;
+              asm("mov.b64 %0, {%1, %2};" : "=l"(fr) : "r"(pk[i] << 16), "r"(pk[i] & 0xffff0000u));
+              asm("mov.b64 %0, {%1, %2};" : "=l"(wr) : "f"(w[2 * i]), "f"(w[2 * i + 1]));
+              asm("mov.b64 %0, {%1, %2};" : "=l"(ir) : "f"(approx_inv(sc8[2 * i])), "f"(approx_inv(sc8[2 * i + 1])));
+              asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(fr) : "l"(fr), "l"(wr));
+              asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(corr2) : "l"(fr), "l"(ir), "l"(corr2));
             }
             *reinterpret_cast<uint4*>(sP + g * kPGroupBytes + r * 128 + (((4u * h + c) ^ swz) << 4)) =
                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
+          float corr_e, corr_o;
+          asm("mov.b64 {%0, %1}, %2;" : "=f"(corr_e), "=f"(corr_o) : "l"(corr2));
+          if (g == 0)
+            corr0 += corr_e + corr_o;
+          else
+            corr1 += corr_e + corr_o;
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -815,13 +850,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // ---- epilogue of this (unit, split): the row sum of both threads
       tmem_st1(tmem + lane_base + kTmemX + 2 + h, __float_as_uint(l_part));
+      // the other thread of the row needs this thread's correction of its group (1 - h)
+      tmem_st1(tmem + lane_base + kTmemX + 4 + h, __float_as_uint(h == 0 ? corr1 : corr0));
       tmem_wait_st();
       tc_fence_before();
       named_bar_sync(pair_bar, pair_n);
       tc_fence_after();
       const uint32_t l_other = tmem_ld1(tmem + lane_base + kTmemX + 3 - h);
       tmem_wait_ld();
+      const uint32_t c_other = tmem_ld1(tmem + lane_base + kTmemX + 5 - h);
+      tmem_wait_ld();
       const float l_sum = l_part + __uint_as_float(l_other);
+      // this thread's O columns are group h's: divided by the sum of the
+      // weights that multiplied them (the LSE keeps the exact sum)
+      const float l_norm = l_sum + ((h == 0 ? corr0 : corr1) + __uint_as_float(c_other));
       ok = warp_wait(&bars[O_FULL], u & 1, abort_flag, kWaitNs);
       if (named_bar_or(pair_bar, pair_n, !ok)) {
         ok = false;
@@ -831,7 +873,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int s_begin = p.split_offset[b];
       const int nsplit = p.split_offset[b + 1] - s_begin;
       const int slot = s_begin + ((b == P.b0) ? P.s0 : 0);
-      const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      const float inv_l = l_sum > 0.f ? 1.f / l_norm : 0.f;
       const size_t orow = static_cast<size_t>(b) * p.rows + row;
       const size_t arow = static_cast<size_t>(slot) * p.rows + row;
       const bool direct = (nsplit == 1);
