@@ -675,9 +675,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t vis = (ok ? sVis[(t & (kVisSlots - 1)) * 2 + h] : 0u) &
                              (lim >= 31 ? 0xffffffffu : (lim < 0 ? 0u : (0xffffffffu >> (31 - lim))));
         if (ok) ok = warp_wait(&bars[S_FULL], t & 1, abort_flag, kWaitNs);
-        float s[32];
+        // scores 2k, 2k + 1 of this thread's 32 as a pair: the elementwise
+        // steps run as packed f32x2 instructions (the same IEEE operations)
+        float2 s2[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) s[j] = 0.f;
+        for (int k = 0; k < 16; ++k) s2[k] = make_float2(0.f, 0.f);
         if (ok) {
           if (tid == 0) MLA_TRACE(4, t);
           tc_fence_after();
@@ -691,14 +693,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j4 = 0; j4 < 8; ++j4) {
                 const float4 sc = ld_shared_v4(sc_base + (a * kT + 4 * j4) * 4);
-                s[4 * j4 + 0] = fmaf(sc.x, __uint_as_float(v[4 * j4 + 0]), s[4 * j4 + 0]);
-                s[4 * j4 + 1] = fmaf(sc.y, __uint_as_float(v[4 * j4 + 1]), s[4 * j4 + 1]);
-                s[4 * j4 + 2] = fmaf(sc.z, __uint_as_float(v[4 * j4 + 2]), s[4 * j4 + 2]);
-                s[4 * j4 + 3] = fmaf(sc.w, __uint_as_float(v[4 * j4 + 3]), s[4 * j4 + 3]);
+                s2[2 * j4] = __ffma2_rn(make_float2(sc.x, sc.y),
+                                        make_float2(__uint_as_float(v[4 * j4]), __uint_as_float(v[4 * j4 + 1])),
+                                        s2[2 * j4]);
+                s2[2 * j4 + 1] = __ffma2_rn(make_float2(sc.z, sc.w),
+                                            make_float2(__uint_as_float(v[4 * j4 + 2]), __uint_as_float(v[4 * j4 + 3])),
+                                            s2[2 * j4 + 1]);
               }
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) s[j] += __uint_as_float(v[j]);
+              for (int k = 0; k < 16; ++k)
+                s2[k] = __fadd2_rn(s2[k], make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])));
             }
           }
           tc_fence_before();
@@ -709,7 +714,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (ok) {
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            st_shared_v4(x_stage + chunk_off(c), s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+            st_shared_v4(x_stage + chunk_off(c), s2[2 * c].x, s2[2 * c].y, s2[2 * c + 1].x, s2[2 * c + 1].y);
           fence_proxy_async_smem();
         }
         if (named_bar_or(pair_bar, pair_n, !ok)) {
@@ -736,17 +741,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const float4 o = ld_shared_v4(x_local + chunk_off(c));
-            s[4 * c + 0] += o.x;
-            s[4 * c + 1] += o.y;
-            s[4 * c + 2] += o.z;
-            s[4 * c + 3] += o.w;
+            s2[2 * c] = __fadd2_rn(s2[2 * c], make_float2(o.x, o.y));
+            s2[2 * c + 1] = __fadd2_rn(s2[2 * c + 1], make_float2(o.z, o.w));
           }
           // mask, scale into the log2 domain, maximum of this thread's 32
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            s[j] = ((vis >> j) & 1u) ? s[j] * p.scale_log2 : -INFINITY;
-            m4[j & 3] = fmaxf(m4[j & 3], s[j]);
+          for (int k = 0; k < 16; ++k) {
+            const float2 x = __fmul2_rn(s2[k], sl2);
+            s2[k].x = ((vis >> (2 * k)) & 1u) ? x.x : -INFINITY;
+            s2[k].y = ((vis >> (2 * k + 1)) & 1u) ? x.y : -INFINITY;
+            m4[(2 * k) & 3] = fmaxf(m4[(2 * k) & 3], s2[k].x);
+            m4[(2 * k + 1) & 3] = fmaxf(m4[(2 * k + 1) & 3], s2[k].y);
           }
           mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           tmem_st1(tmem + lane_base + kTmemX + h, __float_as_uint(mt));
@@ -777,13 +784,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           m_used = mt;
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // ls2[0] = (sum of keys 0 mod 4, 1 mod 4), ls2[1] = (2 mod 4, 3 mod 4)
+        float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float2 nref2 = make_float2(-mref, -mref);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          s[j] = ex2(s[j] - mref);
-          ls[j & 3] += s[j];
+        for (int k = 0; k < 16; ++k) {
+          const float2 d = __fadd2_rn(s2[k], nref2);
+          s2[k] = make_float2(ex2(d.x), ex2(d.y));
+          ls2[k & 1] = __fadd2_rn(ls2[k & 1], s2[k]);
         }
-        l_part += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        l_part += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
         // our partials have left the P buffer (the peer has read them) before P is written there
         ok = warp_wait_cluster(&bars[X_FREE + q], t & 1, abort_flag, kWaitNs);
         if (!ok) {
@@ -812,8 +822,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 4; ++c) {
             const float4 sa = ld_shared_v4(sc_base + (g * kT + 8 * c) * 4);
             const float4 sb = ld_shared_v4(sc_base + (g * kT + 8 * c + 4) * 4);
-            const float w[8] = {s[8 * c] * sa.x,     s[8 * c + 1] * sa.y, s[8 * c + 2] * sa.z, s[8 * c + 3] * sa.w,
-                                s[8 * c + 4] * sb.x, s[8 * c + 5] * sb.y, s[8 * c + 6] * sb.z, s[8 * c + 7] * sb.w};
+            const float2 w01 = __fmul2_rn(s2[4 * c], make_float2(sa.x, sa.y));
+            const float2 w23 = __fmul2_rn(s2[4 * c + 1], make_float2(sa.z, sa.w));
+            const float2 w45 = __fmul2_rn(s2[4 * c + 2], make_float2(sb.x, sb.y));
+            const float2 w67 = __fmul2_rn(s2[4 * c + 3], make_float2(sb.z, sb.w));
+            const float w[8] = {w01.x, w01.y, w23.x, w23.y, w45.x, w45.y, w67.x, w67.y};
             const float sc8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
             uint32_t pk[4];
 #pragma unroll
