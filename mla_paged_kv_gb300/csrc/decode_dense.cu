@@ -940,10 +940,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float mref = (r_t == -INFINITY) ? 0.f : r_t;
         uint32_t pk[kT / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        const float2 cl2 = make_float2(c_log2, c_log2), nref2 = make_float2(-mref, -mref);
 #pragma unroll
         for (int i = 0; i < kT / 2; ++i) {
-          const float p0 = ex2(fmaf(s[2 * i], c_log2, -mref));
-          const float p1 = ex2(fmaf(s[2 * i + 1], c_log2, -mref));
+          // the two exponent offsets as one packed f32x2 FMA (the same IEEE operations)
+          const float2 e = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), cl2, nref2);
+          const float p0 = ex2(e.x);
+          const float p1 = ex2(e.y);
           pk[i] = pack2<kHalf>(p0, p1);
           ls[i & 3] += p0 + p1;
         }
