@@ -817,40 +817,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t sc_base = smem_u32(sScale + st * (2 * kT)) + 128u * h;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
-          uint64_t corr2 = 0;  // (even keys, odd keys) as an f32x2 pair
+          float2 corr2 = make_float2(0.f, 0.f);  // (even keys, odd keys)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float4 sa = ld_shared_v4(sc_base + (g * kT + 8 * c) * 4);
             const float4 sb = ld_shared_v4(sc_base + (g * kT + 8 * c + 4) * 4);
-            const float2 w01 = __fmul2_rn(s2[4 * c], make_float2(sa.x, sa.y));
-            const float2 w23 = __fmul2_rn(s2[4 * c + 1], make_float2(sa.z, sa.w));
-            const float2 w45 = __fmul2_rn(s2[4 * c + 2], make_float2(sb.x, sb.y));
-            const float2 w67 = __fmul2_rn(s2[4 * c + 3], make_float2(sb.z, sb.w));
-            const float w[8] = {w01.x, w01.y, w23.x, w23.y, w45.x, w45.y, w67.x, w67.y};
-            const float sc8[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+            const float2 w2[4] = {__fmul2_rn(s2[4 * c], make_float2(sa.x, sa.y)),
+                                  __fmul2_rn(s2[4 * c + 1], make_float2(sa.z, sa.w)),
+                                  __fmul2_rn(s2[4 * c + 2], make_float2(sb.x, sb.y)),
+                                  __fmul2_rn(s2[4 * c + 3], make_float2(sb.z, sb.w))};
+            const float2 inv2[4] = {make_float2(approx_inv(sa.x), approx_inv(sa.y)),
+                                    make_float2(approx_inv(sa.z), approx_inv(sa.w)),
+                                    make_float2(approx_inv(sb.x), approx_inv(sb.y)),
+                                    make_float2(approx_inv(sb.z), approx_inv(sb.w))};
             uint32_t pk[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const __nv_bfloat162 hv = __floats2bfloat162_rn(w[2 * i], w[2 * i + 1]);
+              const __nv_bfloat162 hv = __floats2bfloat162_rn(w2[i].x, w2[i].y);
               pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
               // the rounding of each weight (an exact difference), in units of
               // p: divided by the key's scale through an approximate inverse
-              uint64_t fr, wr, ir;
-              asm("mov.b64 %0, {%1, %2};" : "=l"(fr) : "r"(pk[i] << 16), "r"(pk[i] & 0xffff0000u));
-              asm("mov.b64 %0, {%1, %2};" : "=l"(wr) : "f"(w[2 * i]), "f"(w[2 * i + 1]));
-              asm("mov.b64 %0, {%1, %2};" : "=l"(ir) : "f"(approx_inv(sc8[2 * i])), "f"(approx_inv(sc8[2 * i + 1])));
-              asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(fr) : "l"(fr), "l"(wr));
-              asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(corr2) : "l"(fr), "l"(ir), "l"(corr2));
+              const float2 rnd = __fadd2_rn(make_float2(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xffff0000u)),
+                                            make_float2(-w2[i].x, -w2[i].y));
+              corr2 = __ffma2_rn(rnd, inv2[i], corr2);
             }
             *reinterpret_cast<uint4*>(sP + g * kPGroupBytes + r * 128 + (((4u * h + c) ^ swz) << 4)) =
                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
-          float corr_e, corr_o;
-          asm("mov.b64 {%0, %1}, %2;" : "=f"(corr_e), "=f"(corr_o) : "l"(corr2));
           if (g == 0)
-            corr0 += corr_e + corr_o;
+            corr0 += corr2.x + corr2.y;
           else
-            corr1 += corr_e + corr_o;
+            corr1 += corr2.x + corr2.y;
         }
         fence_proxy_async_smem();
         tc_fence_before();
