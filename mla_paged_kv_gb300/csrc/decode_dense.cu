@@ -938,31 +938,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (tid == 0) MLA_TRACE(13, t);
         const float r_t = (mt > r_cur + kTau) ? mt : r_cur;
         const float mref = (r_t == -INFINITY) ? 0.f : r_t;
-        uint32_t pk[kT / 2];
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        const float2 cl2 = make_float2(c_log2, c_log2), nref2 = make_float2(-mref, -mref);
-#pragma unroll
-        for (int i = 0; i < kT / 2; ++i) {
-          // the two exponent offsets as one packed f32x2 FMA (the same IEEE operations)
-          const float2 e = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), cl2, nref2);
-          const float p0 = ex2(e.x);
-          const float p1 = ex2(e.y);
-          pk[i] = pack2<kHalf>(p0, p1);
-          ls[i & 3] += p0 + p1;
-        }
-        const float rowsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
         // the own P buffer is free once our P V and the peer's P V of the
-        // previous own tile are done (the latter also means our copy landed)
+        // previous own tile are done (the latter also means our copy landed);
+        // waited for before the exponentials, so that each 16-byte piece of P
+        // is stored as soon as it is formed
         if (own_i >= 1) {
           ok = warp_wait_cluster(&bars[OWN_FREE], (own_i - 1) & 1, abort_flag, kWaitNs);
           if (!ok) break;
         }
         if (tid == 0) MLA_TRACE(14, t);
         uint8_t* prow = sPOwn + r * 128;
+        // row sum in four fp32 partial sums (two packed pairs: keys 0, 1 mod 4
+        // and 2, 3 mod 4), one packed add per pair of keys
+        float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float2 cl2 = make_float2(c_log2, c_log2), nref2 = make_float2(-mref, -mref);
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int i = 4 * cc + q4;
+            // the two exponent offsets as one packed f32x2 FMA (the same IEEE operations)
+            const float2 e = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), cl2, nref2);
+            const float p0 = ex2(e.x);
+            const float p1 = ex2(e.y);
+            pk[q4] = pack2<kHalf>(p0, p1);
+            ls2[i & 1] = __fadd2_rn(ls2[i & 1], make_float2(p0, p1));
+          }
           *reinterpret_cast<uint4*>(prow + ((static_cast<uint32_t>(cc) ^ swz) << 4)) =
-              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        const float rowsum = (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
         fence_proxy_async_smem();
         __syncwarp();
         // this warp's 32 P rows to the peer's receive buffer
