@@ -225,6 +225,21 @@ __host__ __device__ constexpr int k_box(int j) {
 // ends quickly; the other instances keep the 2 s budget of every wait.
 constexpr uint64_t kStallWaitNs = 200000;  // 200 us
 
+// tcgen05.ld of 32 columns (as tmem_ld32) that also returns the maximum of
+// the 32 fp32 values this thread loaded (valid after tcgen05.wait::ld).
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32], float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31]), "=f"(mx)
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void set_abort(volatile int* abort_flag, int32_t* status, int code) {
   *abort_flag = 1;
   report(status, code);
@@ -897,17 +912,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // sat on every own tile's critical path and cost 4-9 us per call.)
         if (sBad[own_i & 1]) keep = 0ull;
         float s[kT];
+        float m_lo, m_hi;  // the loads' own maxima of the two halves
         {
           uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
           uint32_t (&hi32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
-          tmem_ld32(taddr + kTmemS, lo32);
-          tmem_ld32(taddr + kTmemS + 32u, hi32);
+          tmem_ld32_max(taddr + kTmemS, lo32, m_lo);
+          tmem_ld32_max(taddr + kTmemS + 32u, hi32, m_hi);
           tmem_wait_ld();
         }
         tc_fence_before();
         mbar_arrive(&bars[S_FREE]);
         // masked keys (past the last visible one, or on a page outside the pool) ->
         // -inf; raw tile max (the scale is positive, so max commutes with it)
+        // a tile with every key visible takes the loads' maxima; otherwise the
+        // masked keys become -inf and the maximum is taken over the rest
+        float mraw = fmaxf(m_lo, m_hi);
         if (keep != ~0ull) {
           const uint32_t klo = static_cast<uint32_t>(keep), khi = static_cast<uint32_t>(keep >> 32);
 #pragma unroll
@@ -915,16 +934,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!((klo >> j) & 1u)) s[j] = -INFINITY;
             if (!((khi >> j) & 1u)) s[j + 32] = -INFINITY;
           }
+          float mx[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+          for (int j = 16; j < kT; j += 8)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[j + i]);
+          mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         }
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[i + 8]);
-#pragma unroll
-        for (int j = 16; j < kT; j += 8)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[j + i]);
-        const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float mt = mraw * c_log2;  // -inf stays -inf
         // the peer derives this tile's reference from its raw maximum, as we
         // do: it is sent at once and waits for nothing of the peer's
