@@ -24,15 +24,20 @@ def ragged_lengths(n, hi, seed, specials=(0, 1, 63, 64, 65, 127, 128, 129)):
     return lens.tolist()
 
 
-@pytest.mark.parametrize("batch,s_q,h_q,causal,hi", [(1500, 1, 16, False, 200), (700, 2, 32, True, 300)])
-def test_dense_many_short_requests(batch, s_q, h_q, causal, hi):
+@pytest.mark.parametrize("batch,s_q,h_q,causal,hi,h_kv,dtype", [
+    (1500, 1, 16, False, 200, 1, torch.bfloat16),
+    (700, 2, 32, True, 300, 1, torch.bfloat16),
+    (700, 1, 64, False, 200, 2, torch.float16),   # two latent KV heads, fp16 cache and output
+])
+def test_dense_many_short_requests(batch, s_q, h_q, causal, hi, h_kv, dtype):
     lens = ragged_lengths(batch, hi, seed=batch + h_q)  # causal with L < s_q: rows that see no key
-    case = wl.dense_case(batch, s_q, h_q, 0, seqlens=lens, causal=causal, seed=batch + s_q)
+    case = wl.dense_case(batch, s_q, h_q, 0, seqlens=lens, causal=causal, seed=batch + s_q, h_kv=h_kv,
+                         dtype=dtype)
     c = to_dev(case)
-    pl = mla.plan(c.cache_seqlens, batch, s_q * h_q, num_parts=mla.mla_num_parts_dense(s_q, h_q, 1))
+    pl = mla.plan(c.cache_seqlens, batch, s_q * h_q, num_parts=mla.mla_num_parts_dense(s_q, h_q, h_kv))
     # more units than partitions by far: each partition runs through many units
     assert batch >= 8 * pl.num_parts
-    out = torch.full((batch, s_q, h_q, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((batch, s_q, h_q, 512), float("nan"), dtype=dtype, device="cuda")
     lse = torch.full((batch, s_q, h_q), float("nan"), device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     mla.mla_decode_fwd(c.q, c.kv, c.block_table, c.cache_seqlens, pl.sched, pl.split_offset, pl.num_parts,
